@@ -1,0 +1,439 @@
+"""Benchmark of the paged KV cache hot path on one GB300 (or N replicas).
+
+A step is one serving decode step of one layer for the whole batch:
+host metadata (decode appends, prefill allocation, table export, slot
+mapping, H2D), the cache write of the step's new K/V, and paged decode
+attention with split-K and the log-sum-exp merge.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl native|reference]
+
+Prints one JSON line on rank 0.  ``value`` is algorithmic HBM bytes of the
+step (K/V of every attended token read once, q/out, table entries and
+lengths, plus the cache write) per second of device time, summed over
+ranks; each rank runs its own replica of the workload (weak scaling, no
+data-path collective).  L2 is flushed (a memset of twice its size) before
+every timed step, outside the timed events.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn HBM GB/s (% of ~8 TB/s peak) and decode tokens/s at 1 GB300"
+DEFAULT_WORKLOAD = "decode_gqa14x2_d64_fp16"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="native", choices=("native", "reference"))
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- helpers
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in ("paged_kv_cache_128_gb300/csrc/paged_decode.cu", "paged_kv_cache_128_gb300/csrc/common.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per attention call from a committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    entry = rec.get(workload)
+    if not entry or entry.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_call")
+
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------- oracle timing
+
+ORACLE_SNIPPET = r"""
+import json, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+from oracle.block_manager import BlockManager
+from oracle.paged_cache import reshape_and_cache
+from oracle.attention import paged_decode_attention
+from paged_kv_cache_128_gb300.inputs import make_workload, make_values, pad_positions
+import torch
+
+wl = make_workload({name!r})
+vals = make_values(wl)
+def st(t):
+    t = t.contiguous()
+    return t.view(torch.int16).numpy().view(np.uint16) if wl.dtype == "bf16" else t.numpy()
+budget = {budget}
+# sample: the first S decode sequences (a bounded slice of the same step)
+S = min(wl.num_seqs, {max_seqs})
+def setup():
+    mgr = BlockManager(wl.num_blocks, wl.block_size, None if wl.free_order is None else wl.free_order.tolist())
+    shape = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
+    kc = np.zeros(shape, dtype=st(vals.k_step[:1]).dtype)
+    vc = np.zeros_like(kc)
+    ids = set(int(i) for i in wl.decode_ids[:S])
+    off = vals.hist_offsets
+    pos = {{}}
+    for op, sid, n in wl.setup_ops:
+        if op == "prefill":
+            s = mgr.allocate_for_prefill(sid, n)
+        elif op == "append":
+            s = mgr.append_slots(sid, n)
+        else:
+            mgr.free_sequence(sid); continue
+        if sid in ids:
+            b = int(np.nonzero(wl.decode_ids == sid)[0][0])
+            a = off[b] + pos.get(sid, 0)
+            reshape_and_cache(st(vals.k_hist[a:a + n]), st(vals.v_hist[a:a + n]), kc, vc, s)
+            pos[sid] = pos.get(sid, 0) + n
+    return mgr, kc, vc
+mgr, kc, vc = setup()
+sample_ids = wl.decode_ids[:S].tolist()
+q = st(vals.q[:S])
+k_new = st(vals.k_step[:S]); v_new = st(vals.v_step[:S])
+elapsed, steps, bytes_total = 0.0, 0, 0
+es = 4 if wl.dtype == "f32" else 2
+row = wl.num_kv_heads * wl.head_dim * es
+while elapsed < budget and steps < 10000:
+    if not mgr.can_append_slots(sample_ids):   # pool exhausted by growth: rebuild, untimed
+        mgr, kc, vc = setup()
+    t0 = time.perf_counter()
+    slots = mgr.decode_step(sample_ids)
+    mb = max(len(mgr.block_table(s)) for s in sample_ids)
+    tables, lens = mgr.export(sample_ids, mb)
+    reshape_and_cache(k_new, v_new, kc, vc, slots)
+    paged_decode_attention(q, kc, vc, tables, lens, wl.scale, wl.dtype)
+    elapsed += time.perf_counter() - t0
+    steps += 1
+    L = np.asarray(lens, dtype=np.int64)
+    bytes_total += int(L.sum()) * 2 * row + 2 * S * wl.num_heads * wl.head_dim * es \
+        + 4 * (S + int((-(-L // wl.block_size)).sum())) + 2 * 2 * S * row + 4 * S
+print(json.dumps({{"seconds": elapsed, "steps": steps, "seqs": S, "bytes": bytes_total,
+                  "tokens": steps * S}}))
+"""
+
+
+def run_oracle_sample(name, budget, max_seqs):
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    code = ORACLE_SNIPPET.format(root=ROOT, name=name, budget=budget, max_seqs=max_seqs)
+    proc = subprocess.run([sys.executable, "-c", code], env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                          text=True, timeout=budget * 20 + 300)
+    if proc.returncode != 0:
+        raise RuntimeError("oracle sample failed:\n" + proc.stderr[-2000:])
+    return json.loads(proc.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(name, budget):
+    r = run_oracle_sample(name, budget, max_seqs=8)
+    gbs = r["bytes"] / r["seconds"] / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": (f"float64 numpy oracle, one host thread: {r['steps']} decode steps of the first "
+                       f"{r['seqs']} sequences of {name} (manager append + export, cache write, attention), "
+                       f"{r['seconds']:.1f} s"),
+            "decode_tokens_per_s": r["tokens"] / r["seconds"]}
+
+
+# ------------------------------------------------------------- native arm
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def run_native(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_128_gb300 as pk
+    from paged_kv_cache_128_gb300.engine import PagedDecodeEngine
+    from paged_kv_cache_128_gb300.inputs import make_values, make_workload
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = make_workload(args.workload)
+    pk.lib()
+    total_steps = args.warmup + args.steps
+    eng = PagedDecodeEngine(wl, dev, max_steps=2 * total_steps + 4, fill_sentinel=True)
+    vals = make_values(wl, device="cuda") if wl.num_seqs else None
+    eng.setup(vals)
+    q, k_step, v_step = vals.q, vals.k_step, vals.v_step
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---------------- device-resident timing ----------------
+    for _ in range(args.warmup):
+        eng.step(q, k_step, v_step)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    step_bytes, attn_bytes, attn_tokens = [], [], []
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        s0, a0, e1 = ev[i]
+        s0.record()
+        eng.host_metadata()
+        eng.write_step_kv(k_step, v_step)
+        a0.record()
+        eng.attention(q)
+        e1.record()
+        eng.steps_done += 1
+        lens = eng.h_lens.numpy().copy()
+        ab = eng.algorithmic_bytes(lens)
+        step_bytes.append(ab["step"])
+        attn_bytes.append(ab["attention"])
+        attn_tokens.append(int(lens.size))
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    step_ms = [s.elapsed_time(e) for s, _, e in ev]
+    attn_ms = [a.elapsed_time(e) for _, a, e in ev]
+    t_step = sum(step_ms) / 1e3
+    t_attn = sum(attn_ms) / 1e3
+    t_max = torch.tensor([t_step], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    t_step_max = float(t_max.item())
+    bytes_all = sum(step_bytes) * world
+    value_gbs = bytes_all / t_step_max / 1e9
+    tokens_per_s = sum(attn_tokens) * world / t_step_max
+    status = pk.device_error()
+
+    # ---------------- end-to-end through host buffers ----------------
+    pin = dict(pin_memory=True)
+    q_h = q.cpu().pin_memory()
+    k_h = k_step.cpu().pin_memory()
+    v_h = v_step.cpu().pin_memory()
+    out_h = torch.empty(q.shape, dtype=q.dtype, **pin)
+    q_d, k_d, v_d = torch.empty_like(q), torch.empty_like(k_step), torch.empty_like(v_step)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    e2e_bytes = []
+    barrier()
+    for i in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        s0, e1 = e2e_ev[i]
+        s0.record()
+        q_d.copy_(q_h, non_blocking=True)
+        k_d.copy_(k_h, non_blocking=True)
+        v_d.copy_(v_h, non_blocking=True)
+        out = eng.step(q_d, k_d, v_d)
+        out_h.copy_(out, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        e2e_bytes.append(eng.algorithmic_bytes(eng.h_lens.numpy().copy())["step"])
+    torch.cuda.synchronize()
+    t_e2e = torch.tensor([sum(s.elapsed_time(e) for s, e in e2e_ev) / 1e3], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
+    h2d = (q.numel() + k_step.numel() + v_step.numel()) * q.element_size() + 4 * (
+        eng.h_slots.numel() + eng.h_tables.numel() + eng.h_lens.numel())
+    d2h = out_h.numel() * out_h.element_size()
+    e2e_gbs = sum(e2e_bytes) * world / float(t_e2e.item()) / 1e9
+
+    peak, peak_kind = measured_peak()
+    achieved = sum(attn_bytes) / t_attn / 1e9
+    traffic = recorded_traffic(args.workload)
+    mean_attn_bytes = sum(attn_bytes) / len(attn_bytes)
+    result = {
+        "metric": METRIC,
+        "value": value_gbs,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t_step_max / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.dtype,
+        "data": "synthetic (seeded; no dataset on the source pages)",
+        "config": {
+            "workload": wl.name,
+            "num_seqs": wl.num_seqs, "num_heads": wl.num_heads, "num_kv_heads": wl.num_kv_heads,
+            "head_dim": wl.head_dim, "block_size": wl.block_size, "num_blocks": wl.num_blocks,
+            "mean_seq_len": float(np.mean(wl.cached_lens)) + 1,
+            "prefill_tokens_per_step": int(wl.prefill_lens.sum()), "padded_slots_per_step": wl.num_pad,
+            "l2": "flushed before every step (memset of 2x L2), outside the timed events",
+            "parallelism": f"replicas x{world}",
+            "plan": {"kernel": "tma_mma" if eng.plan.kernel == 1 else "simt",
+                     "blocks_per_split": eng.plan.blocks_per_split, "num_splits": eng.plan.num_splits},
+        },
+        "decode_tokens_per_s": tokens_per_s,
+        "hbm_frac_of_nominal_8tbs": value_gbs / world / NOMINAL_HBM_GBS,
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "paged_decode_attention call (attention kernel + log-sum-exp merge when split)",
+            "achieved": achieved,
+            "peak": peak,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": traffic,
+            "algorithmic_bytes_per_call": mean_attn_bytes,
+            "mean_call_us": t_attn / args.steps * 1e6,
+        },
+        "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": float(t_e2e.item()) / args.steps * 1e3},
+        "gpu_launches": args.steps * eng.launches_per_step,
+        "clocks": clk,
+        "device_error": status,
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        try:
+            result["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_budget)
+        except Exception as exc:  # reported, not fatal
+            result["cpu_baseline"] = {"value": None, "error": str(exc)[-300:]}
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+# ---------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    per_step = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    from paged_kv_cache_128_gb300.inputs import make_workload
+    wl = make_workload(args.workload)
+    samples = []
+    for i in range(args.warmup + args.steps):
+        r = run_oracle_sample(args.workload, per_step, max_seqs=min(8, wl.num_seqs))
+        if i >= args.warmup:
+            samples.append(r)
+    secs = sum(r["seconds"] for r in samples)
+    gbs = sum(r["bytes"] for r in samples) / secs / 1e9
+    tokens = sum(r["tokens"] for r in samples) / secs
+    out = {
+        "impl": "reference",
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": secs / max(1, sum(r["steps"] for r in samples)) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded)", "config": {"workload": wl.name},
+        "decode_tokens_per_s": tokens,
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": (f"float64 numpy oracle on one host thread; each step a {per_step:.0f}-second "
+                                    f"sample of decode steps over the first {samples[0]['seqs']} sequences")},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

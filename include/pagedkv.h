@@ -1,0 +1,254 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 paged KV cache library (libpagedkv.so).
+ *
+ * Two planes sit behind this header, as in "MiniPaged-Qwen: Paged KV Cache
+ * 与 KV Block Manager" (blog.zsmgc.love) §8: a host-side metadata plane (the
+ * block manager, plain C++) and a device data plane (per-layer K/V caches and
+ * the CUDA kernels that write and read them, sm_103a).
+ *
+ * Conventions for every entry point:
+ *   - The return value is a kv_status_t; KV_OK (0) means success.  No C++
+ *     exception crosses this boundary.  kv_status_string() names each code.
+ *   - Host pointers: caller-owned host memory, read or written only during
+ *     the call.  Device pointers: caller-owned device memory (for example
+ *     torch tensors); the library never frees them.
+ *   - Kernel entry points are asynchronous on the given stream (a
+ *     cudaStream_t passed as void*; NULL is the legacy default stream).  They
+ *     validate arguments on the host, launch, and report launch errors as
+ *     KV_ERR_CUDA without synchronising.  Device-side bounds violations are
+ *     recorded in a device error word (see kv_device_error) and the offending
+ *     access is skipped; nothing traps.
+ *   - Tensors are dense and row-major unless a stride argument says
+ *     otherwise.  Cache layout, per layer: [num_blocks, block_size,
+ *     num_kv_heads, head_dim], elements of the given dtype.
+ *   - Integers that index tokens, slots or blocks are int32 on the device
+ *     (block tables, seq_lens, slot_mapping), so a pool holds at most
+ *     2^31 - 1 slots.
+ */
+#ifndef PAGEDKV_H_
+#define PAGEDKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status */
+
+typedef enum {
+  KV_OK = 0,
+  KV_ERR_INVALID_ARG = 1,   /* bad sizes, ids, dtype or head_dim; LLM-algo ch.22 rejects
+                               request_id < 0 and prompt_len <= 0 (Step 4, Request) */
+  KV_ERR_OOM = 2,           /* not enough free blocks; state unchanged (LLM-algo ch.22
+                               Step 4: atomic prefill, decode rollback) */
+  KV_ERR_UNKNOWN_SEQ = 3,   /* the sequence id is not live */
+  KV_ERR_DUPLICATE_SEQ = 4, /* second prefill of a live sequence (LLM-algo ch.22) */
+  KV_ERR_DOUBLE_FREE = 5,   /* release of an already released sequence ("从零实现一个
+                               mini vLLM: Block Manager", section on releasing blocks) */
+  KV_ERR_INVARIANT = 6,     /* manager state violates an invariant (MiniPaged-Qwen §15) */
+  KV_ERR_CUDA = 7,          /* a CUDA runtime call or launch failed */
+  KV_ERR_DEVICE_BOUNDS = 8, /* a kernel met a block index or slot outside the pool */
+  KV_ERR_WORKSPACE = 9,     /* the workspace passed is smaller than required */
+  KV_ERR_DEVICE_TIMEOUT = 10/* a bounded device-side wait gave up */
+} kv_status_t;
+
+/* Static, NUL-terminated text for a status code (never NULL). */
+const char* kv_status_string(int status);
+
+typedef enum { KV_DTYPE_F32 = 0, KV_DTYPE_F16 = 1, KV_DTYPE_BF16 = 2 } kv_dtype_t;
+
+/* ------------------------------------------------- host metadata plane */
+/*
+ * The block manager: MiniPaged-Qwen §8 (SequenceState, KVBlockManager),
+ * §9 (append_token), §15 (invariants); "从零实现一个 mini vLLM: Block
+ * Manager" (allocate_for_prefill, append_slot_for_decode, free_sequence,
+ * can_allocate, can_append_slots); LLM-algo ch.22 Step 4 (atomic prefill,
+ * decode rollback, release validation, allocation report).
+ *
+ * Free-list policy: blocks are taken from the front of the free list;
+ * released blocks are appended at the back in block-table order.  The
+ * handle is not thread-safe: serialise calls on one handle.
+ */
+typedef struct kvbm_s* kvbm_t;
+
+/* Create a manager over blocks 0..num_blocks-1 of block_size slots each.
+ * initial_free_order: NULL for 0..num_blocks-1, else a host array of
+ * num_blocks int32 that must be a permutation of the pool (else
+ * KV_ERR_INVALID_ARG).  num_blocks * block_size must fit in int32.
+ * *out receives the handle; release it with kvbm_destroy. */
+int kvbm_create(int64_t num_blocks, int32_t block_size, const int32_t* initial_free_order,
+                kvbm_t* out);
+int kvbm_destroy(kvbm_t h);
+
+/* *ok = 1 iff ceil(num_tokens / block_size) blocks are free (num_tokens >= 1). */
+int kvbm_can_allocate(kvbm_t h, int64_t num_tokens, int* ok);
+
+/* Prefill: allocate ceil(num_tokens / block_size) blocks at once for a new
+ * sequence seq_id (>= 0) holding num_tokens (>= 1) tokens.  slots_out, if not
+ * NULL, receives num_tokens int32 slots: slot[t] = table[t / bs] * bs + t % bs
+ * (MiniPaged-Qwen §3).  All or nothing: on KV_ERR_OOM nothing changes.
+ * KV_ERR_DUPLICATE_SEQ if seq_id is live. */
+int kvbm_allocate_for_prefill(kvbm_t h, int64_t seq_id, int64_t num_tokens, int32_t* slots_out);
+
+/* Decode append (MiniPaged-Qwen §9): *slot_out = slot of position L (the
+ * current length), allocating a block only when L / bs == len(table); then
+ * L += 1.  On KV_ERR_OOM the length and table are unchanged. */
+int kvbm_append_slot_for_decode(kvbm_t h, int64_t seq_id, int32_t* slot_out);
+
+/* num_tokens consecutive appends to a live sequence (chunked prefill), all
+ * or nothing on OOM.  slots_out (nullable) receives num_tokens slots. */
+int kvbm_append_slots(kvbm_t h, int64_t seq_id, int64_t num_tokens, int32_t* slots_out);
+
+/* *ok = 1 iff one decode append to each listed sequence fits in the free
+ * blocks (counts sequences whose next write opens a new block). */
+int kvbm_can_append_slots(kvbm_t h, const int64_t* seq_ids, int64_t n, int* ok);
+
+/* One decode step for n distinct live sequences: append one slot to each
+ * (slots_out[n], nullable), then export their tables and lengths as
+ * kvbm_export does (block_tables / seq_lens nullable).  All or nothing on
+ * OOM.  A repeated id is KV_ERR_INVALID_ARG. */
+int kvbm_decode_step(kvbm_t h, const int64_t* seq_ids, int64_t n, int64_t max_blocks,
+                     int32_t* slots_out, int32_t* block_tables, int32_t* seq_lens);
+
+/* Release every block of seq_id once (MiniPaged-Qwen §5.3).  The table is
+ * validated first; a corrupt table gives KV_ERR_INVARIANT and changes
+ * nothing.  KV_ERR_DOUBLE_FREE for an id already released (and not
+ * prefilled again), KV_ERR_UNKNOWN_SEQ for an id never seen. */
+int kvbm_free_sequence(kvbm_t h, int64_t seq_id);
+
+int kvbm_num_free_blocks(kvbm_t h, int64_t* out);
+
+/* Copy the free list, front first, into out[cap]; *n_out = its length.
+ * KV_ERR_INVALID_ARG if cap is too small. */
+int kvbm_get_free_list(kvbm_t h, int32_t* out, int64_t cap, int64_t* n_out);
+
+int kvbm_seq_len(kvbm_t h, int64_t seq_id, int64_t* out);
+
+/* Copy seq_id's block table into out[cap]; *n_out = its length. */
+int kvbm_get_block_table(kvbm_t h, int64_t seq_id, int32_t* out, int64_t cap, int64_t* n_out);
+
+/* Metadata export (MiniPaged-Qwen §16.2 get_block_table_tensor /
+ * get_seq_lens_tensor): block_tables[n][max_blocks] row-major, padded with
+ * -1; seq_lens[n].  Either output may be NULL.  KV_ERR_INVALID_ARG if a
+ * table is longer than max_blocks. */
+int kvbm_export(kvbm_t h, const int64_t* seq_ids, int64_t n, int64_t max_blocks,
+                int32_t* block_tables, int32_t* seq_lens);
+
+/* KV_OK iff: every table entry is in range and owned once, no allocated
+ * block is free, allocated + free = the pool, len(table) = ceil(L / bs)
+ * (MiniPaged-Qwen §15; LLM-algo ch.22 Step 3).  Else KV_ERR_INVARIANT. */
+int kvbm_check_invariants(kvbm_t h);
+
+typedef struct {
+  int64_t num_blocks;
+  int64_t block_size;
+  int64_t num_free_blocks;
+  int64_t num_sequences;
+  int64_t logical_tokens;     /* sum of sequence lengths */
+  int64_t allocated_tokens;   /* sum of len(table) * block_size */
+  int64_t unused_tail_tokens; /* allocated - logical (MiniPaged-Qwen §6.2) */
+} kvbm_stats_t;
+
+int kvbm_stats(kvbm_t h, kvbm_stats_t* out);
+
+/* LLM-algo ch.22 allocation_report for one sequence: allocated tokens,
+ * unused tail tokens, utilisation = logical / allocated. */
+int kvbm_allocation_report(kvbm_t h, int64_t seq_id, int64_t* logical_tokens,
+                           int64_t* allocated_tokens, int64_t* unused_tail_tokens,
+                           double* utilization);
+
+/* Debug aid from "从零实现一个 mini vLLM: Block Manager" (invariants section):
+ * out[num_blocks] receives the owning sequence id of each block, -1 if free. */
+int kvbm_owner_table(kvbm_t h, int64_t* out, int64_t cap);
+
+/* KV capacity ledger (LLM-algo ch.22 estimate_kv_cache_bytes; MiniPaged-Qwen
+ * §2): bytes/token = 2 * layers * kv_heads * head_dim * dtype_bytes; a block
+ * holds block_size tokens; the pool num_blocks blocks.  Outputs nullable. */
+int kv_cache_ledger(int64_t num_blocks, int64_t block_size, int64_t num_layers,
+                    int64_t num_kv_heads, int64_t head_dim, int64_t dtype_bytes,
+                    int64_t* bytes_per_token, int64_t* bytes_per_block, int64_t* total_bytes);
+
+/* ---------------------------------------------------- device data plane */
+
+/* Cache write (MiniPaged-Qwen §12): for each token t < num_tokens with
+ * slot = slot_mapping[t] != -1, copy k[t] ([num_kv_heads, head_dim]) to
+ * k_cache[slot / block_size][slot % block_size] and v[t] likewise.
+ * slot == -1 marks a padded token: nothing is read or written for it.  Any
+ * other slot outside [0, num_blocks * block_size) is skipped and recorded as
+ * KV_ERR_DEVICE_BOUNDS in the device error word.  Bit-exact copy.
+ *   k, v: device, token t at k + t * k_token_stride (elements); the heads of
+ *         one token are contiguous ([num_kv_heads, head_dim]).
+ *         Pass stride = num_kv_heads * head_dim for a dense [N, Hkv, D].
+ *   k_cache, v_cache: device, [num_blocks, block_size, num_kv_heads, head_dim].
+ *   slot_mapping: device int32[num_tokens].
+ * num_tokens == 0 launches nothing.  Two tokens with the same slot race. */
+int paged_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                            const int32_t* slot_mapping, int64_t num_tokens,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                            int64_t num_blocks, int64_t k_token_stride, int64_t v_token_stride,
+                            int dtype, void* stream);
+
+/* Split-K plan for a decode call with these sizes.  blocks_per_split: 0
+ * chooses automatically (from the SM count of the current device, the
+ * number of (sequence, kv head) pairs and max_seq_len); > 0 forces that many
+ * logical blocks per split.  Outputs (each nullable): *kernel_out = 0 for the
+ * SIMT kernel, 1 for the TMA + tensor-core kernel; the blocks per split; the
+ * number of splits S; the workspace bytes (0 when S == 1).  With S > 1 a call
+ * launches two kernels (attention, then the log-sum-exp merge), else one.
+ * max_seq_len is an upper bound of the seq_lens the call will see. */
+int paged_decode_plan(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, int64_t max_seq_len, int32_t blocks_per_split, int dtype,
+                      int32_t* kernel_out, int32_t* blocks_per_split_out, int32_t* num_splits_out,
+                      size_t* workspace_bytes_out);
+
+/* Bytes of device workspace paged_decode_attention needs for these sizes
+ * (0 when no split is needed); same arguments as paged_decode_plan. */
+int paged_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t block_size, int64_t max_seq_len,
+                                int32_t blocks_per_split, int dtype, size_t* bytes_out);
+
+/* Single-query paged decode attention (MiniPaged-Qwen §13, §14, §17.3):
+ *   out[b, qh, :] = sum_{j < seq_lens[b]} softmax_j(scale * q[b, qh] . K_j) V_j,
+ * with kv head kvh = qh / (num_heads / num_kv_heads) and K_j, V_j read at
+ * cache[block_tables[b][j / bs]][j % bs][kvh].  Only the first
+ * ceil(seq_lens[b] / bs) table entries are read; slots past seq_lens[b] in
+ * the last block are never used, whatever they hold.  seq_lens[b] == 0
+ * gives a zero output row.  fp32 accumulation, one rounding to dtype.
+ *   out, q: device, [num_seqs, num_heads, head_dim] of dtype, 16-byte aligned.
+ *   k_cache, v_cache: device caches as above, 16-byte aligned.
+ *   block_tables: device int32 [num_seqs, max_blocks_per_seq].
+ *   seq_lens: device int32 [num_seqs], each <= max_seq_len.
+ *   max_seq_len: host upper bound of seq_lens; sizes the split-K partition.
+ *   blocks_per_split: 0 = automatic, else forced (see paged_decode_plan).
+ *   workspace: device, >= paged_decode_workspace_size() bytes, 256-byte
+ *     aligned, or NULL when that size is 0 (else KV_ERR_WORKSPACE).
+ *     Clobbered; calls that share a workspace must be ordered on one stream.
+ * num_heads must be a multiple of num_kv_heads.  head_dim: fp32 a multiple
+ * of 4 up to 256; fp16/bf16 a multiple of 8 up to 256.
+ * Bounds violations (a table entry outside [0, num_blocks), a seq_len above
+ * max_blocks_per_seq * block_size or above what the split plan covers) are
+ * skipped or clamped and recorded as KV_ERR_DEVICE_BOUNDS in the device
+ * error word; that row's result is then unspecified. */
+int paged_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int32_t* seq_lens,
+                           int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                           int32_t max_blocks_per_seq, int64_t max_seq_len, float scale,
+                           int32_t blocks_per_split, int dtype, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* Read (and, if reset != 0, clear) the device error word of the current
+ * device: *status_out = KV_OK or the first KV_ERR_DEVICE_* code recorded by
+ * a kernel since the last reset.  Synchronises the current device. */
+int kv_device_error(int reset, int* status_out);
+
+/* Library version string (static). */
+const char* kv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H_ */

@@ -1,0 +1,419 @@
+// Host metadata plane: the KV block manager behind the kvbm_* C ABI.
+//
+// Follows "MiniPaged-Qwen: Paged KV Cache 与 KV Block Manager" §8
+// (SequenceState, KVBlockManager), §9 (append_token), §5.3 (release),
+// §15 (invariants); "从零实现一个 mini vLLM: Block Manager" (prefill
+// allocation, decode slot append, release once, can_allocate /
+// can_append_slots, owner table); and the LLM-algo ch.22 "vLLM
+// PagedAttention" exercise (atomic prefill, decode rollback, release
+// validation, allocation report, capacity ledger).
+//
+// Free-list policy: take from the front, release to the back in table
+// order (no sort), so a seeded initial order and churn carry through.
+//
+// Design: the free list is a ring buffer of int32 with an is_free bitmap
+// for O(1) membership; each sequence keeps its table in a std::vector.
+// Every mutating call validates fully before it changes anything, so a
+// failed call leaves the state exactly as it was.
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include "../../include/pagedkv.h"
+
+namespace {
+
+struct Sequence {
+  int64_t length = 0;            // tokens written == next append position
+  std::vector<int32_t> table;    // logical block -> physical block
+};
+
+// FIFO of free block ids over a fixed ring of num_blocks entries.
+class FreeList {
+ public:
+  explicit FreeList(int64_t cap) : ring_(static_cast<size_t>(cap)) {}
+  int64_t size() const { return size_; }
+  int32_t at(int64_t i) const { return ring_[static_cast<size_t>((head_ + i) % cap())]; }
+  int32_t pop_front() {
+    int32_t b = ring_[static_cast<size_t>(head_)];
+    head_ = (head_ + 1) % cap();
+    --size_;
+    return b;
+  }
+  void push_back(int32_t b) {
+    ring_[static_cast<size_t>((head_ + size_) % cap())] = b;
+    ++size_;
+  }
+
+ private:
+  int64_t cap() const { return static_cast<int64_t>(ring_.size()); }
+  std::vector<int32_t> ring_;
+  int64_t head_ = 0;
+  int64_t size_ = 0;
+};
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+struct kvbm_s {
+  int64_t num_blocks;
+  int32_t block_size;
+  FreeList free_list;
+  std::vector<uint8_t> is_free;
+  std::unordered_map<int64_t, Sequence> seqs;
+  std::unordered_set<int64_t> released;
+
+  kvbm_s(int64_t nb, int32_t bs) : num_blocks(nb), block_size(bs), free_list(nb), is_free(nb, 0) {}
+
+  int32_t take_front() {
+    int32_t b = free_list.pop_front();
+    is_free[static_cast<size_t>(b)] = 0;
+    return b;
+  }
+  void give_back(int32_t b) {
+    free_list.push_back(b);
+    is_free[static_cast<size_t>(b)] = 1;
+  }
+  // MiniPaged-Qwen §3: slot = table[pos / bs] * bs + pos % bs.
+  int32_t slot_of(const Sequence& s, int64_t pos) const {
+    return static_cast<int32_t>(static_cast<int64_t>(s.table[static_cast<size_t>(pos / block_size)]) *
+                                    block_size +
+                                pos % block_size);
+  }
+  // Blocks a sequence must gain to hold `extra` more tokens.
+  int64_t blocks_needed(const Sequence& s, int64_t extra) const {
+    return ceil_div(s.length + extra, block_size) - static_cast<int64_t>(s.table.size());
+  }
+  // MiniPaged-Qwen §9 append_token; the caller has checked a block is free.
+  int32_t append_one(Sequence& s) {
+    if (s.length / block_size == static_cast<int64_t>(s.table.size())) s.table.push_back(take_front());
+    int32_t slot = slot_of(s, s.length);
+    s.length += 1;
+    return slot;
+  }
+  Sequence* find(int64_t id) {
+    auto it = seqs.find(id);
+    return it == seqs.end() ? nullptr : &it->second;
+  }
+};
+
+namespace {
+
+template <typename F>
+int guarded(F&& f) {
+  try {
+    return f();
+  } catch (const std::bad_alloc&) {
+    return KV_ERR_OOM;
+  } catch (...) {
+    return KV_ERR_INVARIANT;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kv_status_string(int status) {
+  switch (status) {
+    case KV_OK: return "ok";
+    case KV_ERR_INVALID_ARG: return "invalid argument";
+    case KV_ERR_OOM: return "out of KV blocks (OOM)";
+    case KV_ERR_UNKNOWN_SEQ: return "unknown sequence id";
+    case KV_ERR_DUPLICATE_SEQ: return "sequence already prefilled";
+    case KV_ERR_DOUBLE_FREE: return "sequence already released (double free)";
+    case KV_ERR_INVARIANT: return "block manager invariant violated";
+    case KV_ERR_CUDA: return "CUDA error";
+    case KV_ERR_DEVICE_BOUNDS: return "device access outside the KV pool (skipped)";
+    case KV_ERR_WORKSPACE: return "workspace too small";
+    case KV_ERR_DEVICE_TIMEOUT: return "bounded device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int kvbm_create(int64_t num_blocks, int32_t block_size, const int32_t* initial_free_order,
+                kvbm_t* out) {
+  if (!out || num_blocks <= 0 || block_size <= 0) return KV_ERR_INVALID_ARG;
+  if (num_blocks > INT32_MAX / block_size) return KV_ERR_INVALID_ARG;  // slots are int32
+  return guarded([&] {
+    auto* h = new kvbm_s(num_blocks, block_size);
+    if (initial_free_order) {
+      std::vector<uint8_t> seen(static_cast<size_t>(num_blocks), 0);
+      for (int64_t i = 0; i < num_blocks; ++i) {
+        int32_t b = initial_free_order[i];
+        if (b < 0 || b >= num_blocks || seen[static_cast<size_t>(b)]) {
+          delete h;
+          return static_cast<int>(KV_ERR_INVALID_ARG);
+        }
+        seen[static_cast<size_t>(b)] = 1;
+        h->give_back(b);
+      }
+    } else {
+      for (int64_t i = 0; i < num_blocks; ++i) h->give_back(static_cast<int32_t>(i));
+    }
+    *out = h;
+    return static_cast<int>(KV_OK);
+  });
+}
+
+int kvbm_destroy(kvbm_t h) {
+  delete h;
+  return KV_OK;
+}
+
+int kvbm_can_allocate(kvbm_t h, int64_t num_tokens, int* ok) {
+  if (!h || !ok || num_tokens <= 0) return KV_ERR_INVALID_ARG;
+  *ok = ceil_div(num_tokens, h->block_size) <= h->free_list.size() ? 1 : 0;
+  return KV_OK;
+}
+
+int kvbm_allocate_for_prefill(kvbm_t h, int64_t seq_id, int64_t num_tokens, int32_t* slots_out) {
+  if (!h || seq_id < 0 || num_tokens <= 0) return KV_ERR_INVALID_ARG;
+  if (h->seqs.count(seq_id)) return KV_ERR_DUPLICATE_SEQ;
+  int64_t need = ceil_div(num_tokens, h->block_size);
+  if (need > h->free_list.size()) return KV_ERR_OOM;  // nothing taken yet: atomic
+  return guarded([&] {
+    Sequence s;
+    s.table.reserve(static_cast<size_t>(need));
+    for (int64_t i = 0; i < need; ++i) s.table.push_back(h->take_front());
+    s.length = num_tokens;
+    if (slots_out)
+      for (int64_t t = 0; t < num_tokens; ++t) slots_out[t] = h->slot_of(s, t);
+    h->seqs.emplace(seq_id, std::move(s));
+    h->released.erase(seq_id);
+    return static_cast<int>(KV_OK);
+  });
+}
+
+int kvbm_append_slot_for_decode(kvbm_t h, int64_t seq_id, int32_t* slot_out) {
+  if (!h) return KV_ERR_INVALID_ARG;
+  Sequence* s = h->find(seq_id);
+  if (!s) return KV_ERR_UNKNOWN_SEQ;
+  if (h->blocks_needed(*s, 1) > h->free_list.size()) return KV_ERR_OOM;
+  int32_t slot = h->append_one(*s);
+  if (slot_out) *slot_out = slot;
+  return KV_OK;
+}
+
+int kvbm_append_slots(kvbm_t h, int64_t seq_id, int64_t num_tokens, int32_t* slots_out) {
+  if (!h || num_tokens <= 0) return KV_ERR_INVALID_ARG;
+  Sequence* s = h->find(seq_id);
+  if (!s) return KV_ERR_UNKNOWN_SEQ;
+  if (h->blocks_needed(*s, num_tokens) > h->free_list.size()) return KV_ERR_OOM;
+  return guarded([&] {
+    s->table.reserve(static_cast<size_t>(ceil_div(s->length + num_tokens, h->block_size)));
+    for (int64_t t = 0; t < num_tokens; ++t) {
+      int32_t slot = h->append_one(*s);
+      if (slots_out) slots_out[t] = slot;
+    }
+    return static_cast<int>(KV_OK);
+  });
+}
+
+int kvbm_can_append_slots(kvbm_t h, const int64_t* seq_ids, int64_t n, int* ok) {
+  if (!h || !ok || n < 0 || (n > 0 && !seq_ids)) return KV_ERR_INVALID_ARG;
+  int64_t need = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    Sequence* s = h->find(seq_ids[i]);
+    if (!s) return KV_ERR_UNKNOWN_SEQ;
+    need += h->blocks_needed(*s, 1);
+  }
+  *ok = need <= h->free_list.size() ? 1 : 0;
+  return KV_OK;
+}
+
+int kvbm_export(kvbm_t h, const int64_t* seq_ids, int64_t n, int64_t max_blocks,
+                int32_t* block_tables, int32_t* seq_lens) {
+  if (!h || n < 0 || max_blocks < 0 || (n > 0 && !seq_ids)) return KV_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < n; ++i) {  // validate everything before writing
+    Sequence* s = h->find(seq_ids[i]);
+    if (!s) return KV_ERR_UNKNOWN_SEQ;
+    if (static_cast<int64_t>(s->table.size()) > max_blocks) return KV_ERR_INVALID_ARG;
+    if (s->length > INT32_MAX) return KV_ERR_INVALID_ARG;
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    const Sequence& s = *h->find(seq_ids[i]);
+    if (block_tables) {
+      int32_t* row = block_tables + i * max_blocks;
+      std::copy(s.table.begin(), s.table.end(), row);
+      std::fill(row + s.table.size(), row + max_blocks, -1);
+    }
+    if (seq_lens) seq_lens[i] = static_cast<int32_t>(s.length);
+  }
+  return KV_OK;
+}
+
+int kvbm_decode_step(kvbm_t h, const int64_t* seq_ids, int64_t n, int64_t max_blocks,
+                     int32_t* slots_out, int32_t* block_tables, int32_t* seq_lens) {
+  if (!h || n < 0 || (n > 0 && !seq_ids) || max_blocks < 0) return KV_ERR_INVALID_ARG;
+  return guarded([&] {
+    std::vector<Sequence*> seqs(static_cast<size_t>(n));
+    std::unordered_set<int64_t> seen;
+    seen.reserve(static_cast<size_t>(n) * 2);
+    int64_t need = 0;
+    for (int64_t i = 0; i < n; ++i) {
+      if (!seen.insert(seq_ids[i]).second) return static_cast<int>(KV_ERR_INVALID_ARG);
+      Sequence* s = h->find(seq_ids[i]);
+      if (!s) return static_cast<int>(KV_ERR_UNKNOWN_SEQ);
+      int64_t grow = h->blocks_needed(*s, 1);
+      if (static_cast<int64_t>(s->table.size()) + grow > max_blocks && (block_tables || seq_lens))
+        return static_cast<int>(KV_ERR_INVALID_ARG);
+      need += grow;
+      seqs[static_cast<size_t>(i)] = s;
+    }
+    if (need > h->free_list.size()) return static_cast<int>(KV_ERR_OOM);
+    for (int64_t i = 0; i < n; ++i) {
+      int32_t slot = h->append_one(*seqs[static_cast<size_t>(i)]);
+      if (slots_out) slots_out[i] = slot;
+    }
+    if (block_tables || seq_lens) return kvbm_export(h, seq_ids, n, max_blocks, block_tables, seq_lens);
+    return static_cast<int>(KV_OK);
+  });
+}
+
+int kvbm_free_sequence(kvbm_t h, int64_t seq_id) {
+  if (!h) return KV_ERR_INVALID_ARG;
+  auto it = h->seqs.find(seq_id);
+  if (it == h->seqs.end()) return h->released.count(seq_id) ? KV_ERR_DOUBLE_FREE : KV_ERR_UNKNOWN_SEQ;
+  const std::vector<int32_t>& table = it->second.table;
+  // LLM-algo ch.22 release checks: in range, no duplicates, none already free.
+  std::unordered_set<int32_t> seen;
+  for (int32_t b : table) {
+    if (b < 0 || b >= h->num_blocks) return KV_ERR_INVARIANT;
+    if (!seen.insert(b).second) return KV_ERR_INVARIANT;
+    if (h->is_free[static_cast<size_t>(b)]) return KV_ERR_INVARIANT;
+  }
+  return guarded([&] {
+    for (int32_t b : table) h->give_back(b);
+    h->seqs.erase(it);
+    h->released.insert(seq_id);
+    return static_cast<int>(KV_OK);
+  });
+}
+
+int kvbm_num_free_blocks(kvbm_t h, int64_t* out) {
+  if (!h || !out) return KV_ERR_INVALID_ARG;
+  *out = h->free_list.size();
+  return KV_OK;
+}
+
+int kvbm_get_free_list(kvbm_t h, int32_t* out, int64_t cap, int64_t* n_out) {
+  if (!h || !n_out) return KV_ERR_INVALID_ARG;
+  *n_out = h->free_list.size();
+  if (!out) return KV_OK;
+  if (cap < h->free_list.size()) return KV_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < h->free_list.size(); ++i) out[i] = h->free_list.at(i);
+  return KV_OK;
+}
+
+int kvbm_seq_len(kvbm_t h, int64_t seq_id, int64_t* out) {
+  if (!h || !out) return KV_ERR_INVALID_ARG;
+  Sequence* s = h->find(seq_id);
+  if (!s) return KV_ERR_UNKNOWN_SEQ;
+  *out = s->length;
+  return KV_OK;
+}
+
+int kvbm_get_block_table(kvbm_t h, int64_t seq_id, int32_t* out, int64_t cap, int64_t* n_out) {
+  if (!h || !n_out) return KV_ERR_INVALID_ARG;
+  Sequence* s = h->find(seq_id);
+  if (!s) return KV_ERR_UNKNOWN_SEQ;
+  *n_out = static_cast<int64_t>(s->table.size());
+  if (!out) return KV_OK;
+  if (cap < *n_out) return KV_ERR_INVALID_ARG;
+  std::copy(s->table.begin(), s->table.end(), out);
+  return KV_OK;
+}
+
+int kvbm_check_invariants(kvbm_t h) {
+  if (!h) return KV_ERR_INVALID_ARG;
+  return guarded([&] {
+    std::vector<uint8_t> owned(static_cast<size_t>(h->num_blocks), 0);
+    int64_t allocated = 0;
+    for (const auto& kv : h->seqs) {
+      const Sequence& s = kv.second;
+      if (static_cast<int64_t>(s.table.size()) != ceil_div(s.length, h->block_size))
+        return static_cast<int>(KV_ERR_INVARIANT);
+      for (int32_t b : s.table) {
+        if (b < 0 || b >= h->num_blocks) return static_cast<int>(KV_ERR_INVARIANT);
+        if (owned[static_cast<size_t>(b)]) return static_cast<int>(KV_ERR_INVARIANT);
+        owned[static_cast<size_t>(b)] = 1;
+        ++allocated;
+      }
+    }
+    std::vector<uint8_t> in_free(static_cast<size_t>(h->num_blocks), 0);
+    for (int64_t i = 0; i < h->free_list.size(); ++i) {
+      int32_t b = h->free_list.at(i);
+      if (b < 0 || b >= h->num_blocks) return static_cast<int>(KV_ERR_INVARIANT);
+      if (in_free[static_cast<size_t>(b)] || owned[static_cast<size_t>(b)])
+        return static_cast<int>(KV_ERR_INVARIANT);
+      if (!h->is_free[static_cast<size_t>(b)]) return static_cast<int>(KV_ERR_INVARIANT);
+      in_free[static_cast<size_t>(b)] = 1;
+    }
+    if (allocated + h->free_list.size() != h->num_blocks) return static_cast<int>(KV_ERR_INVARIANT);
+    return static_cast<int>(KV_OK);
+  });
+}
+
+int kvbm_stats(kvbm_t h, kvbm_stats_t* out) {
+  if (!h || !out) return KV_ERR_INVALID_ARG;
+  kvbm_stats_t st{};
+  st.num_blocks = h->num_blocks;
+  st.block_size = h->block_size;
+  st.num_free_blocks = h->free_list.size();
+  st.num_sequences = static_cast<int64_t>(h->seqs.size());
+  for (const auto& kv : h->seqs) {
+    st.logical_tokens += kv.second.length;
+    st.allocated_tokens += static_cast<int64_t>(kv.second.table.size()) * h->block_size;
+  }
+  st.unused_tail_tokens = st.allocated_tokens - st.logical_tokens;
+  *out = st;
+  return KV_OK;
+}
+
+int kvbm_allocation_report(kvbm_t h, int64_t seq_id, int64_t* logical_tokens,
+                           int64_t* allocated_tokens, int64_t* unused_tail_tokens,
+                           double* utilization) {
+  if (!h) return KV_ERR_INVALID_ARG;
+  Sequence* s = h->find(seq_id);
+  if (!s) return KV_ERR_UNKNOWN_SEQ;
+  int64_t alloc = static_cast<int64_t>(s->table.size()) * h->block_size;
+  if (logical_tokens) *logical_tokens = s->length;
+  if (allocated_tokens) *allocated_tokens = alloc;
+  if (unused_tail_tokens) *unused_tail_tokens = alloc - s->length;
+  if (utilization) *utilization = alloc ? static_cast<double>(s->length) / static_cast<double>(alloc) : 0.0;
+  return KV_OK;
+}
+
+int kvbm_owner_table(kvbm_t h, int64_t* out, int64_t cap) {
+  if (!h || !out || cap < h->num_blocks) return KV_ERR_INVALID_ARG;
+  std::fill(out, out + h->num_blocks, int64_t{-1});
+  for (const auto& kv : h->seqs)
+    for (int32_t b : kv.second.table) {
+      if (b < 0 || b >= h->num_blocks) return KV_ERR_INVARIANT;
+      out[b] = kv.first;
+    }
+  return KV_OK;
+}
+
+int kv_cache_ledger(int64_t num_blocks, int64_t block_size, int64_t num_layers,
+                    int64_t num_kv_heads, int64_t head_dim, int64_t dtype_bytes,
+                    int64_t* bytes_per_token, int64_t* bytes_per_block, int64_t* total_bytes) {
+  if (num_blocks <= 0 || block_size <= 0 || num_layers <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      dtype_bytes <= 0)
+    return KV_ERR_INVALID_ARG;
+  int64_t per_token = 2 * num_layers * num_kv_heads * head_dim * dtype_bytes;
+  int64_t per_block = block_size * per_token;
+  if (bytes_per_token) *bytes_per_token = per_token;
+  if (bytes_per_block) *bytes_per_block = per_block;
+  if (total_bytes) *total_bytes = num_blocks * per_block;
+  return KV_OK;
+}
+
+}  // extern "C"

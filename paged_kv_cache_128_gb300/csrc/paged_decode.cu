@@ -1,0 +1,878 @@
+// Single-query (decode) paged attention with GQA, split-K and LSE merge.
+//
+// What is computed ("MiniPaged-Qwen: Paged KV Cache 与 KV Block Manager"
+// §13 decode attention through block tables, §14 GQA head mapping, §16.6
+// seq_lens boundary, §17.3 online softmax):
+//   out[b, qh] = sum_{j < L_b} softmax_j(scale * q[b, qh] . K_j) V_j,
+//   kvh = qh / (Hq / Hkv),  K_j = k_cache[table[b][j / bs]][j % bs][kvh].
+//
+// Work decomposition: one CTA per (split, kv head, sequence).  A CTA owns a
+// contiguous range of `blocks_per_split` logical blocks of one sequence and
+// serves all G = Hq / Hkv query heads of its kv head, so each K/V byte is
+// read from HBM once.  When a sequence spans more than one split, each CTA
+// writes an unnormalised partial (acc, m, l) to the workspace and a small
+// merge kernel combines them by log-sum-exp (flash-decoding style split-K).
+//
+// Two kernels share that decomposition:
+//  * decode_tc_kernel (fp16/bf16, head_dim 64/128/256, block_size 16/32,
+//    G <= 16): warp-specialised.  One producer warp walks the block table
+//    (entries fetched 32 at a time and shuffled) and issues TMA tensor loads
+//    of each physical block's [bs, D] K and V slices for this kv head into
+//    a ring of shared-memory stages (128-byte swizzle, mbarrier complete_tx).
+//    Four consumer warps take stages round robin.  Each computes
+//    S^T = K Q^T (tokens in M, query heads in N, m16n8k16 mma.sync with fp32
+//    accumulation), an fp32 online softmax in the exp2 domain, turns P^T
+//    into the B operand with movmatrix, and accumulates O^T += V^T P^T with
+//    V^T fragments from ldmatrix.trans.  The warps' states are merged in
+//    shared memory at the end.
+//  * decode_simt_kernel (any dtype, head_dim a multiple of 4 up to 256, any
+//    block size and group): one warp per block, lane-parallel dot products
+//    reduced with shuffles, the same online softmax.  Used for fp32 and for
+//    shapes the tensor-core kernel does not cover.
+//
+// Tail handling: only ceil(L / bs) table entries are read.  Positions >= L
+// in the last block are excluded by selection (score = -inf), and their V
+// rows are zeroed in shared memory before the PV product, so whatever those
+// slots hold (stale data, NaN) never reaches the output.
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <type_traits>
+
+#include "common.cuh"
+
+namespace pagedkv {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DecodeParams {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  int32_t num_seqs, num_heads, num_kv_heads, group, head_dim, block_size;
+  int64_t num_blocks;
+  int32_t max_blocks_per_seq;
+  int32_t blocks_per_split, num_splits;
+  float scale_log2;  // scale * log2(e): scores live in the exp2 domain
+  float* ws_o;       // [B][Hq][S][D] unnormalised partial outputs
+  float* ws_ml;      // [B][Hq][S][2] (running max, running sum) per split
+};
+
+// Sequence length after bounds checks: at most what the table row and the
+// split partition cover.  A violation is recorded and the length clamped.
+__device__ __forceinline__ int checked_len(const DecodeParams& p, int b) {
+  int L = __ldg(p.seq_lens + b);
+  const int64_t cap = min(static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size,
+                          static_cast<int64_t>(p.num_splits) * p.blocks_per_split * p.block_size);
+  if (L < 0 || L > cap) {
+    record_error(KV_ERR_DEVICE_BOUNDS);
+    L = L < 0 ? 0 : static_cast<int>(cap);
+  }
+  return L;
+}
+
+// Combine per-warp states (m, l, acc) held in shared memory and write either
+// the final output (single split for this sequence) or this split's partial.
+// Ms/Ls: [nw][gstride], Os: [nw][D][gstride].  Threads tid..nthreads.
+template <typename T>
+__device__ __forceinline__ void combine_and_store(const DecodeParams& p, const float* Ms, const float* Ls,
+                                                  const float* Os, int nw, int gstride, int D, int b, int qh0,
+                                                  int gn, int split, bool single, int tid, int nthreads) {
+  for (int idx = tid; idx < gn * D; idx += nthreads) {
+    const int g = idx / D, d = idx - g * D;
+    float mx = -INFINITY;
+    for (int w = 0; w < nw; ++w) mx = fmaxf(mx, Ms[w * gstride + g]);
+    float num = 0.f, den = 0.f;
+    if (mx != -INFINITY) {
+      for (int w = 0; w < nw; ++w) {
+        const float mw = Ms[w * gstride + g];
+        if (mw == -INFINITY) continue;
+        const float sc = fast_exp2(mw - mx);
+        num += sc * Os[(w * D + d) * gstride + g];
+        den += sc * Ls[w * gstride + g];
+      }
+    }
+    const int qh = qh0 + g;
+    if (single) {
+      T* o = static_cast<T*>(p.out) + (static_cast<int64_t>(b) * p.num_heads + qh) * D + d;
+      *o = DType<T>::from_float(den > 0.f ? num / den : 0.f);
+    } else {
+      const int64_t row = (static_cast<int64_t>(b) * p.num_heads + qh) * p.num_splits + split;
+      p.ws_o[row * D + d] = num;
+      if (d == 0) {
+        p.ws_ml[row * 2 + 0] = mx;
+        p.ws_ml[row * 2 + 1] = den;
+      }
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void store_zero_rows(const DecodeParams& p, int b, int qh0, int gn, int D, int tid,
+                                                int nthreads) {
+  T* o = static_cast<T*>(p.out) + (static_cast<int64_t>(b) * p.num_heads + qh0) * D;
+  for (int idx = tid; idx < gn * D; idx += nthreads) o[idx] = DType<T>::from_float(0.f);
+}
+
+// =========================================================================
+// Tensor-core kernel: TMA producer warp + 4 mma.sync consumer warps.
+// =========================================================================
+
+template <int D, int BS, int NG, int NST>
+struct TcCfg {
+  static constexpr int kConsumers = 4;
+  static constexpr int kThreads = 32 * (kConsumers + 1);
+  static constexpr int kSub = D / 64;                  // 128-byte column slabs per row
+  static constexpr int kSlabBytes = BS * 128;          // one slab of one tile
+  static constexpr int kTileBytes = BS * D * 2;        // K or V of one block, one kv head
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kGPad = 8 * NG;
+  static constexpr int kMergeBytes = kConsumers * (D * kGPad + 2 * kGPad) * 4;
+  static constexpr int kDataBytes = (NST * kStageBytes > kMergeBytes) ? NST * kStageBytes : kMergeBytes;
+  static constexpr int kSmemBytes = 1024 + kDataBytes + 2 * NST * 8;
+  static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
+  static_assert(BS % 16 == 0, "block_size must be a multiple of 16");
+  static_assert(kSlabBytes % 1024 == 0, "slabs must keep 1024-byte swizzle alignment");
+};
+
+// Byte offset of element (row t, column d) inside a tile written by TMA with
+// 128-byte swizzle: slab d/64, row t, 16-byte chunk (d%64)/8 XOR (t%8).
+template <int BS>
+__device__ __forceinline__ uint32_t swz(int t, int d) {
+  return static_cast<uint32_t>((d >> 6) * (BS * 128) + t * 128 + ((((d & 63) >> 3) ^ (t & 7)) << 4));
+}
+
+template <typename T, int D, int BS, int NG, int NST>
+__global__ void __launch_bounds__(TcCfg<D, BS, NG, NST>::kThreads)
+decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV) {
+  using C = TcCfg<D, BS, NG, NST>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);
+  uint64_t* empty = full + NST;
+
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.group;
+  const int L = checked_len(p, b);
+  const int nblk = (L + BS - 1) / BS;
+  const int bps = p.blocks_per_split;
+  const int nsplit_b = (nblk + bps - 1) / bps;
+  if (L == 0) {
+    if (split == 0) store_zero_rows<T>(p, b, kvh * G, G, D, threadIdx.x, C::kThreads);
+    return;
+  }
+  if (split >= nsplit_b) return;
+  const int blk0 = split * bps;
+  const int nb = min(nblk - blk0, bps);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ---------------- producer: table walk + TMA issue ----------------
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+    }
+    const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq + blk0;
+    int32_t mine = 0;
+    int ok = 1, issued = 0;
+    for (int j = 0; j < nb && ok; ++j) {
+      if ((j & 31) == 0) mine = (j + lane < nb) ? __ldg(row + j + lane) : 0;
+      int pb = __shfl_sync(0xffffffffu, mine, j & 31);
+      if (lane == 0) {
+        const int s = j % NST;
+        if (j >= NST) ok = mbar_wait_bounded(&empty[s], ((j / NST) - 1) & 1);
+        if (ok) {
+          if (pb < 0 || pb >= p.num_blocks) {
+            record_error(KV_ERR_DEVICE_BOUNDS);
+            pb = 0;
+          }
+          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+          uint8_t* kt = smem + s * C::kStageBytes;
+          uint8_t* vt = kt + C::kTileBytes;
+#pragma unroll
+          for (int c = 0; c < C::kSub; ++c) {
+            tma_load_3d(kt + c * C::kSlabBytes, &tmK, &full[s], c * 64, kvh, pb * BS);
+            tma_load_3d(vt + c * C::kSlabBytes, &tmV, &full[s], c * 64, kvh, pb * BS);
+          }
+          ++issued;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    // Keep the CTA alive until every issued copy has landed (bounded).
+    if (lane == 0) {
+      for (int s = 0; s < NST && s < issued; ++s) {
+        const int last = s + ((issued - 1 - s) / NST) * NST;
+        mbar_wait_bounded(&full[s], (last / NST) & 1);
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const int cw = warp - 1;
+  const int ctid = threadIdx.x - 32;
+  constexpr int KS = D / 16;  // k-steps of S^T = K Q^T; also m-tiles of O^T
+  using M = Mma<T>;
+
+  // Q^T as B operand: b0 = Q[g][kk*16 + 2*(lane%4) + {0,1}], b1 = the same at d + 8.
+  uint32_t qf[KS][NG][2];
+  {
+    const T* qb = static_cast<const T*>(p.q) + (static_cast<int64_t>(b) * p.num_heads + kvh * G) * D;
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+      const int g = ng * 8 + (lane >> 2);
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        const int d = kk * 16 + (lane & 3) * 2;
+        if (g < G) {
+          qf[kk][ng][0] = __ldg(reinterpret_cast<const uint32_t*>(qb + g * D + d));
+          qf[kk][ng][1] = __ldg(reinterpret_cast<const uint32_t*>(qb + g * D + d + 8));
+        } else {
+          qf[kk][ng][0] = 0u;
+          qf[kk][ng][1] = 0u;
+        }
+      }
+    }
+  }
+
+  float acc[KS][NG][4];
+  float mrun[NG][2], lrun[NG][2];
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mt][ng][e] = 0.f;
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng) {
+    mrun[ng][0] = mrun[ng][1] = -INFINITY;
+    lrun[ng][0] = lrun[ng][1] = 0.f;
+  }
+
+  const float sl2 = p.scale_log2;
+  // ldmatrix lane -> (row, column) of the 8x8 matrix it addresses
+  const int k_row = (lane & 7) + ((lane >> 3) & 1) * 8, k_col = (lane >> 4) * 8;   // A = K (non-trans)
+  const int v_row = (lane & 7) + (lane >> 4) * 8, v_col = ((lane >> 3) & 1) * 8;   // A = V^T (trans)
+
+  for (int j = cw; j < nb; j += C::kConsumers) {
+    const int s = j % NST;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait_bounded(&full[s], (j / NST) & 1);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) break;
+    __syncwarp();
+    uint8_t* kt = smem + s * C::kStageBytes;
+    uint8_t* vt = kt + C::kTileBytes;
+    const uint32_t kt_a = smem_u32(kt), vt_a = smem_u32(vt);
+    const int tok0 = (blk0 + j) * BS;
+    const int valid = min(BS, L - tok0);
+    if (valid < BS) {
+      // zero the V rows past the sequence end: P is 0 there, but 0 * NaN is not
+      const int chunks = (BS - valid) * (D / 8);
+      for (int c = lane; c < chunks; c += 32) {
+        const int t = valid + c / (D / 8), d = (c % (D / 8)) * 8;
+        *reinterpret_cast<uint4*>(vt + swz<BS>(t, d)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
+#pragma unroll
+    for (int sub = 0; sub < BS / 16; ++sub) {
+      if (sub * 16 < valid) {
+        // ---- S^T[16 tokens x 8*NG heads] = K Q^T ----
+        float sc[NG][4];
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng) sc[ng][0] = sc[ng][1] = sc[ng][2] = sc[ng][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          uint32_t a[4];
+          ldmatrix_x4(kt_a + swz<BS>(sub * 16 + k_row, kk * 16 + k_col), a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int ng = 0; ng < NG; ++ng) M::run(sc[ng], a, qf[kk][ng][0], qf[kk][ng][1]);
+        }
+        // ---- online softmax (exp2 domain), P^T -> B operand ----
+        const int t_lo = tok0 + sub * 16 + (lane >> 2);
+        const bool in_lo = t_lo < L, in_hi = t_lo + 8 < L;
+        uint32_t pb0[NG], pb1[NG];
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng) {
+          const float x0 = in_lo ? sc[ng][0] * sl2 : -INFINITY;
+          const float x1 = in_lo ? sc[ng][1] * sl2 : -INFINITY;
+          const float x2 = in_hi ? sc[ng][2] * sl2 : -INFINITY;
+          const float x3 = in_hi ? sc[ng][3] * sl2 : -INFINITY;
+          float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+          }
+          const float mn0 = fmaxf(mrun[ng][0], mx0), mn1 = fmaxf(mrun[ng][1], mx1);
+          const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0, mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
+          const float al0 = fast_exp2(mrun[ng][0] - mu0), al1 = fast_exp2(mrun[ng][1] - mu1);
+          const uint32_t lo = M::pack(fast_exp2(x0 - mu0), fast_exp2(x1 - mu1));
+          const uint32_t hi = M::pack(fast_exp2(x2 - mu0), fast_exp2(x3 - mu1));
+          const float2 flo = M::unpack(lo), fhi = M::unpack(hi);
+          lrun[ng][0] = lrun[ng][0] * al0 + (flo.x + fhi.x);
+          lrun[ng][1] = lrun[ng][1] * al1 + (flo.y + fhi.y);
+          mrun[ng][0] = mn0;
+          mrun[ng][1] = mn1;
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+            acc[mt][ng][0] *= al0;
+            acc[mt][ng][1] *= al1;
+            acc[mt][ng][2] *= al0;
+            acc[mt][ng][3] *= al1;
+          }
+          pb0[ng] = movmatrix_trans(lo);
+          pb1[ng] = movmatrix_trans(hi);
+        }
+        // ---- O^T[D x 8*NG] += V^T P^T ----
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          uint32_t a[4];
+          ldmatrix_x4_trans(vt_a + swz<BS>(sub * 16 + v_row, mt * 16 + v_col), a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int ng = 0; ng < NG; ++ng) M::run(acc[mt][ng], a, pb0[ng], pb1[ng]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+
+  // ---------------- merge the consumer warps ----------------
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) lrun[ng][c] += __shfl_xor_sync(0xffffffffu, lrun[ng][c], off);
+
+  named_barrier_sync(1, C::kConsumers * 32);  // all stages consumed: reuse them
+  constexpr int GP = C::kGPad;
+  float* Os = reinterpret_cast<float*>(smem);
+  float* Ms = Os + C::kConsumers * D * GP;
+  float* Ls = Ms + C::kConsumers * GP;
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+      const int d0 = mt * 16 + (lane >> 2), g0 = ng * 8 + (lane & 3) * 2;
+      float* o = Os + cw * D * GP;
+      o[d0 * GP + g0] = acc[mt][ng][0];
+      o[d0 * GP + g0 + 1] = acc[mt][ng][1];
+      o[(d0 + 8) * GP + g0] = acc[mt][ng][2];
+      o[(d0 + 8) * GP + g0 + 1] = acc[mt][ng][3];
+    }
+  if (lane < 4) {
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        Ms[cw * GP + ng * 8 + lane * 2 + c] = mrun[ng][c];
+        Ls[cw * GP + ng * 8 + lane * 2 + c] = lrun[ng][c];
+      }
+  }
+  named_barrier_sync(1, C::kConsumers * 32);
+  combine_and_store<T>(p, Ms, Ls, Os, C::kConsumers, GP, D, b, kvh * G, G, split, nsplit_b == 1, ctid,
+                       C::kConsumers * 32);
+}
+
+// =========================================================================
+// SIMT kernel: any dtype / head_dim (multiple of 4, <= 256) / block size.
+// =========================================================================
+
+constexpr int kSimtWarps = 4;
+constexpr int kSimtHeads = 8;  // query heads per CTA (a group is split across CTAs beyond this)
+
+template <typename T, int DPL>
+__global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(const DecodeParams p) {
+  constexpr int GM = kSimtHeads;
+  __shared__ float Os[kSimtWarps * 32 * DPL * GM];
+  __shared__ float Ms[kSimtWarps * GM], Ls[kSimtWarps * GM];
+
+  const int D = p.head_dim, BS = p.block_size, G = p.group;
+  const int ngroups = (G + GM - 1) / GM;
+  const int split = blockIdx.x, kvh = blockIdx.y / ngroups, hg = blockIdx.y % ngroups, b = blockIdx.z;
+  const int g0 = hg * GM, gn = min(GM, G - g0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int L = checked_len(p, b);
+  const int nblk = (L + BS - 1) / BS;
+  const int bps = p.blocks_per_split;
+  const int nsplit_b = (nblk + bps - 1) / bps;
+  if (L == 0) {
+    if (split == 0) store_zero_rows<T>(p, b, kvh * G + g0, gn, D, threadIdx.x, kSimtWarps * 32);
+    return;
+  }
+  if (split >= nsplit_b) return;
+  const int blk0 = split * bps;
+  const int nb = min(nblk - blk0, bps);
+
+  float qv[GM][DPL], acc[GM][DPL], mrun[GM], lrun[GM];
+  const T* qb = static_cast<const T*>(p.q) + (static_cast<int64_t>(b) * p.num_heads + kvh * G + g0) * D;
+#pragma unroll
+  for (int g = 0; g < GM; ++g) {
+    mrun[g] = -INFINITY;
+    lrun[g] = 0.f;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) {
+      const int d = lane + 32 * i;
+      qv[g][i] = (g < gn && d < D) ? DType<T>::to_float(qb[g * D + d]) : 0.f;
+      acc[g][i] = 0.f;
+    }
+  }
+  const T* kc = static_cast<const T*>(p.k_cache);
+  const T* vc = static_cast<const T*>(p.v_cache);
+  const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq + blk0;
+  for (int j = warp; j < nb; j += kSimtWarps) {
+    const int pb = __ldg(row + j);
+    if (pb < 0 || pb >= p.num_blocks) {
+      if (lane == 0) record_error(KV_ERR_DEVICE_BOUNDS);
+      continue;
+    }
+    const int ntok = min(BS, L - (blk0 + j) * BS);
+    for (int o = 0; o < ntok; ++o) {
+      const int64_t base = ((static_cast<int64_t>(pb) * BS + o) * p.num_kv_heads + kvh) * D;
+      float kd[DPL], vd[DPL];
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) {
+        const int d = lane + 32 * i;
+        kd[i] = d < D ? DType<T>::to_float(kc[base + d]) : 0.f;
+        vd[i] = d < D ? DType<T>::to_float(vc[base + d]) : 0.f;
+      }
+#pragma unroll
+      for (int g = 0; g < GM; ++g) {
+        if (g < gn) {
+          float sdot = 0.f;
+#pragma unroll
+          for (int i = 0; i < DPL; ++i) sdot = fmaf(qv[g][i], kd[i], sdot);
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) sdot += __shfl_xor_sync(0xffffffffu, sdot, off);
+          const float x = sdot * p.scale_log2;
+          const float mn = fmaxf(mrun[g], x);
+          const float al = fast_exp2(mrun[g] - mn), pw = fast_exp2(x - mn);
+          lrun[g] = lrun[g] * al + pw;
+#pragma unroll
+          for (int i = 0; i < DPL; ++i) acc[g][i] = fmaf(acc[g][i], al, pw * vd[i]);
+          mrun[g] = mn;
+        }
+      }
+    }
+  }
+  // per-warp states -> shared memory; layout Os[w][d][g] with d < 32 * DPL
+  const int DP = 32 * DPL;
+#pragma unroll
+  for (int g = 0; g < GM; ++g) {
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) Os[(warp * DP + lane + 32 * i) * GM + g] = acc[g][i];
+    if (lane == 0) {
+      Ms[warp * GM + g] = mrun[g];
+      Ls[warp * GM + g] = lrun[g];
+    }
+  }
+  __syncthreads();
+  // combine_and_store indexes Os as [w][d][g] with row length D: use DP rows
+  for (int idx = threadIdx.x; idx < gn * D; idx += kSimtWarps * 32) {
+    const int g = idx / D, d = idx - g * D;
+    float mx = -INFINITY;
+    for (int w = 0; w < kSimtWarps; ++w) mx = fmaxf(mx, Ms[w * GM + g]);
+    float num = 0.f, den = 0.f;
+    if (mx != -INFINITY)
+      for (int w = 0; w < kSimtWarps; ++w) {
+        const float mw = Ms[w * GM + g];
+        if (mw == -INFINITY) continue;
+        const float sc = fast_exp2(mw - mx);
+        num += sc * Os[(w * DP + d) * GM + g];
+        den += sc * Ls[w * GM + g];
+      }
+    const int qh = kvh * G + g0 + g;
+    if (nsplit_b == 1) {
+      T* o = static_cast<T*>(p.out) + (static_cast<int64_t>(b) * p.num_heads + qh) * D + d;
+      *o = DType<T>::from_float(den > 0.f ? num / den : 0.f);
+    } else {
+      const int64_t r = (static_cast<int64_t>(b) * p.num_heads + qh) * p.num_splits + split;
+      p.ws_o[r * D + d] = num;
+      if (d == 0) {
+        p.ws_ml[r * 2 + 0] = mx;
+        p.ws_ml[r * 2 + 1] = den;
+      }
+    }
+  }
+}
+
+// =========================================================================
+// Log-sum-exp merge of split partials: one warp per (sequence, query head).
+// M = max_s m_s;  out = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s.
+// =========================================================================
+
+constexpr int kMergeWarps = 4;
+
+template <typename T>
+__global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const DecodeParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * kMergeWarps + warp;
+  if (idx >= static_cast<int64_t>(p.num_seqs) * p.num_heads) return;
+  const int b = static_cast<int>(idx / p.num_heads);
+  const int L = checked_len(p, b);
+  const int nblk = (L + p.block_size - 1) / p.block_size;
+  const int ns = (nblk + p.blocks_per_split - 1) / p.blocks_per_split;
+  if (ns <= 1) return;  // written directly by the attention kernel
+  const int D = p.head_dim;
+  const float* ml = p.ws_ml + idx * p.num_splits * 2;
+  const float* po = p.ws_o + idx * p.num_splits * D;
+  float mx = -INFINITY;
+  for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, ml[2 * s]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  float den = 0.f;
+  for (int s = lane; s < ns; s += 32) den += fast_exp2(ml[2 * s] - mx) * ml[2 * s + 1];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  T* o = static_cast<T*>(p.out) + idx * D;
+  for (int d = lane; d < D; d += 32) {
+    float num = 0.f;
+    for (int s = 0; s < ns; ++s) num += fast_exp2(ml[2 * s] - mx) * po[static_cast<int64_t>(s) * D + d];
+    o[d] = DType<T>::from_float(num * inv);
+  }
+}
+
+// =========================================================================
+// Host side: planning, tensor maps, dispatch.
+// =========================================================================
+
+enum KernelKind { kSimt = 0, kTensorCore = 1 };
+
+struct Plan {
+  int kind;
+  int bps;
+  int num_splits;
+  size_t ws_bytes;
+};
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
+
+bool tc_supported(int dtype, int D, int BS, int G) {
+  return dtype != KV_DTYPE_F32 && (D == 64 || D == 128 || D == 256) && (BS == 16 || BS == 32) && G >= 1 &&
+         G <= 16;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+Plan make_plan(int B, int Hq, int Hkv, int D, int BS, int64_t max_seq_len, int bps_req, int dtype,
+               bool query_device) {
+  Plan pl{};
+  const int G = Hkv > 0 ? Hq / Hkv : 1;
+  pl.kind = tc_supported(dtype, D, BS, G) ? kTensorCore : kSimt;
+  const int64_t maxblk = std::max<int64_t>(1, (max_seq_len + BS - 1) / BS);
+  int64_t bps;
+  if (bps_req > 0) {
+    bps = bps_req;
+  } else {
+    const int64_t units = static_cast<int64_t>(B) * Hkv * (pl.kind == kSimt ? (G + kSimtHeads - 1) / kSimtHeads : 1);
+    const int64_t slots = static_cast<int64_t>(query_device ? sm_count() : 152) * 3;
+    const int64_t target = 2 * slots;
+    const int64_t min_bps = std::max<int64_t>(1, 256 / BS);  // >= 256 tokens per split
+    if (units >= target || maxblk <= min_bps) {
+      bps = maxblk;
+    } else {
+      const int64_t splits = (target + units - 1) / units;
+      bps = std::max<int64_t>((maxblk + splits - 1) / splits, min_bps);
+    }
+  }
+  bps = std::min<int64_t>(bps, maxblk);
+  pl.bps = static_cast<int>(bps);
+  pl.num_splits = static_cast<int>((maxblk + bps - 1) / bps);
+  if (pl.num_splits > 1) {
+    const size_t rows = static_cast<size_t>(B) * Hq * pl.num_splits;
+    pl.ws_bytes = align256(rows * D * sizeof(float)) + align256(rows * 2 * sizeof(float));
+  } else {
+    pl.ws_bytes = 0;
+  }
+  return pl;
+}
+
+// ---- TMA tensor maps -------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+struct MapKey {
+  const void* ptr;
+  int64_t rows;
+  int hkv, d, bs;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && rows == o.rows && hkv == o.hkv && d == o.d && bs == o.bs;
+  }
+};
+
+// Cache viewed as a 3-D tensor {D, Hkv, NB * BS} of 16-bit elements; a box
+// {64, 1, BS} is one 128-byte column slab of one block's rows for one head.
+bool get_tensor_map(const void* cache, int64_t rows, int hkv, int d, int bs, CUtensorMap* out) {
+  static std::mutex mu;
+  static MapKey keys[16];
+  static CUtensorMap maps[16];
+  static int used = 0, next = 0;
+  const MapKey key{cache, rows, hkv, d, bs};
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (keys[i] == key) {
+      *out = maps[i];
+      return true;
+    }
+  auto fn = encode_fn();
+  if (!fn) return false;
+  CUtensorMap m;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(hkv) * d * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(bs)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(cache), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  const int slot = used < 16 ? used++ : (next++ % 16);
+  keys[slot] = key;
+  maps[slot] = m;
+  *out = m;
+  return true;
+}
+
+// ---- launches ----------------------------------------------------------------
+
+template <typename T, int D, int BS, int NG>
+cudaError_t launch_tc(const DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, dim3 grid,
+                      cudaStream_t st) {
+  constexpr int NST = (BS * D * 4 <= 8192) ? 8 : 4;  // stages: ~64 KB of K+V in flight per CTA
+  using C = TcCfg<D, BS, NG, NST>;
+  auto kern = decode_tc_kernel<T, D, BS, NG, NST>;
+  static int configured = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = dev;
+  }
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(p, mk, mv);
+  return cudaGetLastError();
+}
+
+template <typename T, int D, int BS>
+cudaError_t launch_tc_g(const DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, dim3 grid,
+                        cudaStream_t st) {
+  return p.group <= 8 ? launch_tc<T, D, BS, 1>(p, mk, mv, grid, st) : launch_tc<T, D, BS, 2>(p, mk, mv, grid, st);
+}
+
+template <typename T, int D>
+cudaError_t launch_tc_bs(const DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, dim3 grid,
+                         cudaStream_t st) {
+  return p.block_size == 16 ? launch_tc_g<T, D, 16>(p, mk, mv, grid, st) : launch_tc_g<T, D, 32>(p, mk, mv, grid, st);
+}
+
+template <typename T>
+cudaError_t launch_tc_d(const DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, dim3 grid,
+                        cudaStream_t st) {
+  switch (p.head_dim) {
+    case 64: return launch_tc_bs<T, 64>(p, mk, mv, grid, st);
+    case 128: return launch_tc_bs<T, 128>(p, mk, mv, grid, st);
+    default: return launch_tc_bs<T, 256>(p, mk, mv, grid, st);
+  }
+}
+
+template <typename T>
+cudaError_t launch_simt(const DecodeParams& p, dim3 grid, cudaStream_t st) {
+  const int dpl = (p.head_dim + 31) / 32;
+  if (dpl <= 1) decode_simt_kernel<T, 1><<<grid, kSimtWarps * 32, 0, st>>>(p);
+  else if (dpl <= 2) decode_simt_kernel<T, 2><<<grid, kSimtWarps * 32, 0, st>>>(p);
+  else if (dpl <= 4) decode_simt_kernel<T, 4><<<grid, kSimtWarps * 32, 0, st>>>(p);
+  else decode_simt_kernel<T, 8><<<grid, kSimtWarps * 32, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_merge(const DecodeParams& p, cudaStream_t st) {
+  const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.num_heads;
+  const unsigned grid = static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps);
+  lse_merge_kernel<T><<<grid, kMergeWarps * 32, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t run_decode(const DecodeParams& p, const Plan& pl, cudaStream_t st, bool tc, const CUtensorMap* mk,
+                       const CUtensorMap* mv) {
+  cudaError_t e = cudaSuccess;
+  if constexpr (!std::is_same<T, float>::value) {
+    if (tc) {
+      dim3 grid(pl.num_splits, p.num_kv_heads, p.num_seqs);
+      e = launch_tc_d<T>(p, *mk, *mv, grid, st);
+    }
+  }
+  if (!tc) {
+    const int ngroups = (p.group + kSimtHeads - 1) / kSimtHeads;
+    dim3 grid(pl.num_splits, p.num_kv_heads * ngroups, p.num_seqs);
+    e = launch_simt<T>(p, grid, st);
+  }
+  if (e != cudaSuccess || pl.num_splits <= 1) return e;
+  return launch_merge<T>(p, st);
+}
+
+// Host-side argument checks shared by the plan query and the launch.
+int check_shapes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t BS, int64_t max_seq_len, int dtype) {
+  if (dtype != KV_DTYPE_F32 && dtype != KV_DTYPE_F16 && dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || BS <= 0 || max_seq_len < 0) return KV_ERR_INVALID_ARG;
+  if (D <= 0 || D > 256) return KV_ERR_INVALID_ARG;
+  if (dtype == KV_DTYPE_F32 ? (D % 4 != 0) : (D % 8 != 0)) return KV_ERR_INVALID_ARG;
+  if (max_seq_len > INT32_MAX) return KV_ERR_INVALID_ARG;
+  return KV_OK;
+}
+
+}  // namespace
+}  // namespace pagedkv
+
+using namespace pagedkv;
+
+extern "C" int pagedkv_internal_reshape_error(int reset, int* code);
+
+extern "C" int paged_decode_plan(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t block_size, int64_t max_seq_len, int32_t blocks_per_split, int dtype,
+                                 int32_t* kernel_out, int32_t* blocks_per_split_out, int32_t* num_splits_out,
+                                 size_t* workspace_bytes_out) {
+  int st = check_shapes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_seq_len, dtype);
+  if (st != KV_OK) return st;
+  if (blocks_per_split < 0) return KV_ERR_INVALID_ARG;
+  Plan pl = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_seq_len, blocks_per_split, dtype,
+                      true);
+  if (kernel_out) *kernel_out = pl.kind;
+  if (blocks_per_split_out) *blocks_per_split_out = pl.bps;
+  if (num_splits_out) *num_splits_out = pl.num_splits;
+  if (workspace_bytes_out) *workspace_bytes_out = pl.ws_bytes;
+  return KV_OK;
+}
+
+extern "C" int paged_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                           int32_t head_dim, int32_t block_size, int64_t max_seq_len,
+                                           int32_t blocks_per_split, int dtype, size_t* bytes_out) {
+  if (!bytes_out) return KV_ERR_INVALID_ARG;
+  return paged_decode_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_seq_len, blocks_per_split,
+                           dtype, nullptr, nullptr, nullptr, bytes_out);
+}
+
+extern "C" int paged_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, const int32_t* seq_lens, int32_t num_seqs,
+                                      int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq,
+                                      int64_t max_seq_len, float scale, int32_t blocks_per_split, int dtype,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_shapes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_seq_len, dtype);
+  if (st != KV_OK) return st;
+  if (num_blocks <= 0 || num_blocks > INT32_MAX / block_size || max_blocks_per_seq <= 0 || blocks_per_split < 0)
+    return KV_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return KV_ERR_INVALID_ARG;
+  if (num_seqs == 0) return KV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return KV_ERR_INVALID_ARG;
+  const uintptr_t align_bits = reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(q) |
+                               reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache);
+  if (align_bits % 16 != 0) return KV_ERR_INVALID_ARG;
+  Plan pl = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_seq_len, blocks_per_split,
+                      dtype, true);
+  if (pl.ws_bytes > 0) {
+    if (!workspace || workspace_bytes < pl.ws_bytes) return KV_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return KV_ERR_INVALID_ARG;
+  }
+  DecodeParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.num_seqs = num_seqs;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_heads / num_kv_heads;
+  p.head_dim = head_dim;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.blocks_per_split = pl.bps;
+  p.num_splits = pl.num_splits;
+  p.scale_log2 = scale * kLog2e;
+  if (pl.ws_bytes > 0) {
+    const size_t rows = static_cast<size_t>(num_seqs) * num_heads * pl.num_splits;
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * head_dim * sizeof(float)));
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool tc = pl.kind == kTensorCore;
+  CUtensorMap mk, mv;
+  if (tc) {
+    const int64_t rows = num_blocks * block_size;
+    if (!get_tensor_map(k_cache, rows, num_kv_heads, head_dim, block_size, &mk) ||
+        !get_tensor_map(v_cache, rows, num_kv_heads, head_dim, block_size, &mv))
+      return KV_ERR_CUDA;
+  }
+  cudaError_t e;
+  if (dtype == KV_DTYPE_F32) e = run_decode<float>(p, pl, s, false, nullptr, nullptr);
+  else if (dtype == KV_DTYPE_F16) e = run_decode<__half>(p, pl, s, tc, &mk, &mv);
+  else e = run_decode<__nv_bfloat16>(p, pl, s, tc, &mk, &mv);
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+extern "C" int kv_device_error(int reset, int* status_out) {
+  if (!status_out) return KV_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return KV_ERR_CUDA;
+  int a = 0, c = 0;
+  if (cudaMemcpyFromSymbol(&a, g_device_error, sizeof(int)) != cudaSuccess) return KV_ERR_CUDA;
+  if (reset) {
+    int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return KV_ERR_CUDA;
+  }
+  int r = pagedkv_internal_reshape_error(reset, &c);
+  if (r != KV_OK) return r;
+  *status_out = a ? a : c;
+  return KV_OK;
+}
+
+extern "C" const char* kv_version(void) { return "pagedkv-gb300 0.1 (sm_103a)"; }

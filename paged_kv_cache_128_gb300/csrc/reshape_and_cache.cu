@@ -1,0 +1,130 @@
+// Cache write: scatter each new token's K/V rows into the paged pool.
+//
+// "MiniPaged-Qwen: Paged KV Cache 与 KV Block Manager" §12 (cache write by
+// slot_mapping) and §11 (slot -> physical block, offset).  With the cache
+// laid out [num_blocks, block_size, num_kv_heads, head_dim], all heads of one
+// token are contiguous in both the input ([Hkv, D]) and the destination
+// (cache[slot / bs][slot % bs]), and that destination row starts at
+// slot * Hkv * D.  So the write is one contiguous row copy per token.
+//
+// Kernel shape: one warp per token, grid-stride; each lane moves 16-byte
+// vectors (narrower only when the row size or alignment forces it), issuing
+// all of its loads for K and V before the stores so a warp keeps up to
+// 2 * kUnroll vectors per lane in flight.  The copy is bit-exact.
+
+#include "common.cuh"
+
+namespace pagedkv {
+namespace {
+
+constexpr int kWarpsPerCta = 8;
+constexpr int kUnroll = 4;
+
+template <typename V>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+reshape_and_cache_kernel(const char* __restrict__ k, const char* __restrict__ v, char* __restrict__ k_cache,
+                         char* __restrict__ v_cache, const int32_t* __restrict__ slot_mapping, int64_t num_tokens,
+                         int64_t row_bytes, int64_t k_stride_bytes, int64_t v_stride_bytes, int64_t num_slots) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nvec = row_bytes / static_cast<int64_t>(sizeof(V));
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5); t < num_tokens;
+       t += static_cast<int64_t>(gridDim.x) * kWarpsPerCta) {
+    const int32_t slot = __ldg(slot_mapping + t);
+    if (slot == -1) continue;  // padded token: nothing read, nothing written
+    if (slot < 0 || slot >= num_slots) {
+      if (lane == 0) record_error(KV_ERR_DEVICE_BOUNDS);
+      continue;
+    }
+    const V* ks = reinterpret_cast<const V*>(k + t * k_stride_bytes);
+    const V* vs = reinterpret_cast<const V*>(v + t * v_stride_bytes);
+    V* kd = reinterpret_cast<V*>(k_cache + static_cast<int64_t>(slot) * row_bytes);
+    V* vd = reinterpret_cast<V*>(v_cache + static_cast<int64_t>(slot) * row_bytes);
+    for (int64_t base = lane; base < nvec; base += 32 * kUnroll) {
+      V kr[kUnroll], vr[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t i = base + 32 * u;
+        if (i < nvec) {
+          kr[u] = __ldg(ks + i);
+          vr[u] = __ldg(vs + i);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t i = base + 32 * u;
+        if (i < nvec) {
+          kd[i] = kr[u];
+          vd[i] = vr[u];
+        }
+      }
+    }
+  }
+}
+
+bool aligned(const void* p, int64_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+template <typename V>
+cudaError_t launch(const void* k, const void* v, void* kc, void* vc, const int32_t* slots, int64_t n,
+                   int64_t row_bytes, int64_t ks, int64_t vs, int64_t num_slots, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t need = (n + kWarpsPerCta - 1) / kWarpsPerCta;
+  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * 16;
+  const int grid = static_cast<int>(need < cap ? need : cap);
+  reshape_and_cache_kernel<V><<<grid, kWarpsPerCta * 32, 0, stream>>>(
+      static_cast<const char*>(k), static_cast<const char*>(v), static_cast<char*>(kc), static_cast<char*>(vc),
+      slots, n, row_bytes, ks, vs, num_slots);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace pagedkv
+
+using namespace pagedkv;
+
+extern "C" int paged_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                                       const int32_t* slot_mapping, int64_t num_tokens, int32_t num_kv_heads,
+                                       int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                       int64_t k_token_stride, int64_t v_token_stride, int dtype, void* stream) {
+  if (dtype != KV_DTYPE_F32 && dtype != KV_DTYPE_F16 && dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    return KV_ERR_INVALID_ARG;
+  const int64_t row_elems = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (k_token_stride < row_elems || v_token_stride < row_elems) return KV_ERR_INVALID_ARG;
+  if (num_blocks > INT32_MAX / block_size) return KV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return KV_OK;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping) return KV_ERR_INVALID_ARG;
+  const int64_t es = static_cast<int64_t>(dtype_bytes(dtype));
+  const int64_t row_bytes = row_elems * es, ks = k_token_stride * es, vs = v_token_stride * es;
+  const int64_t num_slots = num_blocks * block_size;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  auto fits = [&](int64_t a) {
+    return row_bytes % a == 0 && ks % a == 0 && vs % a == 0 && aligned(k, a) && aligned(v, a) &&
+           aligned(k_cache, a) && aligned(v_cache, a);
+  };
+  if (fits(16))
+    err = launch<uint4>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, ks, vs, num_slots, st);
+  else if (fits(8))
+    err = launch<uint2>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, ks, vs, num_slots, st);
+  else if (fits(4))
+    err = launch<uint32_t>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, ks, vs, num_slots, st);
+  else if (fits(2))
+    err = launch<uint16_t>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, ks, vs, num_slots, st);
+  else
+    return KV_ERR_INVALID_ARG;
+  return err == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+// Read (and optionally clear) this translation unit's device error word.
+extern "C" int pagedkv_internal_reshape_error(int reset, int* code) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return KV_ERR_CUDA;
+  if (reset) {
+    int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return KV_ERR_CUDA;
+  }
+  *code = v;
+  return KV_OK;
+}

@@ -1,0 +1,132 @@
+"""Torch-facing wrappers of the CUDA entry points in libpagedkv.
+
+Argument marshalling only: shapes, dtypes and device pointers are read off
+the tensors and passed to the C ABI; every step of the computation runs in
+the library's kernels.  There is no CPU path: CPU tensors are rejected.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from ._lib import DTYPE_BF16, DTYPE_F16, DTYPE_F32, KVError, check, lib
+
+_DTYPES = {torch.float32: DTYPE_F32, torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16}
+
+
+def dtype_code(dtype: torch.dtype) -> int:
+    if dtype not in _DTYPES:
+        raise KVError(1, f"unsupported dtype {dtype}")
+    return _DTYPES[dtype]
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _cuda(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not t.is_cuda:
+        raise KVError(1, f"{name} must be a CUDA tensor")
+    return t
+
+
+def reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      slot_mapping: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Write k/v ``[N, Hkv, D]`` (token stride may exceed Hkv*D) into the
+    ``[NB, BS, Hkv, D]`` caches at ``slot_mapping[N]`` (int32, -1 = skip)."""
+    for t, n in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache"), (slot_mapping, "slot_mapping")):
+        _cuda(t, n)
+    nb, bs, hkv, d = k_cache.shape
+    n = slot_mapping.numel()
+    if slot_mapping.dtype != torch.int32 or not slot_mapping.is_contiguous():
+        raise KVError(1, "slot_mapping must be contiguous int32")
+    if k.dtype != k_cache.dtype or v.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
+        raise KVError(1, "k, v and the caches must share one dtype")
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous() and v_cache.shape == k_cache.shape):
+        raise KVError(1, "caches must be contiguous [NB, BS, Hkv, D] of one shape")
+    for t in (k, v):
+        if t.dim() != 3 or t.shape[0] != n or t.shape[1] != hkv or t.shape[2] != d or t.stride(2) != 1 \
+                or t.stride(1) != d:
+            raise KVError(1, "k and v must be [N, Hkv, D] with dense heads")
+    check(lib().paged_reshape_and_cache(k.data_ptr(), v.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                        slot_mapping.data_ptr(), n, hkv, d, bs, nb, k.stride(0), v.stride(0),
+                                        dtype_code(k_cache.dtype), _stream_ptr(stream)),
+          "paged_reshape_and_cache")
+
+
+@dataclass
+class DecodePlan:
+    kernel: int            # 0 = SIMT, 1 = TMA + tensor cores
+    blocks_per_split: int
+    num_splits: int
+    workspace_bytes: int
+
+    @property
+    def launches(self) -> int:
+        return 2 if self.num_splits > 1 else 1
+
+
+def decode_plan(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                max_seq_len: int, dtype: torch.dtype, blocks_per_split: int = 0) -> DecodePlan:
+    k, b, s = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    w = ctypes.c_size_t()
+    check(lib().paged_decode_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_seq_len,
+                                  blocks_per_split, dtype_code(dtype), ctypes.byref(k), ctypes.byref(b),
+                                  ctypes.byref(s), ctypes.byref(w)), "paged_decode_plan")
+    return DecodePlan(k.value, b.value, s.value, w.value)
+
+
+def alloc_workspace(plan: DecodePlan, device) -> Optional[torch.Tensor]:
+    if plan.workspace_bytes == 0:
+        return None
+    return torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=device)
+
+
+def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float, max_seq_len: int,
+                           blocks_per_split: int = 0, workspace: Optional[torch.Tensor] = None,
+                           stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """out[b, qh] = softmax(scale * q[b, qh] K^T) V over seq_lens[b] tokens
+    read through block_tables[b]; kvh = qh // (Hq // Hkv).  ``workspace``
+    must hold ``decode_plan(...).workspace_bytes`` bytes when that is > 0
+    (allocated here if omitted)."""
+    for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (block_tables, "block_tables"), (seq_lens, "seq_lens")):
+        _cuda(t, n)
+    if not (q.is_contiguous() and out.is_contiguous() and k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise KVError(1, "q, out and caches must be contiguous")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32 or not block_tables.is_contiguous() \
+            or not seq_lens.is_contiguous():
+        raise KVError(1, "block_tables and seq_lens must be contiguous int32")
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if d2 != d or out.shape != q.shape or v_cache.shape != k_cache.shape or out.dtype != q.dtype \
+            or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise KVError(1, "shape or dtype mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or seq_lens.numel() != B:
+        raise KVError(1, "block_tables must be [B, max_blocks] and seq_lens [B]")
+    code = dtype_code(q.dtype)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is None:
+        plan = decode_plan(B, hq, hkv, d, bs, max_seq_len, q.dtype, blocks_per_split)
+        workspace = alloc_workspace(plan, q.device)
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    check(lib().paged_decode_attention(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                       block_tables.data_ptr(), seq_lens.data_ptr(), B, hq, hkv, d, bs, nb,
+                                       block_tables.shape[1], max_seq_len, float(scale), blocks_per_split, code,
+                                       ws_ptr, ws_bytes, _stream_ptr(stream)), "paged_decode_attention")
+    return out
+
+
+def device_error(reset: bool = True) -> int:
+    """Status recorded by device-side bounds checks / bounded waits (0 = none).
+    Synchronises the current device."""
+    st = ctypes.c_int()
+    check(lib().kv_device_error(1 if reset else 0, ctypes.byref(st)), "kv_device_error")
+    return st.value
