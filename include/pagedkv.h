@@ -193,10 +193,15 @@ int paged_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v
 /* Split-K plan for a decode call with these sizes.  blocks_per_split: 0
  * chooses automatically (from the SM count of the current device, the
  * number of (sequence, kv head) pairs and max_seq_len); > 0 forces that many
- * logical blocks per split.  Outputs (each nullable): *kernel_out = 0 for the
- * SIMT kernel, 1 for the TMA + tensor-core kernel; the blocks per split; the
- * number of splits S; the workspace bytes (0 when S == 1).  With S > 1 a call
- * launches two kernels (attention, then the log-sum-exp merge), else one.
+ * logical blocks per split (split kernels only).  Outputs (each nullable):
+ * *kernel_out = 0 for the SIMT split kernel (fp32 and shapes the tensor-core
+ * kernels do not take), 1 for the TMA + tensor-core split kernel (forced
+ * splits, or more than 4096 sequences), 2 for the TMA + tensor-core
+ * stream-K kernel (the fp16/bf16 default: one wave of persistent CTAs, each
+ * taking an equal share of all (sequence, kv head, block) tiles); the
+ * blocks per split and number of splits S (split kernels); the workspace
+ * bytes.  Kernel 2 always launches two kernels (attention, then the
+ * log-sum-exp merge); kernels 0 and 1 launch the merge only when S > 1.
  * max_seq_len is an upper bound of the seq_lens the call will see. */
 int paged_decode_plan(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                       int32_t block_size, int64_t max_seq_len, int32_t blocks_per_split, int dtype,
@@ -243,6 +248,11 @@ int paged_decode_attention(void* out, const void* q, const void* k_cache, const 
  * device: *status_out = KV_OK or the first KV_ERR_DEVICE_* code recorded by
  * a kernel since the last reset.  Synchronises the current device. */
 int kv_device_error(int reset, int* status_out);
+
+/* Text of the last CUDA error an entry point of this library met on the
+ * calling thread (the cause of its most recent KV_ERR_CUDA); static storage,
+ * never NULL. */
+const char* kv_last_cuda_error(void);
 
 /* Library version string (static). */
 const char* kv_version(void);

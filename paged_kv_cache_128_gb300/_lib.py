@@ -68,6 +68,7 @@ SIGNATURES = {
                                        c_int32, c_int32, c_int32, c_int32, c_int64, c_int32, c_int64, c_float,
                                        c_int32, c_int, c_void_p, c_size_t, c_void_p]),
     "kv_device_error": (c_int, [c_int, POINTER(c_int)]),
+    "kv_last_cuda_error": (c_char_p, []),
     "kv_version": (c_char_p, []),
 }
 
@@ -97,4 +98,6 @@ def status_string(status: int) -> str:
 
 def check(status: int, where: str) -> None:
     if status != KV_OK:
+        if status == 7:
+            where = f"{where} [{lib().kv_last_cuda_error().decode()}]"
         raise KVError(status, where)

@@ -33,6 +33,16 @@ template <> struct DType<__nv_bfloat16> {
 
 inline size_t dtype_bytes(int dtype) { return dtype == KV_DTYPE_F32 ? 4 : 2; }
 
+// Last CUDA error met by an entry point on this thread (see kv_last_cuda_error).
+const char*& last_cuda_error_text();
+
+// Map a CUDA result to a status, remembering the error text on failure.
+inline int cuda_status(cudaError_t e, const char* what = nullptr) {
+  if (e == cudaSuccess) return KV_OK;
+  last_cuda_error_text() = what ? what : cudaGetErrorString(e);
+  return KV_ERR_CUDA;
+}
+
 // ------------------------------------------------------- device error word
 // Each translation unit that includes this header gets its own word; the
 // host reads them all through kv_device_error().  The first error recorded

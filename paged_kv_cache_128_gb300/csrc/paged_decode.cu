@@ -62,8 +62,10 @@ struct DecodeParams {
   int32_t max_blocks_per_seq;
   int32_t blocks_per_split, num_splits;
   float scale_log2;  // scale * log2(e): scores live in the exp2 domain
-  float* ws_o;       // [B][Hq][S][D] unnormalised partial outputs
-  float* ws_ml;      // [B][Hq][S][2] (running max, running sum) per split
+  int32_t num_ctas;  // stream-K grid size P
+  float* ws_o;       // split: [B][Hq][S][D]; stream-K: [P][2][G][D] unnormalised partial outputs
+  float* ws_ml;      // split: [B][Hq][S][2]; stream-K: [P][2][G][2] (running max, running sum)
+  int32_t* ws_cb;    // stream-K: [B + 1] prefix of per-sequence block counts
 };
 
 // Sequence length after bounds checks: at most what the table row and the
@@ -123,21 +125,23 @@ __device__ __forceinline__ void store_zero_rows(const DecodeParams& p, int b, in
 }
 
 // =========================================================================
-// Tensor-core kernel: TMA producer warp + 4 mma.sync consumer warps.
+// Tensor-core path: shared consumer math.
+//
+// Each consumer warp owns whole tiles (one physical block of one kv head,
+// BS tokens) and keeps its own online-softmax state for the current unit
+// (sequence, kv head).  Per 16-token sub-tile:
+//   S^T[16 tok x 8*NG heads] = K[16 x D] Q^T          (mma m16n8k16, fp32 acc)
+//   softmax update in the exp2 domain, P^T packed to the MMA type,
+//   movmatrix turns the P^T accumulator fragment into a B operand,
+//   O^T[D x 8*NG] += V^T[D x 16] P^T                   (V^T via ldmatrix.trans)
 // =========================================================================
 
-template <int D, int BS, int NG, int NST>
-struct TcCfg {
-  static constexpr int kConsumers = 4;
-  static constexpr int kThreads = 32 * (kConsumers + 1);
-  static constexpr int kSub = D / 64;                  // 128-byte column slabs per row
-  static constexpr int kSlabBytes = BS * 128;          // one slab of one tile
-  static constexpr int kTileBytes = BS * D * 2;        // K or V of one block, one kv head
+template <int D, int BS>
+struct Tile {
+  static constexpr int kSub = D / 64;              // 128-byte column slabs per row
+  static constexpr int kSlabBytes = BS * 128;      // one slab of one tile
+  static constexpr int kTileBytes = BS * D * 2;    // K or V of one block, one kv head
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kGPad = 8 * NG;
-  static constexpr int kMergeBytes = kConsumers * (D * kGPad + 2 * kGPad) * 4;
-  static constexpr int kDataBytes = (NST * kStageBytes > kMergeBytes) ? NST * kStageBytes : kMergeBytes;
-  static constexpr int kSmemBytes = 1024 + kDataBytes + 2 * NST * 8;
   static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
   static_assert(BS % 16 == 0, "block_size must be a multiple of 16");
   static_assert(kSlabBytes % 1024 == 0, "slabs must keep 1024-byte swizzle alignment");
@@ -150,14 +154,500 @@ __device__ __forceinline__ uint32_t swz(int t, int d) {
   return static_cast<uint32_t>((d >> 6) * (BS * 128) + t * 128 + ((((d & 63) >> 3) ^ (t & 7)) << 4));
 }
 
+template <int D, int NG>
+struct WarpState {
+  static constexpr int KS = D / 16;  // k-steps of S^T = K Q^T, and m-tiles of O^T
+  uint32_t qf[KS][NG][2];            // Q^T as B operand
+  float acc[KS][NG][4];              // O^T accumulator fragments
+  float m[NG][2], l[NG][2];          // running max (exp2 domain) and sum, 2 heads per lane
+};
+
+// B operand of S^T = K Q^T: b0 = Q[g][kk*16 + 2*(lane%4) + {0,1}], b1 at d + 8,
+// g = ng*8 + lane/4; heads past G are zero.
+template <typename T, int D, int NG>
+__device__ __forceinline__ void load_q(WarpState<D, NG>& st, const T* qb, int G, int lane) {
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng) {
+    const int g = ng * 8 + (lane >> 2);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int d = kk * 16 + (lane & 3) * 2;
+      if (g < G) {
+        st.qf[kk][ng][0] = __ldg(reinterpret_cast<const uint32_t*>(qb + g * D + d));
+        st.qf[kk][ng][1] = __ldg(reinterpret_cast<const uint32_t*>(qb + g * D + d + 8));
+      } else {
+        st.qf[kk][ng][0] = 0u;
+        st.qf[kk][ng][1] = 0u;
+      }
+    }
+  }
+}
+
+template <int D, int NG>
+__device__ __forceinline__ void reset_state(WarpState<D, NG>& st) {
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) st.acc[mt][ng][e] = 0.f;
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng) {
+    st.m[ng][0] = st.m[ng][1] = -INFINITY;
+    st.l[ng][0] = st.l[ng][1] = 0.f;
+  }
+}
+
+// Accumulate one tile (tokens tok0 .. tok0 + BS - 1 of a sequence of length
+// L) held in shared memory at kt (K) and vt (V).
+template <typename T, int D, int BS, int NG>
+__device__ __forceinline__ void consume_tile(WarpState<D, NG>& st, uint8_t* kt, uint8_t* vt, int tok0, int L,
+                                             float sl2, int lane) {
+  using M = Mma<T>;
+  constexpr int KS = D / 16;
+  const int valid = min(BS, L - tok0);
+  if (valid < BS) {
+    // zero the V rows past the sequence end: P is 0 there, but 0 * NaN is not
+    const int chunks = (BS - valid) * (D / 8);
+    for (int c = lane; c < chunks; c += 32) {
+      const int t = valid + c / (D / 8), d = (c % (D / 8)) * 8;
+      *reinterpret_cast<uint4*>(vt + swz<BS>(t, d)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();  // these bytes are TMA-written again later
+    __syncwarp();
+  }
+  const uint32_t kt_a = smem_u32(kt), vt_a = smem_u32(vt);
+  // ldmatrix lane -> (row, column) of the 8x8 matrix it addresses
+  const int k_row = (lane & 7) + ((lane >> 3) & 1) * 8, k_col = (lane >> 4) * 8;  // A = K (non-trans)
+  const int v_row = (lane & 7) + (lane >> 4) * 8, v_col = ((lane >> 3) & 1) * 8;  // A = V^T (trans)
+#pragma unroll
+  for (int sub = 0; sub < BS / 16; ++sub) {
+    if (sub * 16 < valid) {
+      float sc[NG][4];
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) sc[ng][0] = sc[ng][1] = sc[ng][2] = sc[ng][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        uint32_t a[4];
+        ldmatrix_x4(kt_a + swz<BS>(sub * 16 + k_row, kk * 16 + k_col), a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng) M::run(sc[ng], a, st.qf[kk][ng][0], st.qf[kk][ng][1]);
+      }
+      const int t_lo = tok0 + sub * 16 + (lane >> 2);
+      const bool in_lo = t_lo < L, in_hi = t_lo + 8 < L;
+      uint32_t pb0[NG], pb1[NG];
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) {
+        const float x0 = in_lo ? sc[ng][0] * sl2 : -INFINITY;
+        const float x1 = in_lo ? sc[ng][1] * sl2 : -INFINITY;
+        const float x2 = in_hi ? sc[ng][2] * sl2 : -INFINITY;
+        const float x3 = in_hi ? sc[ng][3] * sl2 : -INFINITY;
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(st.m[ng][0], mx0), mn1 = fmaxf(st.m[ng][1], mx1);
+        const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0, mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
+        const float al0 = fast_exp2(st.m[ng][0] - mu0), al1 = fast_exp2(st.m[ng][1] - mu1);
+        const uint32_t lo = M::pack(fast_exp2(x0 - mu0), fast_exp2(x1 - mu1));
+        const uint32_t hi = M::pack(fast_exp2(x2 - mu0), fast_exp2(x3 - mu1));
+        const float2 flo = M::unpack(lo), fhi = M::unpack(hi);
+        st.l[ng][0] = st.l[ng][0] * al0 + (flo.x + fhi.x);
+        st.l[ng][1] = st.l[ng][1] * al1 + (flo.y + fhi.y);
+        st.m[ng][0] = mn0;
+        st.m[ng][1] = mn1;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          st.acc[mt][ng][0] *= al0;
+          st.acc[mt][ng][1] *= al1;
+          st.acc[mt][ng][2] *= al0;
+          st.acc[mt][ng][3] *= al1;
+        }
+        pb0[ng] = movmatrix_trans(lo);
+        pb1[ng] = movmatrix_trans(hi);
+      }
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        uint32_t a[4];
+        ldmatrix_x4_trans(vt_a + swz<BS>(sub * 16 + v_row, mt * 16 + v_col), a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng) M::run(st.acc[mt][ng], a, pb0[ng], pb1[ng]);
+      }
+    }
+  }
+}
+
+// Reduce l across the lanes that share a head, then store this warp's
+// state: Os[cw][d][GP], Ms[cw][GP], Ls[cw][GP] (GP = 8 * NG).
+template <int D, int NG>
+__device__ __forceinline__ void store_state(WarpState<D, NG>& st, float* Os, float* Ms, float* Ls, int cw,
+                                            int lane) {
+  constexpr int GP = 8 * NG;
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) st.l[ng][c] += __shfl_xor_sync(0xffffffffu, st.l[ng][c], off);
+  float* o = Os + cw * D * GP;
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+      const int d0 = mt * 16 + (lane >> 2), g0 = ng * 8 + (lane & 3) * 2;
+      o[d0 * GP + g0] = st.acc[mt][ng][0];
+      o[d0 * GP + g0 + 1] = st.acc[mt][ng][1];
+      o[(d0 + 8) * GP + g0] = st.acc[mt][ng][2];
+      o[(d0 + 8) * GP + g0 + 1] = st.acc[mt][ng][3];
+    }
+  if (lane < 4) {
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        Ms[cw * GP + ng * 8 + lane * 2 + c] = st.m[ng][c];
+        Ls[cw * GP + ng * 8 + lane * 2 + c] = st.l[ng][c];
+      }
+  }
+}
+
+constexpr int kConsumers = 4;
+constexpr int kTcThreads = 32 * (kConsumers + 1);
+
+template <int D, int NG>
+struct MergeArea {
+  static constexpr int kGP = 8 * NG;
+  static constexpr int kBytes = kConsumers * (D * kGP + 2 * kGP) * 4;
+};
+
+// =========================================================================
+// Stream-K tensor-core kernel (the default for fp16/bf16).
+//
+// The work is the ordered list of tiles (sequence b, kv head, logical
+// block), W = Hkv * sum_b ceil(L_b / bs) of them.  The grid is one wave of
+// persistent CTAs; CTA p takes tiles [p*W/P, (p+1)*W/P), so every CTA moves
+// the same number of bytes whatever the length mix.  A unit (b, kv head)
+// whose tiles all fall in one CTA is finished there and written to `out`;
+// a unit cut by a range boundary leaves one partial (acc, m, l) per CTA it
+// touches -- at most two per CTA, slot 0 for the unit that started before
+// the range and slot 1 for the unit that continues after it -- and the
+// merge kernel combines them.  Every CTA first rebuilds the per-sequence
+// prefix of block counts in shared memory from seq_lens.
+// =========================================================================
+
 template <typename T, int D, int BS, int NG, int NST>
-__global__ void __launch_bounds__(TcCfg<D, BS, NG, NST>::kThreads)
-decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
+struct SkCfg {
+  using TL = Tile<D, BS>;
+  static constexpr int kStages = NST * TL::kStageBytes;
+  static constexpr int kMerge = MergeArea<D, NG>::kBytes;
+  static constexpr int kFixed = 1024 + kStages + kMerge + 2 * NST * 8;
+  static int smem_bytes(int B) { return kFixed + ((B + 1) * 4 + 15) / 16 * 16; }
+};
+
+// cta_of(t): the CTA whose range [p*W/P, (p+1)*W/P) holds tile t.
+__device__ __forceinline__ int sk_cta_of(int64_t t, int64_t W, int P) {
+  return static_cast<int>(((t + 1) * P + W - 1) / W - 1);
+}
+
+template <typename T, int D, int BS, int NG, int NST>
+__global__ void __launch_bounds__(kTcThreads)
+decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV) {
-  using C = TcCfg<D, BS, NG, NST>;
+  using C = SkCfg<T, D, BS, NG, NST>;
+  using TL = Tile<D, BS>;
+  constexpr int GP = 8 * NG;
+  static_assert(NST % kConsumers == 0, "stage s must always be drained by consumer s % kConsumers");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);
+  float* Os = reinterpret_cast<float*>(smem + C::kStages);
+  float* Ms = Os + kConsumers * D * GP;
+  float* Ls = Ms + kConsumers * GP;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages + C::kMerge);
+  uint64_t* empty = full + NST;
+  int* CB = reinterpret_cast<int*>(empty + NST);  // CB[b] = sum_{b' < b} ceil(L_b' / BS)
+
+  const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- prefix of block counts over the batch (block-wide scan) ----
+  {
+    const int per = (B + kTcThreads - 1) / kTcThreads;
+    const int beg = min(B, tid * per), end = min(B, beg + per);
+    int local = 0;
+    for (int i = beg; i < end; ++i) {
+      const int nb = (checked_len(p, i) + BS - 1) / BS;
+      CB[i + 1] = nb;
+      local += nb;
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    __shared__ int warp_tot[kConsumers + 1];
+    if (lane == 31) warp_tot[warp] = incl;
+    if (tid == 0) CB[0] = 0;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += warp_tot[w];
+    int run = base + incl - local;
+    for (int i = beg; i < end; ++i) {
+      const int nb = CB[i + 1];
+      run += nb;
+      CB[i + 1] = run;
+    }
+    if (tid == 0) {
+      for (int s = 0; s < NST; ++s) {
+        mbar_init(&full[s], 1);
+        mbar_init(&empty[s], 1);
+      }
+      fence_mbar_init();
+    }
+    __syncthreads();
+  }
+  if (blockIdx.x == 0)
+    for (int i = tid; i <= B; i += kTcThreads) p.ws_cb[i] = CB[i];
+
+  const int64_t W = static_cast<int64_t>(Hkv) * CB[B];
+  const int P = gridDim.x, pid = blockIdx.x;
+  const int64_t t0 = static_cast<int64_t>(pid) * W / P, t1 = static_cast<int64_t>(pid + 1) * W / P;
+  if (t0 >= t1) return;
+  const int n = static_cast<int>(t1 - t0);
+
+  // ---- locate the first tile: largest b with Hkv * CB[b] <= t0 ----
+  int b0;
+  {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (static_cast<int64_t>(Hkv) * CB[mid] <= t0) lo = mid; else hi = mid - 1;
+    }
+    b0 = lo;
+  }
+  const int nb0 = CB[b0 + 1] - CB[b0];
+  const int rel0 = static_cast<int>(t0 - static_cast<int64_t>(Hkv) * CB[b0]);
+
+  // Tile cursor shared by producer and consumers: advances (blk, kvh, b).
+  struct Cursor {
+    int b, kvh, blk, nb;
+  };
+  auto advance = [&](Cursor& c) {
+    if (++c.blk == c.nb) {
+      c.blk = 0;
+      if (++c.kvh == Hkv) {
+        c.kvh = 0;
+        do {
+          ++c.b;
+        } while (c.b < B && CB[c.b + 1] == CB[c.b]);
+        c.nb = c.b < B ? CB[c.b + 1] - CB[c.b] : 0;
+      }
+    }
+  };
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+    }
+    Cursor c{b0, rel0 / nb0, rel0 % nb0, nb0};
+    int cache_b = -1, cache_chunk = -1, mine = 0;
+    int ok = 1, issued = 0;
+    for (int j = 0; j < n && ok; ++j) {
+      if (c.b != cache_b || (c.blk >> 5) != cache_chunk) {
+        cache_b = c.b;
+        cache_chunk = c.blk >> 5;
+        const int e = (cache_chunk << 5) + lane;
+        mine = e < c.nb ? __ldg(p.block_tables + static_cast<int64_t>(c.b) * p.max_blocks_per_seq + e) : 0;
+      }
+      int pb = __shfl_sync(0xffffffffu, mine, c.blk & 31);
+      if (lane == 0) {
+        const int s = j % NST;
+        if (j >= NST) ok = mbar_wait_bounded(&empty[s], ((j / NST) - 1) & 1);
+        if (ok) {
+          if (pb < 0 || pb >= p.num_blocks) {
+            record_error(KV_ERR_DEVICE_BOUNDS);
+            pb = 0;
+          }
+          mbar_arrive_expect_tx(&full[s], TL::kStageBytes);
+          uint8_t* kt = smem + s * TL::kStageBytes;
+          uint8_t* vt = kt + TL::kTileBytes;
+#pragma unroll
+          for (int sl = 0; sl < TL::kSub; ++sl) {
+            tma_load_3d(kt + sl * TL::kSlabBytes, &tmK, &full[s], sl * 64, c.kvh, pb * BS);
+            tma_load_3d(vt + sl * TL::kSlabBytes, &tmV, &full[s], sl * 64, c.kvh, pb * BS);
+          }
+          ++issued;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      advance(c);
+    }
+    if (lane == 0) {  // keep the CTA alive until every issued copy has landed (bounded)
+      for (int s = 0; s < NST && s < issued; ++s) {
+        const int last = s + ((issued - 1 - s) / NST) * NST;
+        mbar_wait_bounded(&full[s], (last / NST) & 1);
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const int cw = warp - 1, ctid = tid - 32;
+  WarpState<D, NG> st;
+  Cursor c{b0, rel0 / nb0, rel0 % nb0, nb0};
+  const float sl2 = p.scale_log2;
+  int ok = 1;
+  int64_t unit_start = static_cast<int64_t>(Hkv) * CB[c.b] + static_cast<int64_t>(c.kvh) * c.nb;
+  int L = checked_len(p, c.b);
+  load_q<T, D, NG>(st, static_cast<const T*>(p.q) + (static_cast<int64_t>(c.b) * p.num_heads + c.kvh * G) * D,
+                   G, lane);
+  reset_state(st);
+  for (int j = 0; j < n; ++j) {
+    if (ok && (j & (kConsumers - 1)) == cw) {
+      const int s = j % NST;
+      int w = 1;
+      if (lane == 0) w = mbar_wait_bounded(&full[s], (j / NST) & 1);
+      ok = __shfl_sync(0xffffffffu, w, 0);
+      if (ok) {
+        __syncwarp();
+        uint8_t* kt = smem + s * TL::kStageBytes;
+        consume_tile<T, D, BS, NG>(st, kt, kt + TL::kTileBytes, c.blk * BS, L, sl2, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      }
+    }
+    if (j == n - 1 || c.blk + 1 == c.nb) {
+      // ---- end of this CTA's segment of unit (b, kvh): merge the 4 warps ----
+      const int64_t unit_end = unit_start + c.nb;
+      const bool whole = unit_start >= t0 && unit_end <= t1;
+      const int slot = unit_start < t0 ? 0 : 1;
+      store_state(st, Os, Ms, Ls, cw, lane);
+      named_barrier_sync(1, kConsumers * 32);
+      for (int idx = ctid; idx < G * D; idx += kConsumers * 32) {
+        const int g = idx / D, d = idx - g * D;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int w2 = 0; w2 < kConsumers; ++w2) mx = fmaxf(mx, Ms[w2 * GP + g]);
+        float num = 0.f, den = 0.f;
+        if (mx != -INFINITY) {
+#pragma unroll
+          for (int w2 = 0; w2 < kConsumers; ++w2) {
+            const float mw = Ms[w2 * GP + g];
+            if (mw == -INFINITY) continue;
+            const float sc = fast_exp2(mw - mx);
+            num += sc * Os[(w2 * D + d) * GP + g];
+            den += sc * Ls[w2 * GP + g];
+          }
+        }
+        if (whole) {
+          T* o = static_cast<T*>(p.out) + (static_cast<int64_t>(c.b) * p.num_heads + c.kvh * G + g) * D + d;
+          *o = DType<T>::from_float(den > 0.f ? num / den : 0.f);
+        } else {
+          const int64_t r = (static_cast<int64_t>(pid) * 2 + slot) * G + g;
+          p.ws_o[r * D + d] = num;
+          if (d == 0) {
+            p.ws_ml[r * 2 + 0] = mx;
+            p.ws_ml[r * 2 + 1] = den;
+          }
+        }
+      }
+      named_barrier_sync(1, kConsumers * 32);
+      if (j + 1 < n) {
+        advance(c);
+        unit_start = static_cast<int64_t>(Hkv) * CB[c.b] + static_cast<int64_t>(c.kvh) * c.nb;
+        L = checked_len(p, c.b);
+        load_q<T, D, NG>(st,
+                         static_cast<const T*>(p.q) + (static_cast<int64_t>(c.b) * p.num_heads + c.kvh * G) * D,
+                         G, lane);
+        reset_state(st);
+      }
+    } else {
+      advance(c);
+    }
+  }
+}
+
+// Combine the partials of units cut by CTA range boundaries: one warp per
+// (sequence, query head).  Units finished inside one CTA were written by
+// the attention kernel; empty sequences get a zero row here.
+template <typename T>
+__global__ void __launch_bounds__(128) sk_merge_kernel(const DecodeParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * 4 + warp;
+  if (idx >= static_cast<int64_t>(p.num_seqs) * p.num_heads) return;
+  const int b = static_cast<int>(idx / p.num_heads), qh = static_cast<int>(idx % p.num_heads);
+  const int G = p.group, kvh = qh / G, g = qh % G, D = p.head_dim, Hkv = p.num_kv_heads;
+  const int* CB = p.ws_cb;
+  const int nb = CB[b + 1] - CB[b];
+  T* o = static_cast<T*>(p.out) + idx * D;
+  if (nb == 0) {
+    for (int d = lane; d < D; d += 32) o[d] = DType<T>::from_float(0.f);
+    return;
+  }
+  const int64_t W = static_cast<int64_t>(Hkv) * CB[p.num_seqs];
+  const int P = p.num_ctas;
+  const int64_t ub = static_cast<int64_t>(Hkv) * CB[b] + static_cast<int64_t>(kvh) * nb, ue = ub + nb;
+  const int pf = sk_cta_of(ub, W, P), pl = sk_cta_of(ue - 1, W, P);
+  if (pf == pl) return;
+  // CTAs with an empty range (possible when W < P) wrote nothing: skip them
+  auto row_of = [&](int q) -> int64_t {
+    const int64_t q0 = static_cast<int64_t>(q) * W / P, q1 = static_cast<int64_t>(q + 1) * W / P;
+    if (q0 == q1) return -1;
+    return (static_cast<int64_t>(q) * 2 + (ub < q0 ? 0 : 1)) * G + g;
+  };
+  float mx = -INFINITY;
+  for (int q = pf; q <= pl; ++q) {
+    const int64_t r = row_of(q);
+    if (r >= 0) mx = fmaxf(mx, p.ws_ml[r * 2]);
+  }
+  float den = 0.f;
+  for (int q = pf; q <= pl; ++q) {
+    const int64_t r = row_of(q);
+    if (r >= 0) den += fast_exp2(p.ws_ml[r * 2] - mx) * p.ws_ml[r * 2 + 1];
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  for (int d = lane; d < D; d += 32) {
+    float num = 0.f;
+    for (int q = pf; q <= pl; ++q) {
+      const int64_t r = row_of(q);
+      if (r >= 0) num += fast_exp2(p.ws_ml[r * 2] - mx) * p.ws_o[r * D + d];
+    }
+    o[d] = DType<T>::from_float(num * inv);
+  }
+}
+
+// =========================================================================
+// Split tensor-core kernel: one CTA per (split, kv head, sequence).  Used
+// when the batch is too large for the stream-K kernel's shared-memory
+// prefix (more than kMaxSkSeqs sequences).
+// =========================================================================
+
+constexpr int kMaxSkSeqs = 4096;
+
+template <typename T, int D, int BS, int NG, int NST>
+struct SplitCfg {
+  using TL = Tile<D, BS>;
+  static constexpr int kStages = NST * TL::kStageBytes;
+  static constexpr int kMerge = MergeArea<D, NG>::kBytes;
+  static constexpr int kData = kStages > kMerge ? kStages : kMerge;
+  static constexpr int kSmem = 1024 + kData + 2 * NST * 8;
+};
+
+template <typename T, int D, int BS, int NG, int NST>
+__global__ void __launch_bounds__(kTcThreads)
+decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV) {
+  using C = SplitCfg<T, D, BS, NG, NST>;
+  using TL = Tile<D, BS>;
+  constexpr int GP = 8 * NG;
+  static_assert(NST % kConsumers == 0, "stage s must always be drained by consumer s % kConsumers");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kData);
   uint64_t* empty = full + NST;
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -168,7 +658,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   const int bps = p.blocks_per_split;
   const int nsplit_b = (nblk + bps - 1) / bps;
   if (L == 0) {
-    if (split == 0) store_zero_rows<T>(p, b, kvh * G, G, D, threadIdx.x, C::kThreads);
+    if (split == 0) store_zero_rows<T>(p, b, kvh * G, G, D, threadIdx.x, kTcThreads);
     return;
   }
   if (split >= nsplit_b) return;
@@ -185,7 +675,6 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   __syncthreads();
 
   if (warp == 0) {
-    // ---------------- producer: table walk + TMA issue ----------------
     if (lane == 0) {
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
@@ -204,20 +693,19 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
             record_error(KV_ERR_DEVICE_BOUNDS);
             pb = 0;
           }
-          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-          uint8_t* kt = smem + s * C::kStageBytes;
-          uint8_t* vt = kt + C::kTileBytes;
+          mbar_arrive_expect_tx(&full[s], TL::kStageBytes);
+          uint8_t* kt = smem + s * TL::kStageBytes;
+          uint8_t* vt = kt + TL::kTileBytes;
 #pragma unroll
-          for (int c = 0; c < C::kSub; ++c) {
-            tma_load_3d(kt + c * C::kSlabBytes, &tmK, &full[s], c * 64, kvh, pb * BS);
-            tma_load_3d(vt + c * C::kSlabBytes, &tmV, &full[s], c * 64, kvh, pb * BS);
+          for (int c = 0; c < TL::kSub; ++c) {
+            tma_load_3d(kt + c * TL::kSlabBytes, &tmK, &full[s], c * 64, kvh, pb * BS);
+            tma_load_3d(vt + c * TL::kSlabBytes, &tmV, &full[s], c * 64, kvh, pb * BS);
           }
           ++issued;
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
     }
-    // Keep the CTA alive until every issued copy has landed (bounded).
     if (lane == 0) {
       for (int s = 0; s < NST && s < issued; ++s) {
         const int last = s + ((issued - 1 - s) / NST) * NST;
@@ -227,174 +715,31 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     return;
   }
 
-  // ---------------- consumers ----------------
-  const int cw = warp - 1;
-  const int ctid = threadIdx.x - 32;
-  constexpr int KS = D / 16;  // k-steps of S^T = K Q^T; also m-tiles of O^T
-  using M = Mma<T>;
-
-  // Q^T as B operand: b0 = Q[g][kk*16 + 2*(lane%4) + {0,1}], b1 = the same at d + 8.
-  uint32_t qf[KS][NG][2];
-  {
-    const T* qb = static_cast<const T*>(p.q) + (static_cast<int64_t>(b) * p.num_heads + kvh * G) * D;
-#pragma unroll
-    for (int ng = 0; ng < NG; ++ng) {
-      const int g = ng * 8 + (lane >> 2);
-#pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        const int d = kk * 16 + (lane & 3) * 2;
-        if (g < G) {
-          qf[kk][ng][0] = __ldg(reinterpret_cast<const uint32_t*>(qb + g * D + d));
-          qf[kk][ng][1] = __ldg(reinterpret_cast<const uint32_t*>(qb + g * D + d + 8));
-        } else {
-          qf[kk][ng][0] = 0u;
-          qf[kk][ng][1] = 0u;
-        }
-      }
-    }
-  }
-
-  float acc[KS][NG][4];
-  float mrun[NG][2], lrun[NG][2];
-#pragma unroll
-  for (int mt = 0; mt < KS; ++mt)
-#pragma unroll
-    for (int ng = 0; ng < NG; ++ng)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[mt][ng][e] = 0.f;
-#pragma unroll
-  for (int ng = 0; ng < NG; ++ng) {
-    mrun[ng][0] = mrun[ng][1] = -INFINITY;
-    lrun[ng][0] = lrun[ng][1] = 0.f;
-  }
-
-  const float sl2 = p.scale_log2;
-  // ldmatrix lane -> (row, column) of the 8x8 matrix it addresses
-  const int k_row = (lane & 7) + ((lane >> 3) & 1) * 8, k_col = (lane >> 4) * 8;   // A = K (non-trans)
-  const int v_row = (lane & 7) + (lane >> 4) * 8, v_col = ((lane >> 3) & 1) * 8;   // A = V^T (trans)
-
-  for (int j = cw; j < nb; j += C::kConsumers) {
+  const int cw = warp - 1, ctid = threadIdx.x - 32;
+  WarpState<D, NG> st;
+  load_q<T, D, NG>(st, static_cast<const T*>(p.q) + (static_cast<int64_t>(b) * p.num_heads + kvh * G) * D, G,
+                   lane);
+  reset_state(st);
+  for (int j = cw; j < nb; j += kConsumers) {
     const int s = j % NST;
     int ok = 1;
     if (lane == 0) ok = mbar_wait_bounded(&full[s], (j / NST) & 1);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) break;
     __syncwarp();
-    uint8_t* kt = smem + s * C::kStageBytes;
-    uint8_t* vt = kt + C::kTileBytes;
-    const uint32_t kt_a = smem_u32(kt), vt_a = smem_u32(vt);
-    const int tok0 = (blk0 + j) * BS;
-    const int valid = min(BS, L - tok0);
-    if (valid < BS) {
-      // zero the V rows past the sequence end: P is 0 there, but 0 * NaN is not
-      const int chunks = (BS - valid) * (D / 8);
-      for (int c = lane; c < chunks; c += 32) {
-        const int t = valid + c / (D / 8), d = (c % (D / 8)) * 8;
-        *reinterpret_cast<uint4*>(vt + swz<BS>(t, d)) = make_uint4(0u, 0u, 0u, 0u);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-    }
-#pragma unroll
-    for (int sub = 0; sub < BS / 16; ++sub) {
-      if (sub * 16 < valid) {
-        // ---- S^T[16 tokens x 8*NG heads] = K Q^T ----
-        float sc[NG][4];
-#pragma unroll
-        for (int ng = 0; ng < NG; ++ng) sc[ng][0] = sc[ng][1] = sc[ng][2] = sc[ng][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-          uint32_t a[4];
-          ldmatrix_x4(kt_a + swz<BS>(sub * 16 + k_row, kk * 16 + k_col), a[0], a[1], a[2], a[3]);
-#pragma unroll
-          for (int ng = 0; ng < NG; ++ng) M::run(sc[ng], a, qf[kk][ng][0], qf[kk][ng][1]);
-        }
-        // ---- online softmax (exp2 domain), P^T -> B operand ----
-        const int t_lo = tok0 + sub * 16 + (lane >> 2);
-        const bool in_lo = t_lo < L, in_hi = t_lo + 8 < L;
-        uint32_t pb0[NG], pb1[NG];
-#pragma unroll
-        for (int ng = 0; ng < NG; ++ng) {
-          const float x0 = in_lo ? sc[ng][0] * sl2 : -INFINITY;
-          const float x1 = in_lo ? sc[ng][1] * sl2 : -INFINITY;
-          const float x2 = in_hi ? sc[ng][2] * sl2 : -INFINITY;
-          const float x3 = in_hi ? sc[ng][3] * sl2 : -INFINITY;
-          float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-          for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-          }
-          const float mn0 = fmaxf(mrun[ng][0], mx0), mn1 = fmaxf(mrun[ng][1], mx1);
-          const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0, mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
-          const float al0 = fast_exp2(mrun[ng][0] - mu0), al1 = fast_exp2(mrun[ng][1] - mu1);
-          const uint32_t lo = M::pack(fast_exp2(x0 - mu0), fast_exp2(x1 - mu1));
-          const uint32_t hi = M::pack(fast_exp2(x2 - mu0), fast_exp2(x3 - mu1));
-          const float2 flo = M::unpack(lo), fhi = M::unpack(hi);
-          lrun[ng][0] = lrun[ng][0] * al0 + (flo.x + fhi.x);
-          lrun[ng][1] = lrun[ng][1] * al1 + (flo.y + fhi.y);
-          mrun[ng][0] = mn0;
-          mrun[ng][1] = mn1;
-#pragma unroll
-          for (int mt = 0; mt < KS; ++mt) {
-            acc[mt][ng][0] *= al0;
-            acc[mt][ng][1] *= al1;
-            acc[mt][ng][2] *= al0;
-            acc[mt][ng][3] *= al1;
-          }
-          pb0[ng] = movmatrix_trans(lo);
-          pb1[ng] = movmatrix_trans(hi);
-        }
-        // ---- O^T[D x 8*NG] += V^T P^T ----
-#pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-          uint32_t a[4];
-          ldmatrix_x4_trans(vt_a + swz<BS>(sub * 16 + v_row, mt * 16 + v_col), a[0], a[1], a[2], a[3]);
-#pragma unroll
-          for (int ng = 0; ng < NG; ++ng) M::run(acc[mt][ng], a, pb0[ng], pb1[ng]);
-        }
-      }
-    }
+    uint8_t* kt = smem + s * TL::kStageBytes;
+    consume_tile<T, D, BS, NG>(st, kt, kt + TL::kTileBytes, (blk0 + j) * BS, L, p.scale_log2, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
-
-  // ---------------- merge the consumer warps ----------------
-#pragma unroll
-  for (int ng = 0; ng < NG; ++ng)
-#pragma unroll
-    for (int c = 0; c < 2; ++c)
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) lrun[ng][c] += __shfl_xor_sync(0xffffffffu, lrun[ng][c], off);
-
-  named_barrier_sync(1, C::kConsumers * 32);  // all stages consumed: reuse them
-  constexpr int GP = C::kGPad;
+  named_barrier_sync(1, kConsumers * 32);  // all stages consumed: reuse them for the merge
   float* Os = reinterpret_cast<float*>(smem);
-  float* Ms = Os + C::kConsumers * D * GP;
-  float* Ls = Ms + C::kConsumers * GP;
-#pragma unroll
-  for (int mt = 0; mt < KS; ++mt)
-#pragma unroll
-    for (int ng = 0; ng < NG; ++ng) {
-      const int d0 = mt * 16 + (lane >> 2), g0 = ng * 8 + (lane & 3) * 2;
-      float* o = Os + cw * D * GP;
-      o[d0 * GP + g0] = acc[mt][ng][0];
-      o[d0 * GP + g0 + 1] = acc[mt][ng][1];
-      o[(d0 + 8) * GP + g0] = acc[mt][ng][2];
-      o[(d0 + 8) * GP + g0 + 1] = acc[mt][ng][3];
-    }
-  if (lane < 4) {
-#pragma unroll
-    for (int ng = 0; ng < NG; ++ng)
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        Ms[cw * GP + ng * 8 + lane * 2 + c] = mrun[ng][c];
-        Ls[cw * GP + ng * 8 + lane * 2 + c] = lrun[ng][c];
-      }
-  }
-  named_barrier_sync(1, C::kConsumers * 32);
-  combine_and_store<T>(p, Ms, Ls, Os, C::kConsumers, GP, D, b, kvh * G, G, split, nsplit_b == 1, ctid,
-                       C::kConsumers * 32);
+  float* Ms = Os + kConsumers * D * GP;
+  float* Ls = Ms + kConsumers * GP;
+  store_state(st, Os, Ms, Ls, cw, lane);
+  named_barrier_sync(1, kConsumers * 32);
+  combine_and_store<T>(p, Ms, Ls, Os, kConsumers, GP, D, b, kvh * G, G, split, nsplit_b == 1, ctid,
+                       kConsumers * 32);
 }
 
 // =========================================================================
@@ -560,14 +905,17 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lse_merge_kernel(const Decod
 // Host side: planning, tensor maps, dispatch.
 // =========================================================================
 
-enum KernelKind { kSimt = 0, kTensorCore = 1 };
+enum KernelKind { kSimt = 0, kTensorCoreSplit = 1, kTensorCoreStreamK = 2 };
 
 struct Plan {
   int kind;
-  int bps;
-  int num_splits;
+  int bps;         // split kernels: logical blocks per split
+  int num_splits;  // split kernels: splits per sequence
+  int num_ctas;    // stream-K: upper bound of the grid size used to size the workspace
   size_t ws_bytes;
 };
+
+constexpr int kMaxSkCtasPerSm = 4;
 
 int sm_count() {
   static int cached[64] = {0};
@@ -589,19 +937,29 @@ bool tc_supported(int dtype, int D, int BS, int G) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-Plan make_plan(int B, int Hq, int Hkv, int D, int BS, int64_t max_seq_len, int bps_req, int dtype,
-               bool query_device) {
+Plan make_plan(int B, int Hq, int Hkv, int D, int BS, int64_t max_seq_len, int bps_req, int dtype) {
   Plan pl{};
   const int G = Hkv > 0 ? Hq / Hkv : 1;
-  pl.kind = tc_supported(dtype, D, BS, G) ? kTensorCore : kSimt;
   const int64_t maxblk = std::max<int64_t>(1, (max_seq_len + BS - 1) / BS);
+  if (tc_supported(dtype, D, BS, G) && bps_req == 0 && B <= kMaxSkSeqs) {
+    pl.kind = kTensorCoreStreamK;
+    const int64_t w_upper = std::max<int64_t>(1, static_cast<int64_t>(B) * Hkv * maxblk);
+    pl.num_ctas = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(sm_count()) * kMaxSkCtasPerSm, w_upper));
+    pl.bps = static_cast<int>(maxblk);
+    pl.num_splits = 1;
+    const size_t rows = static_cast<size_t>(pl.num_ctas) * 2 * G;
+    pl.ws_bytes = align256(rows * D * sizeof(float)) + align256(rows * 2 * sizeof(float)) +
+                  align256((static_cast<size_t>(B) + 1) * sizeof(int32_t));
+    return pl;
+  }
+  pl.kind = tc_supported(dtype, D, BS, G) ? kTensorCoreSplit : kSimt;
   int64_t bps;
   if (bps_req > 0) {
     bps = bps_req;
   } else {
-    const int64_t units = static_cast<int64_t>(B) * Hkv * (pl.kind == kSimt ? (G + kSimtHeads - 1) / kSimtHeads : 1);
-    const int64_t slots = static_cast<int64_t>(query_device ? sm_count() : 152) * 3;
-    const int64_t target = 2 * slots;
+    const int64_t units =
+        static_cast<int64_t>(B) * Hkv * (pl.kind == kSimt ? (G + kSimtHeads - 1) / kSimtHeads : 1);
+    const int64_t target = static_cast<int64_t>(sm_count()) * 6;
     const int64_t min_bps = std::max<int64_t>(1, 256 / BS);  // >= 256 tokens per split
     if (units >= target || maxblk <= min_bps) {
       bps = maxblk;
@@ -616,8 +974,6 @@ Plan make_plan(int B, int Hq, int Hkv, int D, int BS, int64_t max_seq_len, int b
   if (pl.num_splits > 1) {
     const size_t rows = static_cast<size_t>(B) * Hq * pl.num_splits;
     pl.ws_bytes = align256(rows * D * sizeof(float)) + align256(rows * 2 * sizeof(float));
-  } else {
-    pl.ws_bytes = 0;
   }
   return pl;
 }
@@ -681,43 +1037,101 @@ bool get_tensor_map(const void* cache, int64_t rows, int hkv, int d, int bs, CUt
 
 // ---- launches ----------------------------------------------------------------
 
-template <typename T, int D, int BS, int NG>
-cudaError_t launch_tc(const DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, dim3 grid,
-                      cudaStream_t st) {
-  constexpr int NST = (BS * D * 4 <= 8192) ? 8 : 4;  // stages: ~64 KB of K+V in flight per CTA
-  using C = TcCfg<D, BS, NG, NST>;
-  auto kern = decode_tc_kernel<T, D, BS, NG, NST>;
-  static int configured = -1;
+// Pipeline depth: about 64 KB of K+V in flight per CTA, 4..12 stages.
+// The stage count must be a multiple of the consumer count: stage s is then
+// always drained by consumer s % kConsumers, each consumer meets a stage's
+// phases in order, and a parity wait can never be satisfied by a phase one
+// round old (with 6 stages and 4 consumers, tile j + 6 would belong to a
+// different warp than tile j and could pass its wait before tile j landed).
+template <int D, int BS>
+struct Stages {
+  static constexpr int kRaw = ((64 * 1024) / Tile<D, BS>::kStageBytes) / kConsumers * kConsumers;
+  static constexpr int value = kRaw < kConsumers ? kConsumers : (kRaw > 12 ? 12 : kRaw);
+  static_assert(value % kConsumers == 0, "stages must be a multiple of the consumer warps");
+};
+
+// Raise a kernel's dynamic shared memory limit to `bytes` (per device, only
+// when it grows).
+template <typename K>
+cudaError_t allow_smem(K kern, int bytes, int* configured_bytes) {
   int dev = 0;
   cudaGetDevice(&dev);
-  if (configured != dev) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (configured_bytes[dev] >= bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) configured_bytes[dev] = bytes;
+  return e;
+}
+
+template <typename T, int D, int BS, int NG>
+cudaError_t launch_sk(DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, int max_ctas, cudaStream_t st) {
+  constexpr int NST = Stages<D, BS>::value;
+  using C = SkCfg<T, D, BS, NG, NST>;
+  auto kern = decode_sk_kernel<T, D, BS, NG, NST>;
+  static int configured[64] = {0};
+  cudaError_t e = allow_smem(kern, C::smem_bytes(p.num_seqs), configured);
+  if (e != cudaSuccess) return e;
+  const int smem = C::smem_bytes(p.num_seqs);
+  static int occ_cache[64][2] = {{0}};  // per device: (smem bytes, CTAs per SM)
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (occ_cache[dev][0] != smem) {
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kTcThreads, smem);
     if (e != cudaSuccess) return e;
-    configured = dev;
+    occ_cache[dev][0] = smem;
+    occ_cache[dev][1] = std::max(1, std::min(occ, kMaxSkCtasPerSm));
   }
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(p, mk, mv);
+  const int ctas = std::min(max_ctas, sm_count() * occ_cache[dev][1]);
+  p.num_ctas = ctas;
+  kern<<<ctas, kTcThreads, smem, st>>>(p, mk, mv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.num_heads;
+  sk_merge_kernel<T><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, st>>>(p);
   return cudaGetLastError();
 }
 
+template <typename T, int D, int BS, int NG>
+cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, dim3 grid,
+                         cudaStream_t st) {
+  constexpr int NST = Stages<D, BS>::value;
+  using C = SplitCfg<T, D, BS, NG, NST>;
+  auto kern = decode_split_kernel<T, D, BS, NG, NST>;
+  static int configured[64] = {0};
+  cudaError_t e = allow_smem(kern, C::kSmem, configured);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kTcThreads, C::kSmem, st>>>(p, mk, mv);
+  return cudaGetLastError();
+}
+
+template <typename T, int D, int BS, int NG>
+cudaError_t launch_tc_inst(DecodeParams& p, const Plan& pl, const CUtensorMap& mk, const CUtensorMap& mv,
+                           cudaStream_t st) {
+  if (pl.kind == kTensorCoreStreamK) return launch_sk<T, D, BS, NG>(p, mk, mv, pl.num_ctas, st);
+  return launch_split<T, D, BS, NG>(p, mk, mv, dim3(pl.num_splits, p.num_kv_heads, p.num_seqs), st);
+}
+
 template <typename T, int D, int BS>
-cudaError_t launch_tc_g(const DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, dim3 grid,
+cudaError_t launch_tc_g(DecodeParams& p, const Plan& pl, const CUtensorMap& mk, const CUtensorMap& mv,
                         cudaStream_t st) {
-  return p.group <= 8 ? launch_tc<T, D, BS, 1>(p, mk, mv, grid, st) : launch_tc<T, D, BS, 2>(p, mk, mv, grid, st);
+  return p.group <= 8 ? launch_tc_inst<T, D, BS, 1>(p, pl, mk, mv, st) : launch_tc_inst<T, D, BS, 2>(p, pl, mk, mv, st);
 }
 
 template <typename T, int D>
-cudaError_t launch_tc_bs(const DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, dim3 grid,
+cudaError_t launch_tc_bs(DecodeParams& p, const Plan& pl, const CUtensorMap& mk, const CUtensorMap& mv,
                          cudaStream_t st) {
-  return p.block_size == 16 ? launch_tc_g<T, D, 16>(p, mk, mv, grid, st) : launch_tc_g<T, D, 32>(p, mk, mv, grid, st);
+  return p.block_size == 16 ? launch_tc_g<T, D, 16>(p, pl, mk, mv, st) : launch_tc_g<T, D, 32>(p, pl, mk, mv, st);
 }
 
 template <typename T>
-cudaError_t launch_tc_d(const DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, dim3 grid,
-                        cudaStream_t st) {
+cudaError_t launch_tc(DecodeParams& p, const Plan& pl, const CUtensorMap& mk, const CUtensorMap& mv,
+                      cudaStream_t st) {
   switch (p.head_dim) {
-    case 64: return launch_tc_bs<T, 64>(p, mk, mv, grid, st);
-    case 128: return launch_tc_bs<T, 128>(p, mk, mv, grid, st);
-    default: return launch_tc_bs<T, 256>(p, mk, mv, grid, st);
+    case 64: return launch_tc_bs<T, 64>(p, pl, mk, mv, st);
+    case 128: return launch_tc_bs<T, 128>(p, pl, mk, mv, st);
+    default: return launch_tc_bs<T, 256>(p, pl, mk, mv, st);
   }
 }
 
@@ -740,20 +1154,19 @@ cudaError_t launch_merge(const DecodeParams& p, cudaStream_t st) {
 }
 
 template <typename T>
-cudaError_t run_decode(const DecodeParams& p, const Plan& pl, cudaStream_t st, bool tc, const CUtensorMap* mk,
+cudaError_t run_decode(DecodeParams& p, const Plan& pl, cudaStream_t st, const CUtensorMap* mk,
                        const CUtensorMap* mv) {
   cudaError_t e = cudaSuccess;
   if constexpr (!std::is_same<T, float>::value) {
-    if (tc) {
-      dim3 grid(pl.num_splits, p.num_kv_heads, p.num_seqs);
-      e = launch_tc_d<T>(p, *mk, *mv, grid, st);
+    if (pl.kind != kSimt) {
+      e = launch_tc<T>(p, pl, *mk, *mv, st);
+      if (e != cudaSuccess || pl.kind == kTensorCoreStreamK || pl.num_splits <= 1) return e;
+      return launch_merge<T>(p, st);
     }
   }
-  if (!tc) {
-    const int ngroups = (p.group + kSimtHeads - 1) / kSimtHeads;
-    dim3 grid(pl.num_splits, p.num_kv_heads * ngroups, p.num_seqs);
-    e = launch_simt<T>(p, grid, st);
-  }
+  const int ngroups = (p.group + kSimtHeads - 1) / kSimtHeads;
+  dim3 grid(pl.num_splits, p.num_kv_heads * ngroups, p.num_seqs);
+  e = launch_simt<T>(p, grid, st);
   if (e != cudaSuccess || pl.num_splits <= 1) return e;
   return launch_merge<T>(p, st);
 }
@@ -782,8 +1195,7 @@ extern "C" int paged_decode_plan(int32_t num_seqs, int32_t num_heads, int32_t nu
   int st = check_shapes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_seq_len, dtype);
   if (st != KV_OK) return st;
   if (blocks_per_split < 0) return KV_ERR_INVALID_ARG;
-  Plan pl = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_seq_len, blocks_per_split, dtype,
-                      true);
+  Plan pl = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_seq_len, blocks_per_split, dtype);
   if (kernel_out) *kernel_out = pl.kind;
   if (blocks_per_split_out) *blocks_per_split_out = pl.bps;
   if (num_splits_out) *num_splits_out = pl.num_splits;
@@ -815,8 +1227,7 @@ extern "C" int paged_decode_attention(void* out, const void* q, const void* k_ca
   const uintptr_t align_bits = reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(q) |
                                reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache);
   if (align_bits % 16 != 0) return KV_ERR_INVALID_ARG;
-  Plan pl = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_seq_len, blocks_per_split,
-                      dtype, true);
+  Plan pl = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_seq_len, blocks_per_split, dtype);
   if (pl.ws_bytes > 0) {
     if (!workspace || workspace_bytes < pl.ws_bytes) return KV_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return KV_ERR_INVALID_ARG;
@@ -836,28 +1247,39 @@ extern "C" int paged_decode_attention(void* out, const void* q, const void* k_ca
   p.block_size = block_size;
   p.num_blocks = num_blocks;
   p.max_blocks_per_seq = max_blocks_per_seq;
-  p.blocks_per_split = pl.bps;
-  p.num_splits = pl.num_splits;
   p.scale_log2 = scale * kLog2e;
-  if (pl.ws_bytes > 0) {
-    const size_t rows = static_cast<size_t>(num_seqs) * num_heads * pl.num_splits;
-    p.ws_o = static_cast<float*>(workspace);
-    p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * head_dim * sizeof(float)));
+  char* ws = static_cast<char*>(workspace);
+  if (pl.kind == kTensorCoreStreamK) {
+    // lengths are bounded by the table rows only; the grid adapts to them
+    p.blocks_per_split = max_blocks_per_seq;
+    p.num_splits = 1;
+    const size_t rows = static_cast<size_t>(pl.num_ctas) * 2 * p.group;
+    p.ws_o = reinterpret_cast<float*>(ws);
+    p.ws_ml = reinterpret_cast<float*>(ws + align256(rows * head_dim * sizeof(float)));
+    p.ws_cb = reinterpret_cast<int32_t*>(ws + align256(rows * head_dim * sizeof(float)) +
+                                         align256(rows * 2 * sizeof(float)));
+  } else {
+    p.blocks_per_split = pl.bps;
+    p.num_splits = pl.num_splits;
+    if (pl.ws_bytes > 0) {
+      const size_t rows = static_cast<size_t>(num_seqs) * num_heads * pl.num_splits;
+      p.ws_o = reinterpret_cast<float*>(ws);
+      p.ws_ml = reinterpret_cast<float*>(ws + align256(rows * head_dim * sizeof(float)));
+    }
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool tc = pl.kind == kTensorCore;
   CUtensorMap mk, mv;
-  if (tc) {
+  if (pl.kind != kSimt) {
     const int64_t rows = num_blocks * block_size;
     if (!get_tensor_map(k_cache, rows, num_kv_heads, head_dim, block_size, &mk) ||
         !get_tensor_map(v_cache, rows, num_kv_heads, head_dim, block_size, &mv))
-      return KV_ERR_CUDA;
+      return cuda_status(cudaErrorInvalidValue, "cuTensorMapEncodeTiled failed");
   }
   cudaError_t e;
-  if (dtype == KV_DTYPE_F32) e = run_decode<float>(p, pl, s, false, nullptr, nullptr);
-  else if (dtype == KV_DTYPE_F16) e = run_decode<__half>(p, pl, s, tc, &mk, &mv);
-  else e = run_decode<__nv_bfloat16>(p, pl, s, tc, &mk, &mv);
-  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+  if (dtype == KV_DTYPE_F32) e = run_decode<float>(p, pl, s, nullptr, nullptr);
+  else if (dtype == KV_DTYPE_F16) e = run_decode<__half>(p, pl, s, &mk, &mv);
+  else e = run_decode<__nv_bfloat16>(p, pl, s, &mk, &mv);
+  return cuda_status(e);
 }
 
 extern "C" int kv_device_error(int reset, int* status_out) {
@@ -876,3 +1298,12 @@ extern "C" int kv_device_error(int reset, int* status_out) {
 }
 
 extern "C" const char* kv_version(void) { return "pagedkv-gb300 0.1 (sm_103a)"; }
+
+namespace pagedkv {
+const char*& last_cuda_error_text() {
+  static thread_local const char* text = "no error";
+  return text;
+}
+}  // namespace pagedkv
+
+extern "C" const char* kv_last_cuda_error(void) { return last_cuda_error_text(); }

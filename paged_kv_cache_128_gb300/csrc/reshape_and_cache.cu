@@ -114,7 +114,7 @@ extern "C" int paged_reshape_and_cache(const void* k, const void* v, void* k_cac
     err = launch<uint16_t>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, ks, vs, num_slots, st);
   else
     return KV_ERR_INVALID_ARG;
-  return err == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+  return cuda_status(err);
 }
 
 // Read (and optionally clear) this translation unit's device error word.

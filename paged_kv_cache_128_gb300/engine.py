@@ -36,8 +36,10 @@ def _signed(bits: int, width: int) -> int:
 
 
 class PagedDecodeEngine:
-    def __init__(self, wl: Workload, device="cuda", max_steps: int = 64, fill_sentinel: bool = True):
+    def __init__(self, wl: Workload, device="cuda", max_steps: int = 64, fill_sentinel: bool = True,
+                 blocks_per_split: int = 0):
         self.wl = wl
+        self.blocks_per_split = blocks_per_split
         self.device = torch.device(device)
         self.mgr = KVBlockManager(wl.num_blocks, wl.block_size, wl.free_order)
         dt = wl.torch_dtype
@@ -54,7 +56,7 @@ class PagedDecodeEngine:
         self.max_seq_len = int(wl.cached_lens.max()) + 1 + max_steps
         self.max_blocks = -(-self.max_seq_len // wl.block_size)
         self.plan = decode_plan(B, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size, self.max_seq_len,
-                                dt)
+                                dt, blocks_per_split)
         self.workspace = alloc_workspace(self.plan, self.device)
         n_step = wl.num_step_tokens
         pin = dict(pin_memory=True)
@@ -147,7 +149,7 @@ class PagedDecodeEngine:
         """a3-a8: decode attention for every running sequence."""
         wl = self.wl
         return paged_decode_attention(self.out, q, self.k_cache, self.v_cache, self.d_tables, self.d_lens,
-                                      wl.scale, self.max_seq_len, self.plan.blocks_per_split, self.workspace)
+                                      wl.scale, self.max_seq_len, self.blocks_per_split, self.workspace)
 
     def step(self, q: torch.Tensor, k_step: torch.Tensor, v_step: torch.Tensor) -> torch.Tensor:
         if self.steps_done + 1 > self.max_seq_len - int(self.wl.cached_lens.max()):

@@ -61,14 +61,15 @@ def reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v
 
 @dataclass
 class DecodePlan:
-    kernel: int            # 0 = SIMT, 1 = TMA + tensor cores
+    kernel: int            # 0 = SIMT, 1 = split TMA + tensor cores, 2 = stream-K TMA + tensor cores
     blocks_per_split: int
     num_splits: int
     workspace_bytes: int
 
     @property
     def launches(self) -> int:
-        return 2 if self.num_splits > 1 else 1
+        """Kernels one attention call launches (attention, then merge if any)."""
+        return 2 if (self.kernel == 2 or self.num_splits > 1) else 1
 
 
 def decode_plan(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,

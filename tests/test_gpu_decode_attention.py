@@ -20,7 +20,7 @@ from tests.helpers import TOL, TORCH, oracle_paged_pool, sentinel_tensor, to_f64
 pytestmark = pytest.mark.gpu
 
 
-def run_case(dtype, hq, hkv, d, bs, lens, seed, bps=0, nb=None, scale=None, value_scale=1.0):
+def run_case(dtype, hq, hkv, d, bs, lens, seed, bps=0, nb=None, scale=None, value_scale=1.0, max_seq_len=None):
     rng = np.random.default_rng(seed)
     B = len(lens)
     nb = nb or sum(-(-L // bs) for L in lens) + 3
@@ -52,7 +52,7 @@ def run_case(dtype, hq, hkv, d, bs, lens, seed, bps=0, nb=None, scale=None, valu
         seq_lens[live] = l
     out = torch.empty(B, hq, d, dtype=dt, device=dev)
     pk.paged_decode_attention(out, q.to(dev), kc, vc, torch.from_numpy(tables).to(dev),
-                              torch.from_numpy(seq_lens).to(dev), scale, max(max(lens), 1), bps)
+                              torch.from_numpy(seq_lens).to(dev), scale, max_seq_len or max(max(lens), 1), bps)
     assert pk.device_error() == 0
 
     # oracle side
@@ -88,8 +88,10 @@ LENS_B = [33, 1, 64, 0, 129, 31, 512, 2]
 ])
 def test_tensor_core_path(dtype, hq, hkv, d, bs):
     plan = pk.decode_plan(len(LENS_A), hq, hkv, d, bs, max(LENS_A), TORCH[dtype])
-    assert plan.kernel == 1
+    assert plan.kernel == 2                                   # stream-K by default
     run_case(dtype, hq, hkv, d, bs, LENS_A, seed=hq * 1000 + d + bs)
+    assert pk.decode_plan(len(LENS_A), hq, hkv, d, bs, max(LENS_A), TORCH[dtype], 5).kernel == 1
+    run_case(dtype, hq, hkv, d, bs, LENS_A, seed=hq * 1000 + d + bs, bps=5)   # split kernel
 
 
 @pytest.mark.parametrize("dtype,hq,hkv,d,bs", [
@@ -119,6 +121,13 @@ def test_split_invariance(dtype, hq, hkv, d, bs):
         assert np.max(np.abs(o - outs[0])) <= 2 * TOL[dtype]
 
 
+def test_stream_k_more_ctas_than_tiles():
+    """A generous max_seq_len makes the stream-K grid larger than the tile
+    count, so some CTAs get empty ranges between the parts of one unit."""
+    run_case("bf16", 8, 2, 128, 16, [40, 3, 70], seed=21, max_seq_len=20000)
+    run_case("f16", 14, 2, 64, 16, [1, 2, 33], seed=22, max_seq_len=50000)
+
+
 def test_zero_length_rows_are_zero():
     got, _ = run_case("bf16", 8, 2, 128, 16, [0, 5, 0, 40], seed=3)
     assert np.all(got[0] == 0) and np.all(got[2] == 0)
@@ -128,9 +137,10 @@ def test_zero_length_rows_are_zero():
 
 def test_long_sequence_auto_split():
     lens = [6000, 17, 3000]
-    plan = pk.decode_plan(3, 32, 8, 128, 16, 6000, torch.bfloat16)
-    assert plan.num_splits > 1
     run_case("bf16", 32, 8, 128, 16, lens, seed=11)
+    plan = pk.decode_plan(3, 4, 2, 32, 16, 6000, torch.float32)
+    assert plan.kernel == 0 and plan.num_splits > 1
+    run_case("f32", 4, 2, 32, 16, lens, seed=12)
 
 
 def test_closed_form_single_token_and_equal_keys():
