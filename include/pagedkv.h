@@ -197,11 +197,12 @@ int paged_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v
  * *kernel_out = 0 for the SIMT split kernel (fp32 and shapes the tensor-core
  * kernels do not take), 1 for the TMA + tensor-core split kernel (forced
  * splits, or more than 4096 sequences), 2 for the TMA + tensor-core
- * stream-K kernel (the fp16/bf16 default: one wave of persistent CTAs, each
- * taking an equal share of all (sequence, kv head, block) tiles); the
+ * stream-K kernel (the fp16/bf16 default: one cooperative wave of
+ * persistent CTAs, each taking an equal share of all (sequence, kv head,
+ * block) tiles, and combining cut sequences inside the same launch); the
  * blocks per split and number of splits S (split kernels); the workspace
- * bytes.  Kernel 2 always launches two kernels (attention, then the
- * log-sum-exp merge); kernels 0 and 1 launch the merge only when S > 1.
+ * bytes.  Kernel 2 launches one kernel; kernels 0 and 1 add a log-sum-exp
+ * merge kernel when S > 1.
  * max_seq_len is an upper bound of the seq_lens the call will see. */
 int paged_decode_plan(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                       int32_t block_size, int64_t max_seq_len, int32_t blocks_per_split, int dtype,

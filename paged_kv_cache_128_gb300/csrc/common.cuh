@@ -130,6 +130,40 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Release store / acquire load of a 64-bit flag at GPU scope (inter-CTA
+// hand-off of data written to global memory).
+__device__ __forceinline__ void st_release_gpu(uint64_t* ptr, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(ptr), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_acquire_gpu(const uint64_t* ptr) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+// Spin until *flag == value, for at most kWaitLimitNs.  Returns false (and
+// records KV_ERR_DEVICE_TIMEOUT) on timeout.
+__device__ __forceinline__ bool wait_flag_bounded(const uint64_t* flag, uint64_t value) {
+  if (ld_acquire_gpu(flag) == value) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_gpu(flag) != value) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      record_error(KV_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start
+// launching (its CTAs wait in griddep_wait until this grid has completed and
+// its memory is visible).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Named barrier over a subset of the CTA's warps.
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

@@ -40,7 +40,10 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <atomic>
+#include <chrono>
 #include <mutex>
+#include <random>
 #include <type_traits>
 
 #include "common.cuh"
@@ -65,7 +68,9 @@ struct DecodeParams {
   int32_t num_ctas;  // stream-K grid size P
   float* ws_o;       // split: [B][Hq][S][D]; stream-K: [P][2][G][D] unnormalised partial outputs
   float* ws_ml;      // split: [B][Hq][S][2]; stream-K: [P][2][G][2] (running max, running sum)
-  int32_t* ws_cb;    // stream-K: [B + 1] prefix of per-sequence block counts
+  uint64_t* ws_flags;  // stream-K: [P] "partial in slot 0 ready" flags, holding the call's epoch
+  uint64_t epoch;      // stream-K: tag unique to this call (flags from other calls never match)
+  int32_t seg_cost;    // stream-K: extra tiles charged per unit when ranges are drawn
 };
 
 // Sequence length after bounds checks: at most what the table row and the
@@ -165,7 +170,7 @@ struct WarpState {
 // B operand of S^T = K Q^T: b0 = Q[g][kk*16 + 2*(lane%4) + {0,1}], b1 at d + 8,
 // g = ng*8 + lane/4; heads past G are zero.
 template <typename T, int D, int NG>
-__device__ __forceinline__ void load_q(WarpState<D, NG>& st, const T* qb, int G, int lane) {
+__device__ __forceinline__ void load_q_frags(uint32_t (&qf)[D / 16][NG][2], const T* qb, int G, int lane) {
 #pragma unroll
   for (int ng = 0; ng < NG; ++ng) {
     const int g = ng * 8 + (lane >> 2);
@@ -173,14 +178,19 @@ __device__ __forceinline__ void load_q(WarpState<D, NG>& st, const T* qb, int G,
     for (int kk = 0; kk < D / 16; ++kk) {
       const int d = kk * 16 + (lane & 3) * 2;
       if (g < G) {
-        st.qf[kk][ng][0] = __ldg(reinterpret_cast<const uint32_t*>(qb + g * D + d));
-        st.qf[kk][ng][1] = __ldg(reinterpret_cast<const uint32_t*>(qb + g * D + d + 8));
+        qf[kk][ng][0] = __ldg(reinterpret_cast<const uint32_t*>(qb + g * D + d));
+        qf[kk][ng][1] = __ldg(reinterpret_cast<const uint32_t*>(qb + g * D + d + 8));
       } else {
-        st.qf[kk][ng][0] = 0u;
-        st.qf[kk][ng][1] = 0u;
+        qf[kk][ng][0] = 0u;
+        qf[kk][ng][1] = 0u;
       }
     }
   }
+}
+
+template <typename T, int D, int NG>
+__device__ __forceinline__ void load_q(WarpState<D, NG>& st, const T* qb, int G, int lane) {
+  load_q_frags<T, D, NG>(st.qf, qb, G, lane);
 }
 
 template <int D, int NG>
@@ -337,16 +347,21 @@ struct MergeArea {
 // prefix of block counts in shared memory from seq_lens.
 // =========================================================================
 
+// Grid cap: an owner CTA combines up to kMaxSkCtas parts with one row index
+// and G <= 16 weights each, staged in the (idle) stage ring.
+constexpr int kMaxSkCtas = 640;
+
 template <typename T, int D, int BS, int NG, int NST>
 struct SkCfg {
   using TL = Tile<D, BS>;
   static constexpr int kStages = NST * TL::kStageBytes;
-  static constexpr int kMerge = MergeArea<D, NG>::kBytes;
+  static constexpr int kMerge = 2 * MergeArea<D, NG>::kBytes;  // double-buffered per segment
   static constexpr int kFixed = 1024 + kStages + kMerge + 2 * NST * 8;
-  static int smem_bytes(int B) { return kFixed + ((B + 1) * 4 + 15) / 16 * 16; }
+  static int smem_bytes(int B) { return kFixed + (2 * (B + 1) * 4 + 15) / 16 * 16; }
+  static_assert(kStages >= (kMaxSkCtas + 8) * 4, "owner merge part list must fit in the stage ring");
 };
 
-// cta_of(t): the CTA whose range [p*W/P, (p+1)*W/P) holds tile t.
+// cta_of(x): the CTA whose range [p*W/P, (p+1)*W/P) holds position x.
 __device__ __forceinline__ int sk_cta_of(int64_t t, int64_t W, int P) {
   return static_cast<int>(((t + 1) * P + W - 1) / W - 1);
 }
@@ -361,43 +376,56 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   static_assert(NST % kConsumers == 0, "stage s must always be drained by consumer s % kConsumers");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* Os = reinterpret_cast<float*>(smem + C::kStages);
-  float* Ms = Os + kConsumers * D * GP;
-  float* Ls = Ms + kConsumers * GP;
+  float* merge_base = reinterpret_cast<float*>(smem + C::kStages);
+  constexpr int kMergeFloats = MergeArea<D, NG>::kBytes / 4;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages + C::kMerge);
   uint64_t* empty = full + NST;
   int* CB = reinterpret_cast<int*>(empty + NST);  // CB[b] = sum_{b' < b} ceil(L_b' / BS)
 
   const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
+  int* CC = CB + (B + 1);  // CC[b] = sum_{b' < b} cost_b' (tiles + seg_cost, 0 if empty)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // ---- prefix of block counts over the batch (block-wide scan) ----
+  // ---- prefixes of block counts and costs over the batch (block-wide scans) ----
   {
     const int per = (B + kTcThreads - 1) / kTcThreads;
     const int beg = min(B, tid * per), end = min(B, beg + per);
-    int local = 0;
+    int local = 0, local_c = 0;
     for (int i = beg; i < end; ++i) {
       const int nb = (checked_len(p, i) + BS - 1) / BS;
       CB[i + 1] = nb;
       local += nb;
+      local_c += nb > 0 ? nb + p.seg_cost : 0;
     }
-    int incl = local;
+    int incl = local, incl_c = local_c;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += y;
+      const int yc = __shfl_up_sync(0xffffffffu, incl_c, off);
+      if (lane >= off) {
+        incl += y;
+        incl_c += yc;
+      }
     }
-    __shared__ int warp_tot[kConsumers + 1];
-    if (lane == 31) warp_tot[warp] = incl;
-    if (tid == 0) CB[0] = 0;
+    __shared__ int warp_tot[kConsumers + 1], warp_tot_c[kConsumers + 1];
+    if (lane == 31) {
+      warp_tot[warp] = incl;
+      warp_tot_c[warp] = incl_c;
+    }
+    if (tid == 0) CB[0] = CC[0] = 0;
     __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; ++w) base += warp_tot[w];
-    int run = base + incl - local;
+    int base = 0, base_c = 0;
+    for (int w = 0; w < warp; ++w) {
+      base += warp_tot[w];
+      base_c += warp_tot_c[w];
+    }
+    int run = base + incl - local, run_c = base_c + incl_c - local_c;
     for (int i = beg; i < end; ++i) {
       const int nb = CB[i + 1];
       run += nb;
+      run_c += nb > 0 ? nb + p.seg_cost : 0;
       CB[i + 1] = run;
+      CC[i + 1] = run_c;
     }
     if (tid == 0) {
       for (int s = 0; s < NST; ++s) {
@@ -408,12 +436,35 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     }
     __syncthreads();
   }
-  if (blockIdx.x == 0)
-    for (int i = tid; i <= B; i += kTcThreads) p.ws_cb[i] = CB[i];
+  // sequences with no tokens get zero rows (no tile covers them)
+  for (int bz = blockIdx.x; bz < B; bz += gridDim.x)
+    if (CB[bz + 1] == CB[bz]) {
+      T* o = static_cast<T*>(p.out) + static_cast<int64_t>(bz) * p.num_heads * D;
+      for (int i = tid; i < p.num_heads * D; i += kTcThreads) o[i] = DType<T>::from_float(0.f);
+    }
 
+  // CTA ranges are drawn in cost space, where unit (b, kvh) occupies
+  // seg_cost virtual positions followed by its ceil(L_b / BS) tiles, so a
+  // CTA whose range holds many short units (each paying a merge) gets fewer
+  // tiles.  Tile range of CTA p: the tiles whose positions fall in
+  // [p * Wc / P, (p + 1) * Wc / P).
   const int64_t W = static_cast<int64_t>(Hkv) * CB[B];
+  const int64_t Wc = static_cast<int64_t>(Hkv) * CC[B];
   const int P = gridDim.x, pid = blockIdx.x;
-  const int64_t t0 = static_cast<int64_t>(pid) * W / P, t1 = static_cast<int64_t>(pid + 1) * W / P;
+  auto tiles_before = [&](int64_t x) -> int64_t {  // tiles at cost positions < x
+    if (x >= Wc) return W;
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (static_cast<int64_t>(Hkv) * CC[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    const int cs = CC[lo + 1] - CC[lo], nb = CB[lo + 1] - CB[lo];
+    const int64_t rel = x - static_cast<int64_t>(Hkv) * CC[lo];
+    const int kvh = static_cast<int>(rel / cs), r = static_cast<int>(rel % cs);
+    return static_cast<int64_t>(Hkv) * CB[lo] + static_cast<int64_t>(kvh) * nb + max(0, r - p.seg_cost);
+  };
+  const int64_t t0 = tiles_before(static_cast<int64_t>(pid) * Wc / P);
+  const int64_t t1 = tiles_before(static_cast<int64_t>(pid + 1) * Wc / P);
   if (t0 >= t1) return;
   const int n = static_cast<int>(t1 - t0);
 
@@ -454,14 +505,39 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       prefetch_tensormap(&tmV);
     }
     Cursor c{b0, rel0 / nb0, rel0 % nb0, nb0};
+    // Block-table entries are fetched 32 at a time (one per lane) and the
+    // chunk the walk needs next is fetched while the current one is used.
+    auto fetch = [&](int b, int chunk, int nb) -> int {
+      const int e = (chunk << 5) + lane;
+      return e < nb ? __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq + e) : 0;
+    };
     int cache_b = -1, cache_chunk = -1, mine = 0;
+    int next_b = -1, next_chunk = -1, nxt = 0;
     int ok = 1, issued = 0;
     for (int j = 0; j < n && ok; ++j) {
       if (c.b != cache_b || (c.blk >> 5) != cache_chunk) {
+        mine = (c.b == next_b && (c.blk >> 5) == next_chunk) ? nxt : fetch(c.b, c.blk >> 5, c.nb);
         cache_b = c.b;
         cache_chunk = c.blk >> 5;
-        const int e = (cache_chunk << 5) + lane;
-        mine = e < c.nb ? __ldg(p.block_tables + static_cast<int64_t>(c.b) * p.max_blocks_per_seq + e) : 0;
+        // the chunk after this one in walk order: next chunk of the row, the
+        // row's first chunk again for the next kv head, or the next sequence
+        int nbk = c.b, nck = cache_chunk + 1, nnb = c.nb;
+        if (nck * 32 >= c.nb) {
+          nck = 0;
+          if (c.kvh + 1 >= Hkv) {
+            do {
+              ++nbk;
+            } while (nbk < B && CB[nbk + 1] == CB[nbk]);
+            nnb = nbk < B ? CB[nbk + 1] - CB[nbk] : 0;
+          }
+        }
+        if (nbk < B && !(nbk == cache_b && nck == cache_chunk)) {
+          nxt = fetch(nbk, nck, nnb);
+          next_b = nbk;
+          next_chunk = nck;
+        } else {
+          next_b = -1;
+        }
       }
       int pb = __shfl_sync(0xffffffffu, mine, c.blk & 31);
       if (lane == 0) {
@@ -503,9 +579,28 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   int ok = 1;
   int64_t unit_start = static_cast<int64_t>(Hkv) * CB[c.b] + static_cast<int64_t>(c.kvh) * c.nb;
   int L = checked_len(p, c.b);
-  load_q<T, D, NG>(st, static_cast<const T*>(p.q) + (static_cast<int64_t>(c.b) * p.num_heads + c.kvh * G) * D,
-                   G, lane);
+  auto q_of = [&](const Cursor& u) {
+    return static_cast<const T*>(p.q) + (static_cast<int64_t>(u.b) * p.num_heads + u.kvh * G) * D;
+  };
+  // The next unit's Q fragments are loaded one segment ahead, so a unit
+  // boundary does not stall on a cold global load (skipped where the extra
+  // registers would not fit).
+  constexpr bool kPrefetchQ = (D / 16) * NG * 2 <= 16;
+  uint32_t qn[D / 16][NG][2];
+  auto prefetch_next = [&](const Cursor& u, int64_t u_start) {
+    if (kPrefetchQ && u_start + u.nb < t1) {
+      Cursor nx = u;
+      nx.blk = nx.nb - 1;
+      advance(nx);
+      load_q_frags<T, D, NG>(qn, q_of(nx), G, lane);
+    }
+  };
+  load_q<T, D, NG>(st, q_of(c), G, lane);
+  prefetch_next(c, unit_start);
   reset_state(st);
+  int seg = 0;
+  bool owner = false;
+  int own_nb = 0, own_b = 0, own_kvh = 0;
   for (int j = 0; j < n; ++j) {
     if (ok && (j & (kConsumers - 1)) == cw) {
       const int s = j % NST;
@@ -525,6 +620,13 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       const int64_t unit_end = unit_start + c.nb;
       const bool whole = unit_start >= t0 && unit_end <= t1;
       const int slot = unit_start < t0 ? 0 : 1;
+      // Two merge buffers alternate between segments: the one barrier below
+      // also guarantees that every thread has finished reading the buffer
+      // of the segment before, which the next segment will overwrite.
+      float* Os = merge_base + (seg & 1) * kMergeFloats;
+      float* Ms = Os + kConsumers * D * GP;
+      float* Ls = Ms + kConsumers * GP;
+      ++seg;
       store_state(st, Os, Ms, Ls, cw, lane);
       named_barrier_sync(1, kConsumers * 32);
       for (int idx = ctid; idx < G * D; idx += kConsumers * 32) {
@@ -555,68 +657,107 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           }
         }
       }
-      named_barrier_sync(1, kConsumers * 32);
+      if (!whole && slot == 0) {
+        // publish the partial of a unit that started in an earlier CTA: all
+        // consumer threads' stores precede the release of the flag
+        named_barrier_sync(1, kConsumers * 32);
+        if (ctid == 0) {
+          __threadfence();
+          st_release_gpu(p.ws_flags + pid, p.epoch);
+        }
+      }
+      if (j == n - 1 && !whole && slot == 1) {
+        owner = true;  // the unit continues in later CTAs: this CTA combines it
+        own_nb = c.nb;
+        own_b = c.b;
+        own_kvh = c.kvh;
+      }
       if (j + 1 < n) {
         advance(c);
         unit_start = static_cast<int64_t>(Hkv) * CB[c.b] + static_cast<int64_t>(c.kvh) * c.nb;
         L = checked_len(p, c.b);
-        load_q<T, D, NG>(st,
-                         static_cast<const T*>(p.q) + (static_cast<int64_t>(c.b) * p.num_heads + c.kvh * G) * D,
-                         G, lane);
+        if constexpr (kPrefetchQ) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+            for (int ng = 0; ng < NG; ++ng) {
+              st.qf[kk][ng][0] = qn[kk][ng][0];
+              st.qf[kk][ng][1] = qn[kk][ng][1];
+            }
+          prefetch_next(c, unit_start);
+        } else {
+          load_q<T, D, NG>(st, q_of(c), G, lane);
+        }
         reset_state(st);
       }
     } else {
       advance(c);
     }
   }
-}
+  if (!owner) return;
 
-// Combine the partials of units cut by CTA range boundaries: one warp per
-// (sequence, query head).  Units finished inside one CTA were written by
-// the attention kernel; empty sequences get a zero row here.
-template <typename T>
-__global__ void __launch_bounds__(128) sk_merge_kernel(const DecodeParams p) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * 4 + warp;
-  if (idx >= static_cast<int64_t>(p.num_seqs) * p.num_heads) return;
-  const int b = static_cast<int>(idx / p.num_heads), qh = static_cast<int>(idx % p.num_heads);
-  const int G = p.group, kvh = qh / G, g = qh % G, D = p.head_dim, Hkv = p.num_kv_heads;
-  const int* CB = p.ws_cb;
-  const int nb = CB[b + 1] - CB[b];
-  T* o = static_cast<T*>(p.out) + idx * D;
-  if (nb == 0) {
-    for (int d = lane; d < D; d += 32) o[d] = DType<T>::from_float(0.f);
-    return;
-  }
-  const int64_t W = static_cast<int64_t>(Hkv) * CB[p.num_seqs];
-  const int P = p.num_ctas;
-  const int64_t ub = static_cast<int64_t>(Hkv) * CB[b] + static_cast<int64_t>(kvh) * nb, ue = ub + nb;
-  const int pf = sk_cta_of(ub, W, P), pl = sk_cta_of(ue - 1, W, P);
-  if (pf == pl) return;
-  // CTAs with an empty range (possible when W < P) wrote nothing: skip them
-  auto row_of = [&](int q) -> int64_t {
-    const int64_t q0 = static_cast<int64_t>(q) * W / P, q1 = static_cast<int64_t>(q + 1) * W / P;
-    if (q0 == q1) return -1;
-    return (static_cast<int64_t>(q) * 2 + (ub < q0 ? 0 : 1)) * G + g;
-  };
-  float mx = -INFINITY;
-  for (int q = pf; q <= pl; ++q) {
-    const int64_t r = row_of(q);
-    if (r >= 0) mx = fmaxf(mx, p.ws_ml[r * 2]);
-  }
-  float den = 0.f;
-  for (int q = pf; q <= pl; ++q) {
-    const int64_t r = row_of(q);
-    if (r >= 0) den += fast_exp2(p.ws_ml[r * 2] - mx) * p.ws_ml[r * 2 + 1];
-  }
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  for (int d = lane; d < D; d += 32) {
-    float num = 0.f;
-    for (int q = pf; q <= pl; ++q) {
-      const int64_t r = row_of(q);
-      if (r >= 0) num += fast_exp2(p.ws_ml[r * 2] - mx) * p.ws_o[r * D + d];
+  // ---- this CTA holds the first part of a unit that later CTAs continue:
+  // wait for their slot-0 partials and write the unit's output ----
+  named_barrier_sync(1, kConsumers * 32);  // own slot-1 partial stored
+  // cost position of the unit's last tile -> the last CTA holding part of it
+  const int own_cs = CC[own_b + 1] - CC[own_b];
+  const int64_t last_pos = static_cast<int64_t>(Hkv) * CC[own_b] + static_cast<int64_t>(own_kvh) * own_cs +
+                           p.seg_cost + own_nb - 1;
+  const int last = sk_cta_of(last_pos, Wc, P);
+  // CTAs between this one and `last` with a non-empty cost range lie inside
+  // the unit's tiles, so each of them holds a part of it.
+  const int nparts = last - pid + 1;
+  const int npad = (nparts + 7) & ~7;  // padded to the 8-part batches below
+  // the stage ring is idle now: every issued tile has been consumed
+  int* part_row = reinterpret_cast<int*>(smem);  // [npad]: row base (cta * 2 + slot) * G, or -1
+  if (cw == 0) {
+    // every wait points at a later CTA of the same (co-resident) grid, and
+    // those publish before they wait on anyone: no cycle
+    for (int q = pid + 1 + lane; q <= last; q += 32) {
+      const int64_t q0 = static_cast<int64_t>(q) * Wc / P, q1 = static_cast<int64_t>(q + 1) * Wc / P;
+      if (q0 != q1) wait_flag_bounded(p.ws_flags + q, p.epoch);
     }
-    o[d] = DType<T>::from_float(num * inv);
+  } else {
+    for (int k = ctid - 32; k < npad; k += (kConsumers - 1) * 32) {
+      const int q = pid + k;
+      int row = -1;
+      if (k == 0) {
+        row = (pid * 2 + 1) * G;
+      } else if (k < nparts) {
+        const int64_t q0 = static_cast<int64_t>(q) * Wc / P, q1 = static_cast<int64_t>(q + 1) * Wc / P;
+        row = q0 == q1 ? -1 : q * 2 * G;
+      }
+      part_row[k] = row;
+    }
+  }
+  named_barrier_sync(1, kConsumers * 32);
+  // Each output combines all parts by an online log-sum-exp over batches of
+  // 8 parts; a batch's (m, l, acc) loads are all issued before any is used.
+  T* o = static_cast<T*>(p.out) + (static_cast<int64_t>(own_b) * p.num_heads + own_kvh * G) * D;
+  for (int idx = ctid; idx < G * D; idx += kConsumers * 32) {
+    const int g = idx / D, d = idx - g * D;
+    float mx = -INFINITY, num = 0.f, den = 0.f;
+    for (int k0 = 0; k0 < npad; k0 += 8) {
+      float mk[8], lk[8], ok8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int rb = part_row[k0 + u];
+        const int64_t r = rb + g;
+        mk[u] = rb >= 0 ? p.ws_ml[r * 2] : -INFINITY;
+        lk[u] = rb >= 0 ? p.ws_ml[r * 2 + 1] : 0.f;
+        ok8[u] = rb >= 0 ? p.ws_o[r * D + d] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (mk[u] == -INFINITY) continue;
+        const float nm = fmaxf(mx, mk[u]);
+        const float so = fast_exp2(mx - nm), sn = fast_exp2(mk[u] - nm);
+        num = num * so + sn * ok8[u];
+        den = den * so + sn * lk[u];
+        mx = nm;
+      }
+    }
+    o[idx] = DType<T>::from_float(den > 0.f ? num / den : 0.f);
   }
 }
 
@@ -917,6 +1058,25 @@ struct Plan {
 
 constexpr int kMaxSkCtasPerSm = 4;
 
+// Tiles' worth of time one unit boundary costs a stream-K CTA (cross-warp
+// merge, output or partial write): about 64 KB of streaming, measured on
+// GB300 over the 4-16 KB stage sizes (the sweep was flat within 1-2x).
+int seg_cost_tiles(int stage_bytes) { return std::max(1, 65536 / stage_bytes); }
+
+// Tag of one stream-K call: a per-process random base plus a call counter,
+// so a ready flag left by any other call (or uninitialised workspace) does
+// not match.
+uint64_t next_epoch() {
+  static std::atomic<uint64_t> counter{0};
+  static const uint64_t base = [] {
+    std::random_device rd;
+    uint64_t x = (static_cast<uint64_t>(rd()) << 32) ^ rd();
+    x ^= static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count()) * 0x9E3779B97F4A7C15ull;
+    return x;
+  }();
+  return base + 2 * (counter.fetch_add(1) + 1);
+}
+
 int sm_count() {
   static int cached[64] = {0};
   int dev = 0;
@@ -944,12 +1104,13 @@ Plan make_plan(int B, int Hq, int Hkv, int D, int BS, int64_t max_seq_len, int b
   if (tc_supported(dtype, D, BS, G) && bps_req == 0 && B <= kMaxSkSeqs) {
     pl.kind = kTensorCoreStreamK;
     const int64_t w_upper = std::max<int64_t>(1, static_cast<int64_t>(B) * Hkv * maxblk);
-    pl.num_ctas = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(sm_count()) * kMaxSkCtasPerSm, w_upper));
+    pl.num_ctas = static_cast<int>(std::min<int64_t>(
+        std::min<int64_t>(static_cast<int64_t>(sm_count()) * kMaxSkCtasPerSm, kMaxSkCtas), w_upper));
     pl.bps = static_cast<int>(maxblk);
     pl.num_splits = 1;
     const size_t rows = static_cast<size_t>(pl.num_ctas) * 2 * G;
     pl.ws_bytes = align256(rows * D * sizeof(float)) + align256(rows * 2 * sizeof(float)) +
-                  align256((static_cast<size_t>(B) + 1) * sizeof(int32_t));
+                  align256(static_cast<size_t>(pl.num_ctas) * sizeof(uint64_t));
     return pl;
   }
   pl.kind = tc_supported(dtype, D, BS, G) ? kTensorCoreSplit : kSimt;
@@ -1083,14 +1244,23 @@ cudaError_t launch_sk(DecodeParams& p, const CUtensorMap& mk, const CUtensorMap&
     occ_cache[dev][0] = smem;
     occ_cache[dev][1] = std::max(1, std::min(occ, kMaxSkCtasPerSm));
   }
-  const int ctas = std::min(max_ctas, sm_count() * occ_cache[dev][1]);
+  const int ctas = std::min({max_ctas, sm_count() * occ_cache[dev][1], kMaxSkCtas});
   p.num_ctas = ctas;
-  kern<<<ctas, kTcThreads, smem, st>>>(p, mk, mv);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.num_heads;
-  sk_merge_kernel<T><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, st>>>(p);
-  return cudaGetLastError();
+  p.epoch = next_epoch();
+  p.seg_cost = seg_cost_tiles(Tile<D, BS>::kStageBytes);
+  // Cooperative: the driver refuses the launch unless all CTAs can be
+  // resident at once, which the owners' waits on later CTAs rely on.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p, mk, mv);
 }
 
 template <typename T, int D, int BS, int NG>
@@ -1256,8 +1426,8 @@ extern "C" int paged_decode_attention(void* out, const void* q, const void* k_ca
     const size_t rows = static_cast<size_t>(pl.num_ctas) * 2 * p.group;
     p.ws_o = reinterpret_cast<float*>(ws);
     p.ws_ml = reinterpret_cast<float*>(ws + align256(rows * head_dim * sizeof(float)));
-    p.ws_cb = reinterpret_cast<int32_t*>(ws + align256(rows * head_dim * sizeof(float)) +
-                                         align256(rows * 2 * sizeof(float)));
+    p.ws_flags = reinterpret_cast<uint64_t*>(ws + align256(rows * head_dim * sizeof(float)) +
+                                             align256(rows * 2 * sizeof(float)));
   } else {
     p.blocks_per_split = pl.bps;
     p.num_splits = pl.num_splits;

@@ -68,8 +68,9 @@ class DecodePlan:
 
     @property
     def launches(self) -> int:
-        """Kernels one attention call launches (attention, then merge if any)."""
-        return 2 if (self.kernel == 2 or self.num_splits > 1) else 1
+        """Kernels one attention call launches: the split kernels add a merge
+        kernel when a sequence spans several splits; stream-K merges inside."""
+        return 2 if (self.kernel != 2 and self.num_splits > 1) else 1
 
 
 def decode_plan(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
