@@ -245,6 +245,34 @@ int paged_decode_attention(void* out, const void* q, const void* k_cache, const 
                            int32_t blocks_per_split, int dtype, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/* paged_decode_attention without a workspace argument, for callers that
+ * cannot allocate device memory themselves (their GPU memory belongs to
+ * another allocator, or allocation is forbidden or too slow where they run).
+ * The pages have no counterpart: this is a deployment convenience.
+ * Scratch comes from one fixed array the library defines in device memory,
+ * paged_decode_static_scratch_bytes() bytes (8 MiB), which every GPU that
+ * loads the library holds until the process exits.  The call allocates
+ * nothing.  Its first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, synchronous) with that device current: make that
+ * first call before any stream capture.  Sizes whose workspace
+ * (paged_decode_workspace_size) exceeds the array return KV_ERR_WORKSPACE
+ * and launch nothing.  All calls on a device share the array: calls that
+ * overlap on the GPU (other streams, other threads) race; order them on one
+ * stream.  Nothing in it needs clearing between calls.  Other arguments,
+ * results and errors are those of paged_decode_attention. */
+int paged_decode_attention_static_scratch(void* out, const void* q, const void* k_cache,
+                                          const void* v_cache, const int32_t* block_tables,
+                                          const int32_t* seq_lens, int32_t num_seqs,
+                                          int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                          int32_t block_size, int64_t num_blocks,
+                                          int32_t max_blocks_per_seq, int64_t max_seq_len,
+                                          float scale, int32_t blocks_per_split, int dtype,
+                                          void* stream);
+
+/* Size in bytes of the fixed scratch array behind
+ * paged_decode_attention_static_scratch. */
+size_t paged_decode_static_scratch_bytes(void);
+
 /* Read (and, if reset != 0, clear) the device error word of the current
  * device: *status_out = KV_OK or the first KV_ERR_DEVICE_* code recorded by
  * a kernel since the last reset.  Synchronises the current device. */

@@ -67,6 +67,10 @@ SIGNATURES = {
     "paged_decode_attention": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
                                        c_int32, c_int32, c_int32, c_int32, c_int64, c_int32, c_int64, c_float,
                                        c_int32, c_int, c_void_p, c_size_t, c_void_p]),
+    "paged_decode_attention_static_scratch": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                                      c_int32, c_int32, c_int32, c_int32, c_int32, c_int64,
+                                                      c_int32, c_int64, c_float, c_int32, c_int, c_void_p]),
+    "paged_decode_static_scratch_bytes": (c_size_t, []),
     "kv_device_error": (c_int, [c_int, POINTER(c_int)]),
     "kv_last_cuda_error": (c_char_p, []),
     "kv_version": (c_char_p, []),

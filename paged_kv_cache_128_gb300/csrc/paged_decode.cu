@@ -1452,6 +1452,68 @@ extern "C" int paged_decode_attention(void* out, const void* q, const void* k_ca
   return cuda_status(e);
 }
 
+// ---------------------------------------------------------------------------
+// Decode attention for callers that cannot allocate device memory.
+//
+// Some callers may not call cudaMalloc at all: a host process whose GPU memory
+// is owned by another allocator (a framework caching allocator or a serving
+// runtime that reserves nearly all HBM up front), a plugin interface that
+// forbids allocation while it executes, or a latency-critical loop where an
+// allocation could synchronise the device.  paged_decode_attention needs a
+// caller-provided workspace; this variant instead uses one fixed scratch array
+// in device memory that the library defines at file scope, so the call itself
+// allocates nothing.
+//
+// The array is a static __device__ object of kStaticScratchBytes: every GPU
+// that loads this library holds it until the process exits.  In host code its
+// name is only a host-side stand-in, so the device address is looked up once
+// per device (cudaGetSymbolAddress, with that device current) on the first
+// call made on it.  All calls on a device share the array and it keeps the
+// last call's contents; the kernels write every scratch value they read in the
+// same call (the stream-K ready flags carry a per-call tag), so nothing needs
+// clearing between calls, but calls that overlap on the GPU race on it.
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+namespace {
+void* static_scratch_address(int dev, cudaError_t* err) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    *err = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    addr[dev] = ptr;
+  }
+  *err = cudaSuccess;
+  return addr[dev];
+}
+}  // namespace
+
+extern "C" int paged_decode_attention_static_scratch(
+    void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq, int64_t max_seq_len, float scale,
+    int32_t blocks_per_split, int dtype, void* stream) {
+  size_t need = 0;
+  int st = paged_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_seq_len,
+                                       blocks_per_split, dtype, &need);
+  if (st != KV_OK) return st;
+  if (need > kStaticScratchBytes) return KV_ERR_WORKSPACE;  // beyond the fixed scratch: use the workspace call
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (dev < 0 || dev >= 64) return KV_ERR_INVALID_ARG;
+  void* scratch = static_scratch_address(dev, &e);
+  if (!scratch) return cuda_status(e, "cudaGetSymbolAddress of the decode scratch failed");
+  return paged_decode_attention(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads, num_kv_heads,
+                                head_dim, block_size, num_blocks, max_blocks_per_seq, max_seq_len, scale,
+                                blocks_per_split, dtype, scratch, kStaticScratchBytes, stream);
+}
+
+extern "C" size_t paged_decode_static_scratch_bytes(void) { return kStaticScratchBytes; }
+
 extern "C" int kv_device_error(int reset, int* status_out) {
   if (!status_out) return KV_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return KV_ERR_CUDA;

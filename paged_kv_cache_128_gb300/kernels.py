@@ -132,3 +132,39 @@ def device_error(reset: bool = True) -> int:
     st = ctypes.c_int()
     check(lib().kv_device_error(1 if reset else 0, ctypes.byref(st)), "kv_device_error")
     return st.value
+
+
+def paged_decode_attention_static_scratch(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                                          v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                          seq_lens: torch.Tensor, scale: float, max_seq_len: int,
+                                          blocks_per_split: int = 0,
+                                          stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """``paged_decode_attention`` for callers that must not allocate device
+    memory: the library's fixed scratch array stands in for the workspace
+    (see include/pagedkv.h).  Nothing is allocated here either.  Raises
+    KVError(WORKSPACE) when these sizes need more scratch than the array."""
+    for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (block_tables, "block_tables"), (seq_lens, "seq_lens")):
+        _cuda(t, n)
+    if not (q.is_contiguous() and out.is_contiguous() and k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise KVError(1, "q, out and caches must be contiguous")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32 or not block_tables.is_contiguous() \
+            or not seq_lens.is_contiguous():
+        raise KVError(1, "block_tables and seq_lens must be contiguous int32")
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if d2 != d or out.shape != q.shape or v_cache.shape != k_cache.shape or out.dtype != q.dtype \
+            or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise KVError(1, "shape or dtype mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or seq_lens.numel() != B:
+        raise KVError(1, "block_tables must be [B, max_blocks] and seq_lens [B]")
+    check(lib().paged_decode_attention_static_scratch(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        seq_lens.data_ptr(), B, hq, hkv, d, bs, nb, block_tables.shape[1], max_seq_len, float(scale),
+        blocks_per_split, dtype_code(q.dtype), _stream_ptr(stream)), "paged_decode_attention_static_scratch")
+    return out
+
+
+def static_scratch_bytes() -> int:
+    """Size of the fixed scratch array behind the no-allocation decode call."""
+    return int(lib().paged_decode_static_scratch_bytes())
