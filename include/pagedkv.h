@@ -112,6 +112,25 @@ int kvbm_can_append_slots(kvbm_t h, const int64_t* seq_ids, int64_t n, int* ok);
 int kvbm_decode_step(kvbm_t h, const int64_t* seq_ids, int64_t n, int64_t max_blocks,
                      int32_t* slots_out, int32_t* block_tables, int32_t* seq_lens);
 
+/* One serving step's host metadata in a single call ("从零实现一个 mini vLLM:
+ * Block Manager", section on the ModelRunner: slot mapping, block tables and
+ * context lengths built from the manager's state):
+ *   1. release free_ids (e.g. the previous step's finished sequences);
+ *   2. prefill-allocate each new sequence prefill_ids[i] of prefill_lens[i]
+ *      tokens, as kvbm_allocate_for_prefill;
+ *   3. append one decode slot to each of decode_ids;
+ *   4. write slot_mapping[n_slots], n_slots = sum(prefill_lens) + n_decode +
+ *      n_pad: the prefill slots in order, then the decode slots, with -1 at
+ *      the strictly increasing positions pad_positions[n_pad];
+ *   5. export the decode sequences' tables and lengths as kvbm_export.
+ * Steps 2-3 are all or nothing: everything is validated (ids, lengths,
+ * padding, free blocks) before any allocation, so on an error only the
+ * releases of step 1 have happened.  Outputs are nullable. */
+int kvbm_prepare_step(kvbm_t h, const int64_t* free_ids, int64_t n_free, const int64_t* prefill_ids,
+                      const int64_t* prefill_lens, int64_t n_prefill, const int64_t* decode_ids,
+                      int64_t n_decode, const int64_t* pad_positions, int64_t n_pad, int64_t max_blocks,
+                      int32_t* slot_mapping, int32_t* block_tables, int32_t* seq_lens);
+
 /* Release every block of seq_id once (MiniPaged-Qwen §5.3).  The table is
  * validated first; a corrupt table gives KV_ERR_INVARIANT and changes
  * nothing.  KV_ERR_DOUBLE_FREE for an id already released (and not

@@ -47,6 +47,8 @@ SIGNATURES = {
     "kvbm_append_slots": (c_int, [c_void_p, c_int64, c_int64, P32]),
     "kvbm_can_append_slots": (c_int, [c_void_p, P64, c_int64, POINTER(c_int)]),
     "kvbm_decode_step": (c_int, [c_void_p, P64, c_int64, c_int64, P32, P32, P32]),
+    "kvbm_prepare_step": (c_int, [c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_int64, c_void_p, c_int64,
+                                  c_void_p, c_int64, c_int64, c_void_p, c_void_p, c_void_p]),
     "kvbm_free_sequence": (c_int, [c_void_p, c_int64]),
     "kvbm_num_free_blocks": (c_int, [c_void_p, P64]),
     "kvbm_get_free_list": (c_int, [c_void_p, P32, c_int64, P64]),

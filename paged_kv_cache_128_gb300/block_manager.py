@@ -102,6 +102,28 @@ class KVBlockManager:
                                          _i32(lens)), "kvbm_decode_step")
         return slots, tables, lens
 
+    def prepare_step(self, free_ids, prefill_ids, prefill_lens, decode_ids, pad_positions, max_blocks: int,
+                     slots_out: Optional[np.ndarray] = None, tables_out: Optional[np.ndarray] = None,
+                     lens_out: Optional[np.ndarray] = None):
+        """One step's metadata in one native call (kvbm_prepare_step):
+        release ``free_ids``, prefill-allocate ``prefill_ids``/``prefill_lens``,
+        append one slot to each of ``decode_ids``, and return (slot mapping
+        with -1 at ``pad_positions``, decode block tables, decode seq_lens)."""
+        fr, pi, pl, di, pp = (_ids(x) for x in (free_ids, prefill_ids, prefill_lens, decode_ids, pad_positions))
+        n_slots = int(pl.sum()) + di.size + pp.size
+        slots = slots_out if slots_out is not None else np.empty(n_slots, dtype=np.int32)
+        tables = tables_out if tables_out is not None else np.empty((di.size, max_blocks), dtype=np.int32)
+        lens = lens_out if lens_out is not None else np.empty(di.size, dtype=np.int32)
+        check(self._lib.kvbm_prepare_step(self._h, fr.ctypes.data, fr.size, pi.ctypes.data, pl.ctypes.data, pi.size,
+                                          di.ctypes.data, di.size, pp.ctypes.data, pp.size, max_blocks,
+                                          slots.ctypes.data, tables.ctypes.data, lens.ctypes.data),
+              "kvbm_prepare_step")
+        return slots, tables, lens
+
+    def prepare_step_raw(self, *args) -> int:
+        """kvbm_prepare_step with pre-computed buffer addresses (hot loops)."""
+        return self._lib.kvbm_prepare_step(self._h, *args)
+
     def free_sequence(self, seq_id: int) -> None:
         check(self._lib.kvbm_free_sequence(self._h, seq_id), "kvbm_free_sequence")
 

@@ -277,6 +277,84 @@ int kvbm_decode_step(kvbm_t h, const int64_t* seq_ids, int64_t n, int64_t max_bl
   });
 }
 
+int kvbm_prepare_step(kvbm_t h, const int64_t* free_ids, int64_t n_free, const int64_t* prefill_ids,
+                      const int64_t* prefill_lens, int64_t n_prefill, const int64_t* decode_ids, int64_t n_decode,
+                      const int64_t* pad_positions, int64_t n_pad, int64_t max_blocks, int32_t* slot_mapping,
+                      int32_t* block_tables, int32_t* seq_lens) {
+  if (!h || n_free < 0 || n_prefill < 0 || n_decode < 0 || n_pad < 0 || max_blocks < 0) return KV_ERR_INVALID_ARG;
+  if ((n_free && !free_ids) || (n_prefill && (!prefill_ids || !prefill_lens)) || (n_decode && !decode_ids) ||
+      (n_pad && !pad_positions))
+    return KV_ERR_INVALID_ARG;
+  return guarded([&] {
+    // 1. releases: validate all, then release all
+    for (int64_t i = 0; i < n_free; ++i) {
+      if (!h->seqs.count(free_ids[i]))
+        return static_cast<int>(h->released.count(free_ids[i]) ? KV_ERR_DOUBLE_FREE : KV_ERR_UNKNOWN_SEQ);
+      for (int64_t k = 0; k < i; ++k)
+        if (free_ids[k] == free_ids[i]) return static_cast<int>(KV_ERR_DOUBLE_FREE);
+    }
+    for (int64_t i = 0; i < n_free; ++i) {
+      int st = kvbm_free_sequence(h, free_ids[i]);
+      if (st != KV_OK) return st;
+    }
+    // 2-3. validate the prefills and appends and their block need, before any change
+    std::unordered_set<int64_t> seen;
+    int64_t n_prefill_tokens = 0, need = 0;
+    for (int64_t i = 0; i < n_prefill; ++i) {
+      if (prefill_ids[i] < 0 || prefill_lens[i] <= 0) return static_cast<int>(KV_ERR_INVALID_ARG);
+      if (h->seqs.count(prefill_ids[i])) return static_cast<int>(KV_ERR_DUPLICATE_SEQ);
+      if (!seen.insert(prefill_ids[i]).second) return static_cast<int>(KV_ERR_DUPLICATE_SEQ);
+      n_prefill_tokens += prefill_lens[i];
+      need += ceil_div(prefill_lens[i], h->block_size);
+    }
+    std::vector<Sequence*> dec(static_cast<size_t>(n_decode));
+    for (int64_t i = 0; i < n_decode; ++i) {
+      Sequence* sq = h->find(decode_ids[i]);
+      if (!sq) return static_cast<int>(seen.count(decode_ids[i]) ? KV_ERR_INVALID_ARG : KV_ERR_UNKNOWN_SEQ);
+      if (!seen.insert(decode_ids[i]).second) return static_cast<int>(KV_ERR_INVALID_ARG);
+      const int64_t grow = h->blocks_needed(*sq, 1);
+      if ((block_tables || seq_lens) && static_cast<int64_t>(sq->table.size()) + grow > max_blocks)
+        return static_cast<int>(KV_ERR_INVALID_ARG);
+      need += grow;
+      dec[static_cast<size_t>(i)] = sq;
+    }
+    const int64_t n_slots = n_prefill_tokens + n_decode + n_pad;
+    for (int64_t i = 0; i < n_pad; ++i)
+      if (pad_positions[i] < 0 || pad_positions[i] >= n_slots || (i && pad_positions[i] <= pad_positions[i - 1]))
+        return static_cast<int>(KV_ERR_INVALID_ARG);
+    if (need > h->free_list.size()) return static_cast<int>(KV_ERR_OOM);
+    // 4. perform: prefills, then appends, writing slots around the padding
+    int64_t pos = 0, pad = 0;
+    auto put = [&](int32_t slot) {
+      while (pad < n_pad && pad_positions[pad] == pos) {
+        if (slot_mapping) slot_mapping[pos] = -1;
+        ++pos;
+        ++pad;
+      }
+      if (slot_mapping) slot_mapping[pos] = slot;
+      ++pos;
+    };
+    for (int64_t i = 0; i < n_prefill; ++i) {
+      Sequence sq;
+      const int64_t nb = ceil_div(prefill_lens[i], h->block_size);
+      sq.table.reserve(static_cast<size_t>(nb));
+      for (int64_t k = 0; k < nb; ++k) sq.table.push_back(h->take_front());
+      sq.length = prefill_lens[i];
+      for (int64_t t = 0; t < prefill_lens[i]; ++t) put(h->slot_of(sq, t));
+      h->seqs.emplace(prefill_ids[i], std::move(sq));
+      h->released.erase(prefill_ids[i]);
+    }
+    for (int64_t i = 0; i < n_decode; ++i) put(h->append_one(*dec[static_cast<size_t>(i)]));
+    while (pad < n_pad) {  // trailing padding
+      if (slot_mapping) slot_mapping[pos] = -1;
+      ++pos;
+      ++pad;
+    }
+    if (block_tables || seq_lens) return kvbm_export(h, decode_ids, n_decode, max_blocks, block_tables, seq_lens);
+    return static_cast<int>(KV_OK);
+  });
+}
+
 int kvbm_free_sequence(kvbm_t h, int64_t seq_id) {
   if (!h) return KV_ERR_INVALID_ARG;
   auto it = h->seqs.find(seq_id);

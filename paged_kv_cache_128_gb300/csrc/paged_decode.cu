@@ -713,9 +713,15 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   if (cw == 0) {
     // every wait points at a later CTA of the same (co-resident) grid, and
     // those publish before they wait on anyone: no cycle
+    // Each flag has exactly this one reader, which clears it once seen, so
+    // flags are zero between calls even when a replayed launch reuses its
+    // epoch.
     for (int q = pid + 1 + lane; q <= last; q += 32) {
       const int64_t q0 = static_cast<int64_t>(q) * Wc / P, q1 = static_cast<int64_t>(q + 1) * Wc / P;
-      if (q0 != q1) wait_flag_bounded(p.ws_flags + q, p.epoch);
+      if (q0 != q1) {
+        wait_flag_bounded(p.ws_flags + q, p.epoch);
+        p.ws_flags[q] = 0;
+      }
     }
   } else {
     for (int k = ctid - 32; k < npad; k += (kConsumers - 1) * 32) {

@@ -19,11 +19,12 @@ tests and the benchmark exercise exactly one code path.
 
 from __future__ import annotations
 
-from typing import List, Optional
+from typing import Optional
 
 import numpy as np
 import torch
 
+from ._lib import check
 from .block_manager import KVBlockManager
 from .inputs import Values, Workload, pad_positions, sentinel_bits
 from .kernels import alloc_workspace, decode_plan, paged_decode_attention, reshape_and_cache
@@ -59,13 +60,19 @@ class PagedDecodeEngine:
                                 dt, blocks_per_split)
         self.workspace = alloc_workspace(self.plan, self.device)
         n_step = wl.num_step_tokens
-        pin = dict(pin_memory=True)
-        self.h_slots = torch.empty(n_step, dtype=torch.int32, **pin)
-        self.h_tables = torch.empty(B, self.max_blocks, dtype=torch.int32, **pin)
-        self.h_lens = torch.empty(B, dtype=torch.int32, **pin)
-        self.d_slots = torch.empty(n_step, dtype=torch.int32, device=self.device)
-        self.d_tables = torch.empty(B, self.max_blocks, dtype=torch.int32, device=self.device)
-        self.d_lens = torch.empty(B, dtype=torch.int32, device=self.device)
+        # One int32 buffer holds a step's metadata (slot mapping, block
+        # tables, seq_lens) so it crosses to the device in one copy.  Two
+        # pinned host copies alternate between steps, so the host can write
+        # step i + 1 while step i's copy may still be queued.
+        self._meta_split = (n_step, n_step + B * self.max_blocks)
+        meta_len = n_step + B * self.max_blocks + B
+        self.h_meta = [torch.empty(meta_len, dtype=torch.int32, pin_memory=True) for _ in range(2)]
+        self.d_meta = torch.empty(meta_len, dtype=torch.int32, device=self.device)
+        self.d_slots, self.d_tables, self.d_lens = self._views(self.d_meta)
+        self._cur = 1
+        self._meta_free = [None, None]   # event after which h_meta[i] may be rewritten
+        self._meta_events = [torch.cuda.Event(), torch.cuda.Event()]
+        self.graphs = None
         self.out = torch.empty(B, wl.num_heads, wl.head_dim, dtype=dt, device=self.device)
         pads = pad_positions(wl)
         is_pad = np.zeros(n_step, dtype=bool)
@@ -73,12 +80,38 @@ class PagedDecodeEngine:
         self.valid_pos = np.nonzero(~is_pad)[0]
         self.pad_pos = pads
         self.n_prefill = int(wl.prefill_lens.sum())
-        self.prefill_ids: List[int] = []
         self.next_id = wl.next_id
+        # inputs of kvbm_prepare_step, kept in place so their addresses are fixed
+        self._decode_ids = np.ascontiguousarray(wl.decode_ids, dtype=np.int64)
+        self._prefill_lens = np.ascontiguousarray(wl.prefill_lens, dtype=np.int64)
+        self._prefill_ids = np.zeros(self._prefill_lens.size, dtype=np.int64)
+        self._free_ids = np.zeros(self._prefill_lens.size, dtype=np.int64)
+        self._pad_pos = np.ascontiguousarray(pads, dtype=np.int64)
+        self._prefilled_once = False
+        self._meta_addr = []
+        for m in self.h_meta:
+            sl, tb, ln = self._views(m)
+            self._meta_addr.append((sl.data_ptr(), tb.data_ptr(), ln.data_ptr()))
         self.steps_done = 0
-        self._h2d_done = torch.cuda.Event()
-        self._h2d_pending = False
         self.history_slots: Optional[np.ndarray] = None
+
+    def _views(self, meta: torch.Tensor):
+        a, b = self._meta_split
+        B = self.wl.num_seqs
+        return meta[:a], meta[a:b].view(B, self.max_blocks), meta[b:]
+
+    # the pinned metadata of the step written last
+    @property
+    def h_slots(self) -> torch.Tensor:
+        return self._views(self.h_meta[self._cur])[0]
+
+    @property
+    def h_tables(self) -> torch.Tensor:
+        return self._views(self.h_meta[self._cur])[1]
+
+    @property
+    def h_lens(self) -> torch.Tensor:
+        return self._views(self.h_meta[self._cur])[2]
 
     # ---------------------------------------------------------------- setup
     def setup(self, values: Values) -> None:
@@ -111,35 +144,39 @@ class PagedDecodeEngine:
 
     # ------------------------------------------------------------------ step
     def host_metadata(self) -> None:
-        """a1: allocate the step's prefill sequences, append one decode slot
-        per running sequence, export tables/lens into pinned buffers and
-        queue the H2D copies."""
-        wl = self.wl
-        if self._h2d_pending:
-            self._h2d_done.synchronize()       # pinned buffers are about to be rewritten
-        slots = self.h_slots.numpy()
-        step_slots = np.empty(self.n_prefill + wl.num_seqs, dtype=np.int32)
-        if self.n_prefill:
-            for sid in self.prefill_ids:
-                self.mgr.free_sequence(sid)
-            self.prefill_ids = []
-            pos = 0
-            for n in wl.prefill_lens:
-                sid = self.next_id
-                self.next_id += 1
-                self.mgr.allocate_for_prefill(sid, int(n), step_slots[pos:pos + int(n)])
-                self.prefill_ids.append(sid)
-                pos += int(n)
-        self.mgr.decode_step(wl.decode_ids, self.max_blocks, step_slots[self.n_prefill:], self.h_tables.numpy(),
-                             self.h_lens.numpy())
-        slots[self.valid_pos] = step_slots
-        if self.pad_pos.size:
-            slots[self.pad_pos] = -1
-        self.d_slots.copy_(self.h_slots, non_blocking=True)
-        self.d_tables.copy_(self.h_tables, non_blocking=True)
-        self.d_lens.copy_(self.h_lens, non_blocking=True)
-        self._h2d_done.record()
-        self._h2d_pending = True
+        """a1 on the host: one native call (kvbm_prepare_step) releases the
+        previous step's prefill sequences, allocates this step's, appends
+        one decode slot per running sequence, and writes slot mapping (with
+        -1 padding), block tables and seq_lens into the next pinned
+        metadata buffer."""
+        self._cur ^= 1
+        ev = self._meta_free[self._cur]
+        if ev is not None:
+            ev.synchronize()       # the copy that last read this buffer has run
+        n_pre = self._prefill_ids.size
+        n_free = n_pre if self._prefilled_once else 0   # the previous step's prefills end now
+        if n_pre:
+            self._free_ids[:] = self._prefill_ids
+            self._prefill_ids[:] = np.arange(self.next_id, self.next_id + n_pre)
+            self.next_id += n_pre
+            self._prefilled_once = True
+        slots_a, tables_a, lens_a = self._meta_addr[self._cur]
+        st = self.mgr.prepare_step_raw(
+            self._free_ids.ctypes.data if n_free else None, n_free,
+            self._prefill_ids.ctypes.data if n_pre else None, self._prefill_lens.ctypes.data if n_pre else None,
+            n_pre, self._decode_ids.ctypes.data, self._decode_ids.size,
+            self._pad_pos.ctypes.data if self._pad_pos.size else None, self._pad_pos.size, self.max_blocks,
+            slots_a, tables_a, lens_a)
+        check(st, "kvbm_prepare_step")
+
+    def upload_metadata(self) -> None:
+        """a1 crossing: one async H2D copy of the step's metadata."""
+        self.d_meta.copy_(self.h_meta[self._cur], non_blocking=True)
+
+    def _mark_meta_used(self) -> None:
+        ev = self._meta_events[self._cur]
+        ev.record()
+        self._meta_free[self._cur] = ev
 
     def write_step_kv(self, k_step: torch.Tensor, v_step: torch.Tensor) -> None:
         """a2: cache write of the step's new tokens."""
@@ -151,17 +188,61 @@ class PagedDecodeEngine:
         return paged_decode_attention(self.out, q, self.k_cache, self.v_cache, self.d_tables, self.d_lens,
                                       wl.scale, self.max_seq_len, self.blocks_per_split, self.workspace)
 
-    def step(self, q: torch.Tensor, k_step: torch.Tensor, v_step: torch.Tensor) -> torch.Tensor:
+    def _check_room(self) -> None:
         if self.steps_done + 1 > self.max_seq_len - int(self.wl.cached_lens.max()):
             raise RuntimeError("engine sized for fewer steps")
+
+    def step(self, q: torch.Tensor, k_step: torch.Tensor, v_step: torch.Tensor) -> torch.Tensor:
+        """One step with direct launches."""
+        self._check_room()
         self.host_metadata()
+        self.upload_metadata()
+        self._mark_meta_used()
         self.write_step_kv(k_step, v_step)
         out = self.attention(q)
         self.steps_done += 1
         return out
 
+    # ---------------------------------------------------------- CUDA graphs
+    def capture(self, q: torch.Tensor, k_step: torch.Tensor, v_step: torch.Tensor, host_io=None) -> None:
+        """Capture the device part of a step -- metadata copy, cache write,
+        attention -- as two CUDA graphs, one per pinned metadata buffer.
+        ``host_io`` = (q_h, k_h, v_h, out_h) pinned host tensors adds the
+        inputs' H2D copies into q/k_step/v_step and the output's D2H copy.
+        Call after at least one ``step`` so every lazy set-up has run."""
+        if self.steps_done == 0:
+            raise RuntimeError("run one step before capturing")
+        torch.cuda.synchronize()
+        graphs = []
+        side = torch.cuda.Stream()
+        for i in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                self.d_meta.copy_(self.h_meta[i], non_blocking=True)
+                if host_io is not None:
+                    q.copy_(host_io[0], non_blocking=True)
+                    k_step.copy_(host_io[1], non_blocking=True)
+                    v_step.copy_(host_io[2], non_blocking=True)
+                self.write_step_kv(k_step, v_step)
+                out = self.attention(q)
+                if host_io is not None:
+                    host_io[3].copy_(out, non_blocking=True)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        self.graphs = graphs
+
+    def step_graph(self) -> torch.Tensor:
+        """One step: host metadata, then one graph launch for the device part."""
+        self._check_room()
+        self.host_metadata()
+        self.graphs[self._cur].replay()
+        self._mark_meta_used()
+        self.steps_done += 1
+        return self.out
+
     @property
     def launches_per_step(self) -> int:
+        """Library kernels per step: the cache write plus the attention call."""
         return 1 + self.plan.launches
 
     def algorithmic_bytes(self, seq_lens: np.ndarray) -> dict:

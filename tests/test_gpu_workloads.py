@@ -114,3 +114,28 @@ def test_workload_step_matches_oracle(name):
         ref = decode_attention_contiguous(q64[b], K, V, wl.scale)
         worst = max(worst, float(np.max(np.abs(got[b] - ref))))
     assert worst <= TOL[wl.dtype], f"{name}: max abs err {worst:.3e}"
+
+
+@pytest.mark.parametrize("name", ["decode_gqa14x2_d64_fp16", "mixed_batch_bf16"])
+def test_graph_steps_match_direct_steps(name):
+    """The benchmark replays each step's device part as a CUDA graph; its
+    outputs, cache writes and metadata equal those of direct launches."""
+    wl = make_workload(name)
+    dev = torch.device("cuda")
+    vals = make_values(wl, device="cuda")
+    direct = PagedDecodeEngine(wl, dev, max_steps=6)
+    graphed = PagedDecodeEngine(wl, dev, max_steps=6)
+    direct.setup(vals)
+    graphed.setup(vals)
+    a = direct.step(vals.q, vals.k_step, vals.v_step).clone()
+    b = graphed.step(vals.q, vals.k_step, vals.v_step).clone()
+    assert torch.equal(a, b)
+    graphed.capture(vals.q, vals.k_step, vals.v_step)
+    for _ in range(4):
+        a = direct.step(vals.q, vals.k_step, vals.v_step).clone()
+        b = graphed.step_graph().clone()
+        torch.cuda.synchronize()
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        assert torch.equal(direct.h_tables, graphed.h_tables) and torch.equal(direct.h_lens, graphed.h_lens)
+    assert torch.equal(direct.k_cache.view(torch.int16), graphed.k_cache.view(torch.int16))
+    assert pk.device_error() == 0

@@ -209,3 +209,84 @@ def test_workload_setup_replays_identically(name):
     assert tables.tolist() == t_o and lens.tolist() == l_o
     assert nat.free_list().tolist() == ora.free_blocks
     assert nat.check_invariants()
+
+
+def _oracle_prepare(ora, free_ids, pre_ids, pre_lens, dec_ids, pads, mb):
+    for s in free_ids:
+        ora.free_sequence(s)
+    step = []
+    for sid, n in zip(pre_ids, pre_lens):
+        step += ora.allocate_for_prefill(sid, n)
+    step += ora.decode_step(dec_ids)
+    total = len(step) + len(pads)
+    it = iter(step)
+    mapping = [-1 if p in set(pads) else next(it) for p in range(total)]
+    tables, lens = ora.export(dec_ids, mb)
+    return mapping, tables, lens
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_prepare_step_matches_oracle_sequence(seed):
+    """kvbm_prepare_step = release, prefill each, decode step, pad, export --
+    bit-exact against the oracle doing those operations one by one."""
+    rng = random.Random(500 + seed)
+    nb, bs = rng.choice([(64, 4), (200, 16), (40, 2)])
+    order = list(range(nb))
+    rng.shuffle(order)
+    nat, ora = KVBlockManager(nb, bs, order), OracleManager(nb, bs, order)
+    running = []
+    for sid in range(6):
+        n = rng.randint(1, 3 * bs)
+        nat.allocate_for_prefill(sid, n)
+        ora.allocate_for_prefill(sid, n)
+        running.append(sid)
+    next_id, prev = 100, []
+    for _ in range(8):
+        pre_ids = [next_id + i for i in range(rng.randint(0, 3))]
+        next_id += 10
+        pre_lens = [rng.randint(1, 2 * bs) for _ in pre_ids]
+        n_tot = sum(pre_lens) + len(running)
+        n_pad = rng.randint(0, 4)
+        pads = sorted(rng.sample(range(n_tot + n_pad), n_pad))
+        mb = 64
+        try:
+            want = _oracle_prepare(ora, prev, pre_ids, pre_lens, running, pads, mb)
+            err_o = None
+        except OracleError as e:
+            err_o = e.code
+        try:
+            got = nat.prepare_step(prev, pre_ids, pre_lens, running, pads, mb)
+            err_n = None
+        except KVError as e:
+            err_n = e.code
+        assert err_n == err_o
+        if err_o is None:
+            assert got[0].tolist() == want[0]
+            assert got[1].tolist() == want[1] and got[2].tolist() == want[2]
+            prev = pre_ids
+        else:
+            break
+        _same_state(nat, ora)
+
+
+def test_prepare_step_is_atomic_and_validates():
+    nat = KVBlockManager(4, 4)
+    nat.allocate_for_prefill(0, 4)            # full block: the next decode needs one more
+    nat.allocate_for_prefill(1, 3)
+    before = nat.free_list().tolist()
+    with pytest.raises(KVError) as e:          # 2 prefill blocks + 1 decode block > 2 free
+        nat.prepare_step([], [7], [8], [0, 1], [], 8)
+    assert e.value.code == "OOM"
+    assert nat.free_list().tolist() == before and nat.seq_len(0) == 4
+    with pytest.raises(KVError) as e:
+        nat.prepare_step([], [], [], [0, 1], [0, 0], 8)       # padding positions not increasing
+    assert e.value.code == "INVALID_ARG"
+    with pytest.raises(KVError) as e:
+        nat.prepare_step([], [1], [2], [0], [], 8)            # prefill of a live sequence
+    assert e.value.code == "DUPLICATE_SEQ"
+    with pytest.raises(KVError) as e:
+        nat.prepare_step([], [], [], [0, 0], [], 8)           # one sequence twice
+    assert e.value.code == "INVALID_ARG"
+    slots, tables, lens = nat.prepare_step([1], [5], [3], [0], [0, 4], 8)
+    assert slots.size == 3 + 1 + 2 and slots[0] == -1 and slots[4] == -1
+    assert lens.tolist() == [5] and nat.check_invariants()
