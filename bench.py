@@ -47,6 +47,9 @@ def parse_args():
     ap.add_argument("--impl", default="native", choices=("native", "reference"))
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-calls", type=int, default=0,
+                    help="only set the workload up and run this many attention calls (L2 flushed before each); "
+                         "the small case used under ncu")
     return ap.parse_args()
 
 
@@ -487,8 +490,40 @@ def run_reference(args):
     print(json.dumps(out))
 
 
+def run_profile_calls(args):
+    """One engine, one step, then ``--profile-calls`` attention calls with L2
+    flushed before each: a short, fixed launch sequence for ncu captures."""
+    import torch
+
+    import paged_kv_cache_128_gb300 as pk
+    from paged_kv_cache_128_gb300.engine import PagedDecodeEngine
+    from paged_kv_cache_128_gb300.inputs import make_values, make_workload
+
+    dev = torch.device("cuda")
+    wl = make_workload(args.workload)
+    eng = PagedDecodeEngine(wl, dev, max_steps=4, fill_sentinel=False)
+    vals = make_values(wl, device="cuda")
+    eng.setup(vals)
+    eng.step(vals.q, vals.k_step, vals.v_step)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    for _ in range(args.profile_calls):
+        flush.zero_()
+        eng.attention(vals.q)
+    torch.cuda.synchronize()
+    status = pk.device_error()
+    print(json.dumps({"workload": wl.name, "calls": args.profile_calls, "plan": eng.plan.__dict__,
+                      "attention_bytes": eng.algorithmic_bytes(wl.cached_lens + 1)["attention"],
+                      "device_error": status}))
+    if status:
+        sys.exit(1)
+
+
 def main():
     args = parse_args()
+    if args.profile_calls:
+        run_profile_calls(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

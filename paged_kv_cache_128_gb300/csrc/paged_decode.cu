@@ -738,32 +738,52 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   }
   named_barrier_sync(1, kConsumers * 32);
   // Each output combines all parts by an online log-sum-exp over batches of
-  // 8 parts; a batch's (m, l, acc) loads are all issued before any is used.
+  // 8 parts.  A thread takes up to 4 outputs at once and issues all their
+  // (m, l, acc) loads for a batch before using any, so a batch costs one
+  // round trip to L2 whatever the output count.
   T* o = static_cast<T*>(p.out) + (static_cast<int64_t>(own_b) * p.num_heads + own_kvh * G) * D;
-  for (int idx = ctid; idx < G * D; idx += kConsumers * 32) {
-    const int g = idx / D, d = idx - g * D;
-    float mx = -INFINITY, num = 0.f, den = 0.f;
-    for (int k0 = 0; k0 < npad; k0 += 8) {
-      float mk[8], lk[8], ok8[8];
+  constexpr int kOut = 4, kParts = 8, kStride = kConsumers * 32;
+  for (int base = ctid; base < G * D; base += kStride * kOut) {
+    float mx[kOut], num[kOut], den[kOut];
+    int gi[kOut], di[kOut];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int rb = part_row[k0 + u];
-        const int64_t r = rb + g;
-        mk[u] = rb >= 0 ? p.ws_ml[r * 2] : -INFINITY;
-        lk[u] = rb >= 0 ? p.ws_ml[r * 2 + 1] : 0.f;
-        ok8[u] = rb >= 0 ? p.ws_o[r * D + d] : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (mk[u] == -INFINITY) continue;
-        const float nm = fmaxf(mx, mk[u]);
-        const float so = fast_exp2(mx - nm), sn = fast_exp2(mk[u] - nm);
-        num = num * so + sn * ok8[u];
-        den = den * so + sn * lk[u];
-        mx = nm;
-      }
+    for (int i = 0; i < kOut; ++i) {
+      const int idx = min(base + i * kStride, G * D - 1);
+      gi[i] = idx / D;
+      di[i] = idx - gi[i] * D;
+      mx[i] = -INFINITY;
+      num[i] = den[i] = 0.f;
     }
-    o[idx] = DType<T>::from_float(den > 0.f ? num / den : 0.f);
+    for (int k0 = 0; k0 < npad; k0 += kParts) {
+      float mk[kOut][kParts], lk[kOut][kParts], ak[kOut][kParts];
+#pragma unroll
+      for (int u = 0; u < kParts; ++u) {
+        const int rb = part_row[k0 + u];
+#pragma unroll
+        for (int i = 0; i < kOut; ++i) {
+          const int64_t r = rb + gi[i];
+          mk[i][u] = rb >= 0 ? p.ws_ml[r * 2] : -INFINITY;
+          lk[i][u] = rb >= 0 ? p.ws_ml[r * 2 + 1] : 0.f;
+          ak[i][u] = rb >= 0 ? p.ws_o[r * D + di[i]] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kOut; ++i)
+#pragma unroll
+        for (int u = 0; u < kParts; ++u) {
+          if (mk[i][u] == -INFINITY) continue;
+          const float nm = fmaxf(mx[i], mk[i][u]);
+          const float so = fast_exp2(mx[i] - nm), sn = fast_exp2(mk[i][u] - nm);
+          num[i] = num[i] * so + sn * ak[i][u];
+          den[i] = den[i] * so + sn * lk[i][u];
+          mx[i] = nm;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kOut; ++i) {
+      const int idx = base + i * kStride;
+      if (idx < G * D) o[idx] = DType<T>::from_float(den[i] > 0.f ? num[i] / den[i] : 0.f);
+    }
   }
 }
 
