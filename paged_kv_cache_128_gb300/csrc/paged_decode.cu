@@ -353,7 +353,11 @@ constexpr int kMaxSkCtas = 640;
 
 template <typename T, int D, int BS, int NG, int NST>
 struct SkCfg {
-  using TL = Tile<D, BS>;
+  // A stream-K tile is 32 tokens: one block of 32, or two consecutive
+  // blocks of 16 of the same sequence (fewer, larger pipeline transactions).
+  static constexpr int kBlocksPerTile = BS >= 32 ? 1 : 32 / BS;
+  static constexpr int kTileTokens = BS * kBlocksPerTile;
+  using TL = Tile<D, kTileTokens>;
   static constexpr int kStages = NST * TL::kStageBytes;
   static constexpr int kMerge = 2 * MergeArea<D, NG>::kBytes;  // double-buffered per segment
   static constexpr int kFixed = 1024 + kStages + kMerge + 2 * NST * 8;
@@ -371,7 +375,8 @@ __global__ void __launch_bounds__(kTcThreads)
 decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV) {
   using C = SkCfg<T, D, BS, NG, NST>;
-  using TL = Tile<D, BS>;
+  using TL = typename C::TL;
+  constexpr int TPB = C::kBlocksPerTile, TT = C::kTileTokens;
   constexpr int GP = 8 * NG;
   static_assert(NST % kConsumers == 0, "stage s must always be drained by consumer s % kConsumers");
   extern __shared__ uint8_t smem_raw[];
@@ -380,7 +385,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   constexpr int kMergeFloats = MergeArea<D, NG>::kBytes / 4;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages + C::kMerge);
   uint64_t* empty = full + NST;
-  int* CB = reinterpret_cast<int*>(empty + NST);  // CB[b] = sum_{b' < b} ceil(L_b' / BS)
+  int* CB = reinterpret_cast<int*>(empty + NST);  // CB[b] = sum_{b' < b} ceil(L_b' / TT) (tiles)
 
   const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
   int* CC = CB + (B + 1);  // CC[b] = sum_{b' < b} cost_b' (tiles + seg_cost, 0 if empty)
@@ -392,7 +397,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     const int beg = min(B, tid * per), end = min(B, beg + per);
     int local = 0, local_c = 0;
     for (int i = beg; i < end; ++i) {
-      const int nb = (checked_len(p, i) + BS - 1) / BS;
+      const int nb = (checked_len(p, i) + TT - 1) / TT;
       CB[i + 1] = nb;
       local += nb;
       local_c += nb > 0 ? nb + p.seg_cost : 0;
@@ -504,57 +509,71 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
     }
-    Cursor c{b0, rel0 / nb0, rel0 % nb0, nb0};
-    // Block-table entries are fetched 32 at a time (one per lane) and the
-    // chunk the walk needs next is fetched while the current one is used.
-    auto fetch = [&](int b, int chunk, int nb) -> int {
+    Cursor c{b0, rel0 / nb0, rel0 % nb0, nb0};  // c.blk counts tiles of TPB blocks
+    // Block-table entries are fetched 32 at a time (one per lane; entries
+    // past the sequence are fetched but never used) and the chunk the walk
+    // needs next is fetched while the current one is used.
+    auto fetch = [&](int b, int chunk) -> int {
       const int e = (chunk << 5) + lane;
-      return e < nb ? __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq + e) : 0;
+      return e < p.max_blocks_per_seq ? __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq + e)
+                                      : 0;
     };
-    int cache_b = -1, cache_chunk = -1, mine = 0;
+    auto nblocks = [&](int b) { return (checked_len(p, b) + BS - 1) / BS; };
+    int cache_b = -1, cache_chunk = -1, cache_nblk = 0, mine = 0;
     int next_b = -1, next_chunk = -1, nxt = 0;
     int ok = 1, issued = 0;
     for (int j = 0; j < n && ok; ++j) {
-      if (c.b != cache_b || (c.blk >> 5) != cache_chunk) {
-        mine = (c.b == next_b && (c.blk >> 5) == next_chunk) ? nxt : fetch(c.b, c.blk >> 5, c.nb);
+      const int blk = c.blk * TPB;  // first block of this tile
+      if (c.b != cache_b || (blk >> 5) != cache_chunk) {
+        mine = (c.b == next_b && (blk >> 5) == next_chunk) ? nxt : fetch(c.b, blk >> 5);
+        if (c.b != cache_b) cache_nblk = nblocks(c.b);
         cache_b = c.b;
-        cache_chunk = c.blk >> 5;
+        cache_chunk = blk >> 5;
         // the chunk after this one in walk order: next chunk of the row, the
         // row's first chunk again for the next kv head, or the next sequence
-        int nbk = c.b, nck = cache_chunk + 1, nnb = c.nb;
-        if (nck * 32 >= c.nb) {
+        int nbk = c.b, nck = cache_chunk + 1;
+        if (nck * 32 >= cache_nblk) {
           nck = 0;
           if (c.kvh + 1 >= Hkv) {
             do {
               ++nbk;
             } while (nbk < B && CB[nbk + 1] == CB[nbk]);
-            nnb = nbk < B ? CB[nbk + 1] - CB[nbk] : 0;
           }
         }
         if (nbk < B && !(nbk == cache_b && nck == cache_chunk)) {
-          nxt = fetch(nbk, nck, nnb);
+          nxt = fetch(nbk, nck);
           next_b = nbk;
           next_chunk = nck;
         } else {
           next_b = -1;
         }
       }
-      int pb = __shfl_sync(0xffffffffu, mine, c.blk & 31);
+      int pbs[TPB];
+#pragma unroll
+      for (int r = 0; r < TPB; ++r) pbs[r] = __shfl_sync(0xffffffffu, mine, (blk + r) & 31);
+      const int here = min(TPB, cache_nblk - blk);  // blocks of this tile inside the sequence (>= 1)
       if (lane == 0) {
         const int s = j % NST;
         if (j >= NST) ok = mbar_wait_bounded(&empty[s], ((j / NST) - 1) & 1);
         if (ok) {
-          if (pb < 0 || pb >= p.num_blocks) {
-            record_error(KV_ERR_DEVICE_BOUNDS);
-            pb = 0;
-          }
-          mbar_arrive_expect_tx(&full[s], TL::kStageBytes);
+          mbar_arrive_expect_tx(&full[s], here * (TL::kStageBytes / TPB));
           uint8_t* kt = smem + s * TL::kStageBytes;
           uint8_t* vt = kt + TL::kTileBytes;
 #pragma unroll
-          for (int sl = 0; sl < TL::kSub; ++sl) {
-            tma_load_3d(kt + sl * TL::kSlabBytes, &tmK, &full[s], sl * 64, c.kvh, pb * BS);
-            tma_load_3d(vt + sl * TL::kSlabBytes, &tmV, &full[s], sl * 64, c.kvh, pb * BS);
+          for (int r = 0; r < TPB; ++r) {
+            if (r < here) {
+              int pb = pbs[r];
+              if (pb < 0 || pb >= p.num_blocks) {
+                record_error(KV_ERR_DEVICE_BOUNDS);
+                pb = 0;
+              }
+#pragma unroll
+              for (int sl = 0; sl < TL::kSub; ++sl) {
+                const int off = sl * TL::kSlabBytes + r * BS * 128;
+                tma_load_3d(kt + off, &tmK, &full[s], sl * 64, c.kvh, pb * BS);
+                tma_load_3d(vt + off, &tmV, &full[s], sl * 64, c.kvh, pb * BS);
+              }
+            }
           }
           ++issued;
         }
@@ -610,7 +629,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       if (ok) {
         __syncwarp();
         uint8_t* kt = smem + s * TL::kStageBytes;
-        consume_tile<T, D, BS, NG>(st, kt, kt + TL::kTileBytes, c.blk * BS, L, sl2, lane);
+        consume_tile<T, D, TT, NG>(st, kt, kt + TL::kTileBytes, c.blk * TT, L, sl2, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
       }
@@ -1252,7 +1271,8 @@ cudaError_t allow_smem(K kern, int bytes, int* configured_bytes) {
 
 template <typename T, int D, int BS, int NG>
 cudaError_t launch_sk(DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, int max_ctas, cudaStream_t st) {
-  constexpr int NST = Stages<D, BS>::value;
+  constexpr int kTileTokens = BS >= 32 ? BS : 32;  // matches SkCfg::kTileTokens
+  constexpr int NST = Stages<D, kTileTokens>::value;
   using C = SkCfg<T, D, BS, NG, NST>;
   auto kern = decode_sk_kernel<T, D, BS, NG, NST>;
   static int configured[64] = {0};
@@ -1273,7 +1293,7 @@ cudaError_t launch_sk(DecodeParams& p, const CUtensorMap& mk, const CUtensorMap&
   const int ctas = std::min({max_ctas, sm_count() * occ_cache[dev][1], kMaxSkCtas});
   p.num_ctas = ctas;
   p.epoch = next_epoch();
-  p.seg_cost = seg_cost_tiles(Tile<D, BS>::kStageBytes);
+  p.seg_cost = seg_cost_tiles(Tile<D, kTileTokens>::kStageBytes);
   // Cooperative: the driver refuses the launch unless all CTAs can be
   // resident at once, which the owners' waits on later CTAs rely on.
   cudaLaunchConfig_t cfg{};
