@@ -130,6 +130,22 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Contiguous bulk copy global -> shared, completing on an mbarrier.  Both
+// addresses 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses (and what they
+// acquired) before its later async-proxy accesses to global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Release store / acquire load of a 64-bit flag at GPU scope (inter-CTA
 // hand-off of data written to global memory).
 __device__ __forceinline__ void st_release_gpu(uint64_t* ptr, uint64_t v) {
@@ -139,21 +155,6 @@ __device__ __forceinline__ uint64_t ld_acquire_gpu(const uint64_t* ptr) {
   uint64_t v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
   return v;
-}
-
-// Spin until *flag == value, for at most kWaitLimitNs.  Returns false (and
-// records KV_ERR_DEVICE_TIMEOUT) on timeout.
-__device__ __forceinline__ bool wait_flag_bounded(const uint64_t* flag, uint64_t value) {
-  if (ld_acquire_gpu(flag) == value) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (ld_acquire_gpu(flag) != value) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      record_error(KV_ERR_DEVICE_TIMEOUT);
-      return false;
-    }
-    __nanosleep(64);
-  }
-  return true;
 }
 
 // Programmatic dependent launch: let the next kernel in the stream start

@@ -208,13 +208,102 @@ __device__ __forceinline__ void reset_state(WarpState<D, NG>& st) {
   }
 }
 
+// Accumulate NS 16-token sub-tiles (tokens tok0 .. tok0 + 16 * NS - 1) of
+// one tile held in shared memory at kt_a (K) and vt_a (V) as one step of the
+// online softmax: the score chains of the sub-tiles are interleaved, and
+// the running max, the rescale of the accumulator and l are updated once.
+template <typename T, int D, int BS, int NG, int NS>
+__device__ __forceinline__ void consume_subtiles(WarpState<D, NG>& st, uint32_t kt_a, uint32_t vt_a, int tok0, int L,
+                                                 float sl2, int lane) {
+  using M = Mma<T>;
+  constexpr int KS = D / 16;
+  // ldmatrix lane -> (row, column) of the 8x8 matrix it addresses
+  const int k_row = (lane & 7) + ((lane >> 3) & 1) * 8, k_col = (lane >> 4) * 8;  // A = K (non-trans)
+  const int v_row = (lane & 7) + (lane >> 4) * 8, v_col = ((lane >> 3) & 1) * 8;  // A = V^T (trans)
+  float sc[NS][NG][4];
+#pragma unroll
+  for (int u = 0; u < NS; ++u)
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) sc[u][ng][0] = sc[u][ng][1] = sc[u][ng][2] = sc[u][ng][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < KS; ++kk) {
+    uint32_t a[NS][4];
+#pragma unroll
+    for (int u = 0; u < NS; ++u)
+      ldmatrix_x4(kt_a + swz<BS>(u * 16 + k_row, kk * 16 + k_col), a[u][0], a[u][1], a[u][2], a[u][3]);
+#pragma unroll
+    for (int u = 0; u < NS; ++u)
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) M::run(sc[u][ng], a[u], st.qf[kk][ng][0], st.qf[kk][ng][1]);
+  }
+  uint32_t pb[NS][NG][2];
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng) {
+    // scores in the exp2 domain; rows past the sequence end are -inf
+    float x[NS][4];
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < NS; ++u) {
+      const int t_lo = tok0 + u * 16 + (lane >> 2);
+      const bool in_lo = t_lo < L, in_hi = t_lo + 8 < L;
+      x[u][0] = in_lo ? sc[u][ng][0] * sl2 : -INFINITY;
+      x[u][1] = in_lo ? sc[u][ng][1] * sl2 : -INFINITY;
+      x[u][2] = in_hi ? sc[u][ng][2] * sl2 : -INFINITY;
+      x[u][3] = in_hi ? sc[u][ng][3] * sl2 : -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(x[u][0], x[u][2]));
+      mx1 = fmaxf(mx1, fmaxf(x[u][1], x[u][3]));
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(st.m[ng][0], mx0), mn1 = fmaxf(st.m[ng][1], mx1);
+    const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0, mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
+    const float al0 = fast_exp2(st.m[ng][0] - mu0), al1 = fast_exp2(st.m[ng][1] - mu1);
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int u = 0; u < NS; ++u) {
+      // l sums the probabilities as rounded for the PV product
+      const uint32_t lo = M::pack(fast_exp2(x[u][0] - mu0), fast_exp2(x[u][1] - mu1));
+      const uint32_t hi = M::pack(fast_exp2(x[u][2] - mu0), fast_exp2(x[u][3] - mu1));
+      const float2 flo = M::unpack(lo), fhi = M::unpack(hi);
+      s0 += flo.x + fhi.x;
+      s1 += flo.y + fhi.y;
+      pb[u][ng][0] = movmatrix_trans(lo);
+      pb[u][ng][1] = movmatrix_trans(hi);
+    }
+    st.l[ng][0] = st.l[ng][0] * al0 + s0;
+    st.l[ng][1] = st.l[ng][1] * al1 + s1;
+    st.m[ng][0] = mn0;
+    st.m[ng][1] = mn1;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      st.acc[mt][ng][0] *= al0;
+      st.acc[mt][ng][1] *= al1;
+      st.acc[mt][ng][2] *= al0;
+      st.acc[mt][ng][3] *= al1;
+    }
+  }
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) {
+    uint32_t a[NS][4];
+#pragma unroll
+    for (int u = 0; u < NS; ++u)
+      ldmatrix_x4_trans(vt_a + swz<BS>(u * 16 + v_row, mt * 16 + v_col), a[u][0], a[u][1], a[u][2], a[u][3]);
+#pragma unroll
+    for (int u = 0; u < NS; ++u)
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) M::run(st.acc[mt][ng], a[u], pb[u][ng][0], pb[u][ng][1]);
+  }
+}
+
 // Accumulate one tile (tokens tok0 .. tok0 + BS - 1 of a sequence of length
-// L) held in shared memory at kt (K) and vt (V).
+// L) held in shared memory at kt (K) and vt (V).  Sub-tiles wholly past the
+// sequence end are skipped.
 template <typename T, int D, int BS, int NG>
 __device__ __forceinline__ void consume_tile(WarpState<D, NG>& st, uint8_t* kt, uint8_t* vt, int tok0, int L,
                                              float sl2, int lane) {
-  using M = Mma<T>;
-  constexpr int KS = D / 16;
   const int valid = min(BS, L - tok0);
   if (valid < BS) {
     // zero the V rows past the sequence end: P is 0 there, but 0 * NaN is not
@@ -227,65 +316,12 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NG>& st, uint8_t* kt, 
     __syncwarp();
   }
   const uint32_t kt_a = smem_u32(kt), vt_a = smem_u32(vt);
-  // ldmatrix lane -> (row, column) of the 8x8 matrix it addresses
-  const int k_row = (lane & 7) + ((lane >> 3) & 1) * 8, k_col = (lane >> 4) * 8;  // A = K (non-trans)
-  const int v_row = (lane & 7) + (lane >> 4) * 8, v_col = ((lane >> 3) & 1) * 8;  // A = V^T (trans)
-#pragma unroll
-  for (int sub = 0; sub < BS / 16; ++sub) {
-    if (sub * 16 < valid) {
-      float sc[NG][4];
-#pragma unroll
-      for (int ng = 0; ng < NG; ++ng) sc[ng][0] = sc[ng][1] = sc[ng][2] = sc[ng][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        uint32_t a[4];
-        ldmatrix_x4(kt_a + swz<BS>(sub * 16 + k_row, kk * 16 + k_col), a[0], a[1], a[2], a[3]);
-#pragma unroll
-        for (int ng = 0; ng < NG; ++ng) M::run(sc[ng], a, st.qf[kk][ng][0], st.qf[kk][ng][1]);
-      }
-      const int t_lo = tok0 + sub * 16 + (lane >> 2);
-      const bool in_lo = t_lo < L, in_hi = t_lo + 8 < L;
-      uint32_t pb0[NG], pb1[NG];
-#pragma unroll
-      for (int ng = 0; ng < NG; ++ng) {
-        const float x0 = in_lo ? sc[ng][0] * sl2 : -INFINITY;
-        const float x1 = in_lo ? sc[ng][1] * sl2 : -INFINITY;
-        const float x2 = in_hi ? sc[ng][2] * sl2 : -INFINITY;
-        const float x3 = in_hi ? sc[ng][3] * sl2 : -INFINITY;
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const float mn0 = fmaxf(st.m[ng][0], mx0), mn1 = fmaxf(st.m[ng][1], mx1);
-        const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0, mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
-        const float al0 = fast_exp2(st.m[ng][0] - mu0), al1 = fast_exp2(st.m[ng][1] - mu1);
-        const uint32_t lo = M::pack(fast_exp2(x0 - mu0), fast_exp2(x1 - mu1));
-        const uint32_t hi = M::pack(fast_exp2(x2 - mu0), fast_exp2(x3 - mu1));
-        const float2 flo = M::unpack(lo), fhi = M::unpack(hi);
-        st.l[ng][0] = st.l[ng][0] * al0 + (flo.x + fhi.x);
-        st.l[ng][1] = st.l[ng][1] * al1 + (flo.y + fhi.y);
-        st.m[ng][0] = mn0;
-        st.m[ng][1] = mn1;
-#pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-          st.acc[mt][ng][0] *= al0;
-          st.acc[mt][ng][1] *= al1;
-          st.acc[mt][ng][2] *= al0;
-          st.acc[mt][ng][3] *= al1;
-        }
-        pb0[ng] = movmatrix_trans(lo);
-        pb1[ng] = movmatrix_trans(hi);
-      }
-#pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        uint32_t a[4];
-        ldmatrix_x4_trans(vt_a + swz<BS>(sub * 16 + v_row, mt * 16 + v_col), a[0], a[1], a[2], a[3]);
-#pragma unroll
-        for (int ng = 0; ng < NG; ++ng) M::run(st.acc[mt][ng], a, pb0[ng], pb1[ng]);
-      }
-    }
+  if constexpr (BS == 32) {
+    if (valid > 16) consume_subtiles<T, D, BS, NG, 2>(st, kt_a, vt_a, tok0, L, sl2, lane);
+    else consume_subtiles<T, D, BS, NG, 1>(st, kt_a, vt_a, tok0, L, sl2, lane);
+  } else {
+    static_assert(BS == 16, "tiles are 16 or 32 tokens");
+    consume_subtiles<T, D, BS, NG, 1>(st, kt_a, vt_a, tok0, L, sl2, lane);
   }
 }
 
@@ -332,24 +368,54 @@ struct MergeArea {
   static constexpr int kBytes = kConsumers * (D * kGP + 2 * kGP) * 4;
 };
 
+// Output (g, d) of the consumer warps' states stored by store_state:
+// running max, unnormalised numerator and denominator after rescaling every
+// warp to the common max (all -inf: no token seen, zeros).
+template <int D, int GP>
+__device__ __forceinline__ void warp_merge(const float* Os, const float* Ms, const float* Ls, int g, int d, float& mx,
+                                           float& num, float& den) {
+  mx = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kConsumers; ++w) mx = fmaxf(mx, Ms[w * GP + g]);
+  num = den = 0.f;
+  if (mx == -INFINITY) return;
+#pragma unroll
+  for (int w = 0; w < kConsumers; ++w) {
+    const float mw = Ms[w * GP + g];
+    if (mw == -INFINITY) continue;
+    const float sc = fast_exp2(mw - mx);
+    num += sc * Os[(w * D + d) * GP + g];
+    den += sc * Ls[w * GP + g];
+  }
+}
+
 // =========================================================================
 // Stream-K tensor-core kernel (the default for fp16/bf16).
 //
-// The work is the ordered list of tiles (sequence b, kv head, logical
-// block), W = Hkv * sum_b ceil(L_b / bs) of them.  The grid is one wave of
-// persistent CTAs; CTA p takes tiles [p*W/P, (p+1)*W/P), so every CTA moves
-// the same number of bytes whatever the length mix.  A unit (b, kv head)
-// whose tiles all fall in one CTA is finished there and written to `out`;
-// a unit cut by a range boundary leaves one partial (acc, m, l) per CTA it
-// touches -- at most two per CTA, slot 0 for the unit that started before
-// the range and slot 1 for the unit that continues after it -- and the
-// merge kernel combines them.  Every CTA first rebuilds the per-sequence
-// prefix of block counts in shared memory from seq_lens.
+// The work is the ordered list of tiles (sequence b, kv head, 32 tokens),
+// W = Hkv * sum_b ceil(L_b / 32) of them.  The grid is one wave of
+// persistent CTAs; CTA p takes the tiles whose positions in a cost space
+// (tiles plus a fixed charge per unit) fall in [p*Wc/P, (p+1)*Wc/P), so
+// every CTA moves about the same number of bytes whatever the length mix.
+// A unit (b, kv head) whose tiles all fall in one CTA is finished there and
+// written to `out`.  A unit cut by range boundaries is finished by its
+// owner, the CTA holding its first tiles (the end of the owner's range):
+// every later CTA holding a piece of it writes an unnormalised partial
+// (acc, m, l) to the workspace and releases a ready flag.  Once the owner's
+// producer warp has issued its last tile it waits for those flags and
+// bulk-copies the partials into the stage that frees up next, so the
+// owner's combine, right after its last tile, reads them from shared memory
+// and its own piece from the warp-merge buffer.  Every CTA first rebuilds
+// the per-sequence prefixes of tile counts and costs in shared memory from
+// seq_lens.
 // =========================================================================
 
-// Grid cap: an owner CTA combines up to kMaxSkCtas parts with one row index
-// and G <= 16 weights each, staged in the (idle) stage ring.
+// Grid cap: an owner CTA indexes up to kMaxSkCtas pieces in shared memory.
 constexpr int kMaxSkCtas = 640;
+// An owner's producer warp waits for the later pieces and copies them into
+// stages as the consumers free them on their last tiles (else the consumers
+// wait and read every piece from global memory after the last tile).
+constexpr bool kPrefetchParts = true;
 
 template <typename T, int D, int BS, int NG, int NST>
 struct SkCfg {
@@ -360,9 +426,9 @@ struct SkCfg {
   using TL = Tile<D, kTileTokens>;
   static constexpr int kStages = NST * TL::kStageBytes;
   static constexpr int kMerge = 2 * MergeArea<D, NG>::kBytes;  // double-buffered per segment
-  static constexpr int kFixed = 1024 + kStages + kMerge + 2 * NST * 8;
+  static constexpr int kPartRows = kMaxSkCtas + 8;  // row index per part of a combined unit
+  static constexpr int kFixed = 1024 + kStages + kMerge + 2 * NST * 8 + 16 + kPartRows * 4;
   static int smem_bytes(int B) { return kFixed + (2 * (B + 1) * 4 + 15) / 16 * 16; }
-  static_assert(kStages >= (kMaxSkCtas + 8) * 4, "owner merge part list must fit in the stage ring");
 };
 
 // cta_of(x): the CTA whose range [p*W/P, (p+1)*W/P) holds position x.
@@ -370,13 +436,16 @@ __device__ __forceinline__ int sk_cta_of(int64_t t, int64_t W, int P) {
   return static_cast<int>(((t + 1) * P + W - 1) / W - 1);
 }
 
+
 template <typename T, int D, int BS, int NG, int NST>
-__global__ void __launch_bounds__(kTcThreads)
+__global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)  // two CTAs per SM where shared memory allows
 decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV) {
   using C = SkCfg<T, D, BS, NG, NST>;
   using TL = typename C::TL;
   constexpr int TPB = C::kBlocksPerTile, TT = C::kTileTokens;
+  constexpr int kCopies = 2 * TL::kSub * TPB;  // TMA copies per tile (K and V slabs of each block)
+  static_assert(kCopies <= 32, "one copy per producer lane");
   constexpr int GP = 8 * NG;
   static_assert(NST % kConsumers == 0, "stage s must always be drained by consumer s % kConsumers");
   extern __shared__ uint8_t smem_raw[];
@@ -385,7 +454,9 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   constexpr int kMergeFloats = MergeArea<D, NG>::kBytes / 4;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages + C::kMerge);
   uint64_t* empty = full + NST;
-  int* CB = reinterpret_cast<int*>(empty + NST);  // CB[b] = sum_{b' < b} ceil(L_b' / TT) (tiles)
+  uint64_t* pre_bar = empty + NST;                       // owner: later pieces copied in
+  int* part_row = reinterpret_cast<int*>(pre_bar + 2);  // [kPartRows]
+  int* CB = part_row + C::kPartRows;  // CB[b] = sum_{b' < b} ceil(L_b' / TT) (tiles)
 
   const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
   int* CC = CB + (B + 1);  // CC[b] = sum_{b' < b} cost_b' (tiles + seg_cost, 0 if empty)
@@ -437,6 +508,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
         mbar_init(&full[s], 1);
         mbar_init(&empty[s], 1);
       }
+      mbar_init(pre_bar, 1);
       fence_mbar_init();
     }
     __syncthreads();
@@ -473,19 +545,6 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   if (t0 >= t1) return;
   const int n = static_cast<int>(t1 - t0);
 
-  // ---- locate the first tile: largest b with Hkv * CB[b] <= t0 ----
-  int b0;
-  {
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (static_cast<int64_t>(Hkv) * CB[mid] <= t0) lo = mid; else hi = mid - 1;
-    }
-    b0 = lo;
-  }
-  const int nb0 = CB[b0 + 1] - CB[b0];
-  const int rel0 = static_cast<int>(t0 - static_cast<int64_t>(Hkv) * CB[b0]);
-
   // Tile cursor shared by producer and consumers: advances (blk, kvh, b).
   struct Cursor {
     int b, kvh, blk, nb;
@@ -502,6 +561,48 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       }
     }
   };
+  // cursor of tile t < W: the largest b with Hkv * CB[b] <= t is never empty
+  auto locate = [&](int64_t t) -> Cursor {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (static_cast<int64_t>(Hkv) * CB[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int nb = CB[lo + 1] - CB[lo];
+    const int rel = static_cast<int>(t - static_cast<int64_t>(Hkv) * CB[lo]);
+    return Cursor{lo, rel / nb, rel % nb, nb};
+  };
+
+  // ---- the unit cut at the range end, if any: this CTA (its owner)
+  // combines it with the pieces later CTAs hold ----
+  // Given the cursor of the range's last tile: the unit started inside the
+  // range and goes on after it.  Its other pieces are the later CTAs up to
+  // `last` (the one holding the unit's last tile) whose cost ranges are not
+  // empty: their ranges lie inside the unit's tiles.
+  auto owner_of = [&](const Cursor& lc, int& last) -> bool {
+    const bool own = lc.blk <= n - 1 && lc.blk + 1 < lc.nb;
+    last = pid;
+    if (own) {
+      const int cs = CC[lc.b + 1] - CC[lc.b];
+      last = sk_cta_of(
+          static_cast<int64_t>(Hkv) * CC[lc.b] + static_cast<int64_t>(lc.kvh) * cs + p.seg_cost + lc.nb - 1, Wc, P);
+    }
+    return own;
+  };
+  // The first pieces (up to the capacity of one stage) are copied into the
+  // stage that frees up after the last tile, so the owner's combine reads
+  // them from shared memory; further pieces are read from global memory.
+  // Piece i goes to the stage virtual tile n + i / per_stage would use,
+  // which frees up once tile n + i / per_stage - NST is consumed.
+  const int part_o = G * D * 4, part_ml = (G * 8 + 15) & ~15, part_bytes = part_o + part_ml;
+  const int per_stage = TL::kStageBytes / part_bytes;  // >= 1 for every supported shape
+  auto npre_of = [&](int last) {
+    return kPrefetchParts && Wc >= P ? min(min(NST * per_stage, 32), last - pid) : 0;
+  };
+  auto pre_part = [&](int i) {
+    return smem + ((n + i / per_stage) % NST) * TL::kStageBytes + (i % per_stage) * part_bytes;
+  };
+  const Cursor c_first = locate(t0);
 
   if (warp == 0) {
     // ---------------- producer ----------------
@@ -509,7 +610,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
     }
-    Cursor c{b0, rel0 / nb0, rel0 % nb0, nb0};  // c.blk counts tiles of TPB blocks
+    Cursor c = c_first;  // c.blk counts tiles of TPB blocks
     // Block-table entries are fetched 32 at a time (one per lane; entries
     // past the sequence are fetched but never used) and the chunk the walk
     // needs next is fetched while the current one is used.
@@ -548,44 +649,75 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           next_b = -1;
         }
       }
-      int pbs[TPB];
-#pragma unroll
-      for (int r = 0; r < TPB; ++r) pbs[r] = __shfl_sync(0xffffffffu, mine, (blk + r) & 31);
+      // One copy per lane: lane l < kCopies loads block r = l / (2 * kSub) of
+      // the tile, column slab (l / 2) % kSub, K for even l and V for odd l.
+      const int cr = lane / (2 * TL::kSub), csl = (lane >> 1) % TL::kSub;
+      int pb = __shfl_sync(0xffffffffu, mine, (blk + min(cr, TPB - 1)) & 31);
       const int here = min(TPB, cache_nblk - blk);  // blocks of this tile inside the sequence (>= 1)
+      const int s = j % NST;
       if (lane == 0) {
-        const int s = j % NST;
         if (j >= NST) ok = mbar_wait_bounded(&empty[s], ((j / NST) - 1) & 1);
-        if (ok) {
-          mbar_arrive_expect_tx(&full[s], here * (TL::kStageBytes / TPB));
-          uint8_t* kt = smem + s * TL::kStageBytes;
-          uint8_t* vt = kt + TL::kTileBytes;
-#pragma unroll
-          for (int r = 0; r < TPB; ++r) {
-            if (r < here) {
-              int pb = pbs[r];
-              if (pb < 0 || pb >= p.num_blocks) {
-                record_error(KV_ERR_DEVICE_BOUNDS);
-                pb = 0;
-              }
-#pragma unroll
-              for (int sl = 0; sl < TL::kSub; ++sl) {
-                const int off = sl * TL::kSlabBytes + r * BS * 128;
-                tma_load_3d(kt + off, &tmK, &full[s], sl * 64, c.kvh, pb * BS);
-                tma_load_3d(vt + off, &tmV, &full[s], sl * 64, c.kvh, pb * BS);
-              }
+        if (ok) mbar_arrive_expect_tx(&full[s], here * (TL::kStageBytes / TPB));
+      }
+      __syncwarp();
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (ok && lane < kCopies && cr < here) {
+        if (pb < 0 || pb >= p.num_blocks) {
+          record_error(KV_ERR_DEVICE_BOUNDS);
+          pb = 0;
+        }
+        uint8_t* dst = smem + s * TL::kStageBytes + (lane & 1) * TL::kTileBytes + csl * TL::kSlabBytes + cr * BS * 128;
+        tma_load_3d(dst, (lane & 1) ? &tmV : &tmK, &full[s], csl * 64, c.kvh, pb * BS);
+      }
+      if (ok) ++issued;
+      if (j + 1 < n) advance(c);
+    }
+    int last;
+    const bool owner = owner_of(c, last);
+    const int npre = npre_of(last);
+    if (kPrefetchParts && owner) {
+      // Wait (bounded) for every later piece's ready flag; each flag has
+      // this one reader, which clears it, so flags are zero between calls
+      // even when a replayed launch reuses its epoch.  Those CTAs publish
+      // their first piece before they wait on anyone: no cycle.
+      for (int q0 = pid + 1; q0 <= last; q0 += 32) {
+        const int q = q0 + lane;
+        if (q <= last && static_cast<int64_t>(q) * Wc / P != static_cast<int64_t>(q + 1) * Wc / P) {
+          const uint64_t t_start = globaltimer_ns();
+          while (ok && ld_acquire_gpu(p.ws_flags + q) != p.epoch) {
+            if (globaltimer_ns() - t_start > kWaitLimitNs) {
+              record_error(KV_ERR_DEVICE_TIMEOUT);
+              ok = 0;
             }
+            __nanosleep(32);
           }
-          ++issued;
+          p.ws_flags[q] = 0;
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      advance(c);
+      fence_proxy_async_global();  // the partials acquired above, before the bulk copies read them
+      if (lane == 0) {
+        if (npre > 0) {
+          mbar_arrive_expect_tx(pre_bar, npre * (part_o + part_ml));
+          // the stages the pieces go to (virtual tiles n, n + 1, ...) must be free
+          for (int v = n; (v - n) * per_stage < npre; ++v)
+            if (v >= NST) mbar_wait_bounded(&empty[v % NST], ((v / NST) - 1) & 1);
+        } else {
+          mbar_arrive(pre_bar);
+        }
+      }
+      __syncwarp();
+      if (lane < npre) {  // lane i acquired piece i's flag above and copies it (npre <= 32)
+        const int64_t row = static_cast<int64_t>(pid + 1 + lane) * 2 * G;  // slot 0 of CTA pid + 1 + lane
+        bulk_load(pre_part(lane), p.ws_o + row * D, part_o, pre_bar);
+        bulk_load(pre_part(lane) + part_o, p.ws_ml + row * 2, part_ml, pre_bar);
+      }
     }
     if (lane == 0) {  // keep the CTA alive until every issued copy has landed (bounded)
       for (int s = 0; s < NST && s < issued; ++s) {
-        const int last = s + ((issued - 1 - s) / NST) * NST;
-        mbar_wait_bounded(&full[s], (last / NST) & 1);
+        const int lst = s + ((issued - 1 - s) / NST) * NST;
+        mbar_wait_bounded(&full[s], (lst / NST) & 1);
       }
+      if (kPrefetchParts && owner && npre > 0) mbar_wait_bounded(pre_bar, 0);
     }
     return;
   }
@@ -593,7 +725,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   // ---------------- consumers ----------------
   const int cw = warp - 1, ctid = tid - 32;
   WarpState<D, NG> st;
-  Cursor c{b0, rel0 / nb0, rel0 % nb0, nb0};
+  Cursor c = c_first;
   const float sl2 = p.scale_log2;
   int ok = 1;
   int64_t unit_start = static_cast<int64_t>(Hkv) * CB[c.b] + static_cast<int64_t>(c.kvh) * c.nb;
@@ -618,8 +750,6 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   prefetch_next(c, unit_start);
   reset_state(st);
   int seg = 0;
-  bool owner = false;
-  int own_nb = 0, own_b = 0, own_kvh = 0;
   for (int j = 0; j < n; ++j) {
     if (ok && (j & (kConsumers - 1)) == cw) {
       const int s = j % NST;
@@ -648,7 +778,9 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       ++seg;
       store_state(st, Os, Ms, Ls, cw, lane);
       named_barrier_sync(1, kConsumers * 32);
-      for (int idx = ctid; idx < G * D; idx += kConsumers * 32) {
+      // the owner's own piece stays in the merge buffer for its combine
+      const bool keep = kPrefetchParts && j == n - 1 && !whole && slot == 1;
+      for (int idx = keep ? G * D : ctid; idx < G * D; idx += kConsumers * 32) {
         const int g = idx / D, d = idx - g * D;
         float mx = -INFINITY;
 #pragma unroll
@@ -685,12 +817,6 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           st_release_gpu(p.ws_flags + pid, p.epoch);
         }
       }
-      if (j == n - 1 && !whole && slot == 1) {
-        owner = true;  // the unit continues in later CTAs: this CTA combines it
-        own_nb = c.nb;
-        own_b = c.b;
-        own_kvh = c.kvh;
-      }
       if (j + 1 < n) {
         advance(c);
         unit_start = static_cast<int64_t>(Hkv) * CB[c.b] + static_cast<int64_t>(c.kvh) * c.nb;
@@ -713,54 +839,53 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       advance(c);
     }
   }
-  if (!owner) return;
+  int last;
+  if (!owner_of(c, last)) return;
+  const int npre = npre_of(last);
 
-  // ---- this CTA holds the first part of a unit that later CTAs continue:
-  // wait for their slot-0 partials and write the unit's output ----
-  named_barrier_sync(1, kConsumers * 32);  // own slot-1 partial stored
-  // cost position of the unit's last tile -> the last CTA holding part of it
-  const int own_cs = CC[own_b + 1] - CC[own_b];
-  const int64_t last_pos = static_cast<int64_t>(Hkv) * CC[own_b] + static_cast<int64_t>(own_kvh) * own_cs +
-                           p.seg_cost + own_nb - 1;
-  const int last = sk_cta_of(last_pos, Wc, P);
-  // CTAs between this one and `last` with a non-empty cost range lie inside
-  // the unit's tiles, so each of them holds a part of it.
-  const int nparts = last - pid + 1;
-  const int npad = (nparts + 7) & ~7;  // padded to the 8-part batches below
-  // the stage ring is idle now: every issued tile has been consumed
-  int* part_row = reinterpret_cast<int*>(smem);  // [npad]: row base (cta * 2 + slot) * G, or -1
-  if (cw == 0) {
-    // every wait points at a later CTA of the same (co-resident) grid, and
-    // those publish before they wait on anyone: no cycle
-    // Each flag has exactly this one reader, which clears it once seen, so
-    // flags are zero between calls even when a replayed launch reuses its
-    // epoch.
+  // ---- owner: combine this CTA's piece with the later pieces ----
+  const float* Os = merge_base + ((seg - 1) & 1) * kMergeFloats;
+  const float* Ms = Os + kConsumers * D * GP;
+  const float* Ls = Ms + kConsumers * GP;
+  // Pieces read from global memory: CTAs qs..last (this CTA's own slot-1
+  // row first when its piece was not kept in shared memory).
+  const int qs = kPrefetchParts ? pid + 1 + npre : pid;
+  const int nrest = last - qs + 1, nrest_pad = (nrest + 7) & ~7;
+  if (!kPrefetchParts && cw == 0) {
+    // wait for the later pieces' ready flags (bounded) and clear them: each
+    // flag has this one reader, so flags are zero between calls even when a
+    // replayed launch reuses its epoch
     for (int q = pid + 1 + lane; q <= last; q += 32) {
-      const int64_t q0 = static_cast<int64_t>(q) * Wc / P, q1 = static_cast<int64_t>(q + 1) * Wc / P;
-      if (q0 != q1) {
-        wait_flag_bounded(p.ws_flags + q, p.epoch);
+      if (static_cast<int64_t>(q) * Wc / P != static_cast<int64_t>(q + 1) * Wc / P) {
+        const uint64_t t_start = globaltimer_ns();
+        while (ld_acquire_gpu(p.ws_flags + q) != p.epoch) {
+          if (globaltimer_ns() - t_start > kWaitLimitNs) {
+            record_error(KV_ERR_DEVICE_TIMEOUT);
+            break;
+          }
+          __nanosleep(32);
+        }
         p.ws_flags[q] = 0;
       }
     }
-  } else {
-    for (int k = ctid - 32; k < npad; k += (kConsumers - 1) * 32) {
-      const int q = pid + k;
-      int row = -1;
-      if (k == 0) {
-        row = (pid * 2 + 1) * G;
-      } else if (k < nparts) {
-        const int64_t q0 = static_cast<int64_t>(q) * Wc / P, q1 = static_cast<int64_t>(q + 1) * Wc / P;
-        row = q0 == q1 ? -1 : q * 2 * G;
-      }
-      part_row[k] = row;
+  }
+  for (int k = ctid; k < nrest_pad; k += kConsumers * 32) {
+    const int q = qs + k;
+    int row = -1;
+    if (k < nrest) {
+      if (q == pid) row = (pid * 2 + 1) * G;
+      else if (static_cast<int64_t>(q) * Wc / P != static_cast<int64_t>(q + 1) * Wc / P) row = q * 2 * G;
     }
+    part_row[k] = row;
+  }
+  if (kPrefetchParts) {
+    if (lane == 0) mbar_wait_bounded(pre_bar, 0);
+    __syncwarp();
   }
   named_barrier_sync(1, kConsumers * 32);
-  // Each output combines all parts by an online log-sum-exp over batches of
-  // 8 parts.  A thread takes up to 4 outputs at once and issues all their
-  // (m, l, acc) loads for a batch before using any, so a batch costs one
-  // round trip to L2 whatever the output count.
-  T* o = static_cast<T*>(p.out) + (static_cast<int64_t>(own_b) * p.num_heads + own_kvh * G) * D;
+  // A thread takes up to 4 outputs at once and issues all their loads of a
+  // batch of 8 pieces before using any, so a batch costs one round trip.
+  T* o = static_cast<T*>(p.out) + (static_cast<int64_t>(c.b) * p.num_heads + c.kvh * G) * D;
   constexpr int kOut = 4, kParts = 8, kStride = kConsumers * 32;
   for (int base = ctid; base < G * D; base += kStride * kOut) {
     float mx[kOut], num[kOut], den[kOut];
@@ -770,10 +895,28 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       const int idx = min(base + i * kStride, G * D - 1);
       gi[i] = idx / D;
       di[i] = idx - gi[i] * D;
-      mx[i] = -INFINITY;
-      num[i] = den[i] = 0.f;
+      if (kPrefetchParts) {
+        warp_merge<D, GP>(Os, Ms, Ls, gi[i], di[i], mx[i], num[i], den[i]);
+      } else {
+        mx[i] = -INFINITY;
+        num[i] = den[i] = 0.f;
+      }
     }
-    for (int k0 = 0; k0 < npad; k0 += kParts) {
+    auto add = [&](int i, float m2, float l2, float a2) {
+      if (m2 == -INFINITY) return;
+      const float nm = fmaxf(mx[i], m2);
+      const float so = fast_exp2(mx[i] - nm), sn = fast_exp2(m2 - nm);
+      num[i] = num[i] * so + sn * a2;
+      den[i] = den[i] * so + sn * l2;
+      mx[i] = nm;
+    };
+    for (int u = 0; u < npre; ++u) {
+      const float* po = reinterpret_cast<const float*>(pre_part(u));
+      const float* pml = reinterpret_cast<const float*>(pre_part(u) + part_o);
+#pragma unroll
+      for (int i = 0; i < kOut; ++i) add(i, pml[gi[i] * 2], pml[gi[i] * 2 + 1], po[gi[i] * D + di[i]]);
+    }
+    for (int k0 = 0; k0 < nrest_pad; k0 += kParts) {
       float mk[kOut][kParts], lk[kOut][kParts], ak[kOut][kParts];
 #pragma unroll
       for (int u = 0; u < kParts; ++u) {
@@ -781,22 +924,15 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
 #pragma unroll
         for (int i = 0; i < kOut; ++i) {
           const int64_t r = rb + gi[i];
-          mk[i][u] = rb >= 0 ? p.ws_ml[r * 2] : -INFINITY;
-          lk[i][u] = rb >= 0 ? p.ws_ml[r * 2 + 1] : 0.f;
-          ak[i][u] = rb >= 0 ? p.ws_o[r * D + di[i]] : 0.f;
+          mk[i][u] = rb >= 0 ? __ldcg(p.ws_ml + r * 2) : -INFINITY;
+          lk[i][u] = rb >= 0 ? __ldcg(p.ws_ml + r * 2 + 1) : 0.f;
+          ak[i][u] = rb >= 0 ? __ldcg(p.ws_o + r * D + di[i]) : 0.f;
         }
       }
 #pragma unroll
       for (int i = 0; i < kOut; ++i)
 #pragma unroll
-        for (int u = 0; u < kParts; ++u) {
-          if (mk[i][u] == -INFINITY) continue;
-          const float nm = fmaxf(mx[i], mk[i][u]);
-          const float so = fast_exp2(mx[i] - nm), sn = fast_exp2(mk[i][u] - nm);
-          num[i] = num[i] * so + sn * ak[i][u];
-          den[i] = den[i] * so + sn * lk[i][u];
-          mx[i] = nm;
-        }
+        for (int u = 0; u < kParts; ++u) add(i, mk[i][u], lk[i][u], ak[i][u]);
     }
 #pragma unroll
     for (int i = 0; i < kOut; ++i) {
@@ -808,8 +944,9 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
 
 // =========================================================================
 // Split tensor-core kernel: one CTA per (split, kv head, sequence).  Used
-// when the batch is too large for the stream-K kernel's shared-memory
-// prefix (more than kMaxSkSeqs sequences).
+// when the stream-K kernel's shared memory would not fit: more than
+// kMaxSkSeqs sequences, or head_dim 256 with more than 8 query heads per kv
+// head (stage ring plus double-buffered warp merge area).
 // =========================================================================
 
 constexpr int kMaxSkSeqs = 4096;
@@ -1135,6 +1272,51 @@ int sm_count() {
   return cached[dev];
 }
 
+// Pipeline depth: about 64 KB of K+V in flight per CTA, 4..12 stages.
+// The stage count must be a multiple of the consumer count: stage s is then
+// always drained by consumer s % kConsumers, each consumer meets a stage's
+// phases in order, and a parity wait can never be satisfied by a phase one
+// round old (with 6 stages and 4 consumers, tile j + 6 would belong to a
+// different warp than tile j and could pass its wait before tile j landed).
+template <int D, int BS>
+struct Stages {
+  static constexpr int kRaw = ((64 * 1024) / Tile<D, BS>::kStageBytes) / kConsumers * kConsumers;
+  static constexpr int value = kRaw < kConsumers ? kConsumers : (kRaw > 12 ? 12 : kRaw);
+  static_assert(value % kConsumers == 0, "stages must be a multiple of the consumer warps");
+};
+
+// Shared memory of the stream-K kernel for a batch of B sequences (type
+// size 2; the stage count follows the 32-token tile).
+template <int D, int BS, int NG>
+int sk_smem_for(int B) {
+  constexpr int kTileTokens = BS >= 32 ? BS : 32;
+  return SkCfg<__half, D, BS, NG, Stages<D, kTileTokens>::value>::smem_bytes(B);
+}
+
+template <int D, int BS>
+int sk_smem_ng(int G, int B) {
+  return G <= 8 ? sk_smem_for<D, BS, 1>(B) : sk_smem_for<D, BS, 2>(B);
+}
+
+int sk_smem_bytes(int D, int BS, int G, int B) {
+  if (D == 64) return BS == 16 ? sk_smem_ng<64, 16>(G, B) : sk_smem_ng<64, 32>(G, B);
+  if (D == 128) return BS == 16 ? sk_smem_ng<128, 16>(G, B) : sk_smem_ng<128, 32>(G, B);
+  return BS == 16 ? sk_smem_ng<256, 16>(G, B) : sk_smem_ng<256, 32>(G, B);
+}
+
+int max_smem_optin() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cached[dev] = n > 0 ? n : 48 * 1024;
+  }
+  return cached[dev];
+}
+
 bool tc_supported(int dtype, int D, int BS, int G) {
   return dtype != KV_DTYPE_F32 && (D == 64 || D == 128 || D == 256) && (BS == 16 || BS == 32) && G >= 1 &&
          G <= 16;
@@ -1146,7 +1328,8 @@ Plan make_plan(int B, int Hq, int Hkv, int D, int BS, int64_t max_seq_len, int b
   Plan pl{};
   const int G = Hkv > 0 ? Hq / Hkv : 1;
   const int64_t maxblk = std::max<int64_t>(1, (max_seq_len + BS - 1) / BS);
-  if (tc_supported(dtype, D, BS, G) && bps_req == 0 && B <= kMaxSkSeqs) {
+  if (tc_supported(dtype, D, BS, G) && bps_req == 0 && B <= kMaxSkSeqs &&
+      sk_smem_bytes(D, BS, G, B) <= max_smem_optin()) {
     pl.kind = kTensorCoreStreamK;
     const int64_t w_upper = std::max<int64_t>(1, static_cast<int64_t>(B) * Hkv * maxblk);
     pl.num_ctas = static_cast<int>(std::min<int64_t>(
@@ -1243,18 +1426,6 @@ bool get_tensor_map(const void* cache, int64_t rows, int hkv, int d, int bs, CUt
 
 // ---- launches ----------------------------------------------------------------
 
-// Pipeline depth: about 64 KB of K+V in flight per CTA, 4..12 stages.
-// The stage count must be a multiple of the consumer count: stage s is then
-// always drained by consumer s % kConsumers, each consumer meets a stage's
-// phases in order, and a parity wait can never be satisfied by a phase one
-// round old (with 6 stages and 4 consumers, tile j + 6 would belong to a
-// different warp than tile j and could pass its wait before tile j landed).
-template <int D, int BS>
-struct Stages {
-  static constexpr int kRaw = ((64 * 1024) / Tile<D, BS>::kStageBytes) / kConsumers * kConsumers;
-  static constexpr int value = kRaw < kConsumers ? kConsumers : (kRaw > 12 ? 12 : kRaw);
-  static_assert(value % kConsumers == 0, "stages must be a multiple of the consumer warps");
-};
 
 // Raise a kernel's dynamic shared memory limit to `bytes` (per device, only
 // when it grows).

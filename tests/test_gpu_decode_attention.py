@@ -94,6 +94,15 @@ def test_tensor_core_path(dtype, hq, hkv, d, bs):
     run_case(dtype, hq, hkv, d, bs, LENS_A, seed=hq * 1000 + d + bs, bps=5)   # split kernel
 
 
+def test_wide_group_d256_takes_split_kernel():
+    """head_dim 256 with 12 query heads per kv head: the stream-K kernel's
+    stage ring and merge area would exceed shared memory, so the plan takes
+    the split tensor-core kernel, which must still match the oracle."""
+    plan = pk.decode_plan(len(LENS_A), 24, 2, 256, 16, max(LENS_A), TORCH["bf16"])
+    assert plan.kernel == 1
+    run_case("bf16", 24, 2, 256, 16, LENS_A, seed=2562)
+
+
 @pytest.mark.parametrize("dtype,hq,hkv,d,bs", [
     ("f32", 2, 1, 8, 4),         # the tiny fp32 workload's shape
     ("f32", 6, 2, 32, 16),

@@ -63,8 +63,9 @@ def test_static_scratch_matches_workspace_call_twice(dtype, hq, hkv, d, bs, lens
 
 def test_static_scratch_rejects_sizes_beyond_its_maximum():
     dev = torch.device("cuda")
-    d, hq, hkv, bs = 256, 32, 2, 16          # 16 heads per kv head at head dim 256
+    d, hq, hkv, bs = 256, 16, 2, 16          # 8 heads per kv head at head dim 256
     plan = pk.decode_plan(2, hq, hkv, d, bs, 4096, torch.bfloat16)
+    assert plan.kernel == 2                  # stream-K: two partial rows per CTA
     assert plan.workspace_bytes > kernels.static_scratch_bytes()
     kc = torch.zeros(8, bs, hkv, d, dtype=torch.bfloat16, device=dev)
     q = torch.zeros(2, hq, d, dtype=torch.bfloat16, device=dev)
