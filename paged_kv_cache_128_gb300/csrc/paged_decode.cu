@@ -88,11 +88,11 @@ __device__ __forceinline__ int checked_len(const DecodeParams& p, int b) {
 
 // Combine per-warp states (m, l, acc) held in shared memory and write either
 // the final output (single split for this sequence) or this split's partial.
-// Ms/Ls: [nw][gstride], Os: [nw][D][gstride].  Threads tid..nthreads.
+// Ms/Ls: [nw][gstride], Os: [nw][gstride][dstride].  Threads tid..nthreads.
 template <typename T>
 __device__ __forceinline__ void combine_and_store(const DecodeParams& p, const float* Ms, const float* Ls,
-                                                  const float* Os, int nw, int gstride, int D, int b, int qh0,
-                                                  int gn, int split, bool single, int tid, int nthreads) {
+                                                  const float* Os, int nw, int gstride, int dstride, int D, int b,
+                                                  int qh0, int gn, int split, bool single, int tid, int nthreads) {
   for (int idx = tid; idx < gn * D; idx += nthreads) {
     const int g = idx / D, d = idx - g * D;
     float mx = -INFINITY;
@@ -103,7 +103,7 @@ __device__ __forceinline__ void combine_and_store(const DecodeParams& p, const f
         const float mw = Ms[w * gstride + g];
         if (mw == -INFINITY) continue;
         const float sc = fast_exp2(mw - mx);
-        num += sc * Os[(w * D + d) * gstride + g];
+        num += sc * Os[(w * gstride + g) * dstride + d];
         den += sc * Ls[w * gstride + g];
       }
     }
@@ -325,8 +325,14 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NG>& st, uint8_t* kt, 
   }
 }
 
+// Row stride of a head's accumulator in the warp-merge buffer: padded by 4
+// floats so that both the fragment stores below and float4 reads of
+// consecutive d are free of bank conflicts.
+template <int D>
+__host__ __device__ constexpr int merge_row() { return D + 4; }
+
 // Reduce l across the lanes that share a head, then store this warp's
-// state: Os[cw][d][GP], Ms[cw][GP], Ls[cw][GP] (GP = 8 * NG).
+// state: Os[cw][g][DP], Ms[cw][GP], Ls[cw][GP] (GP = 8 * NG, DP = D + 4).
 template <int D, int NG>
 __device__ __forceinline__ void store_state(WarpState<D, NG>& st, float* Os, float* Ms, float* Ls, int cw,
                                             int lane) {
@@ -337,16 +343,17 @@ __device__ __forceinline__ void store_state(WarpState<D, NG>& st, float* Os, flo
     for (int c = 0; c < 2; ++c)
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) st.l[ng][c] += __shfl_xor_sync(0xffffffffu, st.l[ng][c], off);
-  float* o = Os + cw * D * GP;
+  constexpr int DP = merge_row<D>();
+  float* o = Os + cw * GP * DP;
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt)
 #pragma unroll
     for (int ng = 0; ng < NG; ++ng) {
       const int d0 = mt * 16 + (lane >> 2), g0 = ng * 8 + (lane & 3) * 2;
-      o[d0 * GP + g0] = st.acc[mt][ng][0];
-      o[d0 * GP + g0 + 1] = st.acc[mt][ng][1];
-      o[(d0 + 8) * GP + g0] = st.acc[mt][ng][2];
-      o[(d0 + 8) * GP + g0 + 1] = st.acc[mt][ng][3];
+      o[g0 * DP + d0] = st.acc[mt][ng][0];
+      o[(g0 + 1) * DP + d0] = st.acc[mt][ng][1];
+      o[g0 * DP + d0 + 8] = st.acc[mt][ng][2];
+      o[(g0 + 1) * DP + d0 + 8] = st.acc[mt][ng][3];
     }
   if (lane < 4) {
 #pragma unroll
@@ -365,7 +372,7 @@ constexpr int kTcThreads = 32 * (kConsumers + 1);
 template <int D, int NG>
 struct MergeArea {
   static constexpr int kGP = 8 * NG;
-  static constexpr int kBytes = kConsumers * (D * kGP + 2 * kGP) * 4;
+  static constexpr int kBytes = kConsumers * (merge_row<D>() * kGP + 2 * kGP) * 4;
 };
 
 // Output (g, d) of the consumer warps' states stored by store_state:
@@ -384,7 +391,7 @@ __device__ __forceinline__ void warp_merge(const float* Os, const float* Ms, con
     const float mw = Ms[w * GP + g];
     if (mw == -INFINITY) continue;
     const float sc = fast_exp2(mw - mx);
-    num += sc * Os[(w * D + d) * GP + g];
+    num += sc * Os[(w * GP + g) * merge_row<D>() + d];
     den += sc * Ls[w * GP + g];
   }
 }
@@ -695,6 +702,10 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
         }
       }
       fence_proxy_async_global();  // the partials acquired above, before the bulk copies read them
+      // Every lane's flags are seen before lane 0 signals pre_bar: with no
+      // piece to copy its arrive alone releases the consumers, who then read
+      // all pieces from global memory.
+      __syncwarp();
       if (lane == 0) {
         if (npre > 0) {
           mbar_arrive_expect_tx(pre_bar, npre * (part_o + part_ml));
@@ -773,35 +784,46 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       // also guarantees that every thread has finished reading the buffer
       // of the segment before, which the next segment will overwrite.
       float* Os = merge_base + (seg & 1) * kMergeFloats;
-      float* Ms = Os + kConsumers * D * GP;
+      float* Ms = Os + kConsumers * merge_row<D>() * GP;
       float* Ls = Ms + kConsumers * GP;
       ++seg;
       store_state(st, Os, Ms, Ls, cw, lane);
       named_barrier_sync(1, kConsumers * 32);
       // the owner's own piece stays in the merge buffer for its combine
       const bool keep = kPrefetchParts && j == n - 1 && !whole && slot == 1;
-      for (int idx = keep ? G * D : ctid; idx < G * D; idx += kConsumers * 32) {
-        const int g = idx / D, d = idx - g * D;
+      // each thread merges four adjacent outputs of one head (float4 reads)
+      constexpr int kD4 = D / 4, DP = merge_row<D>();
+      for (int v = keep ? G * kD4 : ctid; v < G * kD4; v += kConsumers * 32) {
+        const int g = v / kD4, d = (v - g * kD4) * 4;
         float mx = -INFINITY;
 #pragma unroll
         for (int w2 = 0; w2 < kConsumers; ++w2) mx = fmaxf(mx, Ms[w2 * GP + g]);
-        float num = 0.f, den = 0.f;
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+        float den = 0.f;
         if (mx != -INFINITY) {
 #pragma unroll
           for (int w2 = 0; w2 < kConsumers; ++w2) {
             const float mw = Ms[w2 * GP + g];
             if (mw == -INFINITY) continue;
             const float sc = fast_exp2(mw - mx);
-            num += sc * Os[(w2 * D + d) * GP + g];
+            const float4 o4 = *reinterpret_cast<const float4*>(Os + (w2 * GP + g) * DP + d);
+            num.x += sc * o4.x;
+            num.y += sc * o4.y;
+            num.z += sc * o4.z;
+            num.w += sc * o4.w;
             den += sc * Ls[w2 * GP + g];
           }
         }
         if (whole) {
+          const float inv = den > 0.f ? 1.f / den : 0.f;
           T* o = static_cast<T*>(p.out) + (static_cast<int64_t>(c.b) * p.num_heads + c.kvh * G + g) * D + d;
-          *o = DType<T>::from_float(den > 0.f ? num / den : 0.f);
+          o[0] = DType<T>::from_float(num.x * inv);
+          o[1] = DType<T>::from_float(num.y * inv);
+          o[2] = DType<T>::from_float(num.z * inv);
+          o[3] = DType<T>::from_float(num.w * inv);
         } else {
           const int64_t r = (static_cast<int64_t>(pid) * 2 + slot) * G + g;
-          p.ws_o[r * D + d] = num;
+          *reinterpret_cast<float4*>(p.ws_o + r * D + d) = num;
           if (d == 0) {
             p.ws_ml[r * 2 + 0] = mx;
             p.ws_ml[r * 2 + 1] = den;
@@ -812,10 +834,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
         // publish the partial of a unit that started in an earlier CTA: all
         // consumer threads' stores precede the release of the flag
         named_barrier_sync(1, kConsumers * 32);
-        if (ctid == 0) {
-          __threadfence();
-          st_release_gpu(p.ws_flags + pid, p.epoch);
-        }
+        if (ctid == 0) st_release_gpu(p.ws_flags + pid, p.epoch);
       }
       if (j + 1 < n) {
         advance(c);
@@ -845,7 +864,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
 
   // ---- owner: combine this CTA's piece with the later pieces ----
   const float* Os = merge_base + ((seg - 1) & 1) * kMergeFloats;
-  const float* Ms = Os + kConsumers * D * GP;
+  const float* Ms = Os + kConsumers * merge_row<D>() * GP;
   const float* Ls = Ms + kConsumers * GP;
   // Pieces read from global memory: CTAs qs..last (this CTA's own slot-1
   // row first when its piece was not kept in shared memory).
@@ -1057,12 +1076,12 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
   }
   named_barrier_sync(1, kConsumers * 32);  // all stages consumed: reuse them for the merge
   float* Os = reinterpret_cast<float*>(smem);
-  float* Ms = Os + kConsumers * D * GP;
+  float* Ms = Os + kConsumers * merge_row<D>() * GP;
   float* Ls = Ms + kConsumers * GP;
   store_state(st, Os, Ms, Ls, cw, lane);
   named_barrier_sync(1, kConsumers * 32);
-  combine_and_store<T>(p, Ms, Ls, Os, kConsumers, GP, D, b, kvh * G, G, split, nsplit_b == 1, ctid,
-                       kConsumers * 32);
+  combine_and_store<T>(p, Ms, Ls, Os, kConsumers, GP, merge_row<D>(), D, b, kvh * G, G, split, nsplit_b == 1,
+                       ctid, kConsumers * 32);
 }
 
 // =========================================================================
@@ -1241,9 +1260,10 @@ struct Plan {
 constexpr int kMaxSkCtasPerSm = 4;
 
 // Tiles' worth of time one unit boundary costs a stream-K CTA (cross-warp
-// merge, output or partial write): about 64 KB of streaming, measured on
-// GB300 over the 4-16 KB stage sizes (the sweep was flat within 1-2x).
-int seg_cost_tiles(int stage_bytes) { return std::max(1, 65536 / stage_bytes); }
+// merge, output or partial write): about 48 KB of streaming, at most 4
+// tiles, measured on GB300 (charges of 0-6 tiles swept on the 32-token
+// tiles of head_dim 64 and 128; 3-4 within 1 % of the best everywhere).
+int seg_cost_tiles(int stage_bytes) { return std::max(1, std::min(4, 49152 / stage_bytes)); }
 
 // Tag of one stream-K call: a per-process random base plus a call counter,
 // so a ready flag left by any other call (or uninitialised workspace) does

@@ -20,7 +20,8 @@ from tests.helpers import TOL, TORCH, oracle_paged_pool, sentinel_tensor, to_f64
 pytestmark = pytest.mark.gpu
 
 
-def run_case(dtype, hq, hkv, d, bs, lens, seed, bps=0, nb=None, scale=None, value_scale=1.0, max_seq_len=None):
+def run_case(dtype, hq, hkv, d, bs, lens, seed, bps=0, nb=None, scale=None, value_scale=1.0, max_seq_len=None,
+             repeat=1):
     rng = np.random.default_rng(seed)
     B = len(lens)
     nb = nb or sum(-(-L // bs) for L in lens) + 3
@@ -54,6 +55,15 @@ def run_case(dtype, hq, hkv, d, bs, lens, seed, bps=0, nb=None, scale=None, valu
     pk.paged_decode_attention(out, q.to(dev), kc, vc, torch.from_numpy(tables).to(dev),
                               torch.from_numpy(seq_lens).to(dev), scale, max_seq_len or max(max(lens), 1), bps)
     assert pk.device_error() == 0
+    if repeat > 1:
+        # the partition fixes the combine order: every call is bit-identical
+        d_q, d_t, d_l = q.to(dev), torch.from_numpy(tables).to(dev), torch.from_numpy(seq_lens).to(dev)
+        again = torch.empty_like(out)
+        for _ in range(repeat - 1):
+            again.fill_(0)
+            pk.paged_decode_attention(again, d_q, kc, vc, d_t, d_l, scale, max_seq_len or max(max(lens), 1), bps)
+            assert torch.equal(again, out)
+        assert pk.device_error() == 0
 
     # oracle side
     ora, kco, vco, _ = oracle_paged_pool(lens, nb, bs, hkv, d, dtype, order, to_storage(k_hist, dtype),
@@ -128,6 +138,18 @@ def test_split_invariance(dtype, hq, hkv, d, bs):
         outs.append(got)
     for o in outs[1:]:
         assert np.max(np.abs(o - outs[0])) <= 2 * TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype,hq,hkv,d,bs,lens", [
+    ("bf16", 16, 2, 64, 32, LENS_A),                    # fewer cost positions than CTAs: pieces from global
+    ("bf16", 28, 4, 128, 16, [700, 1, 300, 48, 1025] * 4),  # pieces copied into freed stages
+    ("f16", 8, 1, 128, 16, [20000]),                     # one unit over every CTA: more than 32 pieces
+])
+def test_stream_k_repeated_calls_identical(dtype, hq, hkv, d, bs, lens):
+    """Forty calls on the same inputs: each must equal the first bit for bit
+    (and the first the oracle).  An owner that read a later piece before it
+    was published would make some call differ."""
+    run_case(dtype, hq, hkv, d, bs, lens, seed=4242 + d, repeat=40)
 
 
 def test_stream_k_more_ctas_than_tiles():
