@@ -12,10 +12,13 @@ Prints one JSON line on rank 0.  ``value`` is algorithmic HBM bytes of the
 step (K/V of every attended token read once, q/out, table entries and
 lengths, plus the cache write) per second of device time, summed over
 ranks; each rank runs its own replica of the workload (weak scaling, no
-data-path collective).  Steps are issued back to back (the host builds step
-i + 1's metadata while the GPU runs step i) as CUDA graph launches, and
+data-path collective).  Steps are issued back to back through the native
+step runner (one library call per step: host metadata, async H2D copy on a
+side stream, one fused cache-write + attention launch), so the host builds
+step i + 1's metadata and its copy runs while the GPU runs step i; steps
 rotate over enough replica pools that no step finds its K/V in L2.  The
-roofline object times the attention call alone, L2 flushed before each.
+roofline object times the step's device launch alone, L2 flushed before
+each.
 """
 
 from __future__ import annotations
@@ -272,24 +275,19 @@ def run_native(args):
         eng.setup(vals)
         engines.append(eng)
     q, k_step, v_step = vals.q, vals.k_step, vals.v_step
-    for eng in engines:                       # one direct step each, then capture
+    for eng in engines:            # one direct step each (lazy set-up), then the native step runner
         eng.step(q, k_step, v_step)
-    graphs_ok = True
-    try:
-        for eng in engines:
-            eng.capture(q, k_step, v_step)
-    except Exception as exc:                  # direct launches still time the same kernels
-        graphs_ok = False
-        graph_error = str(exc)[-200:]
+        eng.make_runner()
     torch.cuda.synchronize()
 
     def run_step(i):
         eng = engines[i % replicas]
-        if graphs_ok:
-            eng.step_graph()
-        else:
-            eng.step(q, k_step, v_step)
+        eng.runner_step(q, k_step, v_step, eng.out)
         return eng
+
+    def join_all():
+        for eng in engines:
+            eng.runner_join()
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -307,6 +305,7 @@ def run_native(args):
     for i in range(args.steps):
         eng = run_step(args.warmup + i)
         marks.append((eng, eng.steps_done))
+    join_all()
     t_end.record()
     torch.cuda.synchronize()
     barrier()
@@ -326,7 +325,7 @@ def run_native(args):
     tokens_per_s = tokens * world / t_steps_max
     status = pk.device_error()
 
-    # ---------------- attention call alone (the roofline kernel) ----------------
+    # ---------------- the step's device launch alone (the roofline kernel) ----------------
     # Launches are queued behind a GPU-side delay, so the events bracket
     # device time only.  Before each call L2 is flushed (write 2x L2, then
     # read 2x L2 of other data) and the step's metadata is copied host to
@@ -347,41 +346,35 @@ def run_native(args):
             torch.cuda._sleep(200000)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        eng0.attention(q)
+        eng0.device_step(q, k_step, v_step)
         b.record()
         b.synchronize()
         attn_ms.append(a.elapsed_time(b))
     attn_call_s = statistics.fmean(attn_ms[2:] if len(attn_ms) > 4 else attn_ms) / 1e3
-    attn_bytes = eng0.algorithmic_bytes(eng0.wl.cached_lens + eng0.steps_done)["attention"]
+    # the step's device kernels after the metadata copy: one fused launch
+    # (cache write + attention) with the stream-K kernel, over the lengths
+    # in the metadata it was given
+    roof_bytes = eng0.algorithmic_bytes(eng0._views(meta_h)[2].numpy())
+    attn_bytes = roof_bytes["step"] if eng0.fused else roof_bytes["attention"] + roof_bytes["cache_write"]
 
     # ---------------- end to end through host buffers ----------------
+    # The runners copy each step's q/k/v from page-locked host memory and the
+    # output back, on their side streams, inside the timed region.
     q_h = q.cpu().pin_memory()
     k_h = k_step.cpu().pin_memory()
     v_h = v_step.cpu().pin_memory()
-    out_h = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
-    q_d, k_d, v_d = torch.empty_like(q), torch.empty_like(k_step), torch.empty_like(v_step)
-    e2e_graphs = graphs_ok
-    if graphs_ok:
-        try:
-            for eng in engines:
-                eng.capture(q_d, k_d, v_d, host_io=(q_h, k_h, v_h, out_h))
-        except Exception:
-            e2e_graphs = False
+    outs_h = [torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in engines]
+    for eng in engines:
+        eng.make_runner(host_io=True)
 
     def run_e2e(i):
         eng = engines[i % replicas]
-        if e2e_graphs:
-            eng.step_graph()
-        else:
-            q_d.copy_(q_h, non_blocking=True)
-            k_d.copy_(k_h, non_blocking=True)
-            v_d.copy_(v_h, non_blocking=True)
-            out = eng.step(q_d, k_d, v_d)
-            out_h.copy_(out, non_blocking=True)
+        eng.runner_step(q_h, k_h, v_h, outs_h[i % replicas])
         return eng
 
     for i in range(args.warmup):
         run_e2e(i)
+    join_all()
     torch.cuda.synchronize()
     barrier()
     e_marks = []
@@ -390,6 +383,7 @@ def run_native(args):
     for i in range(args.steps):
         eng = run_e2e(i)
         e_marks.append((eng, eng.steps_done))
+    join_all()
     e1.record()
     torch.cuda.synchronize()
     t_e2e = torch.tensor([e0.elapsed_time(e1) / 1e3], dtype=torch.float64, device=dev)
@@ -397,8 +391,10 @@ def run_native(args):
         dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
     e2e_bytes = sum(eng.algorithmic_bytes(eng.wl.cached_lens + done)["step"] for eng, done in e_marks)
     e2e_gbs = e2e_bytes * world / float(t_e2e.item()) / 1e9
-    h2d = (q.numel() + k_step.numel() + v_step.numel()) * q.element_size() + 4 * engines[0].d_meta.numel()
-    d2h = out_h.numel() * out_h.element_size()
+    # per step: q, k, v and the metadata buffer (slot mapping, tables, lengths, decode rows) in; out back
+    h2d = (q.numel() + k_step.numel() + v_step.numel()) * q.element_size() + 4 * (engines[0].d_meta.numel() +
+                                                                                    wl.num_seqs)
+    d2h = outs_h[0].numel() * outs_h[0].element_size()
     status = status or pk.device_error()
 
     peak, peak_kind = measured_peak()
@@ -427,7 +423,8 @@ def run_native(args):
             "l2": (f"inputs larger than L2: steps rotate over {replicas} replica pools so more than 3x L2 "
                    "streams between two uses of one pool; the roofline loop flushes L2 before each call"),
             "pipelining": "host metadata of a step overlaps device work of the previous steps",
-            "cuda_graph": graphs_ok if graphs_ok else f"no ({graph_error})",
+            "step_driver": ("native step runner (kvstep_run): one library call per step does the host "
+                            "metadata, the async H2D copy on a side stream and the fused launch"),
             "parallelism": f"replicas x{world}",
             "plan": {"kernel": {0: "simt_split", 1: "tma_mma_split", 2: "tma_mma_stream_k"}[plan.kernel],
                      "blocks_per_split": plan.blocks_per_split, "num_splits": plan.num_splits},
@@ -436,7 +433,9 @@ def run_native(args):
         "hbm_frac_of_nominal_8tbs": value_gbs / world / NOMINAL_HBM_GBS,
         "roofline": {
             "bound": "hbm",
-            "kernel": "paged_decode_attention call (one cooperative stream-K launch for fp16/bf16)",
+            "kernel": ("paged_decode_step call: one cooperative stream-K launch doing the cache write and "
+                       "decode attention" if eng0.fused and plan.kernel == 2 else
+                       "paged_reshape_and_cache + paged_decode_attention calls"),
             "achieved": achieved,
             "peak": peak,
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
@@ -499,8 +498,9 @@ def run_reference(args):
 
 
 def run_profile_calls(args):
-    """One engine, one step, then ``--profile-calls`` attention calls with L2
-    flushed before each: a short, fixed launch sequence for ncu captures."""
+    """One engine, one step, then ``--profile-calls`` device steps (the fused
+    cache write + attention launch) with L2 flushed before each: a short,
+    fixed launch sequence for ncu captures."""
     import torch
 
     import paged_kv_cache_128_gb300 as pk
@@ -517,11 +517,12 @@ def run_profile_calls(args):
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
     for _ in range(args.profile_calls):
         flush.zero_()
-        eng.attention(vals.q)
+        eng.device_step(vals.q, vals.k_step, vals.v_step)
     torch.cuda.synchronize()
     status = pk.device_error()
+    ab = eng.algorithmic_bytes(wl.cached_lens + 1)
     print(json.dumps({"workload": wl.name, "calls": args.profile_calls, "plan": eng.plan.__dict__,
-                      "attention_bytes": eng.algorithmic_bytes(wl.cached_lens + 1)["attention"],
+                      "fused": eng.fused, "attention_bytes": ab["attention"], "step_bytes": ab["step"],
                       "device_error": status}))
     if status:
         sys.exit(1)

@@ -51,7 +51,9 @@ typedef enum {
   KV_ERR_CUDA = 7,          /* a CUDA runtime call or launch failed */
   KV_ERR_DEVICE_BOUNDS = 8, /* a kernel met a block index or slot outside the pool */
   KV_ERR_WORKSPACE = 9,     /* the workspace passed is smaller than required */
-  KV_ERR_DEVICE_TIMEOUT = 10/* a bounded device-side wait gave up */
+  KV_ERR_DEVICE_TIMEOUT = 10,/* a bounded device-side wait gave up */
+  KV_ERR_DEVICE_STEP = 11   /* paged_decode_step: a sequence's new-token row is not written
+                               to that sequence's newest slot (inconsistent step metadata) */
 } kv_status_t;
 
 /* Static, NUL-terminated text for a status code (never NULL). */
@@ -264,6 +266,43 @@ int paged_decode_attention(void* out, const void* q, const void* k_cache, const 
                            int32_t blocks_per_split, int dtype, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/* One decode step's device work in one call: the cache write of the step's
+ * new tokens (exactly as paged_reshape_and_cache) followed by decode
+ * attention over the batch (exactly as paged_decode_attention with
+ * blocks_per_split = 0), with the new tokens visible to the attention.
+ * "MiniPaged-Qwen" §12 (write the token's K/V at its slot) and §13 (attend
+ * over the history including it); "从零实现一个 mini vLLM: Block Manager"
+ * (a decode step writes the input token's K/V in its own forward).
+ *   k, v, slot_mapping, num_tokens, k/v_token_stride: the step's new tokens,
+ *     as for paged_reshape_and_cache (prefill chunks, decode tokens, -1 pads).
+ *   new_token_row: device int32[num_seqs]; new_token_row[b] is the row of
+ *     k/v holding sequence b's newest token, position seq_lens[b] - 1, or -1
+ *     when the step writes no token of sequence b.  May be NULL only when
+ *     num_tokens == 0.
+ *   The remaining arguments are those of paged_decode_attention.
+ * Requirement: the only slots this step writes that the attention reads are
+ * those positions seq_lens[b] - 1 named by new_token_row.  When the stream-K
+ * kernel applies (paged_decode_plan kernel 2) and the rows of k and v are
+ * 16-byte aligned, the call is ONE launch: its warps scatter the rows while
+ * the first K/V tiles stream in, and the tile holding position
+ * seq_lens[b] - 1 takes that token from row new_token_row[b] rather than
+ * from the cache, so no tile depends on a write of the same launch.  The
+ * kernel checks that slot_mapping[new_token_row[b]] is that position's slot
+ * (block_tables[b][(L - 1) / bs] * bs + (L - 1) % bs) and records
+ * KV_ERR_DEVICE_STEP in the device error word when it is not, or when the
+ * row is >= num_tokens.  Otherwise the call launches the cache write, then
+ * attention, in stream order.  num_seqs == 0 runs the cache write alone.
+ * Results are bit-identical to the two calls in sequence: same cache bytes,
+ * same attention arithmetic. */
+int paged_decode_step(void* out, const void* q, const void* k, const void* v,
+                      const int32_t* slot_mapping, int64_t num_tokens, int64_t k_token_stride,
+                      int64_t v_token_stride, const int32_t* new_token_row, void* k_cache,
+                      void* v_cache, const int32_t* block_tables, const int32_t* seq_lens,
+                      int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq,
+                      int64_t max_seq_len, float scale, int dtype, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
 /* paged_decode_attention without a workspace argument, for callers that
  * cannot allocate device memory themselves (their GPU memory belongs to
  * another allocator, or allocation is forbidden or too slow where they run).
@@ -301,6 +340,84 @@ int kv_device_error(int reset, int* status_out);
  * calling thread (the cause of its most recent KV_ERR_CUDA); static storage,
  * never NULL. */
 const char* kv_last_cuda_error(void);
+
+/* ------------------------------------------------ native step runner */
+/*
+ * One serving decode step of one layer per call ("从零实现一个 mini vLLM:
+ * Block Manager", section on the ModelRunner: the CPU builds slot mapping,
+ * block tables and context lengths from the manager and hands them to the
+ * GPU with the step's K/V; "MiniPaged-Qwen" §8: CPU metadata plane, GPU data
+ * plane).  kvstep_run does, in order:
+ *   1. kvbm_prepare_step on the manager into a page-locked buffer, and each
+ *      decode sequence's row in the step's K/V (the prefill tokens come
+ *      first, then one token per decode sequence, around the pads);
+ *   2. one async host-to-device copy of that buffer on a side stream (with
+ *      host_io, also the step's q, k and v), so the copy overlaps the
+ *      previous step's kernel;
+ *   3. paged_decode_step on cfg.stream after an event wait on that copy;
+ *   4. with host_io, the output back to the caller's host buffer on a
+ *      second side stream.
+ * Two metadata buffers alternate between steps; their reuse is ordered by
+ * events (the host waits only for the copy issued two steps earlier).
+ * The runner allocates its buffers (page-locked host, device) and two side
+ * streams at kvstep_create.  Not thread-safe: one thread drives a runner,
+ * and the manager must not be used by anyone else meanwhile.  The device
+ * current at kvstep_create must be current at every later call.
+ */
+typedef struct kvstep_s* kvstep_t;
+
+typedef struct {
+  int32_t num_seqs;            /* decode sequences per step (n_decode of every kvstep_run) */
+  int32_t num_heads, num_kv_heads, head_dim, block_size;
+  int64_t num_blocks;
+  int32_t max_blocks_per_seq;  /* columns of the exported block tables */
+  int64_t max_seq_len;         /* upper bound of every step's seq_lens */
+  float scale;
+  int32_t dtype;               /* kv_dtype_t */
+  int64_t num_step_tokens;     /* rows of k/v per step = prefill tokens + num_seqs + pads */
+  void* k_cache;               /* device caches [num_blocks, block_size, num_kv_heads, head_dim] */
+  void* v_cache;
+  void* workspace;             /* device, >= paged_decode_workspace_size(..., 0, ...) bytes */
+  size_t workspace_bytes;
+  void* stream;                /* compute stream (cudaStream_t) */
+  int32_t host_io;             /* 0: q/k/v/out given to kvstep_run are device buffers;
+                                  1: page-locked host buffers, copied in and out by the runner */
+} kvstep_config_t;
+
+int kvstep_create(kvbm_t mgr, const kvstep_config_t* cfg, kvstep_t* out);
+
+/* Wait for the runner's outstanding work, then release it. */
+int kvstep_destroy(kvstep_t h);
+
+/* One step.  q [num_seqs, num_heads, head_dim], k and v dense
+ * [num_step_tokens, num_kv_heads, head_dim], out like q: device buffers
+ * (host_io = 0; read and written in cfg.stream order) or page-locked host
+ * buffers (host_io = 1; q/k/v are read by the copy issued here, out is
+ * written when the step's device-to-host copy completes, see kvstep_join).
+ * The id arguments are those of kvbm_prepare_step; n_decode must equal
+ * cfg.num_seqs, the pads must be strictly increasing and in range, and the
+ * step's rows must add up to cfg.num_step_tokens (else KV_ERR_INVALID_ARG,
+ * nothing done).  Manager errors are those of kvbm_prepare_step; nothing is
+ * launched then. */
+int kvstep_run(kvstep_t h, const void* q, const void* k, const void* v, void* out,
+               const int64_t* free_ids, int64_t n_free, const int64_t* prefill_ids,
+               const int64_t* prefill_lens, int64_t n_prefill, const int64_t* decode_ids,
+               int64_t n_decode, const int64_t* pad_positions, int64_t n_pad);
+
+/* Make `stream` wait for every copy and kernel the runner has issued. */
+int kvstep_join(kvstep_t h, void* stream);
+
+/* Host copies of the last step's metadata (valid until the next
+ * kvstep_run): slot mapping, block tables, seq_lens and the decode rows. */
+int kvstep_last_buffers(kvstep_t h, const int32_t** slot_mapping, const int32_t** block_tables,
+                        const int32_t** seq_lens, const int32_t** new_token_row);
+
+/* Device address of page-locked host memory that is mapped into the device
+ * address space (cudaHostAlloc'd or registered memory; with unified
+ * addressing it equals the host address).  Kernels may read such memory in
+ * place, e.g. a step's metadata written by the host.  KV_ERR_INVALID_ARG
+ * when host_ptr is not mapped page-locked memory. */
+int kv_mapped_device_pointer(const void* host_ptr, void** device_ptr_out);
 
 /* Library version string (static). */
 const char* kv_version(void);

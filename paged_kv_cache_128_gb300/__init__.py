@@ -7,6 +7,8 @@ Public API (all work runs in libpagedkv.so; see include/pagedkv.h):
 * ``reshape_and_cache`` -- CUDA cache write by slot_mapping.
 * ``paged_decode_attention`` -- CUDA single-query GQA attention through
   block tables, with split-K and a log-sum-exp merge.
+* ``paged_decode_step`` -- the step's cache write and decode attention in
+  one launch (stream-K kernel), else the two in stream order.
 """
 
 from ._lib import KVError, LIB_PATH, lib  # noqa: F401
@@ -15,7 +17,7 @@ from .block_manager import KVBlockManager, kv_cache_ledger  # noqa: F401
 
 def __getattr__(name):
     # the kernel wrappers need torch; import them on first use
-    if name in ("reshape_and_cache", "paged_decode_attention", "decode_plan", "device_error",
+    if name in ("reshape_and_cache", "paged_decode_attention", "paged_decode_step", "decode_plan", "device_error",
                 "alloc_workspace", "DecodePlan"):
         from . import kernels
         return getattr(kernels, name)

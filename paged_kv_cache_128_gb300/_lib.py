@@ -13,7 +13,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedkv.
 KV_OK = 0
 STATUS_NAMES = {
     0: "OK", 1: "INVALID_ARG", 2: "OOM", 3: "UNKNOWN_SEQ", 4: "DUPLICATE_SEQ", 5: "DOUBLE_FREE",
-    6: "INVARIANT", 7: "CUDA", 8: "DEVICE_BOUNDS", 9: "WORKSPACE", 10: "DEVICE_TIMEOUT",
+    6: "INVARIANT", 7: "CUDA", 8: "DEVICE_BOUNDS", 9: "WORKSPACE", 10: "DEVICE_TIMEOUT", 11: "DEVICE_STEP",
 }
 DTYPE_F32, DTYPE_F16, DTYPE_BF16 = 0, 1, 2
 
@@ -31,6 +31,14 @@ class kvbm_stats_t(ctypes.Structure):
     _fields_ = [("num_blocks", c_int64), ("block_size", c_int64), ("num_free_blocks", c_int64),
                 ("num_sequences", c_int64), ("logical_tokens", c_int64), ("allocated_tokens", c_int64),
                 ("unused_tail_tokens", c_int64)]
+
+
+class kvstep_config_t(ctypes.Structure):
+    _fields_ = [("num_seqs", c_int32), ("num_heads", c_int32), ("num_kv_heads", c_int32), ("head_dim", c_int32),
+                ("block_size", c_int32), ("num_blocks", c_int64), ("max_blocks_per_seq", c_int32),
+                ("max_seq_len", c_int64), ("scale", c_float), ("dtype", c_int32), ("num_step_tokens", c_int64),
+                ("k_cache", c_void_p), ("v_cache", c_void_p), ("workspace", c_void_p),
+                ("workspace_bytes", c_size_t), ("stream", c_void_p), ("host_io", c_int32)]
 
 
 P32 = POINTER(c_int32)
@@ -69,12 +77,24 @@ SIGNATURES = {
     "paged_decode_attention": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
                                        c_int32, c_int32, c_int32, c_int32, c_int64, c_int32, c_int64, c_float,
                                        c_int32, c_int, c_void_p, c_size_t, c_void_p]),
+    "paged_decode_step": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64,
+                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
+                                  c_int32, c_int32, c_int64, c_int32, c_int64, c_float, c_int, c_void_p, c_size_t,
+                                  c_void_p]),
     "paged_decode_attention_static_scratch": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                                       c_int32, c_int32, c_int32, c_int32, c_int32, c_int64,
                                                       c_int32, c_int64, c_float, c_int32, c_int, c_void_p]),
     "paged_decode_static_scratch_bytes": (c_size_t, []),
     "kv_device_error": (c_int, [c_int, POINTER(c_int)]),
     "kv_last_cuda_error": (c_char_p, []),
+    "kvstep_create": (c_int, [c_void_p, POINTER(kvstep_config_t), POINTER(c_void_p)]),
+    "kvstep_destroy": (c_int, [c_void_p]),
+    "kvstep_run": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_void_p,
+                           c_int64, c_void_p, c_int64, c_void_p, c_int64]),
+    "kvstep_join": (c_int, [c_void_p, c_void_p]),
+    "kvstep_last_buffers": (c_int, [c_void_p, POINTER(c_void_p), POINTER(c_void_p), POINTER(c_void_p),
+                                    POINTER(c_void_p)]),
+    "kv_mapped_device_pointer": (c_int, [c_void_p, POINTER(c_void_p)]),
     "kv_version": (c_char_p, []),
 }
 

@@ -133,6 +133,7 @@ const char* kv_status_string(int status) {
     case KV_ERR_DEVICE_BOUNDS: return "device access outside the KV pool (skipped)";
     case KV_ERR_WORKSPACE: return "workspace too small";
     case KV_ERR_DEVICE_TIMEOUT: return "bounded device wait timed out";
+    case KV_ERR_DEVICE_STEP: return "new-token row does not land on its sequence's newest slot";
     default: return "unknown status";
   }
 }

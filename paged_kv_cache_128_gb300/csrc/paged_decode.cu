@@ -71,6 +71,16 @@ struct DecodeParams {
   uint64_t* ws_flags;  // stream-K: [P] "partial in slot 0 ready" flags, holding the call's epoch
   uint64_t epoch;      // stream-K: tag unique to this call (flags from other calls never match)
   int32_t seg_cost;    // stream-K: extra tiles charged per unit when ranges are drawn
+  // Fused step (stream-K only; new_k == nullptr otherwise): the step's new
+  // tokens' rows [num_new][Hkv][D] are scattered into the caches by
+  // slot_mapping, and sequence b's newest position seq_lens[b] - 1 is taken
+  // from row new_row[b] of new_k / new_v (-1: none) instead of the cache.
+  const void* new_k;
+  const void* new_v;
+  const int32_t* slot_mapping;
+  const int32_t* new_row;
+  int64_t num_new;
+  int64_t new_k_stride, new_v_stride;  // bytes between consecutive tokens' rows
 };
 
 // Sequence length after bounds checks: at most what the table row and the
@@ -417,6 +427,53 @@ __device__ __forceinline__ void warp_merge(const float* Os, const float* Ms, con
 // seq_lens.
 // =========================================================================
 
+// Fused step, cache write ("MiniPaged-Qwen" §12): warp gw of nw copies the
+// K and V rows of tokens gw, gw + nw, ... to cache[slot / bs][slot % bs],
+// slot = slot_mapping[t] (-1: padded token, skipped; outside the pool:
+// recorded and skipped).  A lane fetches the slots of 32 of the warp's
+// tokens at once; each row is loaded whole (16-byte vectors) before it is
+// stored.
+template <typename T>
+__device__ __forceinline__ void scatter_new_rows(const DecodeParams& p, int64_t gw, int64_t nw, int lane) {
+  const int row_vecs = p.num_kv_heads * p.head_dim * static_cast<int>(sizeof(T)) / 16;
+  const int64_t row_bytes = static_cast<int64_t>(row_vecs) * 16;
+  const int64_t num_slots = p.num_blocks * p.block_size;
+  constexpr int kVec = 4;
+  for (int64_t base = gw; base < p.num_new; base += 32 * nw) {
+    const int64_t mine = base + lane * nw;
+    const int32_t my_slot = mine < p.num_new ? __ldg(p.slot_mapping + mine) : -1;
+    for (int i = 0; i < 32; ++i) {
+      const int64_t t = base + i * nw;
+      if (t >= p.num_new) break;
+      const int32_t slot = __shfl_sync(0xffffffffu, my_slot, i);
+      if (slot == -1) continue;
+      if (slot < 0 || slot >= num_slots) {
+        if (lane == 0) record_error(KV_ERR_DEVICE_BOUNDS);
+        continue;
+      }
+      const uint4* ks = reinterpret_cast<const uint4*>(static_cast<const char*>(p.new_k) + t * p.new_k_stride);
+      const uint4* vs = reinterpret_cast<const uint4*>(static_cast<const char*>(p.new_v) + t * p.new_v_stride);
+      uint4* kd = reinterpret_cast<uint4*>(static_cast<char*>(const_cast<void*>(p.k_cache)) + slot * row_bytes);
+      uint4* vd = reinterpret_cast<uint4*>(static_cast<char*>(const_cast<void*>(p.v_cache)) + slot * row_bytes);
+      for (int v0 = lane; v0 < row_vecs; v0 += 32 * kVec) {
+        uint4 kr[kVec], vr[kVec];
+#pragma unroll
+        for (int u = 0; u < kVec; ++u)
+          if (v0 + 32 * u < row_vecs) {
+            kr[u] = __ldg(ks + v0 + 32 * u);
+            vr[u] = __ldg(vs + v0 + 32 * u);
+          }
+#pragma unroll
+        for (int u = 0; u < kVec; ++u)
+          if (v0 + 32 * u < row_vecs) {
+            kd[v0 + 32 * u] = kr[u];
+            vd[v0 + 32 * u] = vr[u];
+          }
+      }
+    }
+  }
+}
+
 // Grid cap: an owner CTA indexes up to kMaxSkCtas pieces in shared memory.
 constexpr int kMaxSkCtas = 640;
 // An owner's producer warp waits for the later pieces and copies them into
@@ -549,7 +606,12 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   };
   const int64_t t0 = tiles_before(static_cast<int64_t>(pid) * Wc / P);
   const int64_t t1 = tiles_before(static_cast<int64_t>(pid + 1) * Wc / P);
-  if (t0 >= t1) return;
+  if (t0 >= t1) {
+    if (p.new_k != nullptr && warp != 0)
+      scatter_new_rows<T>(p, static_cast<int64_t>(pid) * kConsumers + warp - 1, static_cast<int64_t>(P) * kConsumers,
+                          lane);
+    return;
+  }
   const int n = static_cast<int>(t1 - t0);
 
   // Tile cursor shared by producer and consumers: advances (blk, kvh, b).
@@ -759,17 +821,73 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   };
   load_q<T, D, NG>(st, q_of(c), G, lane);
   prefetch_next(c, unit_start);
+  // Fused step: the consumer warps write the step's new rows into the
+  // caches while the first tiles are in flight.  No tile of this launch
+  // uses what they write: position L - 1 of a decode sequence (the only
+  // written slot attention reads) is taken from the new row itself below.
+  const bool fused = p.new_k != nullptr;
+  if (fused) scatter_new_rows<T>(p, static_cast<int64_t>(pid) * kConsumers + cw, static_cast<int64_t>(P) * kConsumers,
+                                 lane);
+  // row of the step's new K/V holding sequence b's position L - 1 (-1: none)
+  auto new_row_of = [&](int b) -> int {
+    if (!fused) return -1;
+    const int r = __ldg(p.new_row + b);
+    if (r >= p.num_new) {
+      record_error(KV_ERR_DEVICE_STEP);
+      return -1;
+    }
+    return r;
+  };
+  int nrow = new_row_of(c.b);
   reset_state(st);
   int seg = 0;
+  constexpr int kPatch = (2 * (D / 8) + 31) / 32;  // 16-byte chunks of one token's K and V per lane
   for (int j = 0; j < n; ++j) {
     if (ok && (j & (kConsumers - 1)) == cw) {
       const int s = j % NST;
+      // Fused step: the tile holding position L - 1 takes that token's K
+      // and V for this kv head from the new row (loaded before the wait).
+      const int tl = L - 1 - c.blk * TT;
+      const bool patch = nrow >= 0 && tl >= 0 && tl < TT;
+      uint4 pv[kPatch];
+      if (patch) {
+#pragma unroll
+        for (int u = 0; u < kPatch; ++u) {
+          const int ch = lane + 32 * u;
+          if (ch < 2 * (D / 8)) {
+            const bool isv = ch >= D / 8;
+            const int d = (ch % (D / 8)) * 8;
+            const char* src = static_cast<const char*>(isv ? p.new_v : p.new_k) +
+                              static_cast<int64_t>(nrow) * (isv ? p.new_v_stride : p.new_k_stride) +
+                              (static_cast<int64_t>(c.kvh) * D + d) * static_cast<int64_t>(sizeof(T));
+            pv[u] = __ldg(reinterpret_cast<const uint4*>(src));
+          }
+        }
+        if (lane == 0) {  // the row must be the one the cache write puts at position L - 1
+          const int pb = __ldg(p.block_tables + static_cast<int64_t>(c.b) * p.max_blocks_per_seq + (L - 1) / BS);
+          const int32_t want = pb * BS + (L - 1) % BS;
+          if (__ldg(p.slot_mapping + nrow) != want) record_error(KV_ERR_DEVICE_STEP);
+        }
+      }
       int w = 1;
       if (lane == 0) w = mbar_wait_bounded(&full[s], (j / NST) & 1);
       ok = __shfl_sync(0xffffffffu, w, 0);
       if (ok) {
         __syncwarp();
         uint8_t* kt = smem + s * TL::kStageBytes;
+        if (patch) {
+#pragma unroll
+          for (int u = 0; u < kPatch; ++u) {
+            const int ch = lane + 32 * u;
+            if (ch < 2 * (D / 8)) {
+              const bool isv = ch >= D / 8;
+              const int d = (ch % (D / 8)) * 8;
+              *reinterpret_cast<uint4*>(kt + (isv ? TL::kTileBytes : 0) + swz<TT>(tl, d)) = pv[u];
+            }
+          }
+          fence_proxy_async_smem();  // the stage is TMA-written again later
+          __syncwarp();
+        }
         consume_tile<T, D, TT, NG>(st, kt, kt + TL::kTileBytes, c.blk * TT, L, sl2, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -840,6 +958,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
         advance(c);
         unit_start = static_cast<int64_t>(Hkv) * CB[c.b] + static_cast<int64_t>(c.kvh) * c.nb;
         L = checked_len(p, c.b);
+        nrow = new_row_of(c.b);
         if constexpr (kPrefetchQ) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
@@ -1594,6 +1713,10 @@ int check_shapes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t BS, int6
 using namespace pagedkv;
 
 extern "C" int pagedkv_internal_reshape_error(int reset, int* code);
+extern "C" int paged_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                                       const int32_t* slot_mapping, int64_t num_tokens, int32_t num_kv_heads,
+                                       int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                       int64_t k_token_stride, int64_t v_token_stride, int dtype, void* stream);
 
 extern "C" int paged_decode_plan(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                                  int32_t block_size, int64_t max_seq_len, int32_t blocks_per_split, int dtype,
@@ -1618,12 +1741,21 @@ extern "C" int paged_decode_workspace_size(int32_t num_seqs, int32_t num_heads, 
                            dtype, nullptr, nullptr, nullptr, bytes_out);
 }
 
-extern "C" int paged_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
-                                      const int32_t* block_tables, const int32_t* seq_lens, int32_t num_seqs,
-                                      int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
-                                      int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq,
-                                      int64_t max_seq_len, float scale, int32_t blocks_per_split, int dtype,
-                                      void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+// The step's new tokens for paged_decode_step (null for attention alone).
+struct StepArgs {
+  const void* k;
+  const void* v;
+  const int32_t* slot_mapping;
+  const int32_t* new_token_row;
+  int64_t num_tokens, k_stride, v_stride;  // strides in elements
+};
+
+int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq, int64_t max_seq_len, float scale,
+                int32_t blocks_per_split, int dtype, void* workspace, size_t workspace_bytes, void* stream,
+                const StepArgs* step) {
   int st = check_shapes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_seq_len, dtype);
   if (st != KV_OK) return st;
   if (num_blocks <= 0 || num_blocks > INT32_MAX / block_size || max_blocks_per_seq <= 0 || blocks_per_split < 0)
@@ -1675,6 +1807,22 @@ extern "C" int paged_decode_attention(void* out, const void* q, const void* k_ca
     }
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (step != nullptr && step->num_tokens > 0) {
+    const int64_t es = static_cast<int64_t>(dtype_bytes(dtype));
+    const uintptr_t row_align = reinterpret_cast<uintptr_t>(step->k) | reinterpret_cast<uintptr_t>(step->v) |
+                                static_cast<uintptr_t>(step->k_stride * es) |
+                                static_cast<uintptr_t>(step->v_stride * es);
+    if (pl.kind == kTensorCoreStreamK && row_align % 16 == 0) {
+      // one launch: the stream-K kernel also writes the new rows
+      p.new_k = step->k;
+      p.new_v = step->v;
+      p.slot_mapping = step->slot_mapping;
+      p.new_row = step->new_token_row;
+      p.num_new = step->num_tokens;
+      p.new_k_stride = step->k_stride * es;
+      p.new_v_stride = step->v_stride * es;
+    }
+  }
   CUtensorMap mk, mv;
   if (pl.kind != kSimt) {
     const int64_t rows = num_blocks * block_size;
@@ -1682,11 +1830,54 @@ extern "C" int paged_decode_attention(void* out, const void* q, const void* k_ca
         !get_tensor_map(v_cache, rows, num_kv_heads, head_dim, block_size, &mv))
       return cuda_status(cudaErrorInvalidValue, "cuTensorMapEncodeTiled failed");
   }
+  if (step != nullptr && step->num_tokens > 0 && p.new_k == nullptr) {
+    // other kernels: the cache write first, then attention, in stream order
+    st = paged_reshape_and_cache(step->k, step->v, const_cast<void*>(k_cache), const_cast<void*>(v_cache),
+                                 step->slot_mapping, step->num_tokens, num_kv_heads, head_dim, block_size, num_blocks,
+                                 step->k_stride, step->v_stride, dtype, stream);
+    if (st != KV_OK) return st;
+  }
   cudaError_t e;
   if (dtype == KV_DTYPE_F32) e = run_decode<float>(p, pl, s, nullptr, nullptr);
   else if (dtype == KV_DTYPE_F16) e = run_decode<__half>(p, pl, s, &mk, &mv);
   else e = run_decode<__nv_bfloat16>(p, pl, s, &mk, &mv);
   return cuda_status(e);
+}
+}  // namespace
+
+extern "C" int paged_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, const int32_t* seq_lens, int32_t num_seqs,
+                                      int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq,
+                                      int64_t max_seq_len, float scale, int32_t blocks_per_split, int dtype,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, max_blocks_per_seq, max_seq_len, scale, blocks_per_split, dtype,
+                     workspace, workspace_bytes, stream, nullptr);
+}
+
+extern "C" int paged_decode_step(void* out, const void* q, const void* k, const void* v,
+                                 const int32_t* slot_mapping, int64_t num_tokens, int64_t k_token_stride,
+                                 int64_t v_token_stride, const int32_t* new_token_row, void* k_cache,
+                                 void* v_cache, const int32_t* block_tables, const int32_t* seq_lens,
+                                 int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq,
+                                 int64_t max_seq_len, float scale, int dtype, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (num_tokens < 0) return KV_ERR_INVALID_ARG;
+  if (num_tokens > 0) {
+    const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+    if (!k || !v || !slot_mapping || k_token_stride < row || v_token_stride < row) return KV_ERR_INVALID_ARG;
+    if (num_seqs > 0 && !new_token_row) return KV_ERR_INVALID_ARG;
+  }
+  const StepArgs step{k, v, slot_mapping, new_token_row, num_tokens, k_token_stride, v_token_stride};
+  if (num_seqs == 0) {  // nothing to attend: the cache write alone
+    return paged_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, head_dim,
+                                   block_size, num_blocks, k_token_stride, v_token_stride, dtype, stream);
+  }
+  return decode_impl(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, max_blocks_per_seq, max_seq_len, scale, 0, dtype, workspace,
+                     workspace_bytes, stream, &step);
 }
 
 // ---------------------------------------------------------------------------
@@ -1763,6 +1954,19 @@ extern "C" int kv_device_error(int reset, int* status_out) {
   int r = pagedkv_internal_reshape_error(reset, &c);
   if (r != KV_OK) return r;
   *status_out = a ? a : c;
+  return KV_OK;
+}
+
+extern "C" int kv_mapped_device_pointer(const void* host_ptr, void** device_ptr_out) {
+  if (!host_ptr || !device_ptr_out) return KV_ERR_INVALID_ARG;
+  void* d = nullptr;
+  const cudaError_t e = cudaHostGetDevicePointer(&d, const_cast<void*>(host_ptr), 0);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // not mapped: clear the sticky-free error and report it
+    last_cuda_error_text() = cudaGetErrorString(e);
+    return KV_ERR_INVALID_ARG;
+  }
+  *device_ptr_out = d;
   return KV_OK;
 }
 

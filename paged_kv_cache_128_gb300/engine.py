@@ -24,10 +24,13 @@ from typing import Optional
 import numpy as np
 import torch
 
-from ._lib import check
+import ctypes
+
+from ._lib import check, kvstep_config_t, lib
 from .block_manager import KVBlockManager
 from .inputs import Values, Workload, pad_positions, sentinel_bits
-from .kernels import alloc_workspace, decode_plan, paged_decode_attention, reshape_and_cache
+from .kernels import (alloc_workspace, decode_plan, dtype_code, paged_decode_attention, paged_decode_step,
+                      reshape_and_cache)
 
 _INT_VIEW = {torch.float32: torch.int32, torch.float16: torch.int16, torch.bfloat16: torch.int16}
 
@@ -38,9 +41,12 @@ def _signed(bits: int, width: int) -> int:
 
 class PagedDecodeEngine:
     def __init__(self, wl: Workload, device="cuda", max_steps: int = 64, fill_sentinel: bool = True,
-                 blocks_per_split: int = 0):
+                 blocks_per_split: int = 0, fused: bool = True):
         self.wl = wl
         self.blocks_per_split = blocks_per_split
+        # fused: the step's cache write and attention in one paged_decode_step
+        # call (one launch with the stream-K kernel); else two calls
+        self.fused = fused and blocks_per_split == 0
         self.device = torch.device(device)
         self.mgr = KVBlockManager(wl.num_blocks, wl.block_size, wl.free_order)
         dt = wl.torch_dtype
@@ -73,6 +79,7 @@ class PagedDecodeEngine:
         self._meta_free = [None, None]   # event after which h_meta[i] may be rewritten
         self._meta_events = [torch.cuda.Event(), torch.cuda.Event()]
         self.graphs = None
+        self._runner = None
         self.out = torch.empty(B, wl.num_heads, wl.head_dim, dtype=dt, device=self.device)
         pads = pad_positions(wl)
         is_pad = np.zeros(n_step, dtype=bool)
@@ -80,6 +87,11 @@ class PagedDecodeEngine:
         self.valid_pos = np.nonzero(~is_pad)[0]
         self.pad_pos = pads
         self.n_prefill = int(wl.prefill_lens.sum())
+        # kvbm_prepare_step puts the prefill slots first, then one decode slot
+        # per running sequence, in the non-padded positions: sequence b's new
+        # token is row valid_pos[n_prefill + b] of the step's K/V
+        rows = self.valid_pos[self.n_prefill:self.n_prefill + B].astype(np.int32)
+        self.d_new_rows = torch.from_numpy(np.ascontiguousarray(rows)).to(self.device)
         self.next_id = wl.next_id
         # inputs of kvbm_prepare_step, kept in place so their addresses are fixed
         self._decode_ids = np.ascontiguousarray(wl.decode_ids, dtype=np.int64)
@@ -153,13 +165,7 @@ class PagedDecodeEngine:
         ev = self._meta_free[self._cur]
         if ev is not None:
             ev.synchronize()       # the copy that last read this buffer has run
-        n_pre = self._prefill_ids.size
-        n_free = n_pre if self._prefilled_once else 0   # the previous step's prefills end now
-        if n_pre:
-            self._free_ids[:] = self._prefill_ids
-            self._prefill_ids[:] = np.arange(self.next_id, self.next_id + n_pre)
-            self.next_id += n_pre
-            self._prefilled_once = True
+        n_free, n_pre = self._advance_ids()
         slots_a, tables_a, lens_a = self._meta_addr[self._cur]
         st = self.mgr.prepare_step_raw(
             self._free_ids.ctypes.data if n_free else None, n_free,
@@ -168,6 +174,19 @@ class PagedDecodeEngine:
             self._pad_pos.ctypes.data if self._pad_pos.size else None, self._pad_pos.size, self.max_blocks,
             slots_a, tables_a, lens_a)
         check(st, "kvbm_prepare_step")
+
+    def _advance_ids(self):
+        """This step's sequence ids: the previous step's prefill sequences
+        are released and a fresh id is drawn for each new prefill sequence.
+        Returns (n_free, n_prefill)."""
+        n_pre = self._prefill_ids.size
+        n_free = n_pre if self._prefilled_once else 0   # the previous step's prefills end now
+        if n_pre:
+            self._free_ids[:] = self._prefill_ids
+            self._prefill_ids[:] = np.arange(self.next_id, self.next_id + n_pre)
+            self.next_id += n_pre
+            self._prefilled_once = True
+        return n_free, n_pre
 
     def upload_metadata(self) -> None:
         """a1 crossing: one async H2D copy of the step's metadata."""
@@ -188,6 +207,20 @@ class PagedDecodeEngine:
         return paged_decode_attention(self.out, q, self.k_cache, self.v_cache, self.d_tables, self.d_lens,
                                       wl.scale, self.max_seq_len, self.blocks_per_split, self.workspace)
 
+    def fused_step(self, q: torch.Tensor, k_step: torch.Tensor, v_step: torch.Tensor) -> torch.Tensor:
+        """a2-a8 in one paged_decode_step call."""
+        wl = self.wl
+        return paged_decode_step(self.out, q, k_step, v_step, self.d_slots, self.d_new_rows, self.k_cache,
+                                 self.v_cache, self.d_tables, self.d_lens, wl.scale, self.max_seq_len,
+                                 self.workspace)
+
+    def device_step(self, q: torch.Tensor, k_step: torch.Tensor, v_step: torch.Tensor) -> torch.Tensor:
+        """The device part of a step after the metadata copy: a2, then a3-a8."""
+        if self.fused:
+            return self.fused_step(q, k_step, v_step)
+        self.write_step_kv(k_step, v_step)
+        return self.attention(q)
+
     def _check_room(self) -> None:
         if self.steps_done + 1 > self.max_seq_len - int(self.wl.cached_lens.max()):
             raise RuntimeError("engine sized for fewer steps")
@@ -198,8 +231,7 @@ class PagedDecodeEngine:
         self.host_metadata()
         self.upload_metadata()
         self._mark_meta_used()
-        self.write_step_kv(k_step, v_step)
-        out = self.attention(q)
+        out = self.device_step(q, k_step, v_step)
         self.steps_done += 1
         return out
 
@@ -223,8 +255,7 @@ class PagedDecodeEngine:
                     q.copy_(host_io[0], non_blocking=True)
                     k_step.copy_(host_io[1], non_blocking=True)
                     v_step.copy_(host_io[2], non_blocking=True)
-                self.write_step_kv(k_step, v_step)
-                out = self.attention(q)
+                out = self.device_step(q, k_step, v_step)
                 if host_io is not None:
                     host_io[3].copy_(out, non_blocking=True)
             graphs.append(g)
@@ -240,9 +271,79 @@ class PagedDecodeEngine:
         self.steps_done += 1
         return self.out
 
+    # ------------------------------------------------------- native runner
+    def make_runner(self, host_io: bool = False, stream: Optional[torch.cuda.Stream] = None) -> None:
+        """Create the native step runner (kvstep_*): afterwards each
+        ``runner_step`` is ONE library call doing a1 (kvbm_prepare_step, the
+        async metadata copy on a side stream) and a2-a8 (the fused launch).
+        With ``host_io`` the step's q/k/v and output are page-locked host
+        buffers that the runner copies in and out on its side streams."""
+        wl = self.wl
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        ws = self.workspace
+        cfg = kvstep_config_t(
+            num_seqs=wl.num_seqs, num_heads=wl.num_heads, num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim,
+            block_size=wl.block_size, num_blocks=wl.num_blocks, max_blocks_per_seq=self.max_blocks,
+            max_seq_len=self.max_seq_len, scale=float(wl.scale), dtype=dtype_code(self.k_cache.dtype),
+            num_step_tokens=wl.num_step_tokens, k_cache=self.k_cache.data_ptr(), v_cache=self.v_cache.data_ptr(),
+            workspace=ws.data_ptr() if ws is not None else None,
+            workspace_bytes=ws.numel() if ws is not None else 0, stream=s.cuda_stream, host_io=1 if host_io else 0)
+        self.close_runner()
+        h = ctypes.c_void_p()
+        check(lib().kvstep_create(self.mgr._h, ctypes.byref(cfg), ctypes.byref(h)), "kvstep_create")
+        self._runner = h
+        self._runner_stream = s
+        self._runner_args = (
+            self._decode_ids.ctypes.data, self._decode_ids.size,
+            self._pad_pos.ctypes.data if self._pad_pos.size else None, self._pad_pos.size)
+
+    def runner_step(self, q: torch.Tensor, k_step: torch.Tensor, v_step: torch.Tensor, out: torch.Tensor) -> None:
+        """One step through the native runner (a1-a8 in one call)."""
+        self._check_room()
+        n_free, n_pre = self._advance_ids()
+        dec, n_dec, pads, n_pad = self._runner_args
+        check(lib().kvstep_run(self._runner, q.data_ptr(), k_step.data_ptr(), v_step.data_ptr(), out.data_ptr(),
+                               self._free_ids.ctypes.data if n_free else None, n_free,
+                               self._prefill_ids.ctypes.data if n_pre else None,
+                               self._prefill_lens.ctypes.data if n_pre else None, n_pre, dec, n_dec, pads, n_pad),
+              "kvstep_run")
+        self.steps_done += 1
+
+    def runner_join(self, stream: Optional[torch.cuda.Stream] = None) -> None:
+        """Order ``stream`` (default: the current one) after the runner's work."""
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        check(lib().kvstep_join(self._runner, s.cuda_stream), "kvstep_join")
+
+    def runner_last_metadata(self):
+        """Host copies of the runner's last step: (slot mapping, block
+        tables [B, max_blocks], seq_lens, decode rows) as numpy arrays."""
+        wl = self.wl
+        ptrs = [ctypes.c_void_p() for _ in range(4)]
+        check(lib().kvstep_last_buffers(self._runner, *[ctypes.byref(p) for p in ptrs]), "kvstep_last_buffers")
+        sizes = [wl.num_step_tokens, wl.num_seqs * self.max_blocks, wl.num_seqs, wl.num_seqs]
+        arrs = [np.ctypeslib.as_array(ctypes.cast(p, ctypes.POINTER(ctypes.c_int32)), shape=(n,)).copy()
+                for p, n in zip(ptrs, sizes)]
+        arrs[1] = arrs[1].reshape(wl.num_seqs, self.max_blocks)
+        return tuple(arrs)
+
+    def close_runner(self) -> None:
+        h = getattr(self, "_runner", None)
+        if h:
+            lib().kvstep_destroy(h)
+            self._runner = None
+
+    def __del__(self):
+        try:
+            self.close_runner()
+        except Exception:
+            pass
+
     @property
     def launches_per_step(self) -> int:
-        """Library kernels per step: the cache write plus the attention call."""
+        """Library kernels per step: one fused launch with the stream-K
+        kernel, else the cache write plus the attention call's launches."""
+        if self.fused and self.plan.kernel == 2:
+            return 1
         return 1 + self.plan.launches
 
     def algorithmic_bytes(self, seq_lens: np.ndarray) -> dict:

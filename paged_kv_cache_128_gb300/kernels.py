@@ -126,6 +126,52 @@ def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
     return out
 
 
+def paged_decode_step(out: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                      slot_mapping: torch.Tensor, new_token_row: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                      max_seq_len: int, workspace: Optional[torch.Tensor] = None,
+                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """The step's cache write (``reshape_and_cache(k, v, ..., slot_mapping)``)
+    and decode attention in one call: one launch when the stream-K kernel
+    applies.  ``new_token_row[b]`` (int32) is the row of k/v holding
+    sequence b's newest token, position ``seq_lens[b] - 1``, or -1."""
+    for t, n in ((out, "out"), (q, "q"), (k, "k"), (v, "v"), (slot_mapping, "slot_mapping"),
+                 (new_token_row, "new_token_row"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (block_tables, "block_tables"), (seq_lens, "seq_lens")):
+        _cuda(t, n)
+    if not (q.is_contiguous() and out.is_contiguous() and k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise KVError(1, "q, out and caches must be contiguous")
+    for t, n in ((block_tables, "block_tables"), (seq_lens, "seq_lens"), (slot_mapping, "slot_mapping"),
+                 (new_token_row, "new_token_row")):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise KVError(1, f"{n} must be contiguous int32")
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    n = slot_mapping.numel()
+    if d2 != d or out.shape != q.shape or v_cache.shape != k_cache.shape or out.dtype != q.dtype \
+            or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise KVError(1, "shape or dtype mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or seq_lens.numel() != B \
+            or new_token_row.numel() != B:
+        raise KVError(1, "block_tables must be [B, max_blocks], seq_lens and new_token_row [B]")
+    for t in (k, v):
+        if t.dim() != 3 or t.shape[0] != n or t.shape[1] != hkv or t.shape[2] != d or t.stride(2) != 1 \
+                or t.stride(1) != d:
+            raise KVError(1, "k and v must be [N, Hkv, D] with dense heads")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is None:
+        plan = decode_plan(B, hq, hkv, d, bs, max_seq_len, q.dtype)
+        workspace = alloc_workspace(plan, q.device)
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    check(lib().paged_decode_step(out.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(),
+                                  n, k.stride(0), v.stride(0), new_token_row.data_ptr(), k_cache.data_ptr(),
+                                  v_cache.data_ptr(), block_tables.data_ptr(), seq_lens.data_ptr(), B, hq, hkv, d, bs,
+                                  nb, block_tables.shape[1], max_seq_len, float(scale), dtype_code(q.dtype), ws_ptr,
+                                  ws_bytes, _stream_ptr(stream)), "paged_decode_step")
+    return out
+
+
 def device_error(reset: bool = True) -> int:
     """Status recorded by device-side bounds checks / bounded waits (0 = none).
     Synchronises the current device."""

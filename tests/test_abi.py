@@ -40,7 +40,7 @@ def test_binding_covers_every_declared_symbol():
 
 def test_status_strings():
     lib = pk.lib()
-    for code in range(11):
+    for code in range(12):
         s = lib.kv_status_string(code).decode()
         assert s and s != "unknown status"
     assert lib.kv_status_string(99).decode() == "unknown status"

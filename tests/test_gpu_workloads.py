@@ -64,12 +64,13 @@ def _rows_equal(cache, slots, rows):
     return torch.equal(flat.index_select(0, idx).view(iv), rows.to(cache.device).view(iv))
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "two_calls"])
 @pytest.mark.parametrize("name", WORKLOADS)
-def test_workload_step_matches_oracle(name):
+def test_workload_step_matches_oracle(name, fused):
     wl = make_workload(name)
     vals = make_values(wl)
     dev = torch.device("cuda")
-    eng = PagedDecodeEngine(wl, dev, max_steps=4)
+    eng = PagedDecodeEngine(wl, dev, max_steps=4, fused=fused)
     eng.setup(vals)
     pk.device_error()
     out = eng.step(vals.q.to(dev), vals.k_step.to(dev), vals.v_step.to(dev))
