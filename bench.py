@@ -76,9 +76,9 @@ def kernel_source_hash():
 
 
 def recorded_traffic(workload):
-    """DRAM bytes per attention call from a committed ncu summary, if it
+    """DRAM bytes per fused step call from a committed ncu summary, if it
     was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
+    path = os.path.join(ROOT, "profiles", "decode_step_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)

@@ -357,8 +357,8 @@ const char* kv_last_cuda_error(void);
  *   3. paged_decode_step on cfg.stream after an event wait on that copy;
  *   4. with host_io, the output back to the caller's host buffer on a
  *      second side stream.
- * Two metadata buffers alternate between steps; their reuse is ordered by
- * events (the host waits only for the copy issued two steps earlier).
+ * Four metadata buffers rotate between steps; their reuse is ordered by
+ * events (the host waits only for work issued four steps earlier).
  * The runner allocates its buffers (page-locked host, device) and two side
  * streams at kvstep_create.  Not thread-safe: one thread drives a runner,
  * and the manager must not be used by anyone else meanwhile.  The device

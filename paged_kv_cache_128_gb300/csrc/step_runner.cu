@@ -16,11 +16,11 @@
 //   copy   with host I/O, the output back to the host on a second side
 //          stream.
 //
-// Two metadata buffers (host and device) alternate between steps.  Reuse
+// kNumBufs metadata buffers (host and device) rotate between steps.  Reuse
 // is ordered by events: the host rewrites host buffer i only after the copy
-// that read it two steps ago has run; the copy into device buffer i waits
-// for the kernel that read it two steps ago.  Nothing here synchronises the
-// device except those host waits on two-step-old copies.
+// that last read it has run; the copy into device buffer i waits for the
+// kernel that last read it.  Nothing here synchronises the device except
+// those host waits on copies issued kNumBufs steps earlier.
 
 #include <cuda_runtime.h>
 
@@ -43,27 +43,29 @@ struct Side {
 }  // namespace
 }  // namespace pagedkv
 
+constexpr int kNumBufs = 4;
+
 struct kvstep_s {
   kvbm_t mgr = nullptr;
   kvstep_config_t cfg{};
   int device = 0;
   int64_t meta_ints = 0;  // slot_mapping | block_tables | seq_lens | new_row
-  int32_t* h_meta[2] = {nullptr, nullptr};
-  int32_t* d_meta[2] = {nullptr, nullptr};
-  pagedkv::Side side[2];
+  int32_t* h_meta[kNumBufs] = {};
+  int32_t* d_meta[kNumBufs] = {};
+  pagedkv::Side side[kNumBufs];
   size_t q_bytes = 0, kv_bytes = 0;
   cudaStream_t compute = nullptr, h2d = nullptr, d2h = nullptr;
-  cudaEvent_t copied[2] = {nullptr, nullptr};  // H2D of buffer i done
-  cudaEvent_t done[2] = {nullptr, nullptr};    // kernel that read buffer i done
-  cudaEvent_t out_back[2] = {nullptr, nullptr};  // D2H of output i done (host I/O)
-  bool used[2] = {false, false};
-  int cur = 1;
+  cudaEvent_t copied[kNumBufs] = {};    // H2D of buffer i done
+  cudaEvent_t done[kNumBufs] = {};      // kernel that read buffer i done
+  cudaEvent_t out_back[kNumBufs] = {};  // D2H of output i done (host I/O)
+  bool used[kNumBufs] = {};
+  int cur = kNumBufs - 1;
 };
 
 namespace {
 
 void release(kvstep_s* h) {
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < kNumBufs; ++i) {
     if (h->h_meta[i]) cudaFreeHost(h->h_meta[i]);
     if (h->d_meta[i]) cudaFree(h->d_meta[i]);
     for (void* p : {h->side[i].q, h->side[i].k, h->side[i].v, h->side[i].out})
@@ -109,7 +111,7 @@ extern "C" int kvstep_create(kvbm_t mgr, const kvstep_config_t* cfg, kvstep_t* o
   h->q_bytes = static_cast<size_t>(c.num_seqs) * c.num_heads * c.head_dim * es;
   h->kv_bytes = static_cast<size_t>(c.num_step_tokens) * c.num_kv_heads * c.head_dim * es;
   cudaError_t e = cudaGetDevice(&h->device);
-  for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+  for (int i = 0; i < kNumBufs && e == cudaSuccess; ++i) {
     e = cudaHostAlloc(reinterpret_cast<void**>(&h->h_meta[i]), meta_bytes, cudaHostAllocDefault);
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&h->d_meta[i]), meta_bytes);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->copied[i], cudaEventDisableTiming);
@@ -135,7 +137,7 @@ extern "C" int kvstep_create(kvbm_t mgr, const kvstep_config_t* cfg, kvstep_t* o
 extern "C" int kvstep_destroy(kvstep_t h) {
   if (!h) return KV_ERR_INVALID_ARG;
   cudaError_t e = cudaSuccess;
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < kNumBufs; ++i) {
     if (h->used[i]) {
       cudaError_t a = cudaEventSynchronize(h->done[i]);
       cudaError_t b = cudaEventSynchronize(h->out_back[i]);
@@ -160,7 +162,7 @@ extern "C" int kvstep_run(kvstep_t h, const void* q, const void* k, const void* 
     if (pad_positions[i] < 0 || pad_positions[i] >= c.num_step_tokens || (i && pad_positions[i] <= pad_positions[i - 1]))
       return KV_ERR_INVALID_ARG;
 
-  const int i = h->cur ^ 1;
+  const int i = (h->cur + 1) % kNumBufs;
   cudaError_t e = cudaSuccess;
   if (h->used[i]) {
     e = cudaEventSynchronize(h->copied[i]);  // the copy that last read host buffer i has run
@@ -222,7 +224,7 @@ extern "C" int kvstep_join(kvstep_t h, void* stream) {
   if (!h) return KV_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
-  for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+  for (int i = 0; i < kNumBufs && e == cudaSuccess; ++i) {
     if (!h->used[i]) continue;
     e = cudaStreamWaitEvent(s, h->done[i], 0);
     if (e == cudaSuccess && h->cfg.host_io) e = cudaStreamWaitEvent(s, h->out_back[i], 0);
