@@ -103,8 +103,40 @@ int kvbm_append_slot_for_decode(kvbm_t h, int64_t seq_id, int32_t* slot_out);
  * or nothing on OOM.  slots_out (nullable) receives num_tokens slots. */
 int kvbm_append_slots(kvbm_t h, int64_t seq_id, int64_t num_tokens, int32_t* slots_out);
 
+/* Prefix sharing ("paged-attention-impl-detail", section Copy-on-Write共享:
+ * requests with a common prompt prefix share its physical blocks, each
+ * block counting its sharers).  A new sequence child_id (>= 0, not live)
+ * starts as the first prefix_len tokens of live sequence parent_id
+ * (1 <= prefix_len <= parent's length): its table is the parent's first
+ * ceil(prefix_len / bs) entries and each of those blocks gains a
+ * reference.  No block is taken.  Copy-on-write (same section): when a
+ * sequence's next write lands in a block that another table also holds
+ * (only possible while prefix_len % bs != 0 left it partly filled), the
+ * append first takes a free block, queues a copy old -> new of the whole
+ * block (see kvbm_take_copies), drops one reference from the old block and
+ * writes into the new one.  Appends count that block in their OOM check.
+ * Released blocks return to the free list when no table refers to them.
+ * KV_ERR_UNKNOWN_SEQ (parent not live), KV_ERR_DUPLICATE_SEQ (child live),
+ * KV_ERR_INVALID_ARG (prefix_len out of range). */
+int kvbm_fork(kvbm_t h, int64_t parent_id, int64_t child_id, int64_t prefix_len);
+
+/* Copy-on-write copies queued since the last call, oldest first: block
+ * src[i] must be copied to block dst[i] (K and V, every layer) on the
+ * device before the cache writes of the slots returned by the appends that
+ * queued them, and before any attention over those sequences
+ * (paged_copy_blocks).  *n_out = the number queued.  With src and dst both
+ * NULL the call only reports that number; otherwise the queue is copied
+ * out and emptied when it fits in cap (else KV_ERR_INVALID_ARG and nothing
+ * changes). */
+int kvbm_take_copies(kvbm_t h, int32_t* src, int32_t* dst, int64_t cap, int64_t* n_out);
+
+/* *out = the number of table entries (over all live sequences) that refer
+ * to block (0 = free). */
+int kvbm_block_refcount(kvbm_t h, int32_t block, int32_t* out);
+
 /* *ok = 1 iff one decode append to each listed sequence fits in the free
- * blocks (counts sequences whose next write opens a new block). */
+ * blocks (counts sequences whose next write opens a new block or copies a
+ * shared one). */
 int kvbm_can_append_slots(kvbm_t h, const int64_t* seq_ids, int64_t n, int* ok);
 
 /* One decode step for n distinct live sequences: append one slot to each
@@ -133,10 +165,12 @@ int kvbm_prepare_step(kvbm_t h, const int64_t* free_ids, int64_t n_free, const i
                       int64_t n_decode, const int64_t* pad_positions, int64_t n_pad, int64_t max_blocks,
                       int32_t* slot_mapping, int32_t* block_tables, int32_t* seq_lens);
 
-/* Release every block of seq_id once (MiniPaged-Qwen §5.3).  The table is
- * validated first; a corrupt table gives KV_ERR_INVARIANT and changes
- * nothing.  KV_ERR_DOUBLE_FREE for an id already released (and not
- * prefilled again), KV_ERR_UNKNOWN_SEQ for an id never seen. */
+/* Release every block of seq_id once (MiniPaged-Qwen §5.3): each loses one
+ * reference and returns to the back of the free list, in table order, when
+ * none is left.  The table is validated first; a corrupt table gives
+ * KV_ERR_INVARIANT and changes nothing.  KV_ERR_DOUBLE_FREE for an id
+ * already released (and not prefilled again), KV_ERR_UNKNOWN_SEQ for an id
+ * never seen. */
 int kvbm_free_sequence(kvbm_t h, int64_t seq_id);
 
 int kvbm_num_free_blocks(kvbm_t h, int64_t* out);
@@ -157,9 +191,13 @@ int kvbm_get_block_table(kvbm_t h, int64_t seq_id, int32_t* out, int64_t cap, in
 int kvbm_export(kvbm_t h, const int64_t* seq_ids, int64_t n, int64_t max_blocks,
                 int32_t* block_tables, int32_t* seq_lens);
 
-/* KV_OK iff: every table entry is in range and owned once, no allocated
- * block is free, allocated + free = the pool, len(table) = ceil(L / bs)
- * (MiniPaged-Qwen §15; LLM-algo ch.22 Step 3).  Else KV_ERR_INVARIANT. */
+/* KV_OK iff: every table entry is in range and appears once in its table,
+ * each block's reference count equals the table entries referring to it,
+ * the free list holds exactly the unreferenced blocks once each, referenced
+ * + free = the pool, len(table) = ceil(L / bs) (MiniPaged-Qwen §15;
+ * LLM-algo ch.22 Step 3; a block is shared across sequences only through
+ * kvbm_fork, as "从零实现一个 mini vLLM: Block Manager" allows for prefix
+ * caching and copy-on-write).  Else KV_ERR_INVARIANT. */
 int kvbm_check_invariants(kvbm_t h);
 
 typedef struct {
@@ -181,7 +219,8 @@ int kvbm_allocation_report(kvbm_t h, int64_t seq_id, int64_t* logical_tokens,
                            double* utilization);
 
 /* Debug aid from "从零实现一个 mini vLLM: Block Manager" (invariants section):
- * out[num_blocks] receives the owning sequence id of each block, -1 if free. */
+ * out[num_blocks] receives the owning sequence id of each block, -1 if free,
+ * -2 if several sequences share it (kvbm_fork). */
 int kvbm_owner_table(kvbm_t h, int64_t* out, int64_t cap);
 
 /* KV capacity ledger (LLM-algo ch.22 estimate_kv_cache_bytes; MiniPaged-Qwen
@@ -210,6 +249,21 @@ int paged_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v
                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                             int64_t num_blocks, int64_t k_token_stride, int64_t v_token_stride,
                             int dtype, void* stream);
+
+/* Copy-on-write block copies (kvbm_take_copies): for each i < n, block
+ * dst[i] of every layer's K and V cache becomes a copy of block src[i]
+ * ("paged-attention-impl-detail", copy_on_write: the new block's k and v
+ * take the old block's).  One launch for all pairs and layers.
+ *   k_cache, v_cache: device, num_layers caches [num_blocks, block_size,
+ *     num_kv_heads, head_dim] of dtype, layer l at + l * layer_stride
+ *     elements (16-byte aligned; pass 0 for one layer).
+ *   src, dst: device int32[n].  A pair with an index outside [0, num_blocks)
+ *     is skipped and recorded as KV_ERR_DEVICE_BOUNDS.  A destination that is
+ *     also a source of another pair, or two pairs with one destination, race.
+ * Bit-exact copies.  n == 0 launches nothing. */
+int paged_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int64_t n,
+                      int32_t num_layers, int64_t layer_stride, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, int64_t num_blocks, int dtype, void* stream);
 
 /* Split-K plan for a decode call with these sizes.  blocks_per_split: 0
  * chooses automatically (from the SM count of the current device, the
@@ -348,13 +402,15 @@ const char* kv_last_cuda_error(void);
  * block tables and context lengths from the manager and hands them to the
  * GPU with the step's K/V; "MiniPaged-Qwen" §8: CPU metadata plane, GPU data
  * plane).  kvstep_run does, in order:
- *   1. kvbm_prepare_step on the manager into a page-locked buffer, and each
+ *   1. kvbm_prepare_step on the manager into a page-locked buffer, each
  *      decode sequence's row in the step's K/V (the prefill tokens come
- *      first, then one token per decode sequence, around the pads);
+ *      first, then one token per decode sequence, around the pads), and the
+ *      copy-on-write copies the step's appends queued (kvbm_take_copies);
  *   2. one async host-to-device copy of that buffer on a side stream (with
  *      host_io, also the step's q, k and v), so the copy overlaps the
  *      previous step's kernel;
- *   3. paged_decode_step on cfg.stream after an event wait on that copy;
+ *   3. on cfg.stream after an event wait on that copy: paged_copy_blocks for
+ *      the queued copies (when there are any), then paged_decode_step;
  *   4. with host_io, the output back to the caller's host buffer on a
  *      second side stream.
  * Four metadata buffers rotate between steps; their reuse is ordered by
@@ -397,8 +453,10 @@ int kvstep_destroy(kvstep_t h);
  * The id arguments are those of kvbm_prepare_step; n_decode must equal
  * cfg.num_seqs, the pads must be strictly increasing and in range, and the
  * step's rows must add up to cfg.num_step_tokens (else KV_ERR_INVALID_ARG,
- * nothing done).  Manager errors are those of kvbm_prepare_step; nothing is
- * launched then. */
+ * nothing done).  Copies queued on the manager before the call (by appends
+ * made outside the runner) must have been taken and applied by the caller:
+ * if any are pending the call returns KV_ERR_INVALID_ARG and does nothing.
+ * Manager errors are those of kvbm_prepare_step; nothing is launched then. */
 int kvstep_run(kvstep_t h, const void* q, const void* k, const void* v, void* out,
                const int64_t* free_ids, int64_t n_free, const int64_t* prefill_ids,
                const int64_t* prefill_lens, int64_t n_prefill, const int64_t* decode_ids,

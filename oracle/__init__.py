@@ -30,6 +30,9 @@ Sources (cited by page title and section throughout):
 Modules:
 
 * ``block_manager`` -- the reference block manager (free-list policy).
+* ``prefix_sharing`` -- the same manager with per-block reference counts,
+  forked sequences sharing a prefix, and copy-on-write
+  ("paged-attention-impl-detail", section Copy-on-Write共享).
 * ``paged_cache``   -- address mapping, scatter (cache write), gather.
 * ``attention``     -- float64 decode attention, online-softmax form, and
   the split/merge identity used by split-K.
@@ -39,4 +42,4 @@ Every function here is pinned by ``tests/test_oracle_*.py`` against values
 the pages print, closed forms, invariants, or a library routine.
 """
 
-from . import attention, block_manager, ledger, paged_cache  # noqa: F401
+from . import attention, block_manager, ledger, paged_cache, prefix_sharing  # noqa: F401

@@ -53,6 +53,9 @@ SIGNATURES = {
     "kvbm_allocate_for_prefill": (c_int, [c_void_p, c_int64, c_int64, P32]),
     "kvbm_append_slot_for_decode": (c_int, [c_void_p, c_int64, P32]),
     "kvbm_append_slots": (c_int, [c_void_p, c_int64, c_int64, P32]),
+    "kvbm_fork": (c_int, [c_void_p, c_int64, c_int64, c_int64]),
+    "kvbm_take_copies": (c_int, [c_void_p, P32, P32, c_int64, P64]),
+    "kvbm_block_refcount": (c_int, [c_void_p, c_int32, P32]),
     "kvbm_can_append_slots": (c_int, [c_void_p, P64, c_int64, POINTER(c_int)]),
     "kvbm_decode_step": (c_int, [c_void_p, P64, c_int64, c_int64, P32, P32, P32]),
     "kvbm_prepare_step": (c_int, [c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_int64, c_void_p, c_int64,
@@ -70,6 +73,8 @@ SIGNATURES = {
     "kv_cache_ledger": (c_int, [c_int64, c_int64, c_int64, c_int64, c_int64, c_int64, P64, P64, P64]),
     "paged_reshape_and_cache": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int32,
                                         c_int32, c_int32, c_int64, c_int64, c_int64, c_int, c_void_p]),
+    "paged_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int32, c_int64, c_int32,
+                                  c_int32, c_int32, c_int64, c_int, c_void_p]),
     "paged_decode_plan": (c_int, [c_int32, c_int32, c_int32, c_int32, c_int32, c_int64, c_int32, c_int,
                                   P32, P32, P32, POINTER(c_size_t)]),
     "paged_decode_workspace_size": (c_int, [c_int32, c_int32, c_int32, c_int32, c_int32, c_int64, c_int32,

@@ -10,7 +10,7 @@ rollback, validated release).
 from __future__ import annotations
 
 import ctypes
-from typing import Dict, Optional, Sequence
+from typing import Dict, Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -126,6 +126,28 @@ class KVBlockManager:
 
     def free_sequence(self, seq_id: int) -> None:
         check(self._lib.kvbm_free_sequence(self._h, seq_id), "kvbm_free_sequence")
+
+    # -- prefix sharing / copy-on-write ----------------------------------------------
+    def fork(self, parent_id: int, child_id: int, prefix_len: int) -> None:
+        """New sequence ``child_id`` sharing the blocks of ``parent_id``'s
+        first ``prefix_len`` tokens (kvbm_fork)."""
+        check(self._lib.kvbm_fork(self._h, parent_id, child_id, prefix_len), "kvbm_fork")
+
+    def take_copies(self) -> Tuple[np.ndarray, np.ndarray]:
+        """Queued copy-on-write copies (src, dst) since the last call."""
+        n = ctypes.c_int64()
+        check(self._lib.kvbm_take_copies(self._h, None, None, 0, ctypes.byref(n)), "kvbm_take_copies")
+        src = np.empty(n.value, dtype=np.int32)
+        dst = np.empty(n.value, dtype=np.int32)
+        if n.value:
+            check(self._lib.kvbm_take_copies(self._h, _i32(src), _i32(dst), n.value, ctypes.byref(n)),
+                  "kvbm_take_copies")
+        return src, dst
+
+    def block_refcount(self, block: int) -> int:
+        out = ctypes.c_int32()
+        check(self._lib.kvbm_block_refcount(self._h, block, ctypes.byref(out)), "kvbm_block_refcount")
+        return out.value
 
     # -- queries -----------------------------------------------------------------------
     def num_free_blocks(self) -> int:

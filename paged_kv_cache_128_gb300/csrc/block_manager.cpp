@@ -11,10 +11,18 @@
 // Free-list policy: take from the front, release to the back in table
 // order (no sort), so a seeded initial order and churn carry through.
 //
-// Design: the free list is a ring buffer of int32 with an is_free bitmap
-// for O(1) membership; each sequence keeps its table in a std::vector.
-// Every mutating call validates fully before it changes anything, so a
-// failed call leaves the state exactly as it was.
+// Prefix sharing and copy-on-write ("paged-attention-impl-detail",
+// section Copy-on-Write共享): a forked sequence shares its parent's blocks,
+// each block carries a reference count, and a sequence about to write into
+// a block that others also hold first copies it to a fresh block (the
+// count of the old block drops by one, the new block's count is 1).  A
+// released block returns to the free list only when its count reaches 0.
+// The copies are queued for the device (kvbm_take_copies).
+//
+// Design: the free list is a ring buffer of int32; ref_count[b] == 0 iff b
+// is free; each sequence keeps its table in a std::vector.  Every mutating
+// call validates fully before it changes anything, so a failed call leaves
+// the state exactly as it was.
 
 #include <algorithm>
 #include <cstdint>
@@ -65,20 +73,30 @@ struct kvbm_s {
   int64_t num_blocks;
   int32_t block_size;
   FreeList free_list;
-  std::vector<uint8_t> is_free;
+  std::vector<int32_t> ref_count;  // table entries referring to each block; 0 = free
   std::unordered_map<int64_t, Sequence> seqs;
   std::unordered_set<int64_t> released;
+  std::vector<int32_t> copy_src, copy_dst;  // copy-on-write copies not yet taken
 
-  kvbm_s(int64_t nb, int32_t bs) : num_blocks(nb), block_size(bs), free_list(nb), is_free(nb, 0) {}
+  kvbm_s(int64_t nb, int32_t bs) : num_blocks(nb), block_size(bs), free_list(nb), ref_count(nb, 0) {}
 
+  bool is_free(int32_t b) const { return ref_count[static_cast<size_t>(b)] == 0; }
   int32_t take_front() {
     int32_t b = free_list.pop_front();
-    is_free[static_cast<size_t>(b)] = 0;
+    ref_count[static_cast<size_t>(b)] = 1;
     return b;
   }
-  void give_back(int32_t b) {
+  void give_back(int32_t b) {  // b's count is 0
     free_list.push_back(b);
-    is_free[static_cast<size_t>(b)] = 1;
+  }
+  // Drop one reference; the block is free again when none is left.
+  void unref(int32_t b) {
+    if (--ref_count[static_cast<size_t>(b)] == 0) give_back(b);
+  }
+  // The next write of s lands in its last block while another table also
+  // holds that block: it must be copied first.
+  bool needs_copy(const Sequence& s) const {
+    return s.length % block_size != 0 && !s.table.empty() && ref_count[static_cast<size_t>(s.table.back())] > 1;
   }
   // MiniPaged-Qwen §3: slot = table[pos / bs] * bs + pos % bs.
   int32_t slot_of(const Sequence& s, int64_t pos) const {
@@ -86,13 +104,25 @@ struct kvbm_s {
                                     block_size +
                                 pos % block_size);
   }
-  // Blocks a sequence must gain to hold `extra` more tokens.
+  // Blocks a sequence must gain to hold `extra` more tokens: new logical
+  // blocks, plus one when its first write needs a copy of a shared block.
   int64_t blocks_needed(const Sequence& s, int64_t extra) const {
-    return ceil_div(s.length + extra, block_size) - static_cast<int64_t>(s.table.size());
+    return ceil_div(s.length + extra, block_size) - static_cast<int64_t>(s.table.size()) +
+           (extra > 0 && needs_copy(s) ? 1 : 0);
   }
-  // MiniPaged-Qwen §9 append_token; the caller has checked a block is free.
+  // MiniPaged-Qwen §9 append_token, with copy-on-write of a shared last
+  // block; the caller has checked a block is free.
   int32_t append_one(Sequence& s) {
-    if (s.length / block_size == static_cast<int64_t>(s.table.size())) s.table.push_back(take_front());
+    if (s.length / block_size == static_cast<int64_t>(s.table.size())) {
+      s.table.push_back(take_front());
+    } else if (needs_copy(s)) {
+      const int32_t old = s.table.back();
+      const int32_t fresh = take_front();
+      --ref_count[static_cast<size_t>(old)];  // others still hold it: count stays >= 1
+      s.table.back() = fresh;
+      copy_src.push_back(old);
+      copy_dst.push_back(fresh);
+    }
     int32_t slot = slot_of(s, s.length);
     s.length += 1;
     return slot;
@@ -217,6 +247,43 @@ int kvbm_append_slots(kvbm_t h, int64_t seq_id, int64_t num_tokens, int32_t* slo
   });
 }
 
+int kvbm_fork(kvbm_t h, int64_t parent_id, int64_t child_id, int64_t prefix_len) {
+  if (!h || child_id < 0) return KV_ERR_INVALID_ARG;
+  Sequence* p = h->find(parent_id);
+  if (!p) return KV_ERR_UNKNOWN_SEQ;
+  if (h->seqs.count(child_id)) return KV_ERR_DUPLICATE_SEQ;
+  if (prefix_len < 1 || prefix_len > p->length) return KV_ERR_INVALID_ARG;
+  return guarded([&] {
+    Sequence c;
+    const int64_t nb = ceil_div(prefix_len, h->block_size);
+    c.table.assign(p->table.begin(), p->table.begin() + nb);
+    c.length = prefix_len;
+    for (int32_t b : c.table) ++h->ref_count[static_cast<size_t>(b)];
+    h->seqs.emplace(child_id, std::move(c));
+    h->released.erase(child_id);
+    return static_cast<int>(KV_OK);
+  });
+}
+
+int kvbm_take_copies(kvbm_t h, int32_t* src, int32_t* dst, int64_t cap, int64_t* n_out) {
+  if (!h || !n_out) return KV_ERR_INVALID_ARG;
+  const int64_t n = static_cast<int64_t>(h->copy_src.size());
+  *n_out = n;
+  if (n == 0 || (!src && !dst)) return KV_OK;  // nothing queued, or a size query
+  if (!src || !dst || cap < n) return KV_ERR_INVALID_ARG;
+  std::copy(h->copy_src.begin(), h->copy_src.end(), src);
+  std::copy(h->copy_dst.begin(), h->copy_dst.end(), dst);
+  h->copy_src.clear();
+  h->copy_dst.clear();
+  return KV_OK;
+}
+
+int kvbm_block_refcount(kvbm_t h, int32_t block, int32_t* out) {
+  if (!h || !out || block < 0 || block >= h->num_blocks) return KV_ERR_INVALID_ARG;
+  *out = h->ref_count[static_cast<size_t>(block)];
+  return KV_OK;
+}
+
 int kvbm_can_append_slots(kvbm_t h, const int64_t* seq_ids, int64_t n, int* ok) {
   if (!h || !ok || n < 0 || (n > 0 && !seq_ids)) return KV_ERR_INVALID_ARG;
   int64_t need = 0;
@@ -263,7 +330,7 @@ int kvbm_decode_step(kvbm_t h, const int64_t* seq_ids, int64_t n, int64_t max_bl
       Sequence* s = h->find(seq_ids[i]);
       if (!s) return static_cast<int>(KV_ERR_UNKNOWN_SEQ);
       int64_t grow = h->blocks_needed(*s, 1);
-      if (static_cast<int64_t>(s->table.size()) + grow > max_blocks && (block_tables || seq_lens))
+      if (ceil_div(s->length + 1, h->block_size) > max_blocks && (block_tables || seq_lens))
         return static_cast<int>(KV_ERR_INVALID_ARG);
       need += grow;
       seqs[static_cast<size_t>(i)] = s;
@@ -314,7 +381,7 @@ int kvbm_prepare_step(kvbm_t h, const int64_t* free_ids, int64_t n_free, const i
       if (!sq) return static_cast<int>(seen.count(decode_ids[i]) ? KV_ERR_INVALID_ARG : KV_ERR_UNKNOWN_SEQ);
       if (!seen.insert(decode_ids[i]).second) return static_cast<int>(KV_ERR_INVALID_ARG);
       const int64_t grow = h->blocks_needed(*sq, 1);
-      if ((block_tables || seq_lens) && static_cast<int64_t>(sq->table.size()) + grow > max_blocks)
+      if ((block_tables || seq_lens) && ceil_div(sq->length + 1, h->block_size) > max_blocks)
         return static_cast<int>(KV_ERR_INVALID_ARG);
       need += grow;
       dec[static_cast<size_t>(i)] = sq;
@@ -366,10 +433,10 @@ int kvbm_free_sequence(kvbm_t h, int64_t seq_id) {
   for (int32_t b : table) {
     if (b < 0 || b >= h->num_blocks) return KV_ERR_INVARIANT;
     if (!seen.insert(b).second) return KV_ERR_INVARIANT;
-    if (h->is_free[static_cast<size_t>(b)]) return KV_ERR_INVARIANT;
+    if (h->is_free(b)) return KV_ERR_INVARIANT;
   }
   return guarded([&] {
-    for (int32_t b : table) h->give_back(b);
+    for (int32_t b : table) h->unref(b);
     h->seqs.erase(it);
     h->released.insert(seq_id);
     return static_cast<int>(KV_OK);
@@ -413,26 +480,32 @@ int kvbm_get_block_table(kvbm_t h, int64_t seq_id, int32_t* out, int64_t cap, in
 int kvbm_check_invariants(kvbm_t h) {
   if (!h) return KV_ERR_INVALID_ARG;
   return guarded([&] {
-    std::vector<uint8_t> owned(static_cast<size_t>(h->num_blocks), 0);
-    int64_t allocated = 0;
+    // references per block, counted from the tables; no block twice in one
+    // table (a block is shared only across sequences)
+    std::vector<int32_t> refs(static_cast<size_t>(h->num_blocks), 0);
     for (const auto& kv : h->seqs) {
       const Sequence& s = kv.second;
       if (static_cast<int64_t>(s.table.size()) != ceil_div(s.length, h->block_size))
         return static_cast<int>(KV_ERR_INVARIANT);
+      std::unordered_set<int32_t> in_table;
       for (int32_t b : s.table) {
         if (b < 0 || b >= h->num_blocks) return static_cast<int>(KV_ERR_INVARIANT);
-        if (owned[static_cast<size_t>(b)]) return static_cast<int>(KV_ERR_INVARIANT);
-        owned[static_cast<size_t>(b)] = 1;
-        ++allocated;
+        if (!in_table.insert(b).second) return static_cast<int>(KV_ERR_INVARIANT);
+        ++refs[static_cast<size_t>(b)];
       }
     }
+    int64_t allocated = 0;
+    for (int64_t b = 0; b < h->num_blocks; ++b) {
+      if (refs[static_cast<size_t>(b)] != h->ref_count[static_cast<size_t>(b)]) return static_cast<int>(KV_ERR_INVARIANT);
+      if (refs[static_cast<size_t>(b)] > 0) ++allocated;
+    }
+    // the free list holds exactly the unreferenced blocks, once each
     std::vector<uint8_t> in_free(static_cast<size_t>(h->num_blocks), 0);
     for (int64_t i = 0; i < h->free_list.size(); ++i) {
       int32_t b = h->free_list.at(i);
       if (b < 0 || b >= h->num_blocks) return static_cast<int>(KV_ERR_INVARIANT);
-      if (in_free[static_cast<size_t>(b)] || owned[static_cast<size_t>(b)])
+      if (in_free[static_cast<size_t>(b)] || refs[static_cast<size_t>(b)] != 0)
         return static_cast<int>(KV_ERR_INVARIANT);
-      if (!h->is_free[static_cast<size_t>(b)]) return static_cast<int>(KV_ERR_INVARIANT);
       in_free[static_cast<size_t>(b)] = 1;
     }
     if (allocated + h->free_list.size() != h->num_blocks) return static_cast<int>(KV_ERR_INVARIANT);
@@ -476,7 +549,7 @@ int kvbm_owner_table(kvbm_t h, int64_t* out, int64_t cap) {
   for (const auto& kv : h->seqs)
     for (int32_t b : kv.second.table) {
       if (b < 0 || b >= h->num_blocks) return KV_ERR_INVARIANT;
-      out[b] = kv.first;
+      out[b] = out[b] == -1 ? kv.first : -2;  // -2: held by several sequences
     }
   return KV_OK;
 }

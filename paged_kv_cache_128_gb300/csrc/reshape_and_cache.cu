@@ -128,3 +128,69 @@ extern "C" int pagedkv_internal_reshape_error(int reset, int* code) {
   *code = v;
   return KV_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Copy-on-write block copies ("paged-attention-impl-detail", section
+// Copy-on-Write共享: a writer to a shared block first copies its K and V to a
+// fresh block).  One CTA per (pair, layer); the CTA streams the block's K
+// then V bytes with 16-byte vectors, all loads of a round before its stores.
+
+namespace pagedkv {
+namespace {
+
+constexpr int kCopyThreads = 256;
+
+__global__ void __launch_bounds__(kCopyThreads)
+copy_blocks_kernel(char* __restrict__ k_cache, char* __restrict__ v_cache, const int32_t* __restrict__ src,
+                   const int32_t* __restrict__ dst, int64_t n, int64_t layer_stride_bytes, int64_t block_bytes,
+                   int64_t num_blocks) {
+  const int64_t pair = blockIdx.x;
+  const int64_t layer = blockIdx.y;
+  if (pair >= n) return;
+  const int32_t s = __ldg(src + pair), d = __ldg(dst + pair);
+  if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+    if (threadIdx.x == 0) record_error(KV_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  const int64_t nvec = block_bytes / 16;
+  for (int which = 0; which < 2; ++which) {
+    char* base = (which ? v_cache : k_cache) + layer * layer_stride_bytes;
+    const uint4* from = reinterpret_cast<const uint4*>(base + s * block_bytes);
+    uint4* to = reinterpret_cast<uint4*>(base + d * block_bytes);
+    for (int64_t i0 = threadIdx.x; i0 < nvec; i0 += kCopyThreads * 4) {
+      uint4 r[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i0 + u * kCopyThreads < nvec) r[u] = from[i0 + u * kCopyThreads];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i0 + u * kCopyThreads < nvec) to[i0 + u * kCopyThreads] = r[u];
+    }
+  }
+}
+
+}  // namespace
+}  // namespace pagedkv
+
+extern "C" int paged_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int64_t n,
+                                 int32_t num_layers, int64_t layer_stride, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t block_size, int64_t num_blocks, int dtype, void* stream) {
+  using namespace pagedkv;
+  if (dtype != KV_DTYPE_F32 && dtype != KV_DTYPE_F16 && dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
+  if (n < 0 || num_layers <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
+      layer_stride < 0)
+    return KV_ERR_INVALID_ARG;
+  if (n == 0) return KV_OK;
+  if (!k_cache || !v_cache || !src || !dst) return KV_ERR_INVALID_ARG;
+  const int64_t es = static_cast<int64_t>(dtype_bytes(dtype));
+  const int64_t block_bytes = static_cast<int64_t>(block_size) * num_kv_heads * head_dim * es;
+  if (num_layers > 1 && layer_stride < num_blocks * block_size * static_cast<int64_t>(num_kv_heads) * head_dim)
+    return KV_ERR_INVALID_ARG;  // layers would overlap
+  if (block_bytes % 16 != 0 || (layer_stride * es) % 16 != 0 || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return KV_ERR_INVALID_ARG;
+  if (n > 0x7fffffff || num_layers > 65535) return KV_ERR_INVALID_ARG;
+  copy_blocks_kernel<<<dim3(static_cast<unsigned>(n), static_cast<unsigned>(num_layers)), kCopyThreads, 0,
+                       static_cast<cudaStream_t>(stream)>>>(static_cast<char*>(k_cache), static_cast<char*>(v_cache),
+                                                             src, dst, n, layer_stride * es, block_bytes, num_blocks);
+  return cuda_status(cudaGetLastError());
+}

@@ -7,11 +7,13 @@
 // plane, GPU data plane):
 //
 //   host   kvbm_prepare_step into a page-locked buffer, plus each decode
-//          sequence's row in the step's K/V (its newest token);
+//          sequence's row in the step's K/V (its newest token) and the
+//          copy-on-write copies its appends queued (kvbm_take_copies);
 //   copy   one async H2D copy of that buffer on a side stream (and, with
 //          host I/O, the step's q/k/v), so it overlaps the previous step's
 //          kernel instead of sitting between two kernels;
-//   device paged_decode_step on the compute stream after an event wait:
+//   device paged_copy_blocks for those copies, if any, then
+//          paged_decode_step on the compute stream after an event wait:
 //          one launch doing the cache write and decode attention;
 //   copy   with host I/O, the output back to the host on a second side
 //          stream.
@@ -49,7 +51,7 @@ struct kvstep_s {
   kvbm_t mgr = nullptr;
   kvstep_config_t cfg{};
   int device = 0;
-  int64_t meta_ints = 0;  // slot_mapping | block_tables | seq_lens | new_row
+  int64_t meta_ints = 0;  // slot_mapping | block_tables | seq_lens | new_row | copy src | copy dst
   int32_t* h_meta[kNumBufs] = {};
   int32_t* d_meta[kNumBufs] = {};
   pagedkv::Side side[kNumBufs];
@@ -105,7 +107,8 @@ extern "C" int kvstep_create(kvbm_t mgr, const kvstep_config_t* cfg, kvstep_t* o
   h->mgr = mgr;
   h->cfg = c;
   h->compute = static_cast<cudaStream_t>(c.stream);
-  h->meta_ints = c.num_step_tokens + static_cast<int64_t>(c.num_seqs) * c.max_blocks_per_seq + 2 * c.num_seqs;
+  // at most one copy-on-write copy per decode append (prefills never copy)
+  h->meta_ints = c.num_step_tokens + static_cast<int64_t>(c.num_seqs) * c.max_blocks_per_seq + 4 * c.num_seqs;
   const size_t meta_bytes = static_cast<size_t>(h->meta_ints) * sizeof(int32_t);
   const size_t es = pagedkv::dtype_bytes(c.dtype);
   h->q_bytes = static_cast<size_t>(c.num_seqs) * c.num_heads * c.head_dim * es;
@@ -173,8 +176,16 @@ extern "C" int kvstep_run(kvstep_t h, const void* q, const void* k, const void* 
   int32_t* tables = slots + c.num_step_tokens;
   int32_t* lens = tables + B * maxb;
   int32_t* rows = lens + B;
-  int st = kvbm_prepare_step(h->mgr, free_ids, n_free, prefill_ids, prefill_lens, n_prefill, decode_ids, n_decode,
-                             pad_positions, n_pad, maxb, slots, tables, lens);
+  int32_t* cp_src = rows + B;
+  int32_t* cp_dst = cp_src + B;
+  int64_t n_copies = 0;
+  int st = kvbm_take_copies(h->mgr, nullptr, nullptr, 0, &n_copies);
+  if (st != KV_OK) return st;
+  if (n_copies != 0) return KV_ERR_INVALID_ARG;  // copies queued outside the runner must be applied by their caller
+  st = kvbm_prepare_step(h->mgr, free_ids, n_free, prefill_ids, prefill_lens, n_prefill, decode_ids, n_decode,
+                         pad_positions, n_pad, maxb, slots, tables, lens);
+  if (st != KV_OK) return st;
+  st = kvbm_take_copies(h->mgr, cp_src, cp_dst, B, &n_copies);
   if (st != KV_OK) return st;
   decode_rows(pad_positions, n_pad, n_pre_tokens, n_decode, rows);
   h->cur = i;
@@ -204,6 +215,11 @@ extern "C" int kvstep_run(kvstep_t h, const void* q, const void* k, const void* 
   int32_t* d_tables = d_slots + c.num_step_tokens;
   int32_t* d_lens = d_tables + B * maxb;
   int32_t* d_rows = d_lens + B;
+  if (n_copies > 0) {  // copy-on-write copies before the step's writes and reads
+    st = paged_copy_blocks(c.k_cache, c.v_cache, d_rows + B, d_rows + 2 * B, n_copies, 1, 0, c.num_kv_heads,
+                           c.head_dim, c.block_size, c.num_blocks, c.dtype, h->compute);
+    if (st != KV_OK) return st;
+  }
   const int64_t row = static_cast<int64_t>(c.num_kv_heads) * c.head_dim;
   st = paged_decode_step(dout, dq, dk, dv, d_slots, c.num_step_tokens, row, row, d_rows, c.k_cache, c.v_cache,
                          d_tables, d_lens, c.num_seqs, c.num_heads, c.num_kv_heads, c.head_dim, c.block_size,

@@ -59,6 +59,32 @@ def reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v
           "paged_reshape_and_cache")
 
 
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src: torch.Tensor, dst: torch.Tensor,
+                stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Copy-on-write copies: block ``dst[i]`` of every layer's K and V cache
+    becomes a copy of block ``src[i]`` (int32 device tensors).  Caches are
+    ``[NB, BS, Hkv, D]`` or ``[layers, NB, BS, Hkv, D]``, contiguous."""
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (src, "src"), (dst, "dst")):
+        _cuda(t, n)
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous() and k_cache.shape == v_cache.shape
+            and k_cache.dtype == v_cache.dtype):
+        raise KVError(1, "caches must be contiguous, of one shape and dtype")
+    if src.dtype != torch.int32 or dst.dtype != torch.int32 or src.numel() != dst.numel() \
+            or not src.is_contiguous() or not dst.is_contiguous():
+        raise KVError(1, "src and dst must be contiguous int32 of one length")
+    if k_cache.dim() == 4:
+        layers, (nb, bs, hkv, d) = 1, k_cache.shape
+        stride = 0
+    elif k_cache.dim() == 5:
+        layers, nb, bs, hkv, d = k_cache.shape
+        stride = k_cache.stride(0)
+    else:
+        raise KVError(1, "caches must be 4-D or 5-D")
+    check(lib().paged_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), src.data_ptr(), dst.data_ptr(),
+                                  src.numel(), layers, stride, hkv, d, bs, nb, dtype_code(k_cache.dtype),
+                                  _stream_ptr(stream)), "paged_copy_blocks")
+
+
 @dataclass
 class DecodePlan:
     kernel: int            # 0 = SIMT, 1 = split TMA + tensor cores, 2 = stream-K TMA + tensor cores
