@@ -250,6 +250,23 @@ int paged_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v
                             int64_t num_blocks, int64_t k_token_stride, int64_t v_token_stride,
                             int dtype, void* stream);
 
+/* paged_reshape_and_cache for num_layers layers in one launch.  One block
+ * table and one slot mapping serve every layer ("MiniPaged-Qwen" §16: the
+ * step's metadata is built once and read by every layer's attention; the
+ * capacity ledger's per-block bytes cover all layers, see kv_cache_ledger).
+ *   k, v: layer l's rows at + l * k_layer_stride / v_layer_stride elements,
+ *     then as for paged_reshape_and_cache (token stride, dense heads).
+ *   k_cache, v_cache: layer l's cache [num_blocks, block_size, num_kv_heads,
+ *     head_dim] at + l * cache_layer_stride elements (>= one layer's cache
+ *     when num_layers > 1, else KV_ERR_INVALID_ARG).
+ * Everything else (padding, bounds, bit-exactness) as paged_reshape_and_cache. */
+int paged_reshape_and_cache_layers(const void* k, const void* v, void* k_cache, void* v_cache,
+                                   const int32_t* slot_mapping, int64_t num_tokens, int32_t num_layers,
+                                   int64_t k_layer_stride, int64_t v_layer_stride,
+                                   int64_t cache_layer_stride, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int64_t num_blocks, int64_t k_token_stride,
+                                   int64_t v_token_stride, int dtype, void* stream);
+
 /* Copy-on-write block copies (kvbm_take_copies): for each i < n, block
  * dst[i] of every layer's K and V cache becomes a copy of block src[i]
  * ("paged-attention-impl-detail", copy_on_write: the new block's k and v
@@ -438,6 +455,8 @@ typedef struct {
   void* stream;                /* compute stream (cudaStream_t) */
   int32_t host_io;             /* 0: q/k/v/out given to kvstep_run are device buffers;
                                   1: page-locked host buffers, copied in and out by the runner */
+  int32_t num_layers;          /* layers sharing the block tables (0 or 1: one) */
+  int64_t cache_layer_stride;  /* elements between consecutive layers' caches (num_layers > 1) */
 } kvstep_config_t;
 
 int kvstep_create(kvbm_t mgr, const kvstep_config_t* cfg, kvstep_t* out);
@@ -446,7 +465,10 @@ int kvstep_create(kvbm_t mgr, const kvstep_config_t* cfg, kvstep_t* out);
 int kvstep_destroy(kvstep_t h);
 
 /* One step.  q [num_seqs, num_heads, head_dim], k and v dense
- * [num_step_tokens, num_kv_heads, head_dim], out like q: device buffers
+ * [num_step_tokens, num_kv_heads, head_dim], out like q (with num_layers
+ * layers, each of the four is that many such tensors back to back, and the
+ * step's metadata, built and copied once, serves one fused launch per
+ * layer over that layer's cache): device buffers
  * (host_io = 0; read and written in cfg.stream order) or page-locked host
  * buffers (host_io = 1; q/k/v are read by the copy issued here, out is
  * written when the step's device-to-host copy completes, see kvstep_join).

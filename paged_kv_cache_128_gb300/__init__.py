@@ -17,7 +17,7 @@ from .block_manager import KVBlockManager, kv_cache_ledger  # noqa: F401
 
 def __getattr__(name):
     # the kernel wrappers need torch; import them on first use
-    if name in ("reshape_and_cache", "paged_decode_attention", "paged_decode_step", "copy_blocks", "decode_plan",
+    if name in ("reshape_and_cache", "reshape_and_cache_layers", "paged_decode_attention", "paged_decode_step", "copy_blocks", "decode_plan",
                 "device_error", "alloc_workspace", "DecodePlan"):
         from . import kernels
         return getattr(kernels, name)

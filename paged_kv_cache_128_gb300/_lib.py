@@ -38,7 +38,8 @@ class kvstep_config_t(ctypes.Structure):
                 ("block_size", c_int32), ("num_blocks", c_int64), ("max_blocks_per_seq", c_int32),
                 ("max_seq_len", c_int64), ("scale", c_float), ("dtype", c_int32), ("num_step_tokens", c_int64),
                 ("k_cache", c_void_p), ("v_cache", c_void_p), ("workspace", c_void_p),
-                ("workspace_bytes", c_size_t), ("stream", c_void_p), ("host_io", c_int32)]
+                ("workspace_bytes", c_size_t), ("stream", c_void_p), ("host_io", c_int32),
+                ("num_layers", c_int32), ("cache_layer_stride", c_int64)]
 
 
 P32 = POINTER(c_int32)
@@ -73,6 +74,9 @@ SIGNATURES = {
     "kv_cache_ledger": (c_int, [c_int64, c_int64, c_int64, c_int64, c_int64, c_int64, P64, P64, P64]),
     "paged_reshape_and_cache": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int32,
                                         c_int32, c_int32, c_int64, c_int64, c_int64, c_int, c_void_p]),
+    "paged_reshape_and_cache_layers": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int32,
+                                               c_int64, c_int64, c_int64, c_int32, c_int32, c_int32, c_int64,
+                                               c_int64, c_int64, c_int, c_void_p]),
     "paged_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int32, c_int64, c_int32,
                                   c_int32, c_int32, c_int64, c_int, c_void_p]),
     "paged_decode_plan": (c_int, [c_int32, c_int32, c_int32, c_int32, c_int32, c_int64, c_int32, c_int,

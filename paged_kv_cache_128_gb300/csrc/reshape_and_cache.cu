@@ -11,6 +11,11 @@
 // vectors (narrower only when the row size or alignment forces it), issuing
 // all of its loads for K and V before the stores so a warp keeps up to
 // 2 * kUnroll vectors per lane in flight.  The copy is bit-exact.
+//
+// Several layers' caches under one block table ("MiniPaged-Qwen" §16: the
+// block tables and slot mapping are built once per step and shared by every
+// layer's attention) are written by one launch: grid.y runs over layers,
+// each with its own input and cache base.
 
 #include "common.cuh"
 
@@ -24,8 +29,14 @@ template <typename V>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 reshape_and_cache_kernel(const char* __restrict__ k, const char* __restrict__ v, char* __restrict__ k_cache,
                          char* __restrict__ v_cache, const int32_t* __restrict__ slot_mapping, int64_t num_tokens,
-                         int64_t row_bytes, int64_t k_stride_bytes, int64_t v_stride_bytes, int64_t num_slots) {
+                         int64_t row_bytes, int64_t k_stride_bytes, int64_t v_stride_bytes, int64_t num_slots,
+                         int64_t k_layer_bytes, int64_t v_layer_bytes, int64_t cache_layer_bytes) {
   const int lane = threadIdx.x & 31;
+  const int64_t layer = blockIdx.y;
+  k += layer * k_layer_bytes;
+  v += layer * v_layer_bytes;
+  k_cache += layer * cache_layer_bytes;
+  v_cache += layer * cache_layer_bytes;
   const int64_t nvec = row_bytes / static_cast<int64_t>(sizeof(V));
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5); t < num_tokens;
        t += static_cast<int64_t>(gridDim.x) * kWarpsPerCta) {
@@ -63,58 +74,95 @@ reshape_and_cache_kernel(const char* __restrict__ k, const char* __restrict__ v,
 
 bool aligned(const void* p, int64_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+struct LayerStrides {
+  int32_t layers;
+  int64_t k_bytes, v_bytes, cache_bytes;  // between consecutive layers
+};
+
 template <typename V>
 cudaError_t launch(const void* k, const void* v, void* kc, void* vc, const int32_t* slots, int64_t n,
-                   int64_t row_bytes, int64_t ks, int64_t vs, int64_t num_slots, cudaStream_t stream) {
+                   int64_t row_bytes, int64_t ks, int64_t vs, int64_t num_slots, const LayerStrides& ls,
+                   cudaStream_t stream) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t need = (n + kWarpsPerCta - 1) / kWarpsPerCta;
-  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * 16;
+  const int64_t cap = (static_cast<int64_t>(sms > 0 ? sms : 1) * 16 + ls.layers - 1) / ls.layers;
   const int grid = static_cast<int>(need < cap ? need : cap);
-  reshape_and_cache_kernel<V><<<grid, kWarpsPerCta * 32, 0, stream>>>(
+  reshape_and_cache_kernel<V><<<dim3(grid, ls.layers), kWarpsPerCta * 32, 0, stream>>>(
       static_cast<const char*>(k), static_cast<const char*>(v), static_cast<char*>(kc), static_cast<char*>(vc),
-      slots, n, row_bytes, ks, vs, num_slots);
+      slots, n, row_bytes, ks, vs, num_slots, ls.k_bytes, ls.v_bytes, ls.cache_bytes);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+// The cache write of num_layers layers (1 for paged_reshape_and_cache).
+int cache_write(const void* k, const void* v, void* k_cache, void* v_cache, const int32_t* slot_mapping,
+                int64_t num_tokens, int32_t num_layers, int64_t k_layer_stride, int64_t v_layer_stride,
+                int64_t cache_layer_stride, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                int64_t num_blocks, int64_t k_token_stride, int64_t v_token_stride, int dtype, void* stream);
 }  // namespace pagedkv
 
 using namespace pagedkv;
+
+int pagedkv::cache_write(const void* k, const void* v, void* k_cache, void* v_cache, const int32_t* slot_mapping,
+                         int64_t num_tokens, int32_t num_layers, int64_t k_layer_stride, int64_t v_layer_stride,
+                         int64_t cache_layer_stride, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                         int64_t num_blocks, int64_t k_token_stride, int64_t v_token_stride, int dtype,
+                         void* stream) {
+  if (dtype != KV_DTYPE_F32 && dtype != KV_DTYPE_F16 && dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    return KV_ERR_INVALID_ARG;
+  if (num_layers <= 0 || num_layers > 65535 || k_layer_stride < 0 || v_layer_stride < 0 || cache_layer_stride < 0)
+    return KV_ERR_INVALID_ARG;
+  const int64_t row_elems = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (k_token_stride < row_elems || v_token_stride < row_elems) return KV_ERR_INVALID_ARG;
+  if (num_blocks > INT32_MAX / block_size) return KV_ERR_INVALID_ARG;
+  const int64_t num_slots = num_blocks * block_size;
+  if (num_layers > 1 && cache_layer_stride < num_slots * row_elems) return KV_ERR_INVALID_ARG;  // layers overlap
+  if (num_tokens == 0) return KV_OK;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping) return KV_ERR_INVALID_ARG;
+  const int64_t es = static_cast<int64_t>(dtype_bytes(dtype));
+  const int64_t row_bytes = row_elems * es, ks = k_token_stride * es, vs = v_token_stride * es;
+  const LayerStrides ls{num_layers, k_layer_stride * es, v_layer_stride * es, cache_layer_stride * es};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  auto fits = [&](int64_t a) {
+    return row_bytes % a == 0 && ks % a == 0 && vs % a == 0 && aligned(k, a) && aligned(v, a) &&
+           aligned(k_cache, a) && aligned(v_cache, a) && ls.k_bytes % a == 0 && ls.v_bytes % a == 0 &&
+           ls.cache_bytes % a == 0;
+  };
+  if (fits(16))
+    err = launch<uint4>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, ks, vs, num_slots, ls, st);
+  else if (fits(8))
+    err = launch<uint2>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, ks, vs, num_slots, ls, st);
+  else if (fits(4))
+    err = launch<uint32_t>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, ks, vs, num_slots, ls, st);
+  else if (fits(2))
+    err = launch<uint16_t>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, ks, vs, num_slots, ls, st);
+  else
+    return KV_ERR_INVALID_ARG;
+  return cuda_status(err);
+}
 
 extern "C" int paged_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
                                        const int32_t* slot_mapping, int64_t num_tokens, int32_t num_kv_heads,
                                        int32_t head_dim, int32_t block_size, int64_t num_blocks,
                                        int64_t k_token_stride, int64_t v_token_stride, int dtype, void* stream) {
-  if (dtype != KV_DTYPE_F32 && dtype != KV_DTYPE_F16 && dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
-  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
-    return KV_ERR_INVALID_ARG;
-  const int64_t row_elems = static_cast<int64_t>(num_kv_heads) * head_dim;
-  if (k_token_stride < row_elems || v_token_stride < row_elems) return KV_ERR_INVALID_ARG;
-  if (num_blocks > INT32_MAX / block_size) return KV_ERR_INVALID_ARG;
-  if (num_tokens == 0) return KV_OK;
-  if (!k || !v || !k_cache || !v_cache || !slot_mapping) return KV_ERR_INVALID_ARG;
-  const int64_t es = static_cast<int64_t>(dtype_bytes(dtype));
-  const int64_t row_bytes = row_elems * es, ks = k_token_stride * es, vs = v_token_stride * es;
-  const int64_t num_slots = num_blocks * block_size;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t err;
-  auto fits = [&](int64_t a) {
-    return row_bytes % a == 0 && ks % a == 0 && vs % a == 0 && aligned(k, a) && aligned(v, a) &&
-           aligned(k_cache, a) && aligned(v_cache, a);
-  };
-  if (fits(16))
-    err = launch<uint4>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, ks, vs, num_slots, st);
-  else if (fits(8))
-    err = launch<uint2>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, ks, vs, num_slots, st);
-  else if (fits(4))
-    err = launch<uint32_t>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, ks, vs, num_slots, st);
-  else if (fits(2))
-    err = launch<uint16_t>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, ks, vs, num_slots, st);
-  else
-    return KV_ERR_INVALID_ARG;
-  return cuda_status(err);
+  return cache_write(k, v, k_cache, v_cache, slot_mapping, num_tokens, 1, 0, 0, 0, num_kv_heads, head_dim, block_size,
+                     num_blocks, k_token_stride, v_token_stride, dtype, stream);
+}
+
+extern "C" int paged_reshape_and_cache_layers(const void* k, const void* v, void* k_cache, void* v_cache,
+                                              const int32_t* slot_mapping, int64_t num_tokens, int32_t num_layers,
+                                              int64_t k_layer_stride, int64_t v_layer_stride,
+                                              int64_t cache_layer_stride, int32_t num_kv_heads, int32_t head_dim,
+                                              int32_t block_size, int64_t num_blocks, int64_t k_token_stride,
+                                              int64_t v_token_stride, int dtype, void* stream) {
+  return cache_write(k, v, k_cache, v_cache, slot_mapping, num_tokens, num_layers, k_layer_stride, v_layer_stride,
+                     cache_layer_stride, num_kv_heads, head_dim, block_size, num_blocks, k_token_stride,
+                     v_token_stride, dtype, stream);
 }
 
 // Read (and optionally clear) this translation unit's device error word.

@@ -55,7 +55,8 @@ struct kvstep_s {
   int32_t* h_meta[kNumBufs] = {};
   int32_t* d_meta[kNumBufs] = {};
   pagedkv::Side side[kNumBufs];
-  size_t q_bytes = 0, kv_bytes = 0;
+  int32_t layers = 1;
+  size_t q_bytes = 0, kv_bytes = 0;  // one layer's
   cudaStream_t compute = nullptr, h2d = nullptr, d2h = nullptr;
   cudaEvent_t copied[kNumBufs] = {};    // H2D of buffer i done
   cudaEvent_t done[kNumBufs] = {};      // kernel that read buffer i done
@@ -102,11 +103,17 @@ extern "C" int kvstep_create(kvbm_t mgr, const kvstep_config_t* cfg, kvstep_t* o
       c.max_seq_len <= 0 || c.num_step_tokens < c.num_seqs || !c.k_cache || !c.v_cache)
     return KV_ERR_INVALID_ARG;
   if (c.dtype != KV_DTYPE_F32 && c.dtype != KV_DTYPE_F16 && c.dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
+  const int32_t layers = c.num_layers > 1 ? c.num_layers : 1;
+  if (c.num_layers < 0 || c.num_layers > 65535 ||
+      (layers > 1 && c.cache_layer_stride < c.num_blocks * c.block_size * static_cast<int64_t>(c.num_kv_heads) *
+                                                c.head_dim))
+    return KV_ERR_INVALID_ARG;
   kvstep_s* h = new (std::nothrow) kvstep_s();
   if (!h) return KV_ERR_INVALID_ARG;
   h->mgr = mgr;
   h->cfg = c;
   h->compute = static_cast<cudaStream_t>(c.stream);
+  h->layers = layers;
   // at most one copy-on-write copy per decode append (prefills never copy)
   h->meta_ints = c.num_step_tokens + static_cast<int64_t>(c.num_seqs) * c.max_blocks_per_seq + 4 * c.num_seqs;
   const size_t meta_bytes = static_cast<size_t>(h->meta_ints) * sizeof(int32_t);
@@ -121,10 +128,10 @@ extern "C" int kvstep_create(kvbm_t mgr, const kvstep_config_t* cfg, kvstep_t* o
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->done[i], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->out_back[i], cudaEventDisableTiming);
     if (e == cudaSuccess && c.host_io) {
-      e = cudaMalloc(&h->side[i].q, h->q_bytes);
-      if (e == cudaSuccess) e = cudaMalloc(&h->side[i].out, h->q_bytes);
-      if (e == cudaSuccess) e = cudaMalloc(&h->side[i].k, h->kv_bytes);
-      if (e == cudaSuccess) e = cudaMalloc(&h->side[i].v, h->kv_bytes);
+      e = cudaMalloc(&h->side[i].q, h->q_bytes * layers);
+      if (e == cudaSuccess) e = cudaMalloc(&h->side[i].out, h->q_bytes * layers);
+      if (e == cudaSuccess) e = cudaMalloc(&h->side[i].k, h->kv_bytes * layers);
+      if (e == cudaSuccess) e = cudaMalloc(&h->side[i].v, h->kv_bytes * layers);
     }
   }
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->h2d, cudaStreamNonBlocking);
@@ -201,9 +208,10 @@ extern "C" int kvstep_run(kvstep_t h, const void* q, const void* k, const void* 
     dk = h->side[i].k;
     dv = h->side[i].v;
     dout = h->side[i].out;
-    if (e == cudaSuccess) e = cudaMemcpyAsync(h->side[i].q, q, h->q_bytes, cudaMemcpyHostToDevice, h->h2d);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(h->side[i].k, k, h->kv_bytes, cudaMemcpyHostToDevice, h->h2d);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(h->side[i].v, v, h->kv_bytes, cudaMemcpyHostToDevice, h->h2d);
+    const size_t L = static_cast<size_t>(h->layers);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h->side[i].q, q, h->q_bytes * L, cudaMemcpyHostToDevice, h->h2d);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h->side[i].k, k, h->kv_bytes * L, cudaMemcpyHostToDevice, h->h2d);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h->side[i].v, v, h->kv_bytes * L, cudaMemcpyHostToDevice, h->h2d);
   }
   if (e == cudaSuccess) e = cudaEventRecord(h->copied[i], h->h2d);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(h->compute, h->copied[i], 0);
@@ -215,21 +223,31 @@ extern "C" int kvstep_run(kvstep_t h, const void* q, const void* k, const void* 
   int32_t* d_tables = d_slots + c.num_step_tokens;
   int32_t* d_lens = d_tables + B * maxb;
   int32_t* d_rows = d_lens + B;
-  if (n_copies > 0) {  // copy-on-write copies before the step's writes and reads
-    st = paged_copy_blocks(c.k_cache, c.v_cache, d_rows + B, d_rows + 2 * B, n_copies, 1, 0, c.num_kv_heads,
-                           c.head_dim, c.block_size, c.num_blocks, c.dtype, h->compute);
+  if (n_copies > 0) {  // copy-on-write copies (every layer) before the step's writes and reads
+    st = paged_copy_blocks(c.k_cache, c.v_cache, d_rows + B, d_rows + 2 * B, n_copies, h->layers,
+                           h->layers > 1 ? c.cache_layer_stride : 0, c.num_kv_heads, c.head_dim, c.block_size,
+                           c.num_blocks, c.dtype, h->compute);
     if (st != KV_OK) return st;
   }
   const int64_t row = static_cast<int64_t>(c.num_kv_heads) * c.head_dim;
-  st = paged_decode_step(dout, dq, dk, dv, d_slots, c.num_step_tokens, row, row, d_rows, c.k_cache, c.v_cache,
-                         d_tables, d_lens, c.num_seqs, c.num_heads, c.num_kv_heads, c.head_dim, c.block_size,
-                         c.num_blocks, c.max_blocks_per_seq, c.max_seq_len, c.scale, c.dtype, c.workspace,
-                         c.workspace_bytes, h->compute);
-  if (st != KV_OK) return st;
+  const int64_t es = static_cast<int64_t>(pagedkv::dtype_bytes(c.dtype));
+  for (int32_t l = 0; l < h->layers; ++l) {  // one fused launch per layer, same metadata
+    const size_t qo = h->q_bytes * static_cast<size_t>(l), ko = h->kv_bytes * static_cast<size_t>(l);
+    const int64_t co = static_cast<int64_t>(l) * c.cache_layer_stride * es;
+    st = paged_decode_step(static_cast<char*>(dout) + qo, static_cast<const char*>(dq) + qo,
+                           static_cast<const char*>(dk) + ko, static_cast<const char*>(dv) + ko, d_slots,
+                           c.num_step_tokens, row, row, d_rows, static_cast<char*>(c.k_cache) + co,
+                           static_cast<char*>(c.v_cache) + co, d_tables, d_lens, c.num_seqs, c.num_heads,
+                           c.num_kv_heads, c.head_dim, c.block_size, c.num_blocks, c.max_blocks_per_seq,
+                           c.max_seq_len, c.scale, c.dtype, c.workspace, c.workspace_bytes, h->compute);
+    if (st != KV_OK) return st;
+  }
   e = cudaEventRecord(h->done[i], h->compute);
   if (e == cudaSuccess && c.host_io) {
     e = cudaStreamWaitEvent(h->d2h, h->done[i], 0);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(out, h->side[i].out, h->q_bytes, cudaMemcpyDeviceToHost, h->d2h);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(out, h->side[i].out, h->q_bytes * static_cast<size_t>(h->layers), cudaMemcpyDeviceToHost,
+                          h->d2h);
     if (e == cudaSuccess) e = cudaEventRecord(h->out_back[i], h->d2h);
   }
   h->used[i] = true;

@@ -59,6 +59,32 @@ def reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v
           "paged_reshape_and_cache")
 
 
+def reshape_and_cache_layers(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                             slot_mapping: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Write k/v ``[L, N, Hkv, D]`` into L layers' caches ``[L, NB, BS, Hkv,
+    D]`` at ``slot_mapping[N]`` (int32, -1 = skip) in one launch: one block
+    table and slot mapping serve every layer."""
+    for t, n in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache"), (slot_mapping, "slot_mapping")):
+        _cuda(t, n)
+    if k_cache.dim() != 5 or not (k_cache.is_contiguous() and v_cache.is_contiguous()) \
+            or v_cache.shape != k_cache.shape:
+        raise KVError(1, "caches must be contiguous [L, NB, BS, Hkv, D] of one shape")
+    layers, nb, bs, hkv, d = k_cache.shape
+    n = slot_mapping.numel()
+    if slot_mapping.dtype != torch.int32 or not slot_mapping.is_contiguous():
+        raise KVError(1, "slot_mapping must be contiguous int32")
+    if k.dtype != k_cache.dtype or v.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
+        raise KVError(1, "k, v and the caches must share one dtype")
+    for t in (k, v):
+        if t.dim() != 4 or tuple(t.shape) != (layers, n, hkv, d) or t.stride(3) != 1 or t.stride(2) != d:
+            raise KVError(1, "k and v must be [L, N, Hkv, D] with dense heads")
+    check(lib().paged_reshape_and_cache_layers(k.data_ptr(), v.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                               slot_mapping.data_ptr(), n, layers, k.stride(0), v.stride(0),
+                                               k_cache.stride(0), hkv, d, bs, nb, k.stride(1), v.stride(1),
+                                               dtype_code(k_cache.dtype), _stream_ptr(stream)),
+          "paged_reshape_and_cache_layers")
+
+
 def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src: torch.Tensor, dst: torch.Tensor,
                 stream: Optional[torch.cuda.Stream] = None) -> None:
     """Copy-on-write copies: block ``dst[i]`` of every layer's K and V cache
