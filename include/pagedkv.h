@@ -267,6 +267,43 @@ int paged_reshape_and_cache_layers(const void* k, const void* v, void* k_cache, 
                                    int32_t block_size, int64_t num_blocks, int64_t k_token_stride,
                                    int64_t v_token_stride, int dtype, void* stream);
 
+/* fp8 KV cache ("paged-attention-impl-detail", 实践建议 4: the KV cache
+ * inside a block can be quantised on its own).  Codes are OCP FP8 E4M3
+ * bytes in caches [num_blocks, block_size, num_kv_heads, head_dim]; each
+ * (token, kv head) row has one float32 scale, stored in scale arrays
+ * [num_blocks, num_kv_heads, block_size] (a block's scales are its own).
+ * A row is quantised as: scale = amax / 448 (1 for an all-zero row), each
+ * value divided by the scale in float32 with one correct rounding, then
+ * rounded to E4M3, nearest-even, saturating at +-448.  Its dequantised value
+ * is code * scale.  The write replaces paged_reshape_and_cache (same slot
+ * rules: -1 skipped, out-of-pool slots skipped and recorded); k, v are
+ * fp16 or bf16 (dtype), head_dim 64, 128 or 256, token strides even, k/v
+ * 4-byte aligned, caches 8-byte aligned.  Bit-exact against the
+ * definition above. */
+int paged_reshape_and_cache_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
+                                float* k_scales, float* v_scales, const int32_t* slot_mapping,
+                                int64_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                int32_t block_size, int64_t num_blocks, int64_t k_token_stride,
+                                int64_t v_token_stride, int dtype, void* stream);
+
+/* paged_decode_attention over fp8 caches and their scales: K_j, V_j are the
+ * dequantised rows.  q and out are fp16 or bf16 (dtype); head_dim 128,
+ * block_size 16 or 32, at most 16 query heads per kv head and 4096
+ * sequences (else KV_ERR_INVALID_ARG).  The stream-K tensor-core kernel:
+ * TMA brings the E4M3 rows and the scales, E4M3 pairs convert exactly to
+ * the MMA type, each token's K scale multiplies its scores and its V scale
+ * its softmax weight.  workspace: paged_decode_workspace_size() bytes for
+ * the same sizes and dtype, blocks_per_split 0.  Other arguments, results
+ * and errors are those of paged_decode_attention; all pointers 16-byte
+ * aligned. */
+int paged_decode_attention_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const float* k_scales, const float* v_scales,
+                               const int32_t* block_tables, const int32_t* seq_lens, int32_t num_seqs,
+                               int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq,
+                               int64_t max_seq_len, float scale, int dtype, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
 /* Copy-on-write block copies (kvbm_take_copies): for each i < n, block
  * dst[i] of every layer's K and V cache becomes a copy of block src[i]
  * ("paged-attention-impl-detail", copy_on_write: the new block's k and v

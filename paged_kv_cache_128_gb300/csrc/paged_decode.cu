@@ -81,6 +81,9 @@ struct DecodeParams {
   const int32_t* new_row;
   int64_t num_new;
   int64_t new_k_stride, new_v_stride;  // bytes between consecutive tokens' rows
+  // fp8 caches: float32 scales [num_blocks][num_kv_heads][block_size]
+  const float* k_scales;
+  const float* v_scales;
 };
 
 // Sequence length after bounds checks: at most what the table row and the
@@ -335,6 +338,176 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NG>& st, uint8_t* kt, 
   }
 }
 
+// =========================================================================
+// fp8 (E4M3) cache tiles ("paged-attention-impl-detail", 实践建议 4: the KV
+// cache inside a block quantised on its own).  A tile holds TT tokens of
+// one kv head: TMA writes each 128-byte row (128 dims) with the 128-byte
+// swizzle, and the tokens' float32 scales (one per token for K, one for V)
+// sit in a small separate array.  The consumer builds the mma operands from
+// byte loads: E4M3 pairs convert exactly to f16 (cvt.rn.f16x2.e4m3x2), and
+// from there exactly to bf16.  A token's K scale multiplies its scores; its
+// V scale multiplies its softmax weights before the PV product (the softmax
+// sum uses the unscaled weights).
+// =========================================================================
+
+template <int D, int TT>
+struct Tile8 {
+  static constexpr int kSub = D / 128;          // 128-byte column slabs per row
+  static constexpr int kSlabBytes = TT * 128;
+  static constexpr int kTileBytes = TT * D;     // K or V codes of one tile
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static_assert(D % 128 == 0, "fp8 tiles need head_dim a multiple of 128");
+  static_assert(kSlabBytes % 1024 == 0, "slabs must keep 1024-byte swizzle alignment");
+};
+
+template <int TT>
+__device__ __forceinline__ uint32_t swz8(int t, int d) {
+  return static_cast<uint32_t>((d >> 7) * (TT * 128) + t * 128 + ((((d & 127) >> 4) ^ (t & 7)) << 4) + (d & 15));
+}
+
+// Two E4M3 codes (low byte first) -> the MMA type's x2 register, exactly.
+template <typename T>
+__device__ __forceinline__ uint32_t e4m3x2_to(uint32_t two) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<uint16_t>(two)));
+  if constexpr (std::is_same<T, __half>::value) {
+    return h;
+  } else {
+    __half2 hh = *reinterpret_cast<__half2*>(&h);
+    const float2 f = __half22float2(hh);
+    return Mma<__nv_bfloat16>::pack(f.x, f.y);
+  }
+}
+
+__device__ __forceinline__ uint32_t lds_u16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
+
+// One fp8 tile as one online-softmax step (as consume_subtiles, with the
+// operands converted from E4M3 and the per-token scales applied).
+template <typename T, int D, int TT, int NG, int NS>
+__device__ __forceinline__ void consume_subtiles_f8(WarpState<D, NG>& st, const uint8_t* kt, const uint8_t* vt,
+                                                    const float* ks, const float* vs, int tok0, int L, float sl2,
+                                                    int lane) {
+  using M = Mma<T>;
+  constexpr int KS = D / 16;
+  const int g = lane >> 2, t2 = (lane & 3) * 2;
+  float sc[NS][NG][4];
+#pragma unroll
+  for (int u = 0; u < NS; ++u)
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) sc[u][ng][0] = sc[u][ng][1] = sc[u][ng][2] = sc[u][ng][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < KS; ++kk) {
+    uint32_t a[NS][4];
+#pragma unroll
+    for (int u = 0; u < NS; ++u) {
+      const int r = u * 16 + g, c = kk * 16 + t2;
+      a[u][0] = e4m3x2_to<T>(lds_u16(kt + swz8<TT>(r, c)));
+      a[u][1] = e4m3x2_to<T>(lds_u16(kt + swz8<TT>(r + 8, c)));
+      a[u][2] = e4m3x2_to<T>(lds_u16(kt + swz8<TT>(r, c + 8)));
+      a[u][3] = e4m3x2_to<T>(lds_u16(kt + swz8<TT>(r + 8, c + 8)));
+    }
+#pragma unroll
+    for (int u = 0; u < NS; ++u)
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) M::run(sc[u][ng], a[u], st.qf[kk][ng][0], st.qf[kk][ng][1]);
+  }
+  // per-token scales of this lane's two rows per sub-tile; V's are 0 past the end
+  float kslo[NS], kshi[NS], vslo[NS], vshi[NS];
+#pragma unroll
+  for (int u = 0; u < NS; ++u) {
+    const int r = u * 16 + g;
+    kslo[u] = ks[r];
+    kshi[u] = ks[r + 8];
+    vslo[u] = tok0 + r < L ? vs[r] : 0.f;
+    vshi[u] = tok0 + r + 8 < L ? vs[r + 8] : 0.f;
+  }
+  uint32_t pb[NS][NG][2];
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng) {
+    float x[NS][4];
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < NS; ++u) {
+      const int t_lo = tok0 + u * 16 + g;
+      const bool in_lo = t_lo < L, in_hi = t_lo + 8 < L;
+      x[u][0] = in_lo ? sc[u][ng][0] * kslo[u] * sl2 : -INFINITY;
+      x[u][1] = in_lo ? sc[u][ng][1] * kslo[u] * sl2 : -INFINITY;
+      x[u][2] = in_hi ? sc[u][ng][2] * kshi[u] * sl2 : -INFINITY;
+      x[u][3] = in_hi ? sc[u][ng][3] * kshi[u] * sl2 : -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(x[u][0], x[u][2]));
+      mx1 = fmaxf(mx1, fmaxf(x[u][1], x[u][3]));
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(st.m[ng][0], mx0), mn1 = fmaxf(st.m[ng][1], mx1);
+    const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0, mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
+    const float al0 = fast_exp2(st.m[ng][0] - mu0), al1 = fast_exp2(st.m[ng][1] - mu1);
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int u = 0; u < NS; ++u) {
+      const float p0 = fast_exp2(x[u][0] - mu0), p1 = fast_exp2(x[u][1] - mu1);
+      const float p2 = fast_exp2(x[u][2] - mu0), p3 = fast_exp2(x[u][3] - mu1);
+      s0 += p0 + p2;
+      s1 += p1 + p3;
+      pb[u][ng][0] = movmatrix_trans(M::pack(p0 * vslo[u], p1 * vslo[u]));
+      pb[u][ng][1] = movmatrix_trans(M::pack(p2 * vshi[u], p3 * vshi[u]));
+    }
+    st.l[ng][0] = st.l[ng][0] * al0 + s0;
+    st.l[ng][1] = st.l[ng][1] * al1 + s1;
+    st.m[ng][0] = mn0;
+    st.m[ng][1] = mn1;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      st.acc[mt][ng][0] *= al0;
+      st.acc[mt][ng][1] *= al1;
+      st.acc[mt][ng][2] *= al0;
+      st.acc[mt][ng][3] *= al1;
+    }
+  }
+  // O^T[D x heads] += V^T[D x 16] P^T: V^T operand from byte pairs of two tokens
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) {
+    uint32_t a[NS][4];
+#pragma unroll
+    for (int u = 0; u < NS; ++u) {
+      const int tk = u * 16 + t2, dm = mt * 16 + g;
+      auto pair = [&](int tok, int dim) {
+        return static_cast<uint32_t>(vt[swz8<TT>(tok, dim)]) | (static_cast<uint32_t>(vt[swz8<TT>(tok + 1, dim)]) << 8);
+      };
+      a[u][0] = e4m3x2_to<T>(pair(tk, dm));
+      a[u][1] = e4m3x2_to<T>(pair(tk, dm + 8));
+      a[u][2] = e4m3x2_to<T>(pair(tk + 8, dm));
+      a[u][3] = e4m3x2_to<T>(pair(tk + 8, dm + 8));
+    }
+#pragma unroll
+    for (int u = 0; u < NS; ++u)
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) M::run(st.acc[mt][ng], a[u], pb[u][ng][0], pb[u][ng][1]);
+  }
+}
+
+template <typename T, int D, int TT, int NG>
+__device__ __forceinline__ void consume_tile_f8(WarpState<D, NG>& st, uint8_t* kt, uint8_t* vt, const float* ks,
+                                                const float* vs, int tok0, int L, float sl2, int lane) {
+  const int valid = min(TT, L - tok0);
+  if (valid < TT) {
+    // zero the V code rows past the sequence end: their weight is 0, but a
+    // stale code may be the NaN pattern and 0 * NaN is not 0
+    constexpr int kRowChunks = D / 16;
+    for (int c = lane; c < (TT - valid) * kRowChunks; c += 32) {
+      const int t = valid + c / kRowChunks, d = (c % kRowChunks) * 16;
+      *reinterpret_cast<uint4*>(vt + swz8<TT>(t, d)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();  // these bytes are TMA-written again later
+    __syncwarp();
+  }
+  if (valid > 16) consume_subtiles_f8<T, D, TT, NG, 2>(st, kt, vt, ks, vs, tok0, L, sl2, lane);
+  else consume_subtiles_f8<T, D, TT, NG, 1>(st, kt, vt, ks, vs, tok0, L, sl2, lane);
+}
+
 // Row stride of a head's accumulator in the warp-merge buffer: padded by 4
 // floats so that both the fragment stores below and float4 reads of
 // consecutive d are free of bank conflicts.
@@ -481,17 +654,19 @@ constexpr int kMaxSkCtas = 640;
 // wait and read every piece from global memory after the last tile).
 constexpr bool kPrefetchParts = true;
 
-template <typename T, int D, int BS, int NG, int NST>
+template <typename T, int D, int BS, int NG, int NST, bool F8 = false>
 struct SkCfg {
   // A stream-K tile is 32 tokens: one block of 32, or two consecutive
   // blocks of 16 of the same sequence (fewer, larger pipeline transactions).
   static constexpr int kBlocksPerTile = BS >= 32 ? 1 : 32 / BS;
   static constexpr int kTileTokens = BS * kBlocksPerTile;
-  using TL = Tile<D, kTileTokens>;
+  // fp8 caches: E4M3 code tiles, and per stage the tile's K and V scales
+  using TL = typename std::conditional<F8, Tile8<D, kTileTokens>, Tile<D, kTileTokens>>::type;
   static constexpr int kStages = NST * TL::kStageBytes;
+  static constexpr int kScales = F8 ? NST * 2 * kTileTokens * 4 : 0;
   static constexpr int kMerge = 2 * MergeArea<D, NG>::kBytes;  // double-buffered per segment
   static constexpr int kPartRows = kMaxSkCtas + 8;  // row index per part of a combined unit
-  static constexpr int kFixed = 1024 + kStages + kMerge + 2 * NST * 8 + 16 + kPartRows * 4;
+  static constexpr int kFixed = 1024 + kStages + kScales + kMerge + 2 * NST * 8 + 16 + kPartRows * 4;
   static int smem_bytes(int B) { return kFixed + (2 * (B + 1) * 4 + 15) / 16 * 16; }
 };
 
@@ -501,22 +676,27 @@ __device__ __forceinline__ int sk_cta_of(int64_t t, int64_t W, int P) {
 }
 
 
-template <typename T, int D, int BS, int NG, int NST>
+template <typename T, int D, int BS, int NG, int NST, bool F8 = false>
 __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)  // two CTAs per SM where shared memory allows
 decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV) {
-  using C = SkCfg<T, D, BS, NG, NST>;
+  using C = SkCfg<T, D, BS, NG, NST, F8>;
   using TL = typename C::TL;
   constexpr int TPB = C::kBlocksPerTile, TT = C::kTileTokens;
-  constexpr int kCopies = 2 * TL::kSub * TPB;  // TMA copies per tile (K and V slabs of each block)
+  // TMA copies per block of a tile: K and V slabs, and with fp8 the K and V scales
+  constexpr int kPerBlock = 2 * TL::kSub + (F8 ? 2 : 0);
+  constexpr int kCopies = kPerBlock * TPB;
   static_assert(kCopies <= 32, "one copy per producer lane");
+  // bytes one block of a tile brings into its stage
+  constexpr int kBlockTx = F8 ? 2 * BS * D + 2 * BS * 4 : TL::kStageBytes / TPB;
   constexpr int GP = 8 * NG;
   static_assert(NST % kConsumers == 0, "stage s must always be drained by consumer s % kConsumers");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* merge_base = reinterpret_cast<float*>(smem + C::kStages);
+  float* scales = reinterpret_cast<float*>(smem + C::kStages);  // fp8: [NST][2][TT] K, V scales
+  float* merge_base = reinterpret_cast<float*>(smem + C::kStages + C::kScales);
   constexpr int kMergeFloats = MergeArea<D, NG>::kBytes / 4;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages + C::kMerge);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages + C::kScales + C::kMerge);
   uint64_t* empty = full + NST;
   uint64_t* pre_bar = empty + NST;                       // owner: later pieces copied in
   int* part_row = reinterpret_cast<int*>(pre_bar + 2);  // [kPartRows]
@@ -607,7 +787,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   const int64_t t0 = tiles_before(static_cast<int64_t>(pid) * Wc / P);
   const int64_t t1 = tiles_before(static_cast<int64_t>(pid + 1) * Wc / P);
   if (t0 >= t1) {
-    if (p.new_k != nullptr && warp != 0)
+    if (!F8 && p.new_k != nullptr && warp != 0)
       scatter_new_rows<T>(p, static_cast<int64_t>(pid) * kConsumers + warp - 1, static_cast<int64_t>(P) * kConsumers,
                           lane);
     return;
@@ -664,9 +844,9 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   // Piece i goes to the stage virtual tile n + i / per_stage would use,
   // which frees up once tile n + i / per_stage - NST is consumed.
   const int part_o = G * D * 4, part_ml = (G * 8 + 15) & ~15, part_bytes = part_o + part_ml;
-  const int per_stage = TL::kStageBytes / part_bytes;  // >= 1 for every supported shape
+  const int per_stage = TL::kStageBytes / part_bytes;  // 0: pieces too large for a stage, none copied
   auto npre_of = [&](int last) {
-    return kPrefetchParts && Wc >= P ? min(min(NST * per_stage, 32), last - pid) : 0;
+    return kPrefetchParts && Wc >= P && per_stage > 0 ? min(min(NST * per_stage, 32), last - pid) : 0;
   };
   auto pre_part = [&](int i) {
     return smem + ((n + i / per_stage) % NST) * TL::kStageBytes + (i % per_stage) * part_bytes;
@@ -718,15 +898,19 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           next_b = -1;
         }
       }
-      // One copy per lane: lane l < kCopies loads block r = l / (2 * kSub) of
-      // the tile, column slab (l / 2) % kSub, K for even l and V for odd l.
-      const int cr = lane / (2 * TL::kSub), csl = (lane >> 1) % TL::kSub;
+      // One copy per lane: lane l < kCopies loads block r = l / kPerBlock of
+      // the tile; w = l % kPerBlock < 2 kSub is column slab w / 2 of K (even
+      // w) or V (odd w) (TMA tensor copies, 1024-byte aligned destinations);
+      // with fp8, w = 2 kSub and 2 kSub + 1 are the block's K and V scales,
+      // bs contiguous floats each (a bulk copy: 16-byte aligned source and
+      // destination, bs * 4 bytes).
+      const int cr = lane / kPerBlock, cw8 = lane % kPerBlock, csl = (cw8 >> 1) % TL::kSub;
       int pb = __shfl_sync(0xffffffffu, mine, (blk + min(cr, TPB - 1)) & 31);
       const int here = min(TPB, cache_nblk - blk);  // blocks of this tile inside the sequence (>= 1)
       const int s = j % NST;
       if (lane == 0) {
         if (j >= NST) ok = mbar_wait_bounded(&empty[s], ((j / NST) - 1) & 1);
-        if (ok) mbar_arrive_expect_tx(&full[s], here * (TL::kStageBytes / TPB));
+        if (ok) mbar_arrive_expect_tx(&full[s], here * kBlockTx);
       }
       __syncwarp();
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -735,8 +919,15 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           record_error(KV_ERR_DEVICE_BOUNDS);
           pb = 0;
         }
-        uint8_t* dst = smem + s * TL::kStageBytes + (lane & 1) * TL::kTileBytes + csl * TL::kSlabBytes + cr * BS * 128;
-        tma_load_3d(dst, (lane & 1) ? &tmV : &tmK, &full[s], csl * 64, c.kvh, pb * BS);
+        if (cw8 < 2 * TL::kSub) {
+          uint8_t* dst = smem + s * TL::kStageBytes + (cw8 & 1) * TL::kTileBytes + csl * TL::kSlabBytes + cr * BS * 128;
+          tma_load_3d(dst, (cw8 & 1) ? &tmV : &tmK, &full[s], csl * (F8 ? 128 : 64), c.kvh, pb * BS);
+        } else if constexpr (F8) {
+          const int which = cw8 - 2 * TL::kSub;  // 0: K scales, 1: V scales
+          float* dst = scales + (s * 2 + which) * TT + cr * BS;
+          const float* src = (which ? p.v_scales : p.k_scales) + (static_cast<int64_t>(pb) * Hkv + c.kvh) * BS;
+          bulk_load(dst, src, BS * 4, &full[s]);
+        }
       }
       if (ok) ++issued;
       if (j + 1 < n) advance(c);
@@ -825,7 +1016,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   // caches while the first tiles are in flight.  No tile of this launch
   // uses what they write: position L - 1 of a decode sequence (the only
   // written slot attention reads) is taken from the new row itself below.
-  const bool fused = p.new_k != nullptr;
+  const bool fused = !F8 && p.new_k != nullptr;
   if (fused) scatter_new_rows<T>(p, static_cast<int64_t>(pid) * kConsumers + cw, static_cast<int64_t>(P) * kConsumers,
                                  lane);
   // row of the step's new K/V holding sequence b's position L - 1 (-1: none)
@@ -848,7 +1039,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       // Fused step: the tile holding position L - 1 takes that token's K
       // and V for this kv head from the new row (loaded before the wait).
       const int tl = L - 1 - c.blk * TT;
-      const bool patch = nrow >= 0 && tl >= 0 && tl < TT;
+      const bool patch = !F8 && nrow >= 0 && tl >= 0 && tl < TT;
       uint4 pv[kPatch];
       if (patch) {
 #pragma unroll
@@ -888,7 +1079,11 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           fence_proxy_async_smem();  // the stage is TMA-written again later
           __syncwarp();
         }
-        consume_tile<T, D, TT, NG>(st, kt, kt + TL::kTileBytes, c.blk * TT, L, sl2, lane);
+        if constexpr (F8)
+          consume_tile_f8<T, D, TT, NG>(st, kt, kt + TL::kTileBytes, scales + s * 2 * TT, scales + (s * 2 + 1) * TT,
+                                        c.blk * TT, L, sl2, lane);
+        else
+          consume_tile<T, D, TT, NG>(st, kt, kt + TL::kTileBytes, c.blk * TT, L, sl2, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
       }
@@ -1522,23 +1717,27 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// Kinds of tensor map: 16-bit cache slabs and fp8 (E4M3) cache slabs.
+enum MapKind { kMap16 = 0, kMapFp8 = 1 };
+
 struct MapKey {
   const void* ptr;
   int64_t rows;
-  int hkv, d, bs;
+  int hkv, d, bs, kind;
   bool operator==(const MapKey& o) const {
-    return ptr == o.ptr && rows == o.rows && hkv == o.hkv && d == o.d && bs == o.bs;
+    return ptr == o.ptr && rows == o.rows && hkv == o.hkv && d == o.d && bs == o.bs && kind == o.kind;
   }
 };
 
-// Cache viewed as a 3-D tensor {D, Hkv, NB * BS} of 16-bit elements; a box
-// {64, 1, BS} is one 128-byte column slab of one block's rows for one head.
-bool get_tensor_map(const void* cache, int64_t rows, int hkv, int d, int bs, CUtensorMap* out) {
+// kMap16: the cache as a 3-D tensor {D, Hkv, NB * BS} of 16-bit elements; a
+// box {64, 1, BS} is one 128-byte column slab of one block's rows for one
+// head.  kMapFp8: the same of 1-byte codes, box {128, 1, BS}.
+bool get_tensor_map(const void* cache, int64_t rows, int hkv, int d, int bs, CUtensorMap* out, int kind = kMap16) {
   static std::mutex mu;
-  static MapKey keys[16];
-  static CUtensorMap maps[16];
+  static MapKey keys[32];
+  static CUtensorMap maps[32];
   static int used = 0, next = 0;
-  const MapKey key{cache, rows, hkv, d, bs};
+  const MapKey key{cache, rows, hkv, d, bs, kind};
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < used; ++i)
     if (keys[i] == key) {
@@ -1548,15 +1747,17 @@ bool get_tensor_map(const void* cache, int64_t rows, int hkv, int d, int bs, CUt
   auto fn = encode_fn();
   if (!fn) return false;
   CUtensorMap m;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(hkv) * d * 2};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(bs)};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(cache), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const int es = kind == kMapFp8 ? 1 : 2;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es, static_cast<cuuint64_t>(hkv) * d * es};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), 1, static_cast<cuuint32_t>(bs)};
+  const CUresult r = fn(&m, kind == kMapFp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
+                        const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
-  const int slot = used < 16 ? used++ : (next++ % 16);
+  const int slot = used < 32 ? used++ : (next++ % 32);
   keys[slot] = key;
   maps[slot] = m;
   *out = m;
@@ -1579,12 +1780,20 @@ cudaError_t allow_smem(K kern, int bytes, int* configured_bytes) {
   return e;
 }
 
-template <typename T, int D, int BS, int NG>
+// Pipeline depth of the fp8 kernel: about 64 KB of codes in flight per CTA.
+template <int D, int TT>
+struct Stages8 {
+  static constexpr int kRaw = ((64 * 1024) / Tile8<D, TT>::kStageBytes) / kConsumers * kConsumers;
+  static constexpr int value = kRaw < kConsumers ? kConsumers : (kRaw > 12 ? 12 : kRaw);
+};
+
+template <typename T, int D, int BS, int NG, bool F8 = false>
 cudaError_t launch_sk(DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, int max_ctas, cudaStream_t st) {
   constexpr int kTileTokens = BS >= 32 ? BS : 32;  // matches SkCfg::kTileTokens
-  constexpr int NST = Stages<D, kTileTokens>::value;
-  using C = SkCfg<T, D, BS, NG, NST>;
-  auto kern = decode_sk_kernel<T, D, BS, NG, NST>;
+  constexpr int NST =
+      std::conditional<F8, Stages8<D, kTileTokens>, Stages<D, kTileTokens>>::type::value;
+  using C = SkCfg<T, D, BS, NG, NST, F8>;
+  auto kern = decode_sk_kernel<T, D, BS, NG, NST, F8>;
   static int configured[64] = {0};
   cudaError_t e = allow_smem(kern, C::smem_bytes(p.num_seqs), configured);
   if (e != cudaSuccess) return e;
@@ -1603,7 +1812,7 @@ cudaError_t launch_sk(DecodeParams& p, const CUtensorMap& mk, const CUtensorMap&
   const int ctas = std::min({max_ctas, sm_count() * occ_cache[dev][1], kMaxSkCtas});
   p.num_ctas = ctas;
   p.epoch = next_epoch();
-  p.seg_cost = seg_cost_tiles(Tile<D, kTileTokens>::kStageBytes);
+  p.seg_cost = seg_cost_tiles(C::TL::kStageBytes);
   // Cooperative: the driver refuses the launch unless all CTAs can be
   // resident at once, which the owners' waits on later CTAs rely on.
   cudaLaunchConfig_t cfg{};
@@ -1878,6 +2087,83 @@ extern "C" int paged_decode_step(void* out, const void* q, const void* k, const 
   return decode_impl(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads, num_kv_heads, head_dim,
                      block_size, num_blocks, max_blocks_per_seq, max_seq_len, scale, 0, dtype, workspace,
                      workspace_bytes, stream, &step);
+}
+
+// ---------------------------------------------------------------------------
+// Decode attention over fp8 (E4M3) caches with per-token scales.
+
+namespace {
+template <typename T>
+cudaError_t launch_fp8_decode(DecodeParams& p, const Plan& pl, const CUtensorMap* maps, cudaStream_t st) {
+  const bool ng1 = p.group <= 8;
+  if (p.block_size == 16)
+    return ng1 ? launch_sk<T, 128, 16, 1, true>(p, maps[0], maps[1], pl.num_ctas, st)
+               : launch_sk<T, 128, 16, 2, true>(p, maps[0], maps[1], pl.num_ctas, st);
+  return ng1 ? launch_sk<T, 128, 32, 1, true>(p, maps[0], maps[1], pl.num_ctas, st)
+             : launch_sk<T, 128, 32, 2, true>(p, maps[0], maps[1], pl.num_ctas, st);
+}
+}  // namespace
+
+extern "C" int paged_decode_attention_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                          const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                                          const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads,
+                                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                          int64_t num_blocks, int32_t max_blocks_per_seq, int64_t max_seq_len,
+                                          float scale, int dtype, void* workspace, size_t workspace_bytes,
+                                          void* stream) {
+  int st = check_shapes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_seq_len, dtype);
+  if (st != KV_OK) return st;
+  if (dtype == KV_DTYPE_F32 || head_dim != 128 || (block_size != 16 && block_size != 32) ||
+      num_heads / num_kv_heads > 16 || num_seqs > kMaxSkSeqs)
+    return KV_ERR_INVALID_ARG;
+  if (num_blocks <= 0 || num_blocks > INT32_MAX / block_size || max_blocks_per_seq <= 0) return KV_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return KV_ERR_INVALID_ARG;
+  if (num_seqs == 0) return KV_OK;
+  if (!out || !q || !k_cache || !v_cache || !k_scales || !v_scales || !block_tables || !seq_lens)
+    return KV_ERR_INVALID_ARG;
+  const uintptr_t align_bits = reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(q) |
+                               reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+                               reinterpret_cast<uintptr_t>(k_scales) | reinterpret_cast<uintptr_t>(v_scales);
+  if (align_bits % 16 != 0) return KV_ERR_INVALID_ARG;
+  Plan pl = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_seq_len, 0, dtype);
+  if (pl.kind != kTensorCoreStreamK) return KV_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < pl.ws_bytes) return KV_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return KV_ERR_INVALID_ARG;
+  DecodeParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.num_seqs = num_seqs;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_heads / num_kv_heads;
+  p.head_dim = head_dim;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.scale_log2 = scale * kLog2e;
+  p.blocks_per_split = max_blocks_per_seq;
+  p.num_splits = 1;
+  char* ws = static_cast<char*>(workspace);
+  const size_t rows = static_cast<size_t>(pl.num_ctas) * 2 * p.group;
+  p.ws_o = reinterpret_cast<float*>(ws);
+  p.ws_ml = reinterpret_cast<float*>(ws + align256(rows * head_dim * sizeof(float)));
+  p.ws_flags = reinterpret_cast<uint64_t*>(ws + align256(rows * head_dim * sizeof(float)) +
+                                           align256(rows * 2 * sizeof(float)));
+  p.k_scales = k_scales;
+  p.v_scales = v_scales;
+  const int64_t slots = num_blocks * block_size;
+  CUtensorMap maps[2];
+  if (!get_tensor_map(k_cache, slots, num_kv_heads, head_dim, block_size, &maps[0], kMapFp8) ||
+      !get_tensor_map(v_cache, slots, num_kv_heads, head_dim, block_size, &maps[1], kMapFp8))
+    return cuda_status(cudaErrorInvalidValue, "cuTensorMapEncodeTiled failed");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = dtype == KV_DTYPE_F16 ? launch_fp8_decode<__half>(p, pl, maps, s)
+                                              : launch_fp8_decode<__nv_bfloat16>(p, pl, maps, s);
+  return cuda_status(e);
 }
 
 // ---------------------------------------------------------------------------

@@ -242,3 +242,126 @@ extern "C" int paged_copy_blocks(void* k_cache, void* v_cache, const int32_t* sr
                                                              src, dst, n, layer_stride * es, block_bytes, num_blocks);
   return cuda_status(cudaGetLastError());
 }
+
+// ---------------------------------------------------------------------------
+// fp8 (E4M3) cache write ("paged-attention-impl-detail", 实践建议 4: the KV
+// cache inside a block can be quantised on its own).  Each (token, kv head)
+// row of head_dim values gets one float32 scale, amax / 448 (1 for a zero
+// row), kept in the row's block: scales[(block * Hkv + head) * bs + offset].
+// The values are divided by it in float32 (correctly rounded) and rounded to
+// E4M3, nearest-even, saturating at 448.  One warp per token; a lane owns E
+// consecutive values of a row (E = head_dim / 32) and the amax is a warp
+// max-reduction.
+
+namespace pagedkv {
+namespace {
+
+__device__ __forceinline__ uint16_t e4m3x2_from(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <typename T, int E>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+cache_write_fp8_kernel(const T* __restrict__ k, const T* __restrict__ v, uint8_t* __restrict__ k_codes,
+                       uint8_t* __restrict__ v_codes, float* __restrict__ k_scales, float* __restrict__ v_scales,
+                       const int32_t* __restrict__ slot_mapping, int64_t num_tokens, int num_kv_heads,
+                       int block_size, int64_t k_stride, int64_t v_stride, int64_t num_slots) {
+  constexpr int D = 32 * E;
+  const int lane = threadIdx.x & 31;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5); t < num_tokens;
+       t += static_cast<int64_t>(gridDim.x) * kWarpsPerCta) {
+    const int32_t slot = __ldg(slot_mapping + t);
+    if (slot == -1) continue;
+    if (slot < 0 || slot >= num_slots) {
+      if (lane == 0) record_error(KV_ERR_DEVICE_BOUNDS);
+      continue;
+    }
+    const int64_t blk = slot / block_size, off = slot % block_size;
+    for (int h = 0; h < num_kv_heads; ++h) {
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const T* src = (which ? v + t * v_stride : k + t * k_stride) + h * D + lane * E;
+        float x[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) x[e] = DType<T>::to_float(src[e]);
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+        uint16_t packed[E / 2];
+#pragma unroll
+        for (int e = 0; e < E; e += 2) packed[e / 2] = e4m3x2_from(__fdiv_rn(x[e], scale), __fdiv_rn(x[e + 1], scale));
+        uint8_t* dst = (which ? v_codes : k_codes) + (static_cast<int64_t>(slot) * num_kv_heads + h) * D + lane * E;
+        if constexpr (E == 2) {
+          *reinterpret_cast<uint16_t*>(dst) = packed[0];
+        } else if constexpr (E == 4) {
+          *reinterpret_cast<uint32_t*>(dst) = packed[0] | (static_cast<uint32_t>(packed[1]) << 16);
+        } else {
+          *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0] | (static_cast<uint32_t>(packed[1]) << 16),
+                                                      packed[2] | (static_cast<uint32_t>(packed[3]) << 16));
+        }
+        if (lane == 0) (which ? v_scales : k_scales)[(blk * num_kv_heads + h) * block_size + off] = scale;
+      }
+    }
+  }
+}
+
+template <typename T, int E>
+cudaError_t launch_fp8(const void* k, const void* v, void* kc, void* vc, float* ks, float* vs, const int32_t* slots,
+                       int64_t n, int hkv, int bs, int64_t k_stride, int64_t v_stride, int64_t num_slots,
+                       cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t need = (n + kWarpsPerCta - 1) / kWarpsPerCta;
+  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * 16;
+  cache_write_fp8_kernel<T, E><<<static_cast<int>(need < cap ? need : cap), kWarpsPerCta * 32, 0, stream>>>(
+      static_cast<const T*>(k), static_cast<const T*>(v), static_cast<uint8_t*>(kc), static_cast<uint8_t*>(vc), ks, vs,
+      slots, n, hkv, bs, k_stride, v_stride, num_slots);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_fp8_d(int d, const void* k, const void* v, void* kc, void* vc, float* ks, float* vs,
+                         const int32_t* slots, int64_t n, int hkv, int bs, int64_t kst, int64_t vst, int64_t ns,
+                         cudaStream_t st) {
+  if (d == 64) return launch_fp8<T, 2>(k, v, kc, vc, ks, vs, slots, n, hkv, bs, kst, vst, ns, st);
+  if (d == 128) return launch_fp8<T, 4>(k, v, kc, vc, ks, vs, slots, n, hkv, bs, kst, vst, ns, st);
+  return launch_fp8<T, 8>(k, v, kc, vc, ks, vs, slots, n, hkv, bs, kst, vst, ns, st);
+}
+
+}  // namespace
+}  // namespace pagedkv
+
+extern "C" int paged_reshape_and_cache_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
+                                           float* k_scales, float* v_scales, const int32_t* slot_mapping,
+                                           int64_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                           int32_t block_size, int64_t num_blocks, int64_t k_token_stride,
+                                           int64_t v_token_stride, int dtype, void* stream) {
+  using namespace pagedkv;
+  if (dtype != KV_DTYPE_F16 && dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
+  if (num_tokens < 0 || num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0) return KV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KV_ERR_INVALID_ARG;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (k_token_stride < row || v_token_stride < row) return KV_ERR_INVALID_ARG;
+  if (num_blocks > INT32_MAX / block_size) return KV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return KV_OK;
+  if (!k || !v || !k_cache || !v_cache || !k_scales || !v_scales || !slot_mapping) return KV_ERR_INVALID_ARG;
+  if (!aligned(k, 4) || !aligned(v, 4) || (k_token_stride % 2) || (v_token_stride % 2) || !aligned(k_cache, 8) ||
+      !aligned(v_cache, 8) || !aligned(k_scales, 4) || !aligned(v_scales, 4))
+    return KV_ERR_INVALID_ARG;
+  const int64_t num_slots = num_blocks * block_size;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = dtype == KV_DTYPE_F16
+                      ? launch_fp8_d<__half>(head_dim, k, v, k_cache, v_cache, k_scales, v_scales, slot_mapping,
+                                             num_tokens, num_kv_heads, block_size, k_token_stride, v_token_stride,
+                                             num_slots, st)
+                      : launch_fp8_d<__nv_bfloat16>(head_dim, k, v, k_cache, v_cache, k_scales, v_scales,
+                                                    slot_mapping, num_tokens, num_kv_heads, block_size,
+                                                    k_token_stride, v_token_stride, num_slots, st);
+  return cuda_status(e);
+}

@@ -85,6 +85,63 @@ def reshape_and_cache_layers(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Te
           "paged_reshape_and_cache_layers")
 
 
+def reshape_and_cache_fp8(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          k_scales: torch.Tensor, v_scales: torch.Tensor, slot_mapping: torch.Tensor,
+                          stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Quantised cache write: k/v ``[N, Hkv, D]`` (fp16/bf16) to E4M3 codes
+    ``[NB, BS, Hkv, D]`` (uint8) with one float32 scale per (token, kv head)
+    in ``[NB, Hkv, BS]`` scale arrays, at ``slot_mapping[N]`` (-1 = skip)."""
+    for t, n in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache"), (k_scales, "k_scales"),
+                 (v_scales, "v_scales"), (slot_mapping, "slot_mapping")):
+        _cuda(t, n)
+    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8 or k_scales.dtype != torch.float32 \
+            or v_scales.dtype != torch.float32:
+        raise KVError(1, "fp8 caches are uint8 codes with float32 scales")
+    nb, bs, hkv, d = k_cache.shape
+    if v_cache.shape != k_cache.shape or tuple(k_scales.shape) != (nb, hkv, bs) or v_scales.shape != k_scales.shape:
+        raise KVError(1, "caches [NB, BS, Hkv, D], scales [NB, Hkv, BS]")
+    if not all(t.is_contiguous() for t in (k_cache, v_cache, k_scales, v_scales, slot_mapping)) \
+            or slot_mapping.dtype != torch.int32:
+        raise KVError(1, "caches, scales and slot_mapping must be contiguous (slot_mapping int32)")
+    n = slot_mapping.numel()
+    for t in (k, v):
+        if t.dim() != 3 or t.shape[0] != n or t.shape[1] != hkv or t.shape[2] != d or t.stride(2) != 1 \
+                or t.stride(1) != d:
+            raise KVError(1, "k and v must be [N, Hkv, D] with dense heads")
+    check(lib().paged_reshape_and_cache_fp8(k.data_ptr(), v.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                            k_scales.data_ptr(), v_scales.data_ptr(), slot_mapping.data_ptr(), n, hkv,
+                                            d, bs, nb, k.stride(0), v.stride(0), dtype_code(k.dtype),
+                                            _stream_ptr(stream)), "paged_reshape_and_cache_fp8")
+
+
+def paged_decode_attention_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               k_scales: torch.Tensor, v_scales: torch.Tensor, block_tables: torch.Tensor,
+                               seq_lens: torch.Tensor, scale: float, max_seq_len: int,
+                               workspace: Optional[torch.Tensor] = None,
+                               stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Decode attention over fp8 (E4M3) caches with per-token scales; q and
+    out fp16/bf16 ``[B, Hq, D]``."""
+    for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (k_scales, "k_scales"),
+                 (v_scales, "v_scales"), (block_tables, "block_tables"), (seq_lens, "seq_lens")):
+        _cuda(t, n)
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if d2 != d or out.shape != q.shape or out.dtype != q.dtype or k_cache.dtype != torch.uint8:
+        raise KVError(1, "shape or dtype mismatch")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32 or block_tables.dim() != 2 \
+            or block_tables.shape[0] != B or seq_lens.numel() != B:
+        raise KVError(1, "block_tables must be [B, max_blocks] and seq_lens [B], int32")
+    if workspace is None:
+        workspace = alloc_workspace(decode_plan(B, hq, hkv, d, bs, max_seq_len, q.dtype), q.device)
+    ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
+    check(lib().paged_decode_attention_fp8(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                           k_scales.data_ptr(), v_scales.data_ptr(), block_tables.data_ptr(),
+                                           seq_lens.data_ptr(), B, hq, hkv, d, bs, nb, block_tables.shape[1],
+                                           max_seq_len, float(scale), dtype_code(q.dtype), ws_ptr, ws_bytes,
+                                           _stream_ptr(stream)), "paged_decode_attention_fp8")
+    return out
+
+
 def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src: torch.Tensor, dst: torch.Tensor,
                 stream: Optional[torch.cuda.Stream] = None) -> None:
     """Copy-on-write copies: block ``dst[i]`` of every layer's K and V cache
