@@ -48,6 +48,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="native", choices=("native", "reference"))
+    ap.add_argument("--kv-cache", default="native", choices=("native", "fp8"),
+                    help="cache element type: the workload's dtype, or fp8 E4M3 codes with per-token scales "
+                         "(head_dim 128 workloads)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-calls", type=int, default=0,
@@ -260,7 +263,7 @@ def run_native(args):
 
     # Replicas: consecutive steps use different pools until more than 3x L2
     # has streamed, so no step finds its K/V in L2 and no flush is needed.
-    probe = PagedDecodeEngine(wl, dev, max_steps=1, fill_sentinel=False)
+    probe = PagedDecodeEngine(wl, dev, max_steps=1, fill_sentinel=False, kv_cache=args.kv_cache)
     attn_bytes0 = probe.algorithmic_bytes(wl.cached_lens + 1)["attention"]
     pool_bytes = 2 * probe.k_cache.numel() * probe.k_cache.element_size()
     del probe
@@ -270,7 +273,7 @@ def run_native(args):
     engines = []
     vals = None
     for r in range(replicas):
-        eng = PagedDecodeEngine(wl, dev, max_steps=per_replica, fill_sentinel=False)
+        eng = PagedDecodeEngine(wl, dev, max_steps=per_replica, fill_sentinel=False, kv_cache=args.kv_cache)
         vals = make_values(wl, device="cuda") if vals is None else vals
         eng.setup(vals)
         engines.append(eng)
@@ -355,7 +358,7 @@ def run_native(args):
     # (cache write + attention) with the stream-K kernel, over the lengths
     # in the metadata it was given
     roof_bytes = eng0.algorithmic_bytes(eng0._views(meta_h)[2].numpy())
-    attn_bytes = roof_bytes["step"] if eng0.fused else roof_bytes["attention"] + roof_bytes["cache_write"]
+    attn_bytes = roof_bytes["step"]
 
     # ---------------- end to end through host buffers ----------------
     # The runners copy each step's q/k/v from page-locked host memory and the
@@ -399,7 +402,7 @@ def run_native(args):
 
     peak, peak_kind = measured_peak()
     achieved = attn_bytes / attn_call_s / 1e9
-    traffic = recorded_traffic(args.workload)
+    traffic = recorded_traffic(args.workload if args.kv_cache == "native" else f"{args.workload}:fp8")
     plan = engines[0].plan
     result = {
         "metric": METRIC,
@@ -416,6 +419,7 @@ def run_native(args):
         "data": "synthetic (seeded; no dataset on the source pages)",
         "config": {
             "workload": wl.name,
+            "kv_cache": "fp8 E4M3 codes + float32 scale per (token, kv head)" if args.kv_cache == "fp8" else wl.dtype,
             "num_seqs": wl.num_seqs, "num_heads": wl.num_heads, "num_kv_heads": wl.num_kv_heads,
             "head_dim": wl.head_dim, "block_size": wl.block_size, "num_blocks": wl.num_blocks,
             "mean_seq_len": float(np.mean(wl.cached_lens)) + 1,
@@ -435,6 +439,7 @@ def run_native(args):
             "bound": "hbm",
             "kernel": ("paged_decode_step call: one cooperative stream-K launch doing the cache write and "
                        "decode attention" if eng0.fused and plan.kernel == 2 else
+                       "paged_reshape_and_cache_fp8 + paged_decode_attention_fp8 calls" if eng0.fp8 else
                        "paged_reshape_and_cache + paged_decode_attention calls"),
             "achieved": achieved,
             "peak": peak,
@@ -509,7 +514,7 @@ def run_profile_calls(args):
 
     dev = torch.device("cuda")
     wl = make_workload(args.workload)
-    eng = PagedDecodeEngine(wl, dev, max_steps=4, fill_sentinel=False)
+    eng = PagedDecodeEngine(wl, dev, max_steps=4, fill_sentinel=False, kv_cache=args.kv_cache)
     vals = make_values(wl, device="cuda")
     eng.setup(vals)
     eng.step(vals.q, vals.k_step, vals.v_step)

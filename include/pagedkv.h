@@ -494,6 +494,11 @@ typedef struct {
                                   1: page-locked host buffers, copied in and out by the runner */
   int32_t num_layers;          /* layers sharing the block tables (0 or 1: one) */
   int64_t cache_layer_stride;  /* elements between consecutive layers' caches (num_layers > 1) */
+  int32_t cache_fp8;           /* 1: k_cache/v_cache hold E4M3 codes with the scales below; each step
+                                  runs paged_reshape_and_cache_fp8 then paged_decode_attention_fp8
+                                  (two launches per layer; copy-on-write copies are not supported) */
+  float* k_scales;             /* fp8 only: [num_blocks, num_kv_heads, block_size] per layer, */
+  float* v_scales;             /*   layers back to back */
 } kvstep_config_t;
 
 int kvstep_create(kvbm_t mgr, const kvstep_config_t* cfg, kvstep_t* out);

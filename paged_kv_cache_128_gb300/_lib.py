@@ -39,7 +39,8 @@ class kvstep_config_t(ctypes.Structure):
                 ("max_seq_len", c_int64), ("scale", c_float), ("dtype", c_int32), ("num_step_tokens", c_int64),
                 ("k_cache", c_void_p), ("v_cache", c_void_p), ("workspace", c_void_p),
                 ("workspace_bytes", c_size_t), ("stream", c_void_p), ("host_io", c_int32),
-                ("num_layers", c_int32), ("cache_layer_stride", c_int64)]
+                ("num_layers", c_int32), ("cache_layer_stride", c_int64), ("cache_fp8", c_int32),
+                ("k_scales", c_void_p), ("v_scales", c_void_p)]
 
 
 P32 = POINTER(c_int32)

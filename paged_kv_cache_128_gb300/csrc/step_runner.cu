@@ -104,6 +104,7 @@ extern "C" int kvstep_create(kvbm_t mgr, const kvstep_config_t* cfg, kvstep_t* o
     return KV_ERR_INVALID_ARG;
   if (c.dtype != KV_DTYPE_F32 && c.dtype != KV_DTYPE_F16 && c.dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
   const int32_t layers = c.num_layers > 1 ? c.num_layers : 1;
+  if (c.cache_fp8 && (!c.k_scales || !c.v_scales || c.dtype == KV_DTYPE_F32)) return KV_ERR_INVALID_ARG;
   if (c.num_layers < 0 || c.num_layers > 65535 ||
       (layers > 1 && c.cache_layer_stride < c.num_blocks * c.block_size * static_cast<int64_t>(c.num_kv_heads) *
                                                 c.head_dim))
@@ -223,6 +224,7 @@ extern "C" int kvstep_run(kvstep_t h, const void* q, const void* k, const void* 
   int32_t* d_tables = d_slots + c.num_step_tokens;
   int32_t* d_lens = d_tables + B * maxb;
   int32_t* d_rows = d_lens + B;
+  if (n_copies > 0 && c.cache_fp8) return KV_ERR_INVALID_ARG;  // the fp8 runner has no block copy
   if (n_copies > 0) {  // copy-on-write copies (every layer) before the step's writes and reads
     st = paged_copy_blocks(c.k_cache, c.v_cache, d_rows + B, d_rows + 2 * B, n_copies, h->layers,
                            h->layers > 1 ? c.cache_layer_stride : 0, c.num_kv_heads, c.head_dim, c.block_size,
@@ -233,6 +235,22 @@ extern "C" int kvstep_run(kvstep_t h, const void* q, const void* k, const void* 
   const int64_t es = static_cast<int64_t>(pagedkv::dtype_bytes(c.dtype));
   for (int32_t l = 0; l < h->layers; ++l) {  // one fused launch per layer, same metadata
     const size_t qo = h->q_bytes * static_cast<size_t>(l), ko = h->kv_bytes * static_cast<size_t>(l);
+    if (c.cache_fp8) {  // codes: 1 byte per element; scales [NB, Hkv, BS] per layer
+      const int64_t co8 = static_cast<int64_t>(l) * c.cache_layer_stride;
+      const int64_t so = static_cast<int64_t>(l) * c.num_blocks * c.num_kv_heads * c.block_size;
+      char* kc = static_cast<char*>(c.k_cache) + co8;
+      char* vc = static_cast<char*>(c.v_cache) + co8;
+      st = paged_reshape_and_cache_fp8(static_cast<const char*>(dk) + ko, static_cast<const char*>(dv) + ko, kc, vc,
+                                       c.k_scales + so, c.v_scales + so, d_slots, c.num_step_tokens, c.num_kv_heads,
+                                       c.head_dim, c.block_size, c.num_blocks, row, row, c.dtype, h->compute);
+      if (st != KV_OK) return st;
+      st = paged_decode_attention_fp8(static_cast<char*>(dout) + qo, static_cast<const char*>(dq) + qo, kc, vc,
+                                      c.k_scales + so, c.v_scales + so, d_tables, d_lens, c.num_seqs, c.num_heads,
+                                      c.num_kv_heads, c.head_dim, c.block_size, c.num_blocks, c.max_blocks_per_seq,
+                                      c.max_seq_len, c.scale, c.dtype, c.workspace, c.workspace_bytes, h->compute);
+      if (st != KV_OK) return st;
+      continue;
+    }
     const int64_t co = static_cast<int64_t>(l) * c.cache_layer_stride * es;
     st = paged_decode_step(static_cast<char*>(dout) + qo, static_cast<const char*>(dq) + qo,
                            static_cast<const char*>(dk) + ko, static_cast<const char*>(dv) + ko, d_slots,

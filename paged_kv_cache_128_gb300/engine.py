@@ -29,8 +29,8 @@ import ctypes
 from ._lib import check, kvstep_config_t, lib
 from .block_manager import KVBlockManager
 from .inputs import Values, Workload, pad_positions, sentinel_bits
-from .kernels import (alloc_workspace, decode_plan, dtype_code, paged_decode_attention, paged_decode_step,
-                      reshape_and_cache)
+from .kernels import (alloc_workspace, decode_plan, dtype_code, paged_decode_attention, paged_decode_attention_fp8,
+                      paged_decode_step, reshape_and_cache, reshape_and_cache_fp8)
 
 _INT_VIEW = {torch.float32: torch.int32, torch.float16: torch.int16, torch.bfloat16: torch.int16}
 
@@ -41,19 +41,32 @@ def _signed(bits: int, width: int) -> int:
 
 class PagedDecodeEngine:
     def __init__(self, wl: Workload, device="cuda", max_steps: int = 64, fill_sentinel: bool = True,
-                 blocks_per_split: int = 0, fused: bool = True):
+                 blocks_per_split: int = 0, fused: bool = True, kv_cache: str = "native"):
         self.wl = wl
         self.blocks_per_split = blocks_per_split
+        # kv_cache "fp8": E4M3 codes with one float32 scale per (token, kv
+        # head); the step is the quantised cache write, then fp8 attention
+        if kv_cache not in ("native", "fp8"):
+            raise ValueError("kv_cache is 'native' or 'fp8'")
+        self.fp8 = kv_cache == "fp8"
         # fused: the step's cache write and attention in one paged_decode_step
         # call (one launch with the stream-K kernel); else two calls
-        self.fused = fused and blocks_per_split == 0
+        self.fused = fused and blocks_per_split == 0 and not self.fp8
         self.device = torch.device(device)
         self.mgr = KVBlockManager(wl.num_blocks, wl.block_size, wl.free_order)
         dt = wl.torch_dtype
         shape = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
-        self.k_cache = torch.empty(shape, dtype=dt, device=self.device)
-        self.v_cache = torch.empty(shape, dtype=dt, device=self.device)
-        if fill_sentinel:
+        self.k_scales = self.v_scales = None
+        if self.fp8:
+            self.k_cache = torch.full(shape, 0x7F, dtype=torch.uint8, device=self.device)   # 0x7F: the NaN code
+            self.v_cache = torch.full(shape, 0x7F, dtype=torch.uint8, device=self.device)
+            sshape = (wl.num_blocks, wl.num_kv_heads, wl.block_size)
+            self.k_scales = torch.full(sshape, float("nan"), dtype=torch.float32, device=self.device)
+            self.v_scales = torch.full(sshape, float("nan"), dtype=torch.float32, device=self.device)
+        else:
+            self.k_cache = torch.empty(shape, dtype=dt, device=self.device)
+            self.v_cache = torch.empty(shape, dtype=dt, device=self.device)
+        if fill_sentinel and not self.fp8:
             iv = _INT_VIEW[dt]
             width = 32 if iv == torch.int32 else 16
             fill = _signed(sentinel_bits(wl.dtype), width)
@@ -152,7 +165,11 @@ class PagedDecodeEngine:
             chunk = 1 << 20
             for a in range(0, n, chunk):
                 b = min(n, a + chunk)
-                reshape_and_cache(k[a:b], v[a:b], self.k_cache, self.v_cache, d_hist[a:b])
+                if self.fp8:
+                    reshape_and_cache_fp8(k[a:b], v[a:b], self.k_cache, self.v_cache, self.k_scales, self.v_scales,
+                                          d_hist[a:b])
+                else:
+                    reshape_and_cache(k[a:b], v[a:b], self.k_cache, self.v_cache, d_hist[a:b])
 
     # ------------------------------------------------------------------ step
     def host_metadata(self) -> None:
@@ -199,11 +216,18 @@ class PagedDecodeEngine:
 
     def write_step_kv(self, k_step: torch.Tensor, v_step: torch.Tensor) -> None:
         """a2: cache write of the step's new tokens."""
-        reshape_and_cache(k_step, v_step, self.k_cache, self.v_cache, self.d_slots)
+        if self.fp8:
+            reshape_and_cache_fp8(k_step, v_step, self.k_cache, self.v_cache, self.k_scales, self.v_scales,
+                                  self.d_slots)
+        else:
+            reshape_and_cache(k_step, v_step, self.k_cache, self.v_cache, self.d_slots)
 
     def attention(self, q: torch.Tensor) -> torch.Tensor:
         """a3-a8: decode attention for every running sequence."""
         wl = self.wl
+        if self.fp8:
+            return paged_decode_attention_fp8(self.out, q, self.k_cache, self.v_cache, self.k_scales, self.v_scales,
+                                              self.d_tables, self.d_lens, wl.scale, self.max_seq_len, self.workspace)
         return paged_decode_attention(self.out, q, self.k_cache, self.v_cache, self.d_tables, self.d_lens,
                                       wl.scale, self.max_seq_len, self.blocks_per_split, self.workspace)
 
@@ -284,10 +308,12 @@ class PagedDecodeEngine:
         cfg = kvstep_config_t(
             num_seqs=wl.num_seqs, num_heads=wl.num_heads, num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim,
             block_size=wl.block_size, num_blocks=wl.num_blocks, max_blocks_per_seq=self.max_blocks,
-            max_seq_len=self.max_seq_len, scale=float(wl.scale), dtype=dtype_code(self.k_cache.dtype),
+            max_seq_len=self.max_seq_len, scale=float(wl.scale), dtype=dtype_code(wl.torch_dtype),
             num_step_tokens=wl.num_step_tokens, k_cache=self.k_cache.data_ptr(), v_cache=self.v_cache.data_ptr(),
             workspace=ws.data_ptr() if ws is not None else None,
-            workspace_bytes=ws.numel() if ws is not None else 0, stream=s.cuda_stream, host_io=1 if host_io else 0)
+            workspace_bytes=ws.numel() if ws is not None else 0, stream=s.cuda_stream, host_io=1 if host_io else 0,
+            cache_fp8=1 if self.fp8 else 0, k_scales=self.k_scales.data_ptr() if self.fp8 else None,
+            v_scales=self.v_scales.data_ptr() if self.fp8 else None)
         self.close_runner()
         h = ctypes.c_void_p()
         check(lib().kvstep_create(self.mgr._h, ctypes.byref(cfg), ctypes.byref(h)), "kvstep_create")
@@ -344,6 +370,8 @@ class PagedDecodeEngine:
         kernel, else the cache write plus the attention call's launches."""
         if self.fused and self.plan.kernel == 2:
             return 1
+        if self.fp8:
+            return 2
         return 1 + self.plan.launches
 
     def algorithmic_bytes(self, seq_lens: np.ndarray) -> dict:
@@ -353,10 +381,12 @@ class PagedDecodeEngine:
         wl = self.wl
         s = 2 if wl.dtype != "f32" else 4
         row = wl.num_kv_heads * wl.head_dim * s
+        # a cached row: the dtype's bytes, or fp8 codes plus one float32 scale per head
+        crow = wl.num_kv_heads * (wl.head_dim + 4) if self.fp8 else row
         L = seq_lens.astype(np.int64)
         blocks = -(-L // wl.block_size)
-        attn = int(L.sum()) * 2 * row + 2 * wl.num_seqs * wl.num_heads * wl.head_dim * s + 4 * (
+        attn = int(L.sum()) * 2 * crow + 2 * wl.num_seqs * wl.num_heads * wl.head_dim * s + 4 * (
             wl.num_seqs + int(blocks.sum()))
         n_valid = self.n_prefill + wl.num_seqs
-        write = 2 * 2 * n_valid * row + 4 * wl.num_step_tokens
+        write = 2 * n_valid * (row + crow) + 4 * wl.num_step_tokens
         return {"attention": attn, "cache_write": write, "step": attn + write}

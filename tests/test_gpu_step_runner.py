@@ -90,3 +90,30 @@ def test_runner_rejects_bad_steps():
         check(lib().kvstep_create(eng.mgr._h, ctypes.byref(kvstep_config_t(num_seqs=0)), ctypes.byref(h)),
               "kvstep_create")
     eng.close_runner()
+
+
+@pytest.mark.parametrize("name", ["decode_gqa28x4_d128_bf16", "mixed_batch_bf16"])
+def test_runner_fp8_cache_matches_python_step(name):
+    """With fp8 caches the runner's step (quantised write, then fp8
+    attention) equals the Python-driven step bit for bit: outputs, codes and
+    scales."""
+    wl = make_workload(name)
+    dev = torch.device("cuda")
+    vals = make_values(wl, device="cuda")
+    ref = PagedDecodeEngine(wl, dev, max_steps=4, kv_cache="fp8")
+    run = PagedDecodeEngine(wl, dev, max_steps=4, kv_cache="fp8")
+    ref.setup(vals)
+    run.setup(vals)
+    run.make_runner()
+    out = torch.empty_like(vals.q)
+    for _ in range(3):
+        a = ref.step(vals.q, vals.k_step, vals.v_step).clone()
+        run.runner_step(vals.q, vals.k_step, vals.v_step, out)
+        run.runner_join()
+        torch.cuda.synchronize()
+        assert torch.equal(bits(a), bits(out))
+    assert torch.equal(ref.k_cache, run.k_cache) and torch.equal(ref.v_cache, run.v_cache)
+    assert torch.equal(ref.k_scales.view(torch.int32), run.k_scales.view(torch.int32))
+    assert torch.equal(ref.v_scales.view(torch.int32), run.v_scales.view(torch.int32))
+    assert pk.device_error() == 0
+    run.close_runner()
