@@ -338,6 +338,47 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NG>& st, uint8_t* kt, 
   }
 }
 
+// Row stride of a head's accumulator in the warp-merge buffer: padded by 4
+// floats so that both the fragment stores below and float4 reads of
+// consecutive d are free of bank conflicts.
+template <int D>
+__host__ __device__ constexpr int merge_row() { return D + 4; }
+
+// Reduce l across the lanes that share a head, then store this warp's
+// state: Os[cw][g][DP], Ms[cw][GP], Ls[cw][GP] (GP = 8 * NG, DP = D + 4).
+template <int D, int NG>
+__device__ __forceinline__ void store_state(WarpState<D, NG>& st, float* Os, float* Ms, float* Ls, int cw,
+                                            int lane) {
+  constexpr int GP = 8 * NG;
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) st.l[ng][c] += __shfl_xor_sync(0xffffffffu, st.l[ng][c], off);
+  constexpr int DP = merge_row<D>();
+  float* o = Os + cw * GP * DP;
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+      const int d0 = mt * 16 + (lane >> 2), g0 = ng * 8 + (lane & 3) * 2;
+      o[g0 * DP + d0] = st.acc[mt][ng][0];
+      o[(g0 + 1) * DP + d0] = st.acc[mt][ng][1];
+      o[g0 * DP + d0 + 8] = st.acc[mt][ng][2];
+      o[(g0 + 1) * DP + d0 + 8] = st.acc[mt][ng][3];
+    }
+  if (lane < 4) {
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        Ms[cw * GP + ng * 8 + lane * 2 + c] = st.m[ng][c];
+        Ls[cw * GP + ng * 8 + lane * 2 + c] = st.l[ng][c];
+      }
+  }
+}
+
 // =========================================================================
 // fp8 (E4M3) cache tiles ("paged-attention-impl-detail", 实践建议 4: the KV
 // cache inside a block quantised on its own).  A tile holds TT tokens of
@@ -365,61 +406,139 @@ __device__ __forceinline__ uint32_t swz8(int t, int d) {
   return static_cast<uint32_t>((d >> 7) * (TT * 128) + t * 128 + ((((d & 127) >> 4) ^ (t & 7)) << 4) + (d & 15));
 }
 
-// Two E4M3 codes (low byte first) -> the MMA type's x2 register, exactly.
-template <typename T>
-__device__ __forceinline__ uint32_t e4m3x2_to(uint32_t two) {
+// Two E4M3 codes (low byte first) -> f16x2, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_f16(uint32_t two) {
   uint32_t h;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<uint16_t>(two)));
-  if constexpr (std::is_same<T, __half>::value) {
-    return h;
-  } else {
-    __half2 hh = *reinterpret_cast<__half2*>(&h);
-    const float2 f = __half22float2(hh);
-    return Mma<__nv_bfloat16>::pack(f.x, f.y);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<uint16_t>(two & 0xffffu)));
+  return h;
+}
+
+// The fp8 path multiplies in f16 whatever the q/out type: E4M3 -> f16 is
+// exact, and so is bf16 -> f16 for |q| in f16's normal range.
+//
+// Operands come from the byte tiles through ldmatrix, which moves 16-bit
+// elements: to it a 128-byte row of 128 codes is 64 "elements" of two
+// codes.  For S^T = K Q^T, ldmatrix (no transpose) gives a lane 4
+// consecutive codes of one token, dims 4t..4t+3 of a 16-dim k-step; the
+// k-step takes them as its columns 2t, 2t+1 (dims 4t, 4t+1) and 2t+8,
+// 2t+9 (dims 4t+2, 4t+3), and the Q^T fragments are loaded in the same dim
+// order, so the contraction is unchanged.  For O^T += V^T P^T, ldmatrix
+// with transpose gives a lane codes (token 2t, dims 2g, 2g+1) and (token
+// 2t+1, dims 2g, 2g+1); one byte permute pairs them by dim, which makes
+// dim 2g row g and dim 2g+1 row g + 8 of the m-tile.  The accumulator's
+// rows are then permuted within each 16-dim group, and store_state_f8
+// writes them back to their dims.
+
+// Q^T fragments in the fp8 k-step dim order, converted to f16: b0 = Q[g][4t,
+// 4t+1], b1 = Q[g][4t+2, 4t+3] of each k-step, g = ng*8 + lane/4.
+template <typename T, int D, int NG>
+__device__ __forceinline__ void load_q_frags_f8(uint32_t (&qf)[D / 16][NG][2], const T* qb, int G, int lane) {
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng) {
+    const int g = ng * 8 + (lane >> 2);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int d = kk * 16 + (lane & 3) * 4;
+      if (g < G) {
+        const uint2 raw = __ldg(reinterpret_cast<const uint2*>(qb + g * D + d));
+        if constexpr (std::is_same<T, __half>::value) {
+          qf[kk][ng][0] = raw.x;
+          qf[kk][ng][1] = raw.y;
+        } else {
+          const float2 a = Mma<__nv_bfloat16>::unpack(raw.x), b = Mma<__nv_bfloat16>::unpack(raw.y);
+          qf[kk][ng][0] = Mma<__half>::pack(a.x, a.y);
+          qf[kk][ng][1] = Mma<__half>::pack(b.x, b.y);
+        }
+      } else {
+        qf[kk][ng][0] = 0u;
+        qf[kk][ng][1] = 0u;
+      }
+    }
   }
 }
 
-__device__ __forceinline__ uint32_t lds_u16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
+// store_state for the fp8 path: accumulator row g of m-tile mt is dim
+// mt*16 + 2g, row g + 8 is dim mt*16 + 2g + 1.
+template <int D, int NG>
+__device__ __forceinline__ void store_state_f8(WarpState<D, NG>& st, float* Os, float* Ms, float* Ls, int cw,
+                                               int lane) {
+  constexpr int GP = 8 * NG;
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) st.l[ng][c] += __shfl_xor_sync(0xffffffffu, st.l[ng][c], off);
+  constexpr int DP = merge_row<D>();
+  float* o = Os + cw * GP * DP;
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+      const int d0 = mt * 16 + (lane >> 2) * 2, g0 = ng * 8 + (lane & 3) * 2;
+      o[g0 * DP + d0] = st.acc[mt][ng][0];
+      o[(g0 + 1) * DP + d0] = st.acc[mt][ng][1];
+      o[g0 * DP + d0 + 1] = st.acc[mt][ng][2];
+      o[(g0 + 1) * DP + d0 + 1] = st.acc[mt][ng][3];
+    }
+  if (lane < 4) {
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        Ms[cw * GP + ng * 8 + lane * 2 + c] = st.m[ng][c];
+        Ls[cw * GP + ng * 8 + lane * 2 + c] = st.l[ng][c];
+      }
+  }
+}
 
 // One fp8 tile as one online-softmax step (as consume_subtiles, with the
-// operands converted from E4M3 and the per-token scales applied).
-template <typename T, int D, int TT, int NG, int NS>
-__device__ __forceinline__ void consume_subtiles_f8(WarpState<D, NG>& st, const uint8_t* kt, const uint8_t* vt,
+// operands taken from E4M3 codes and the per-token scales applied).
+template <int D, int TT, int NG, int NS>
+__device__ __forceinline__ void consume_subtiles_f8(WarpState<D, NG>& st, uint32_t kt_a, uint32_t vt_a,
                                                     const float* ks, const float* vs, int tok0, int L, float sl2,
                                                     int lane) {
-  using M = Mma<T>;
+  using M = Mma<__half>;
   constexpr int KS = D / 16;
-  const int g = lane >> 2, t2 = (lane & 3) * 2;
+  const int g = lane >> 2;
+  // ldmatrix x4 lane -> (token within the sub-tile, 16-byte column chunk offset)
+  const int lm_tok = (lane & 7) + ((lane >> 3) & 1) * 8, lm_chunk = lane >> 4;
   float sc[NS][NG][4];
 #pragma unroll
   for (int u = 0; u < NS; ++u)
 #pragma unroll
     for (int ng = 0; ng < NG; ++ng) sc[u][ng][0] = sc[u][ng][1] = sc[u][ng][2] = sc[u][ng][3] = 0.f;
 #pragma unroll
-  for (int kk = 0; kk < KS; ++kk) {
-    uint32_t a[NS][4];
-#pragma unroll
-    for (int u = 0; u < NS; ++u) {
-      const int r = u * 16 + g, c = kk * 16 + t2;
-      a[u][0] = e4m3x2_to<T>(lds_u16(kt + swz8<TT>(r, c)));
-      a[u][1] = e4m3x2_to<T>(lds_u16(kt + swz8<TT>(r + 8, c)));
-      a[u][2] = e4m3x2_to<T>(lds_u16(kt + swz8<TT>(r, c + 8)));
-      a[u][3] = e4m3x2_to<T>(lds_u16(kt + swz8<TT>(r + 8, c + 8)));
-    }
+  for (int kp = 0; kp < KS / 2; ++kp) {  // 32 dims: two k-steps per ldmatrix.x4
+    uint32_t r[NS][4];
 #pragma unroll
     for (int u = 0; u < NS; ++u)
+      ldmatrix_x4(kt_a + swz8<TT>(u * 16 + lm_tok, (2 * kp + lm_chunk) * 16), r[u][0], r[u][1], r[u][2], r[u][3]);
 #pragma unroll
-      for (int ng = 0; ng < NG; ++ng) M::run(sc[u][ng], a[u], st.qf[kk][ng][0], st.qf[kk][ng][1]);
+    for (int h = 0; h < 2; ++h) {  // k-step 2kp + h from registers 2h (tokens g) and 2h + 1 (tokens g + 8)
+      uint32_t a[NS][4];
+#pragma unroll
+      for (int u = 0; u < NS; ++u) {
+        a[u][0] = e4m3x2_f16(r[u][2 * h]);
+        a[u][1] = e4m3x2_f16(r[u][2 * h + 1]);
+        a[u][2] = e4m3x2_f16(r[u][2 * h] >> 16);
+        a[u][3] = e4m3x2_f16(r[u][2 * h + 1] >> 16);
+      }
+#pragma unroll
+      for (int u = 0; u < NS; ++u)
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng) M::run(sc[u][ng], a[u], st.qf[2 * kp + h][ng][0], st.qf[2 * kp + h][ng][1]);
+    }
   }
   // per-token scales of this lane's two rows per sub-tile; V's are 0 past the end
   float kslo[NS], kshi[NS], vslo[NS], vshi[NS];
 #pragma unroll
   for (int u = 0; u < NS; ++u) {
-    const int r = u * 16 + g;
-    kslo[u] = ks[r];
-    kshi[u] = ks[r + 8];
-    vslo[u] = tok0 + r < L ? vs[r] : 0.f;
-    vshi[u] = tok0 + r + 8 < L ? vs[r + 8] : 0.f;
+    const int rr = u * 16 + g;
+    kslo[u] = ks[rr];
+    kshi[u] = ks[rr + 8];
+    vslo[u] = tok0 + rr < L ? vs[rr] : 0.f;
+    vshi[u] = tok0 + rr + 8 < L ? vs[rr + 8] : 0.f;
   }
   uint32_t pb[NS][NG][2];
 #pragma unroll
@@ -467,29 +586,35 @@ __device__ __forceinline__ void consume_subtiles_f8(WarpState<D, NG>& st, const 
       st.acc[mt][ng][3] *= al1;
     }
   }
-  // O^T[D x heads] += V^T[D x 16] P^T: V^T operand from byte pairs of two tokens
+  // O^T += V^T P^T, two m-tiles (32 dims) per ldmatrix.x4.trans
 #pragma unroll
-  for (int mt = 0; mt < KS; ++mt) {
-    uint32_t a[NS][4];
-#pragma unroll
-    for (int u = 0; u < NS; ++u) {
-      const int tk = u * 16 + t2, dm = mt * 16 + g;
-      auto pair = [&](int tok, int dim) {
-        return static_cast<uint32_t>(vt[swz8<TT>(tok, dim)]) | (static_cast<uint32_t>(vt[swz8<TT>(tok + 1, dim)]) << 8);
-      };
-      a[u][0] = e4m3x2_to<T>(pair(tk, dm));
-      a[u][1] = e4m3x2_to<T>(pair(tk, dm + 8));
-      a[u][2] = e4m3x2_to<T>(pair(tk + 8, dm));
-      a[u][3] = e4m3x2_to<T>(pair(tk + 8, dm + 8));
-    }
+  for (int mp = 0; mp < KS / 2; ++mp) {
+    uint32_t r[NS][4];
 #pragma unroll
     for (int u = 0; u < NS; ++u)
+      ldmatrix_x4_trans(vt_a + swz8<TT>(u * 16 + lm_tok, (2 * mp + lm_chunk) * 16), r[u][0], r[u][1], r[u][2],
+                        r[u][3]);
 #pragma unroll
-      for (int ng = 0; ng < NG; ++ng) M::run(st.acc[mt][ng], a[u], pb[u][ng][0], pb[u][ng][1]);
+    for (int h = 0; h < 2; ++h) {  // m-tile 2mp + h: registers 2h (tokens 2t, 2t+1) and 2h + 1 (tokens + 8)
+      uint32_t a[NS][4];
+#pragma unroll
+      for (int u = 0; u < NS; ++u) {
+        // bytes (tok 2t: dim 2g, 2g+1; tok 2t+1: dim 2g, 2g+1) -> (dim 2g: both tokens | dim 2g+1: both)
+        const uint32_t lo = __byte_perm(r[u][2 * h], 0u, 0x3120), hi = __byte_perm(r[u][2 * h + 1], 0u, 0x3120);
+        a[u][0] = e4m3x2_f16(lo);        // row g = dim 2g, tokens 2t, 2t+1
+        a[u][1] = e4m3x2_f16(lo >> 16);  // row g + 8 = dim 2g + 1
+        a[u][2] = e4m3x2_f16(hi);        // dim 2g, tokens 2t + 8, 2t + 9
+        a[u][3] = e4m3x2_f16(hi >> 16);
+      }
+#pragma unroll
+      for (int u = 0; u < NS; ++u)
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng) M::run(st.acc[2 * mp + h][ng], a[u], pb[u][ng][0], pb[u][ng][1]);
+    }
   }
 }
 
-template <typename T, int D, int TT, int NG>
+template <int D, int TT, int NG>
 __device__ __forceinline__ void consume_tile_f8(WarpState<D, NG>& st, uint8_t* kt, uint8_t* vt, const float* ks,
                                                 const float* vs, int tok0, int L, float sl2, int lane) {
   const int valid = min(TT, L - tok0);
@@ -504,49 +629,9 @@ __device__ __forceinline__ void consume_tile_f8(WarpState<D, NG>& st, uint8_t* k
     fence_proxy_async_smem();  // these bytes are TMA-written again later
     __syncwarp();
   }
-  if (valid > 16) consume_subtiles_f8<T, D, TT, NG, 2>(st, kt, vt, ks, vs, tok0, L, sl2, lane);
-  else consume_subtiles_f8<T, D, TT, NG, 1>(st, kt, vt, ks, vs, tok0, L, sl2, lane);
-}
-
-// Row stride of a head's accumulator in the warp-merge buffer: padded by 4
-// floats so that both the fragment stores below and float4 reads of
-// consecutive d are free of bank conflicts.
-template <int D>
-__host__ __device__ constexpr int merge_row() { return D + 4; }
-
-// Reduce l across the lanes that share a head, then store this warp's
-// state: Os[cw][g][DP], Ms[cw][GP], Ls[cw][GP] (GP = 8 * NG, DP = D + 4).
-template <int D, int NG>
-__device__ __forceinline__ void store_state(WarpState<D, NG>& st, float* Os, float* Ms, float* Ls, int cw,
-                                            int lane) {
-  constexpr int GP = 8 * NG;
-#pragma unroll
-  for (int ng = 0; ng < NG; ++ng)
-#pragma unroll
-    for (int c = 0; c < 2; ++c)
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) st.l[ng][c] += __shfl_xor_sync(0xffffffffu, st.l[ng][c], off);
-  constexpr int DP = merge_row<D>();
-  float* o = Os + cw * GP * DP;
-#pragma unroll
-  for (int mt = 0; mt < D / 16; ++mt)
-#pragma unroll
-    for (int ng = 0; ng < NG; ++ng) {
-      const int d0 = mt * 16 + (lane >> 2), g0 = ng * 8 + (lane & 3) * 2;
-      o[g0 * DP + d0] = st.acc[mt][ng][0];
-      o[(g0 + 1) * DP + d0] = st.acc[mt][ng][1];
-      o[g0 * DP + d0 + 8] = st.acc[mt][ng][2];
-      o[(g0 + 1) * DP + d0 + 8] = st.acc[mt][ng][3];
-    }
-  if (lane < 4) {
-#pragma unroll
-    for (int ng = 0; ng < NG; ++ng)
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        Ms[cw * GP + ng * 8 + lane * 2 + c] = st.m[ng][c];
-        Ls[cw * GP + ng * 8 + lane * 2 + c] = st.l[ng][c];
-      }
-  }
+  const uint32_t kt_a = smem_u32(kt), vt_a = smem_u32(vt);
+  if (valid > 16) consume_subtiles_f8<D, TT, NG, 2>(st, kt_a, vt_a, ks, vs, tok0, L, sl2, lane);
+  else consume_subtiles_f8<D, TT, NG, 1>(st, kt_a, vt_a, ks, vs, tok0, L, sl2, lane);
 }
 
 constexpr int kConsumers = 4;
@@ -1007,10 +1092,12 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       Cursor nx = u;
       nx.blk = nx.nb - 1;
       advance(nx);
-      load_q_frags<T, D, NG>(qn, q_of(nx), G, lane);
+      if constexpr (F8) load_q_frags_f8<T, D, NG>(qn, q_of(nx), G, lane);
+      else load_q_frags<T, D, NG>(qn, q_of(nx), G, lane);
     }
   };
-  load_q<T, D, NG>(st, q_of(c), G, lane);
+  if constexpr (F8) load_q_frags_f8<T, D, NG>(st.qf, q_of(c), G, lane);
+  else load_q<T, D, NG>(st, q_of(c), G, lane);
   prefetch_next(c, unit_start);
   // Fused step: the consumer warps write the step's new rows into the
   // caches while the first tiles are in flight.  No tile of this launch
@@ -1080,8 +1167,8 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           __syncwarp();
         }
         if constexpr (F8)
-          consume_tile_f8<T, D, TT, NG>(st, kt, kt + TL::kTileBytes, scales + s * 2 * TT, scales + (s * 2 + 1) * TT,
-                                        c.blk * TT, L, sl2, lane);
+          consume_tile_f8<D, TT, NG>(st, kt, kt + TL::kTileBytes, scales + s * 2 * TT, scales + (s * 2 + 1) * TT,
+                                     c.blk * TT, L, sl2, lane);
         else
           consume_tile<T, D, TT, NG>(st, kt, kt + TL::kTileBytes, c.blk * TT, L, sl2, lane);
         __syncwarp();
@@ -1100,7 +1187,8 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       float* Ms = Os + kConsumers * merge_row<D>() * GP;
       float* Ls = Ms + kConsumers * GP;
       ++seg;
-      store_state(st, Os, Ms, Ls, cw, lane);
+      if constexpr (F8) store_state_f8(st, Os, Ms, Ls, cw, lane);
+      else store_state(st, Os, Ms, Ls, cw, lane);
       named_barrier_sync(1, kConsumers * 32);
       // the owner's own piece stays in the merge buffer for its combine
       const bool keep = kPrefetchParts && j == n - 1 && !whole && slot == 1;
@@ -1163,6 +1251,8 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
               st.qf[kk][ng][1] = qn[kk][ng][1];
             }
           prefetch_next(c, unit_start);
+        } else if constexpr (F8) {
+          load_q_frags_f8<T, D, NG>(st.qf, q_of(c), G, lane);
         } else {
           load_q<T, D, NG>(st, q_of(c), G, lane);
         }
