@@ -1842,9 +1842,14 @@ bool get_tensor_map(const void* cache, int64_t rows, int hkv, int d, int bs, CUt
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es, static_cast<cuuint64_t>(hkv) * d * es};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), 1, static_cast<cuuint32_t>(bs)};
+  // L2 fill promotion: 256 bytes for 16-bit caches (one (token, head) row
+  // at head_dim 128: the tile's two slabs), 128 bytes for fp8 (one row); a
+  // 256-byte fill of an fp8 row also fetches the next head's row, which
+  // another CTA reads much later (measured: 10-33 % more DRAM reads)
   const CUresult r = fn(&m, kind == kMapFp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
                         const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_SWIZZLE_128B,
+                        kind == kMapFp8 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   const int slot = used < 32 ? used++ : (next++ % 32);
