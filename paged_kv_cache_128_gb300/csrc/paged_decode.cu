@@ -630,7 +630,10 @@ __device__ __forceinline__ void consume_tile_f8(WarpState<D, NG>& st, uint8_t* k
     __syncwarp();
   }
   const uint32_t kt_a = smem_u32(kt), vt_a = smem_u32(vt);
-  if (valid > 16) consume_subtiles_f8<D, TT, NG, 2>(st, kt_a, vt_a, ks, vs, tok0, L, sl2, lane);
+  static_assert(TT == 32 || TT == 64, "fp8 tiles are 32 or 64 tokens");
+  if (TT == 64 && valid > 48) consume_subtiles_f8<D, TT, NG, TT / 16>(st, kt_a, vt_a, ks, vs, tok0, L, sl2, lane);
+  else if (TT == 64 && valid > 32) consume_subtiles_f8<D, TT, NG, 3>(st, kt_a, vt_a, ks, vs, tok0, L, sl2, lane);
+  else if (valid > 16) consume_subtiles_f8<D, TT, NG, 2>(st, kt_a, vt_a, ks, vs, tok0, L, sl2, lane);
   else consume_subtiles_f8<D, TT, NG, 1>(st, kt_a, vt_a, ks, vs, tok0, L, sl2, lane);
 }
 
@@ -743,7 +746,10 @@ template <typename T, int D, int BS, int NG, int NST, bool F8 = false>
 struct SkCfg {
   // A stream-K tile is 32 tokens: one block of 32, or two consecutive
   // blocks of 16 of the same sequence (fewer, larger pipeline transactions).
-  static constexpr int kBlocksPerTile = BS >= 32 ? 1 : 32 / BS;
+  // fp8 tiles are 64 tokens for up to 8 query heads per kv head, so a stage
+  // carries as many bytes as a 16-bit one (more heads: 32, to fit registers).
+  static constexpr int kWantTokens = F8 && NG == 1 ? 64 : 32;
+  static constexpr int kBlocksPerTile = BS >= kWantTokens ? 1 : kWantTokens / BS;
   static constexpr int kTileTokens = BS * kBlocksPerTile;
   // fp8 caches: E4M3 code tiles, and per stage the tile's K and V scales
   using TL = typename std::conditional<F8, Tile8<D, kTileTokens>, Tile<D, kTileTokens>>::type;
@@ -1884,7 +1890,8 @@ struct Stages8 {
 
 template <typename T, int D, int BS, int NG, bool F8 = false>
 cudaError_t launch_sk(DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, int max_ctas, cudaStream_t st) {
-  constexpr int kTileTokens = BS >= 32 ? BS : 32;  // matches SkCfg::kTileTokens
+  constexpr int kWant = F8 && NG == 1 ? 64 : 32;
+  constexpr int kTileTokens = BS >= kWant ? BS : kWant;  // matches SkCfg::kTileTokens
   constexpr int NST =
       std::conditional<F8, Stages8<D, kTileTokens>, Stages<D, kTileTokens>>::type::value;
   using C = SkCfg<T, D, BS, NG, NST, F8>;
