@@ -304,6 +304,27 @@ int paged_decode_attention_fp8(void* out, const void* q, const void* k_cache, co
                                int64_t max_seq_len, float scale, int dtype, void* workspace,
                                size_t workspace_bytes, void* stream);
 
+/* paged_decode_step for fp8 caches: the step's quantised cache write
+ * (exactly as paged_reshape_and_cache_fp8) and decode attention over the
+ * fp8 caches (exactly as paged_decode_attention_fp8) in one call, under the
+ * requirement and with the checks of paged_decode_step (new_token_row,
+ * KV_ERR_DEVICE_STEP).  One launch when the rows of k and v are 8-byte
+ * aligned: the consumer warps quantise and scatter the rows, and the tile
+ * holding position seq_lens[b] - 1 quantises that token itself with the same
+ * float32 steps, so codes, scales and outputs are bit-identical to the two
+ * calls in sequence.  Otherwise (rows not 8-byte aligned, or more than two
+ * rows per consumer warp of the grid, as with a prefill chunk, where the
+ * in-launch quantisation would hold up the first tiles) the two calls in
+ * stream order. */
+int paged_decode_step_fp8(void* out, const void* q, const void* k, const void* v,
+                          const int32_t* slot_mapping, int64_t num_tokens, int64_t k_token_stride,
+                          int64_t v_token_stride, const int32_t* new_token_row, void* k_cache,
+                          void* v_cache, float* k_scales, float* v_scales, const int32_t* block_tables,
+                          const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                          int32_t max_blocks_per_seq, int64_t max_seq_len, float scale, int dtype,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
 /* Copy-on-write block copies (kvbm_take_copies): for each i < n, block
  * dst[i] of every layer's K and V cache becomes a copy of block src[i]
  * ("paged-attention-impl-detail", copy_on_write: the new block's k and v
@@ -495,8 +516,8 @@ typedef struct {
   int32_t num_layers;          /* layers sharing the block tables (0 or 1: one) */
   int64_t cache_layer_stride;  /* elements between consecutive layers' caches (num_layers > 1) */
   int32_t cache_fp8;           /* 1: k_cache/v_cache hold E4M3 codes with the scales below; each step
-                                  runs paged_reshape_and_cache_fp8 then paged_decode_attention_fp8
-                                  (two launches per layer; copy-on-write copies are not supported) */
+                                  runs paged_decode_step_fp8 per layer (copy-on-write copies are
+                                  not supported) */
   float* k_scales;             /* fp8 only: [num_blocks, num_kv_heads, block_size] per layer, */
   float* v_scales;             /*   layers back to back */
 } kvstep_config_t;

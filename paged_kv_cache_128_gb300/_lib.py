@@ -84,6 +84,10 @@ SIGNATURES = {
     "paged_decode_attention_fp8": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                            c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32, c_int64, c_int32,
                                            c_int64, c_float, c_int, c_void_p, c_size_t, c_void_p]),
+    "paged_decode_step_fp8": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64,
+                                      c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
+                                      c_int32, c_int32, c_int32, c_int32, c_int64, c_int32, c_int64, c_float, c_int,
+                                      c_void_p, c_size_t, c_void_p]),
     "paged_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int32, c_int64, c_int32,
                                   c_int32, c_int32, c_int64, c_int, c_void_p]),
     "paged_decode_plan": (c_int, [c_int32, c_int32, c_int32, c_int32, c_int32, c_int64, c_int32, c_int,

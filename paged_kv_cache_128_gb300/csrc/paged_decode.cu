@@ -735,6 +735,65 @@ __device__ __forceinline__ void scatter_new_rows(const DecodeParams& p, int64_t 
   }
 }
 
+// fp8 (E4M3) quantisation of one (token, kv head) row of 128 values held 4
+// per lane across a warp: scale = amax / 448 (1 for a zero row), values
+// divided by it with one correct rounding and rounded to E4M3 nearest-even,
+// saturating -- the steps of paged_reshape_and_cache_fp8, so the codes and
+// scale are bit-identical.  Returns the lane's 4 codes (lowest dim first).
+template <typename T>
+__device__ __forceinline__ uint32_t quantize4_e4m3(uint2 raw, float& scale) {
+  const T* v = reinterpret_cast<const T*>(&raw);
+  float x[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) x[e] = DType<T>::to_float(v[e]);
+  float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(__fdiv_rn(x[1], scale)), "f"(__fdiv_rn(x[0], scale)));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(__fdiv_rn(x[3], scale)), "f"(__fdiv_rn(x[2], scale)));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// Fused fp8 step, cache write: as scatter_new_rows, each (token, kv head)
+// row quantised into the E4M3 caches and its scale into the scale arrays
+// (head_dim 128).
+template <typename T>
+__device__ __forceinline__ void scatter_new_rows_f8(const DecodeParams& p, int64_t gw, int64_t nw, int lane) {
+  const int64_t num_slots = p.num_blocks * p.block_size;
+  const int Hkv = p.num_kv_heads, BS = p.block_size;
+  for (int64_t base = gw; base < p.num_new; base += 32 * nw) {
+    const int64_t mine = base + lane * nw;
+    const int32_t my_slot = mine < p.num_new ? __ldg(p.slot_mapping + mine) : -1;
+    for (int i = 0; i < 32; ++i) {
+      const int64_t t = base + i * nw;
+      if (t >= p.num_new) break;
+      const int32_t slot = __shfl_sync(0xffffffffu, my_slot, i);
+      if (slot == -1) continue;
+      if (slot < 0 || slot >= num_slots) {
+        if (lane == 0) record_error(KV_ERR_DEVICE_BOUNDS);
+        continue;
+      }
+      const int64_t blk = slot / BS, off = slot % BS;
+      for (int h = 0; h < Hkv; ++h) {
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const char* src = static_cast<const char*>(which ? p.new_v : p.new_k) +
+                            t * (which ? p.new_v_stride : p.new_k_stride) +
+                            (static_cast<int64_t>(h) * 128 + lane * 4) * static_cast<int64_t>(sizeof(T));
+          float scale;
+          const uint32_t codes = quantize4_e4m3<T>(__ldg(reinterpret_cast<const uint2*>(src)), scale);
+          uint8_t* dst = static_cast<uint8_t*>(const_cast<void*>(which ? p.v_cache : p.k_cache)) +
+                         (static_cast<int64_t>(slot) * Hkv + h) * 128 + lane * 4;
+          *reinterpret_cast<uint32_t*>(dst) = codes;
+          if (lane == 0) const_cast<float*>(which ? p.v_scales : p.k_scales)[(blk * Hkv + h) * BS + off] = scale;
+        }
+      }
+    }
+  }
+}
+
 // Grid cap: an owner CTA indexes up to kMaxSkCtas pieces in shared memory.
 constexpr int kMaxSkCtas = 640;
 // An owner's producer warp waits for the later pieces and copies them into
@@ -878,9 +937,11 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   const int64_t t0 = tiles_before(static_cast<int64_t>(pid) * Wc / P);
   const int64_t t1 = tiles_before(static_cast<int64_t>(pid + 1) * Wc / P);
   if (t0 >= t1) {
-    if (!F8 && p.new_k != nullptr && warp != 0)
-      scatter_new_rows<T>(p, static_cast<int64_t>(pid) * kConsumers + warp - 1, static_cast<int64_t>(P) * kConsumers,
-                          lane);
+    if (p.new_k != nullptr && warp != 0) {
+      const int64_t gw = static_cast<int64_t>(pid) * kConsumers + warp - 1, nw = static_cast<int64_t>(P) * kConsumers;
+      if constexpr (F8) scatter_new_rows_f8<T>(p, gw, nw, lane);
+      else scatter_new_rows<T>(p, gw, nw, lane);
+    }
     return;
   }
   const int n = static_cast<int>(t1 - t0);
@@ -1109,9 +1170,12 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   // caches while the first tiles are in flight.  No tile of this launch
   // uses what they write: position L - 1 of a decode sequence (the only
   // written slot attention reads) is taken from the new row itself below.
-  const bool fused = !F8 && p.new_k != nullptr;
-  if (fused) scatter_new_rows<T>(p, static_cast<int64_t>(pid) * kConsumers + cw, static_cast<int64_t>(P) * kConsumers,
-                                 lane);
+  const bool fused = p.new_k != nullptr;
+  if (fused) {
+    const int64_t gw = static_cast<int64_t>(pid) * kConsumers + cw, nw = static_cast<int64_t>(P) * kConsumers;
+    if constexpr (F8) scatter_new_rows_f8<T>(p, gw, nw, lane);
+    else scatter_new_rows<T>(p, gw, nw, lane);
+  }
   // row of the step's new K/V holding sequence b's position L - 1 (-1: none)
   auto new_row_of = [&](int b) -> int {
     if (!fused) return -1;
@@ -1133,6 +1197,20 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       // and V for this kv head from the new row (loaded before the wait).
       const int tl = L - 1 - c.blk * TT;
       const bool patch = !F8 && nrow >= 0 && tl >= 0 && tl < TT;
+      // fp8: the token's K and V for this kv head, 4 values per lane, are
+      // quantised after the wait exactly as the cache write does
+      const bool patch8 = F8 && nrow >= 0 && tl >= 0 && tl < TT;
+      uint2 pk8 = make_uint2(0u, 0u), pv8 = make_uint2(0u, 0u);
+      if (patch8) {
+        const int64_t col = (static_cast<int64_t>(c.kvh) * D + lane * 4) * static_cast<int64_t>(sizeof(T));
+        pk8 = __ldg(reinterpret_cast<const uint2*>(static_cast<const char*>(p.new_k) + nrow * p.new_k_stride + col));
+        pv8 = __ldg(reinterpret_cast<const uint2*>(static_cast<const char*>(p.new_v) + nrow * p.new_v_stride + col));
+        if (lane == 0) {  // the row must be the one the cache write puts at position L - 1
+          const int pb = __ldg(p.block_tables + static_cast<int64_t>(c.b) * p.max_blocks_per_seq + (L - 1) / BS);
+          const int32_t want = pb * BS + (L - 1) % BS;
+          if (__ldg(p.slot_mapping + nrow) != want) record_error(KV_ERR_DEVICE_STEP);
+        }
+      }
       uint4 pv[kPatch];
       if (patch) {
 #pragma unroll
@@ -1171,6 +1249,20 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           }
           fence_proxy_async_smem();  // the stage is TMA-written again later
           __syncwarp();
+        }
+        if constexpr (F8) {
+          if (patch8) {
+            float sk, sv;
+            const uint32_t ck = quantize4_e4m3<T>(pk8, sk), cv = quantize4_e4m3<T>(pv8, sv);
+            *reinterpret_cast<uint32_t*>(kt + swz8<TT>(tl, lane * 4)) = ck;
+            *reinterpret_cast<uint32_t*>(kt + TL::kTileBytes + swz8<TT>(tl, lane * 4)) = cv;
+            if (lane == 0) {
+              scales[s * 2 * TT + tl] = sk;
+              scales[(s * 2 + 1) * TT + tl] = sv;
+            }
+            fence_proxy_async_smem();  // the stage and its scales are written by the async proxy again later
+            __syncwarp();
+          }
         }
         if constexpr (F8)
           consume_tile_f8<D, TT, NG>(st, kt, kt + TL::kTileBytes, scales + s * 2 * TT, scales + (s * 2 + 1) * TT,
@@ -2206,13 +2298,18 @@ cudaError_t launch_fp8_decode(DecodeParams& p, const Plan& pl, const CUtensorMap
 }
 }  // namespace
 
-extern "C" int paged_decode_attention_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
-                                          const float* k_scales, const float* v_scales, const int32_t* block_tables,
-                                          const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads,
-                                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                                          int64_t num_blocks, int32_t max_blocks_per_seq, int64_t max_seq_len,
-                                          float scale, int dtype, void* workspace, size_t workspace_bytes,
-                                          void* stream) {
+extern "C" int paged_reshape_and_cache_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
+                                           float* k_scales, float* v_scales, const int32_t* slot_mapping,
+                                           int64_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                           int32_t block_size, int64_t num_blocks, int64_t k_token_stride,
+                                           int64_t v_token_stride, int dtype, void* stream);
+
+namespace {
+int decode_fp8_impl(void* out, const void* q, const void* k_cache, const void* v_cache, const float* k_scales,
+                    const float* v_scales, const int32_t* block_tables, const int32_t* seq_lens, int32_t num_seqs,
+                    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                    int64_t num_blocks, int32_t max_blocks_per_seq, int64_t max_seq_len, float scale, int dtype,
+                    void* workspace, size_t workspace_bytes, void* stream, const StepArgs* step) {
   int st = check_shapes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_seq_len, dtype);
   if (st != KV_OK) return st;
   if (dtype == KV_DTYPE_F32 || head_dim != 128 || (block_size != 16 && block_size != 32) ||
@@ -2257,15 +2354,81 @@ extern "C" int paged_decode_attention_fp8(void* out, const void* q, const void* 
                                            align256(rows * 2 * sizeof(float)));
   p.k_scales = k_scales;
   p.v_scales = v_scales;
+  bool write_first = false;
+  if (step != nullptr && step->num_tokens > 0) {
+    const uintptr_t row_align = reinterpret_cast<uintptr_t>(step->k) | reinterpret_cast<uintptr_t>(step->v) |
+                                static_cast<uintptr_t>(step->k_stride * 2) | static_cast<uintptr_t>(step->v_stride * 2);
+    // One launch when the rows are 8-byte aligned and few: the consumer
+    // warps quantise the rows before their first tile, so a step with many
+    // rows (a prefill chunk: more than two per consumer warp of the grid)
+    // runs the write as its own launch, on SMs the attention does not hold up.
+    const int64_t consumer_warps = static_cast<int64_t>(sm_count()) * 2 * kConsumers;  // two CTAs per SM
+    const bool few_rows = step->num_tokens <= 2 * consumer_warps;
+    if (row_align % 8 == 0 && few_rows) {  // one launch: the kernel also quantises and writes the new rows
+      p.new_k = step->k;
+      p.new_v = step->v;
+      p.slot_mapping = step->slot_mapping;
+      p.new_row = step->new_token_row;
+      p.num_new = step->num_tokens;
+      p.new_k_stride = step->k_stride * 2;
+      p.new_v_stride = step->v_stride * 2;
+    } else {
+      write_first = true;
+    }
+  }
   const int64_t slots = num_blocks * block_size;
   CUtensorMap maps[2];
   if (!get_tensor_map(k_cache, slots, num_kv_heads, head_dim, block_size, &maps[0], kMapFp8) ||
       !get_tensor_map(v_cache, slots, num_kv_heads, head_dim, block_size, &maps[1], kMapFp8))
     return cuda_status(cudaErrorInvalidValue, "cuTensorMapEncodeTiled failed");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (write_first) {  // rows not 8-byte aligned: the cache write, then attention, in stream order
+    st = paged_reshape_and_cache_fp8(step->k, step->v, const_cast<void*>(k_cache), const_cast<void*>(v_cache),
+                                     const_cast<float*>(k_scales), const_cast<float*>(v_scales), step->slot_mapping,
+                                     step->num_tokens, num_kv_heads, head_dim, block_size, num_blocks, step->k_stride,
+                                     step->v_stride, dtype, stream);
+    if (st != KV_OK) return st;
+  }
   const cudaError_t e = dtype == KV_DTYPE_F16 ? launch_fp8_decode<__half>(p, pl, maps, s)
                                               : launch_fp8_decode<__nv_bfloat16>(p, pl, maps, s);
   return cuda_status(e);
+}
+}  // namespace
+
+extern "C" int paged_decode_attention_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                          const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                                          const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads,
+                                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                          int64_t num_blocks, int32_t max_blocks_per_seq, int64_t max_seq_len,
+                                          float scale, int dtype, void* workspace, size_t workspace_bytes,
+                                          void* stream) {
+  return decode_fp8_impl(out, q, k_cache, v_cache, k_scales, v_scales, block_tables, seq_lens, num_seqs, num_heads,
+                         num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, max_seq_len, scale, dtype,
+                         workspace, workspace_bytes, stream, nullptr);
+}
+
+extern "C" int paged_decode_step_fp8(void* out, const void* q, const void* k, const void* v,
+                                     const int32_t* slot_mapping, int64_t num_tokens, int64_t k_token_stride,
+                                     int64_t v_token_stride, const int32_t* new_token_row, void* k_cache,
+                                     void* v_cache, float* k_scales, float* v_scales, const int32_t* block_tables,
+                                     const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads,
+                                     int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                     int32_t max_blocks_per_seq, int64_t max_seq_len, float scale, int dtype,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (num_tokens < 0) return KV_ERR_INVALID_ARG;
+  if (num_tokens > 0) {
+    const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+    if (!k || !v || !slot_mapping || k_token_stride < row || v_token_stride < row) return KV_ERR_INVALID_ARG;
+    if (num_seqs > 0 && !new_token_row) return KV_ERR_INVALID_ARG;
+  }
+  if (num_seqs == 0)  // nothing to attend: the cache write alone
+    return paged_reshape_and_cache_fp8(k, v, k_cache, v_cache, k_scales, v_scales, slot_mapping, num_tokens,
+                                       num_kv_heads, head_dim, block_size, num_blocks, k_token_stride, v_token_stride,
+                                       dtype, stream);
+  const StepArgs step{k, v, slot_mapping, new_token_row, num_tokens, k_token_stride, v_token_stride};
+  return decode_fp8_impl(out, q, k_cache, v_cache, k_scales, v_scales, block_tables, seq_lens, num_seqs, num_heads,
+                         num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, max_seq_len, scale, dtype,
+                         workspace, workspace_bytes, stream, &step);
 }
 
 // ---------------------------------------------------------------------------

@@ -240,14 +240,12 @@ extern "C" int kvstep_run(kvstep_t h, const void* q, const void* k, const void* 
       const int64_t so = static_cast<int64_t>(l) * c.num_blocks * c.num_kv_heads * c.block_size;
       char* kc = static_cast<char*>(c.k_cache) + co8;
       char* vc = static_cast<char*>(c.v_cache) + co8;
-      st = paged_reshape_and_cache_fp8(static_cast<const char*>(dk) + ko, static_cast<const char*>(dv) + ko, kc, vc,
-                                       c.k_scales + so, c.v_scales + so, d_slots, c.num_step_tokens, c.num_kv_heads,
-                                       c.head_dim, c.block_size, c.num_blocks, row, row, c.dtype, h->compute);
-      if (st != KV_OK) return st;
-      st = paged_decode_attention_fp8(static_cast<char*>(dout) + qo, static_cast<const char*>(dq) + qo, kc, vc,
-                                      c.k_scales + so, c.v_scales + so, d_tables, d_lens, c.num_seqs, c.num_heads,
-                                      c.num_kv_heads, c.head_dim, c.block_size, c.num_blocks, c.max_blocks_per_seq,
-                                      c.max_seq_len, c.scale, c.dtype, c.workspace, c.workspace_bytes, h->compute);
+      st = paged_decode_step_fp8(static_cast<char*>(dout) + qo, static_cast<const char*>(dq) + qo,
+                                 static_cast<const char*>(dk) + ko, static_cast<const char*>(dv) + ko, d_slots,
+                                 c.num_step_tokens, row, row, d_rows, kc, vc, c.k_scales + so, c.v_scales + so,
+                                 d_tables, d_lens, c.num_seqs, c.num_heads, c.num_kv_heads, c.head_dim, c.block_size,
+                                 c.num_blocks, c.max_blocks_per_seq, c.max_seq_len, c.scale, c.dtype, c.workspace,
+                                 c.workspace_bytes, h->compute);
       if (st != KV_OK) return st;
       continue;
     }

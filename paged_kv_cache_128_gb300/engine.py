@@ -30,7 +30,7 @@ from ._lib import check, kvstep_config_t, lib
 from .block_manager import KVBlockManager
 from .inputs import Values, Workload, pad_positions, sentinel_bits
 from .kernels import (alloc_workspace, decode_plan, dtype_code, paged_decode_attention, paged_decode_attention_fp8,
-                      paged_decode_step, reshape_and_cache, reshape_and_cache_fp8)
+                      paged_decode_step, paged_decode_step_fp8, reshape_and_cache, reshape_and_cache_fp8)
 
 _INT_VIEW = {torch.float32: torch.int32, torch.float16: torch.int16, torch.bfloat16: torch.int16}
 
@@ -51,7 +51,7 @@ class PagedDecodeEngine:
         self.fp8 = kv_cache == "fp8"
         # fused: the step's cache write and attention in one paged_decode_step
         # call (one launch with the stream-K kernel); else two calls
-        self.fused = fused and blocks_per_split == 0 and not self.fp8
+        self.fused = fused and blocks_per_split == 0
         self.device = torch.device(device)
         self.mgr = KVBlockManager(wl.num_blocks, wl.block_size, wl.free_order)
         dt = wl.torch_dtype
@@ -232,8 +232,12 @@ class PagedDecodeEngine:
                                       wl.scale, self.max_seq_len, self.blocks_per_split, self.workspace)
 
     def fused_step(self, q: torch.Tensor, k_step: torch.Tensor, v_step: torch.Tensor) -> torch.Tensor:
-        """a2-a8 in one paged_decode_step call."""
+        """a2-a8 in one paged_decode_step(_fp8) call."""
         wl = self.wl
+        if self.fp8:
+            return paged_decode_step_fp8(self.out, q, k_step, v_step, self.d_slots, self.d_new_rows, self.k_cache,
+                                         self.v_cache, self.k_scales, self.v_scales, self.d_tables, self.d_lens,
+                                         wl.scale, self.max_seq_len, self.workspace)
         return paged_decode_step(self.out, q, k_step, v_step, self.d_slots, self.d_new_rows, self.k_cache,
                                  self.v_cache, self.d_tables, self.d_lens, wl.scale, self.max_seq_len,
                                  self.workspace)
@@ -371,7 +375,10 @@ class PagedDecodeEngine:
         if self.fused and self.plan.kernel == 2:
             return 1
         if self.fp8:
-            return 2
+            # the library fuses the fp8 write only for at most two step rows per
+            # consumer warp (4 per CTA, two CTAs per SM)
+            sms = torch.cuda.get_device_properties(self.device).multi_processor_count
+            return 1 if self.fused and self.wl.num_step_tokens <= 2 * sms * 2 * 4 else 2
         return 1 + self.plan.launches
 
     def algorithmic_bytes(self, seq_lens: np.ndarray) -> dict:

@@ -142,6 +142,45 @@ def paged_decode_attention_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torc
     return out
 
 
+def paged_decode_step_fp8(out: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                          slot_mapping: torch.Tensor, new_token_row: torch.Tensor, k_cache: torch.Tensor,
+                          v_cache: torch.Tensor, k_scales: torch.Tensor, v_scales: torch.Tensor,
+                          block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float, max_seq_len: int,
+                          workspace: Optional[torch.Tensor] = None,
+                          stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """The step's quantised cache write and decode attention over fp8
+    caches in one call (one launch when the rows are 8-byte aligned)."""
+    for t, n in ((out, "out"), (q, "q"), (k, "k"), (v, "v"), (slot_mapping, "slot_mapping"),
+                 (new_token_row, "new_token_row"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (k_scales, "k_scales"), (v_scales, "v_scales"), (block_tables, "block_tables"),
+                 (seq_lens, "seq_lens")):
+        _cuda(t, n)
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    n = slot_mapping.numel()
+    if d2 != d or out.shape != q.shape or out.dtype != q.dtype or k_cache.dtype != torch.uint8 \
+            or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise KVError(1, "shape or dtype mismatch")
+    for t, nm in ((block_tables, "block_tables"), (seq_lens, "seq_lens"), (slot_mapping, "slot_mapping"),
+                  (new_token_row, "new_token_row")):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise KVError(1, f"{nm} must be contiguous int32")
+    for t in (k, v):
+        if t.dim() != 3 or t.shape[0] != n or t.shape[1] != hkv or t.shape[2] != d or t.stride(2) != 1 \
+                or t.stride(1) != d:
+            raise KVError(1, "k and v must be [N, Hkv, D] with dense heads")
+    if workspace is None:
+        workspace = alloc_workspace(decode_plan(B, hq, hkv, d, bs, max_seq_len, q.dtype), q.device)
+    ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
+    check(lib().paged_decode_step_fp8(out.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                      slot_mapping.data_ptr(), n, k.stride(0), v.stride(0), new_token_row.data_ptr(),
+                                      k_cache.data_ptr(), v_cache.data_ptr(), k_scales.data_ptr(), v_scales.data_ptr(),
+                                      block_tables.data_ptr(), seq_lens.data_ptr(), B, hq, hkv, d, bs, nb,
+                                      block_tables.shape[1], max_seq_len, float(scale), dtype_code(q.dtype), ws_ptr,
+                                      ws_bytes, _stream_ptr(stream)), "paged_decode_step_fp8")
+    return out
+
+
 def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src: torch.Tensor, dst: torch.Tensor,
                 stream: Optional[torch.cuda.Stream] = None) -> None:
     """Copy-on-write copies: block ``dst[i]`` of every layer's K and V cache

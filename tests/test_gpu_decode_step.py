@@ -27,7 +27,7 @@ from tests.helpers import TOL, TORCH, sentinel_storage, sentinel_tensor, to_f64,
 pytestmark = pytest.mark.gpu
 
 
-def build_step(dtype, hq, hkv, d, bs, cached, has_new, n_prefill, n_pad, seed):
+def build_step(dtype, hq, hkv, d, bs, cached, has_new, n_prefill, n_pad, seed, value_scale=1.0):
     """A pool holding each sequence's history and one step's new rows.
 
     Sequence b holds cached[b] tokens before the step and cached[b] + 1
@@ -35,6 +35,7 @@ def build_step(dtype, hq, hkv, d, bs, cached, has_new, n_prefill, n_pad, seed):
     (row new_row[b]); otherwise that token is already in the cache and
     new_row[b] = -1.  The step also writes n_prefill rows of a sequence
     outside the batch and holds n_pad padded (-1) rows; rows are shuffled.
+    K and V values are N(0, 1) * value_scale.
     """
     rng = np.random.default_rng(seed)
     g = torch.Generator().manual_seed(seed)
@@ -55,10 +56,10 @@ def build_step(dtype, hq, hkv, d, bs, cached, has_new, n_prefill, n_pad, seed):
         assert list(pre_slots) == ora.allocate_for_prefill(B, n_prefill)
     dt = TORCH[dtype]
     q = torch.randn(B, hq, d, generator=g).to(dt)
-    k_all = [torch.randn(L, hkv, d, generator=g).to(dt) for L in lens]
-    v_all = [torch.randn(L, hkv, d, generator=g).to(dt) for L in lens]
-    k_pre = torch.randn(n_prefill, hkv, d, generator=g).to(dt)
-    v_pre = torch.randn(n_prefill, hkv, d, generator=g).to(dt)
+    k_all = [(torch.randn(L, hkv, d, generator=g) * value_scale).to(dt) for L in lens]
+    v_all = [(torch.randn(L, hkv, d, generator=g) * value_scale).to(dt) for L in lens]
+    k_pre = (torch.randn(n_prefill, hkv, d, generator=g) * value_scale).to(dt)
+    v_pre = (torch.randn(n_prefill, hkv, d, generator=g) * value_scale).to(dt)
 
     # history: everything but the step's new tokens
     hist_slots, hist_k, hist_v = [], [], []

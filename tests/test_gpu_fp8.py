@@ -177,3 +177,82 @@ def test_fp8_mid_size_workload():
         worst = max(worst, float(np.max(np.abs(got[b] - ref))))
     assert np.all(np.isfinite(got))
     assert worst <= TOL[wl.dtype], f"max abs err {worst:.3e}"
+
+
+STEP_CASES = [
+    ("bf16", 28, 4, 16, [0, 1, 15, 16, 31, 63, 64, 65, 200, 777]),
+    ("f16", 16, 2, 32, [0, 31, 32, 63, 64, 95, 300]),
+    ("bf16", 32, 2, 16, [5, 17, 40, 129]),      # 16 heads per kv head: 32-token fp8 tiles
+]
+
+
+@pytest.mark.parametrize("case", STEP_CASES, ids=lambda c: f"{c[0]}-g{c[1] // c[2]}-bs{c[3]}")
+@pytest.mark.parametrize("mode", ["all_new", "some_new"])
+def test_fp8_step_equals_write_then_attention(case, mode):
+    """paged_decode_step_fp8 (one launch) equals paged_reshape_and_cache_fp8
+    followed by paged_decode_attention_fp8 bit for bit: outputs, codes and
+    scales; and the output matches the float64 oracle on the dequantised
+    rows, new tokens included."""
+    from tests.test_gpu_decode_step import build_step
+    dtype, hq, hkv, bs, cached = case
+    d = 128
+    seed = 11 + len(cached) + (0 if mode == "all_new" else 50)
+    rng = np.random.default_rng(seed)
+    has_new = [True] * len(cached) if mode == "all_new" else list(rng.random(len(cached)) < 0.5)
+    # values N(0, 1) / 2, as in the small-model workload: sequences of one or
+    # two tokens output a dequantised row or two, where rounding to the
+    # output dtype alone reaches the stated bar for values past 2
+    c = build_step(dtype, hq, hkv, d, bs, cached, has_new, n_prefill=21, n_pad=4, seed=seed, value_scale=0.5)
+    dev = torch.device("cuda")
+    kc, vc, ks, vs = _empty_fp8(c["nb"], bs, hkv, d, dev)
+    if c["hist_slots"].size:
+        pk.reshape_and_cache_fp8(c["hist_k"].to(dev), c["hist_v"].to(dev), kc, vc, ks, vs,
+                                 torch.from_numpy(c["hist_slots"].astype(np.int32)).to(dev))
+    twin = [t.clone() for t in (kc, vc, ks, vs)]
+    q = c["q"].to(dev)
+    sk, sv = c["step_k"].to(dev), c["step_v"].to(dev)
+    slots = torch.from_numpy(c["step_slots"].astype(np.int32)).to(dev)
+    rows = torch.from_numpy(c["new_row"]).to(dev)
+    tables = torch.from_numpy(c["tables"]).to(dev)
+    lens = torch.from_numpy(c["seq_lens"]).to(dev)
+    scale = 1.0 / math.sqrt(d)
+    max_len = int(c["seq_lens"].max())
+    out = torch.empty_like(q)
+    pk.device_error()
+    pk.paged_decode_step_fp8(out, q, sk, sv, slots, rows, kc, vc, ks, vs, tables, lens, scale, max_len)
+    assert pk.device_error() == 0
+    out2 = torch.empty_like(q)
+    pk.reshape_and_cache_fp8(sk, sv, twin[0], twin[1], twin[2], twin[3], slots)
+    pk.paged_decode_attention_fp8(out2, q, twin[0], twin[1], twin[2], twin[3], tables, lens, scale, max_len)
+    assert pk.device_error() == 0
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(kc, twin[0]) and torch.equal(vc, twin[1])
+    assert torch.equal(ks.view(torch.int32), twin[2].view(torch.int32))
+    assert torch.equal(vs.view(torch.int32), twin[3].view(torch.int32))
+    got = to_f64(out, dtype)
+    q64 = to_f64(c["q"], dtype)
+    worst = 0.0
+    for b, L in enumerate(c["lens"]):
+        kq, ksc = quantize_rows(_f32(c["k_all"][b]))
+        vq, vsc = quantize_rows(_f32(c["v_all"][b]))
+        ref = decode_attention_contiguous(q64[b], e4m3_to_float_array(kq) * ksc[..., None].astype(np.float64),
+                                          e4m3_to_float_array(vq) * vsc[..., None].astype(np.float64), scale)
+        worst = max(worst, float(np.max(np.abs(got[b] - ref))))
+    assert worst <= TOL[dtype], f"max abs err {worst:.3e}"
+
+
+def test_fp8_step_reports_inconsistent_row():
+    from tests.test_gpu_decode_step import build_step
+    dtype, hq, hkv, bs, cached = STEP_CASES[0]
+    c = build_step(dtype, hq, hkv, 128, bs, cached, [True] * len(cached), n_prefill=3, n_pad=1, seed=4)
+    dev = torch.device("cuda")
+    kc, vc, ks, vs = _empty_fp8(c["nb"], bs, hkv, 128, dev)
+    rows = c["new_row"].copy()
+    rows[5] = rows[6]
+    out = torch.empty(c["q"].shape, dtype=c["q"].dtype, device=dev)
+    pk.device_error()
+    pk.paged_decode_step_fp8(out, c["q"].to(dev), c["step_k"].to(dev), c["step_v"].to(dev),
+                             torch.from_numpy(c["step_slots"].astype(np.int32)).to(dev), torch.from_numpy(rows).to(dev),
+                             kc, vc, ks, vs, torch.from_numpy(c["tables"]).to(dev), torch.from_numpy(c["seq_lens"]).to(dev),
+                             1.0 / math.sqrt(128), int(c["seq_lens"].max()))
+    assert pk.device_error() == 11
