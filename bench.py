@@ -53,6 +53,8 @@ def parse_args():
                          "(head_dim 128 workloads)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="--impl reference: seconds of oracle time for the whole run (steps + warm-up)")
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="only set the workload up and run this many attention calls (L2 flushed before each); "
                          "the small case used under ncu")
@@ -239,6 +241,18 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """The largest x over the ranks of the process group (x itself for one
+    rank): the timed region of a multi-replica run is the slowest rank's."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_native(args):
     import numpy as np
     import torch
@@ -320,10 +334,7 @@ def run_native(args):
         lens = eng.wl.cached_lens + done
         step_bytes += eng.algorithmic_bytes(lens)["step"]
         tokens += eng.wl.num_seqs
-    t_max = torch.tensor([t_steps], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    t_steps_max = float(t_max.item())
+    t_steps_max = max_over_ranks(t_steps, world, dev)
     value_gbs = step_bytes * world / t_steps_max / 1e9
     tokens_per_s = tokens * world / t_steps_max
     status = pk.device_error()
@@ -389,11 +400,9 @@ def run_native(args):
     join_all()
     e1.record()
     torch.cuda.synchronize()
-    t_e2e = torch.tensor([e0.elapsed_time(e1) / 1e3], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
     e2e_bytes = sum(eng.algorithmic_bytes(eng.wl.cached_lens + done)["step"] for eng, done in e_marks)
-    e2e_gbs = e2e_bytes * world / float(t_e2e.item()) / 1e9
+    e2e_gbs = e2e_bytes * world / t_e2e / 1e9
     # per step: q, k, v and the metadata buffer (slot mapping, tables, lengths, decode rows) in; out back
     h2d = (q.numel() + k_step.numel() + v_step.numel()) * q.element_size() + 4 * (engines[0].d_meta.numel() +
                                                                                     wl.num_seqs)
@@ -453,7 +462,7 @@ def run_native(args):
                            "K/V read from HBM"),
         },
         "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": float(t_e2e.item()) / args.steps * 1e3},
+                "ms_per_step": t_e2e / args.steps * 1e3},
         "gpu_launches": args.steps * engines[0].launches_per_step,
         "clocks": clk,
         "device_error": status,
@@ -473,30 +482,31 @@ def run_native(args):
 # ---------------------------------------------------------- reference arm
 
 def run_reference(args):
+    """The oracle as it stands, on one host thread, over the workload's first
+    8 sequences: one bounded run of about --ref-seconds x K / (K + W)
+    seconds of timed decode steps (its set-up is the untimed warm-up).
+    Under torchrun only rank 0 runs and prints; the others exit at once."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    per_step = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
     from paged_kv_cache_128_gb300.inputs import make_workload
     wl = make_workload(args.workload)
-    samples = []
-    for i in range(args.warmup + args.steps):
-        r = run_oracle_sample(args.workload, per_step, max_seqs=min(8, wl.num_seqs))
-        if i >= args.warmup:
-            samples.append(r)
-    secs = sum(r["seconds"] for r in samples)
-    gbs = sum(r["bytes"] for r in samples) / secs / 1e9
-    tokens = sum(r["tokens"] for r in samples) / secs
+    total = max(1, args.steps + args.warmup)
+    budget = max(0.05, args.ref_seconds * max(1, args.steps) / total)
+    r = run_oracle_sample(args.workload, budget, max_seqs=min(8, wl.num_seqs))
+    secs = r["seconds"]
+    gbs = r["bytes"] / secs / 1e9
     out = {
         "impl": "reference",
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": secs / max(1, sum(r["steps"] for r in samples)) * 1e3,
+        "warmup": args.warmup, "ms_per_step": secs / max(1, r["steps"]) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic (seeded)", "config": {"workload": wl.name},
-        "decode_tokens_per_s": tokens,
+        "decode_tokens_per_s": r["tokens"] / secs,
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": (f"float64 numpy oracle on one host thread; each step a {per_step:.0f}-second "
-                                    f"sample of decode steps over the first {samples[0]['seqs']} sequences")},
+                         "sample": (f"float64 numpy oracle on one host thread: {r['steps']} decode steps of the "
+                                    f"first {r['seqs']} sequences (manager append + export, cache write, "
+                                    f"attention), {secs:.1f} s timed")},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out))
