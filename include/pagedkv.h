@@ -325,6 +325,32 @@ int paged_decode_step_fp8(void* out, const void* q, const void* k, const void* v
                           int32_t max_blocks_per_seq, int64_t max_seq_len, float scale, int dtype,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/* Chunked-prefill attention through block tables ("从零实现一个 mini vLLM:
+ * Block Manager": a chunked prefill allocates the chunk's slots, writes its
+ * K/V, then attends through the table; "MiniPaged-Qwen" §13-§14).  For each
+ * sequence b, its chunk is rows query_start_loc[b] .. query_start_loc[b+1]-1
+ * of q and out: the last n_b of its seq_lens[b] = L_b positions, whose K/V
+ * the cache write has already stored.  Chunk token t (position
+ * p = L_b - n_b + t) attends to keys 0..p of its sequence:
+ *   out[r, qh] = sum_{j <= p} softmax_j(scale * q[r, qh] . K_j) V_j,
+ *   kvh = qh / (num_heads / num_kv_heads), K_j read through block_tables[b].
+ * A chunk of one token is decode.
+ *   q, out: device [total tokens, num_heads, head_dim] of dtype (fp16 or
+ *     bf16), 16-byte aligned; caches as for paged_decode_attention.
+ *   query_start_loc: device int32[num_seqs + 1], non-decreasing.
+ *   max_query_len: host upper bound of the chunk lengths (sizes the grid).
+ *   head_dim 64 or 128.
+ * A chunk longer than its sequence, or a sequence longer than its table
+ * row, is recorded as KV_ERR_DEVICE_BOUNDS (the former's rows are not
+ * written).  Tensor cores through mma.sync, fp32 accumulation and online
+ * softmax, one rounding to dtype. */
+int paged_prefill_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* seq_lens,
+                            const int32_t* query_start_loc, int32_t num_seqs, int32_t num_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                            int32_t max_blocks_per_seq, int32_t max_query_len, float scale, int dtype,
+                            void* stream);
+
 /* Copy-on-write block copies (kvbm_take_copies): for each i < n, block
  * dst[i] of every layer's K and V cache becomes a copy of block src[i]
  * ("paged-attention-impl-detail", copy_on_write: the new block's k and v

@@ -120,3 +120,27 @@ def merge_states(states: List[Tuple[np.ndarray, float, float]]) -> np.ndarray:
     num = sum(np.exp(st[1] - M) * st[0] for st in live)
     den = sum(np.exp(st[1] - M) * st[2] for st in live)
     return num / den
+
+
+def chunked_prefill_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.ndarray:
+    """Attention of a sequence's new chunk over its history and the chunk.
+
+    ``q [n, Hq, D]`` are the chunk's queries, the last n of the sequence's
+    L tokens; ``K, V [L, Hkv, D]`` its logical keys and values (history,
+    then the chunk), float64.  Chunk token t sits at position p = L - n + t
+    and attends to keys 0..p (causal within the chunk, all history before
+    it): "从零实现一个 mini vLLM: Block Manager" (a chunked prefill allocates
+    the chunk's slots, writes their K/V, then attends through the block
+    table) and MiniPaged-Qwen §13 (attention over positions read through the
+    table).  Each row is the decode attention of that token over its prefix,
+    so a chunk of one token is exactly decode.  -> ``o [n, Hq, D]``.
+    """
+    n = q.shape[0]
+    L = K.shape[0]
+    if n > L:
+        raise ValueError("chunk longer than the sequence")
+    out = np.empty(q.shape, dtype=np.float64)
+    for t in range(n):
+        p = L - n + t
+        out[t] = decode_attention_contiguous(q[t], K[:p + 1], V[:p + 1], scale)
+    return out

@@ -19,7 +19,7 @@ def __getattr__(name):
     # the kernel wrappers need torch; import them on first use
     if name in ("reshape_and_cache", "reshape_and_cache_layers", "paged_decode_attention", "paged_decode_step", "copy_blocks", "decode_plan",
                 "device_error", "alloc_workspace", "DecodePlan", "reshape_and_cache_fp8",
-                "paged_decode_attention_fp8", "paged_decode_step_fp8"):
+                "paged_decode_attention_fp8", "paged_decode_step_fp8", "paged_prefill_attention"):
         from . import kernels
         return getattr(kernels, name)
     raise AttributeError(name)

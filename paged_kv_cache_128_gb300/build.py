@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 HEADERS = [os.path.join(ROOT, "include", "pagedkv.h"), os.path.join(CSRC, "common.cuh")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-CUDA_SOURCES = ["reshape_and_cache.cu", "paged_decode.cu", "step_runner.cu"]
+CUDA_SOURCES = ["reshape_and_cache.cu", "paged_decode.cu", "paged_prefill.cu", "step_runner.cu"]
 CXX_SOURCES = ["block_manager.cpp"]
 
 

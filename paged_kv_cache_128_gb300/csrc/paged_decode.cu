@@ -2116,6 +2116,7 @@ int check_shapes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t BS, int6
 using namespace pagedkv;
 
 extern "C" int pagedkv_internal_reshape_error(int reset, int* code);
+extern "C" int pagedkv_internal_prefill_error(int reset, int* code);
 extern "C" int paged_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
                                        const int32_t* slot_mapping, int64_t num_tokens, int32_t num_kv_heads,
                                        int32_t head_dim, int32_t block_size, int64_t num_blocks,
@@ -2504,7 +2505,10 @@ extern "C" int kv_device_error(int reset, int* status_out) {
   }
   int r = pagedkv_internal_reshape_error(reset, &c);
   if (r != KV_OK) return r;
-  *status_out = a ? a : c;
+  int f = 0;
+  r = pagedkv_internal_prefill_error(reset, &f);
+  if (r != KV_OK) return r;
+  *status_out = a ? a : (c ? c : f);
   return KV_OK;
 }
 

@@ -181,6 +181,36 @@ def paged_decode_step_fp8(out: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v
     return out
 
 
+def paged_prefill_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, seq_lens: torch.Tensor, query_start_loc: torch.Tensor,
+                            scale: float, max_query_len: int,
+                            stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Chunked prefill: q/out ``[T, Hq, D]``, sequence b's chunk is rows
+    ``query_start_loc[b]:query_start_loc[b+1]``, its last positions; each
+    chunk token attends causally to its sequence's keys through the table."""
+    for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (block_tables, "block_tables"),
+                 (seq_lens, "seq_lens"), (query_start_loc, "query_start_loc")):
+        _cuda(t, n)
+    if not (q.is_contiguous() and out.is_contiguous() and k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise KVError(1, "q, out and caches must be contiguous")
+    nb, bs, hkv, d = k_cache.shape
+    T, hq, d2 = q.shape
+    B = seq_lens.numel()
+    if d2 != d or out.shape != q.shape or out.dtype != q.dtype or k_cache.dtype != q.dtype \
+            or v_cache.shape != k_cache.shape or v_cache.dtype != q.dtype:
+        raise KVError(1, "shape or dtype mismatch")
+    for t, nm in ((block_tables, "block_tables"), (seq_lens, "seq_lens"), (query_start_loc, "query_start_loc")):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise KVError(1, f"{nm} must be contiguous int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or query_start_loc.numel() != B + 1:
+        raise KVError(1, "block_tables [B, max_blocks], seq_lens [B], query_start_loc [B + 1]")
+    check(lib().paged_prefill_attention(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                        block_tables.data_ptr(), seq_lens.data_ptr(), query_start_loc.data_ptr(), B,
+                                        hq, hkv, d, bs, nb, block_tables.shape[1], max_query_len, float(scale),
+                                        dtype_code(q.dtype), _stream_ptr(stream)), "paged_prefill_attention")
+    return out
+
+
 def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src: torch.Tensor, dst: torch.Tensor,
                 stream: Optional[torch.cuda.Stream] = None) -> None:
     """Copy-on-write copies: block ``dst[i]`` of every layer's K and V cache

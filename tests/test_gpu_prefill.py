@@ -1,0 +1,111 @@
+"""GPU parity of chunked-prefill attention (paged_prefill_attention).
+
+Each sequence holds ctx tokens of history and a chunk of n new tokens (its
+last n positions; all L = ctx + n tokens are written through the cache
+write first).  Every chunk row must match the float64 oracle
+(oracle.attention.chunked_prefill_attention) on the sequence's logical K/V,
+within the dtype's tolerance: chunks with and without history, chunks
+crossing 64-token query tiles and 32-token key tiles, one-token chunks
+(decode), GQA ratios 1 to 8, head_dim 64 and 128, block sizes 16 and 32,
+and the mixed-batch workload's 4096-token prefill chunk (sampled rows).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_128_gb300 as pk
+from oracle.attention import chunked_prefill_attention
+from paged_kv_cache_128_gb300.inputs import make_values, make_workload
+from tests.helpers import TOL, TORCH, sentinel_tensor, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(dtype, hq, hkv, d, bs, seqs, seed, value_scale=0.5, sample_rows=None):
+    """seqs: list of (history length, chunk length)."""
+    rng = np.random.default_rng(seed)
+    g = torch.Generator().manual_seed(seed)
+    dt = TORCH[dtype]
+    lens = [c + n for c, n in seqs]
+    nb = sum(-(-L // bs) for L in lens) + 3
+    mgr = pk.KVBlockManager(nb, bs, rng.permutation(nb).tolist())
+    dev = torch.device("cuda")
+    kc = sentinel_tensor((nb, bs, hkv, d), dtype, dev)
+    vc = sentinel_tensor((nb, bs, hkv, d), dtype, dev)
+    Ks, Vs = [], []
+    for sid, L in enumerate(lens):
+        slots = torch.from_numpy(mgr.allocate_for_prefill(sid, L)).to(dev)
+        k = (torch.randn(L, hkv, d, generator=g) * value_scale).to(dt)
+        v = (torch.randn(L, hkv, d, generator=g) * value_scale).to(dt)
+        pk.reshape_and_cache(k.to(dev), v.to(dev), kc, vc, slots)
+        Ks.append(k)
+        Vs.append(v)
+    maxb = max(-(-L // bs) for L in lens) + 1
+    tables, seq_lens = mgr.export(list(range(len(seqs))), maxb)
+    qsl = np.concatenate([[0], np.cumsum([n for _, n in seqs])]).astype(np.int32)
+    T = int(qsl[-1])
+    q = (torch.randn(T, hq, d, generator=g) * value_scale).to(dt)
+    out = sentinel_tensor((T, hq, d), dtype, dev)
+    scale = 1.0 / math.sqrt(d)
+    pk.device_error()
+    pk.paged_prefill_attention(out, q.to(dev), kc, vc, torch.from_numpy(tables).to(dev),
+                               torch.from_numpy(seq_lens).to(dev), torch.from_numpy(qsl).to(dev), scale,
+                               max(n for _, n in seqs))
+    assert pk.device_error() == 0
+    got = to_f64(out, dtype)
+    assert np.all(np.isfinite(got))
+    q64 = to_f64(q, dtype)
+    worst = 0.0
+    for b, (c, n) in enumerate(seqs):
+        K, V = to_f64(Ks[b], dtype), to_f64(Vs[b], dtype)
+        rows = range(n) if sample_rows is None else sorted(set(rng.integers(0, n, sample_rows).tolist()))
+        for t in rows:
+            p = c + t
+            ref = chunked_prefill_attention(q64[qsl[b] + t:qsl[b] + t + 1], K[:p + 1], V[:p + 1], scale)[0]
+            worst = max(worst, float(np.max(np.abs(got[qsl[b] + t] - ref))))
+    return worst
+
+
+CASES = [
+    ("bf16", 8, 2, 128, 16, [(0, 1), (0, 5), (0, 64), (0, 65), (0, 200), (13, 7), (100, 1), (300, 130), (31, 33)]),
+    ("f16", 14, 2, 64, 16, [(0, 63), (5, 64), (40, 129), (0, 1)]),
+    ("bf16", 32, 8, 128, 32, [(0, 256), (17, 95), (64, 64)]),
+    ("f16", 4, 4, 128, 32, [(7, 40), (0, 3), (500, 70)]),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-g{c[1] // c[2]}-d{c[3]}-bs{c[4]}")
+def test_prefill_matches_oracle(case):
+    dtype, hq, hkv, d, bs, seqs = case
+    worst = _run(dtype, hq, hkv, d, bs, seqs, seed=len(seqs) + d)
+    assert worst <= TOL[dtype], f"max abs err {worst:.3e}"
+
+
+def test_prefill_mixed_batch_chunk():
+    """The mixed-batch workload's prefill chunk: 8 new sequences, 4096
+    tokens in all, Hq 32, Hkv 8, D 128, bs 32 (sampled rows of each)."""
+    wl = make_workload("mixed_batch_bf16")
+    seqs = [(0, int(n)) for n in wl.prefill_lens]
+    assert sum(n for _, n in seqs) == 4096
+    worst = _run("bf16", wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size, seqs, seed=5, value_scale=1.0,
+                 sample_rows=12)
+    assert worst <= TOL["bf16"], f"max abs err {worst:.3e}"
+
+
+def test_prefill_chunk_longer_than_sequence_is_reported():
+    dev = torch.device("cuda")
+    nb, bs, hkv, d, hq = 8, 16, 2, 64, 4
+    kc = torch.zeros(nb, bs, hkv, d, dtype=torch.float16, device=dev)
+    vc = torch.zeros_like(kc)
+    tables = torch.tensor([[0, 1, 2, -1]], dtype=torch.int32, device=dev)
+    lens = torch.tensor([10], dtype=torch.int32, device=dev)
+    qsl = torch.tensor([0, 12], dtype=torch.int32, device=dev)    # 12 chunk tokens, sequence of 10
+    q = torch.randn(12, hq, d, device=dev).half()
+    out = torch.full((12, hq, d), 7.0, dtype=torch.float16, device=dev)
+    pk.device_error()
+    pk.paged_prefill_attention(out, q, kc, vc, tables, lens, qsl, 0.125, 12)
+    assert pk.device_error() == 8
+    assert torch.all(out == 7.0)                                   # nothing written
