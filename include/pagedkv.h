@@ -335,19 +335,22 @@ int paged_decode_step_fp8(void* out, const void* q, const void* k, const void* v
  *   out[r, qh] = sum_{j <= p} softmax_j(scale * q[r, qh] . K_j) V_j,
  *   kvh = qh / (num_heads / num_kv_heads), K_j read through block_tables[b].
  * A chunk of one token is decode.
- *   q, out: device [total tokens, num_heads, head_dim] of dtype (fp16 or
- *     bf16), 16-byte aligned; caches as for paged_decode_attention.
- *   query_start_loc: device int32[num_seqs + 1], non-decreasing.
+ *   q, out: device [num_query_tokens, num_heads, head_dim] of dtype (fp16
+ *     or bf16), 16-byte aligned; caches as for paged_decode_attention.
+ *   query_start_loc: device int32[num_seqs + 1], non-decreasing, every
+ *     entry in [0, num_query_tokens].
  *   max_query_len: host upper bound of the chunk lengths (sizes the grid).
  *   head_dim 64 or 128.
- * A chunk longer than its sequence, or a sequence longer than its table
- * row, is recorded as KV_ERR_DEVICE_BOUNDS (the former's rows are not
- * written).  Tensor cores through mma.sync, fp32 accumulation and online
- * softmax, one rounding to dtype. */
+ * A chunk longer than its sequence or reaching past num_query_tokens, or a
+ * sequence longer than its table row, is recorded as KV_ERR_DEVICE_BOUNDS
+ * (the former two's rows are not written).  Block sizes 16, 32, 64 and 128
+ * run on the 5th-generation tensor cores (tcgen05, accumulators in tensor
+ * memory, K/V tiles by TMA); other block sizes on mma.sync.  fp32
+ * accumulation and online softmax, one rounding to dtype. */
 int paged_prefill_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
                             const int32_t* block_tables, const int32_t* seq_lens,
-                            const int32_t* query_start_loc, int32_t num_seqs, int32_t num_heads,
-                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                            const int32_t* query_start_loc, int64_t num_query_tokens, int32_t num_seqs,
+                            int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t num_blocks,
                             int32_t max_blocks_per_seq, int32_t max_query_len, float scale, int dtype,
                             void* stream);
 

@@ -89,7 +89,7 @@ SIGNATURES = {
                                       c_int32, c_int32, c_int32, c_int32, c_int64, c_int32, c_int64, c_float, c_int,
                                       c_void_p, c_size_t, c_void_p]),
     "paged_prefill_attention": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                        c_int32, c_int32, c_int32, c_int32, c_int32, c_int64, c_int32, c_int32,
+                                        c_int64, c_int32, c_int32, c_int32, c_int32, c_int32, c_int64, c_int32, c_int32,
                                         c_float, c_int, c_void_p]),
     "paged_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int32, c_int64, c_int32,
                                   c_int32, c_int32, c_int64, c_int, c_void_p]),

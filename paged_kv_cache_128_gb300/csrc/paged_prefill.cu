@@ -20,7 +20,13 @@
 // reused from the score registers as the A operand and V fragments by
 // ldmatrix.trans.  The output is rounded once to the q dtype.
 
+#include <cudaTypedefs.h>
+
+#include <mutex>
+#include <type_traits>
+
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace pagedkv {
 namespace {
@@ -41,6 +47,8 @@ struct PrefillParams {
   int64_t num_blocks;
   int32_t max_blocks_per_seq;
   float scale_log2;  // scale * log2(e)
+  int64_t num_tokens;  // rows of q and out
+  int32_t hg_log2;     // tensor-core kernel: log2 of the query heads per row tile
 };
 
 // Byte offset of (key, dim) in a [kPfKeys][D] 16-bit tile: 128-byte slabs of
@@ -73,12 +81,16 @@ __global__ void __launch_bounds__(kPfWarps * 32) prefill_kernel(const PrefillPar
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qs = __ldg(p.query_start + b), n = __ldg(p.query_start + b + 1) - qs;
   if (n <= 0 || qt * kPfRows >= n) return;
+  if (qs < 0 || qs + n > p.num_tokens) {  // the chunk's rows must lie inside q
+    if (tid == 0) record_error(KV_ERR_DEVICE_BOUNDS);
+    return;
+  }
   int L = __ldg(p.seq_lens + b);
   const int64_t cap = static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size;
   if (L < n || L > cap) {  // the chunk must lie inside the sequence and its table
     if (tid == 0) record_error(KV_ERR_DEVICE_BOUNDS);
+    if (L > cap) L = static_cast<int>(cap);
     if (L < n) return;
-    L = static_cast<int>(cap);
   }
   const int ctx = L - n, kvh = h / p.group;
   const int g = lane >> 2, t2 = (lane & 3) * 2;
@@ -242,6 +254,353 @@ cudaError_t launch_prefill(const PrefillParams& p, int head_dim, int max_query_l
   return cudaGetLastError();
 }
 
+
+// ---------------------------------------------------------------------------
+// Tensor-core (tcgen05) kernel, used when block_size divides 128 and is a
+// multiple of 16.
+//
+// One CTA per 128 query rows.  With group G a multiple of a power of two HG
+// (HG = the largest power of two dividing G, at most 8), the rows are HG
+// query heads of one kv head times 128 / HG chunk tokens (row r = token
+// r / HG, head r % HG), so every K/V tile serves all the tile's heads.  Key
+// tiles hold 128 positions.
+//   warp 5: TMA producer -- Q once, then each key tile's K and V, one box per
+//     (block, 64-dim slab), through the block table, into a two-stage ring;
+//   warp 4: owns 512 tensor-memory columns; one lane issues the MMAs:
+//     S_j = Q K_j^T (M 128, N 128, K head_dim) into one of two S buffers,
+//     one tile ahead, and O_j = P_j V_j (M 128, N head_dim, K 128) into the
+//     PV buffer once P_j is in shared memory;
+//   warps 0-3: one thread per row: read its S row from tensor memory, mask
+//     keys past the row's position, keep the running max and sum in the exp2
+//     domain, write P (rounded to the q dtype) to a 128-byte-swizzled shared
+//     tile, and accumulate O_j into fp32 registers with the rescale factor.
+// Slots past the last key of the last tile (the tail of its last block and
+// blocks never loaded) are zeroed in the V tile before P V reads it, so a
+// sentinel there cannot reach the output.
+
+constexpr int kTcRows = 128;     // MMA M: query rows per CTA
+constexpr int kTcKeys = 128;     // keys per tile: N of S, K of P V
+constexpr int kTcStages = 2;     // K/V ring depth
+constexpr int kTcThreads = 192;  // warps 0-3 softmax, 4 MMA + tensor memory, 5 TMA
+constexpr uint32_t kTcCols = 512;
+
+template <int D>
+struct TcLayout {
+  static constexpr int kSlab = 128 * 128;           // one 64-column slab of 128 rows
+  static constexpr int kQ = (D / 64) * kSlab;       // Q tile
+  static constexpr int kKV = (D / 64) * kSlab;      // K or V tile
+  static constexpr int kP = (kTcKeys / 64) * kSlab;  // P tile
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = kQ;                 // stage s: K at + 2 s kKV, V at + (2 s + 1) kKV
+  static constexpr int kOffP = kOffKV + kTcStages * 2 * kKV;
+  static constexpr int kOffBar = kOffP + kP;
+  static constexpr int kBytes = kOffBar + 128;
+  static constexpr int kSmem = kBytes + 1024;  // slack for 1024-byte alignment
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+  using Lay = TcLayout<D>;
+  constexpr int kSlabs = D / 64;
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  extern __shared__ uint8_t tc_smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar_q = reinterpret_cast<uint64_t*>(sm + Lay::kOffBar);
+  uint64_t* bar_full = bar_q + 1;               // [kTcStages] K/V tile landed
+  uint64_t* bar_empty = bar_full + kTcStages;   // [kTcStages] P V of the tile done
+  uint64_t* bar_s = bar_empty + kTcStages;      // [2] S buffer written
+  uint64_t* bar_p = bar_s + 2;                  // P written (128 arrivals)
+  uint64_t* bar_pv = bar_p + 1;                 // P V written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_pv + 1);
+
+  const int hg = 1 << p.hg_log2, tpt = kTcRows >> p.hg_log2;
+  const int qt = gridDim.x - 1 - blockIdx.x;  // tiles with the most keys start first
+  const int h0 = blockIdx.y * hg, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qs = __ldg(p.query_start + b), n = __ldg(p.query_start + b + 1) - qs;
+  if (n <= 0 || qt * tpt >= n) return;
+  int L = __ldg(p.seq_lens + b);
+  const int64_t cap = static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size;
+  if (L < n || qs < 0 || qs + n > p.num_tokens) {  // the chunk must lie inside its sequence and in q
+    if (threadIdx.x == 0) record_error(KV_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  if (L > cap) {
+    if (threadIdx.x == 0) record_error(KV_ERR_DEVICE_BOUNDS);
+    L = static_cast<int>(cap);
+    if (L < n) return;
+  }
+  const int ctx = L - n, kvh = h0 / p.group;
+  const int tok0 = qt * tpt, rows_here = min(n - tok0, tpt);
+  const int nkeys = min(ctx + tok0 + rows_here, L);
+  const int ntiles = (nkeys + kTcKeys - 1) / kTcKeys;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(bar_full + s, 1);
+      mbar_init(bar_empty + s, 1);
+    }
+    mbar_init(bar_s, 1);
+    mbar_init(bar_s + 1, 1);
+    mbar_init(bar_p, 4 * 32);
+    mbar_init(bar_pv, 1);
+    fence_mbar_init();
+  }
+  if (warp == 4) tc::alloc(tmem_slot, kTcCols);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tPV = tmem + 2 * kTcKeys;
+
+  if (warp == 5) {
+    if (lane == 0) {
+      // ---- TMA producer
+      prefetch_tensormap(&tmQ);
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      mbar_arrive_expect_tx(bar_q, kSlabs * kTcRows * 128);
+      for (int s = 0; s < kSlabs; ++s)
+        tma_load_3d(sm + Lay::kOffQ + s * Lay::kSlab, &tmQ, bar_q, s * 64, h0, qs + tok0);
+      const int32_t* table = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
+      const int bs = p.block_size;
+      bool ok = true;
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int st = j % kTcStages;
+        if (j >= kTcStages) ok = mbar_wait_bounded(bar_empty + st, ((j / kTcStages) - 1) & 1);
+        if (!ok) break;
+        const int k0 = j * kTcKeys, k1 = min(k0 + kTcKeys, nkeys);
+        const int blk0 = k0 / bs, blk1 = (k1 + bs - 1) / bs;
+        mbar_arrive_expect_tx(bar_full + st, static_cast<uint32_t>((blk1 - blk0) * bs * D * 2 * 2));
+        uint8_t* kt = sm + Lay::kOffKV + st * 2 * Lay::kKV;
+        for (int bi = blk0; bi < blk1; ++bi) {
+          int pb = __ldg(table + bi);
+          if (pb < 0 || pb >= p.num_blocks) {
+            record_error(KV_ERR_DEVICE_BOUNDS);
+            pb = 0;
+          }
+          const int r = (bi - blk0) * bs;
+          for (int s = 0; s < kSlabs; ++s) {
+            tma_load_3d(kt + s * Lay::kSlab + r * 128, &tmK, bar_full + st, s * 64, kvh, pb * bs);
+            tma_load_3d(kt + Lay::kKV + s * Lay::kSlab + r * 128, &tmV, bar_full + st, s * 64, kvh, pb * bs);
+          }
+        }
+      }
+      // every stage's last P V has completed (no copy or commit in flight at exit)
+      for (int j = max(0, ntiles - kTcStages); j < ntiles; ++j)
+        mbar_wait_bounded(bar_empty + (j % kTcStages), (j / kTcStages) & 1);
+    }
+  } else if (warp == 4) {
+    if (lane == 0) {
+      // ---- MMA issue
+      constexpr uint32_t idS = tc::idesc_f16(kBf16, kTcRows, kTcKeys, false);
+      constexpr uint32_t idPV = tc::idesc_f16(kBf16, kTcRows, D, true);
+      const uint32_t aQ = smem_u32(sm + Lay::kOffQ), aP = smem_u32(sm + Lay::kOffP);
+      bool ok = mbar_wait_bounded(bar_q, 0);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % kTcStages;
+        if (!mbar_wait_bounded(bar_full + st, (j / kTcStages) & 1)) return false;
+        tc::fence_after();
+        const uint32_t kb = smem_u32(sm + Lay::kOffKV + st * 2 * Lay::kKV);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * Lay::kSlab + (kk & 3) * 32;  // 64-dim slab, 16-dim step inside it
+          tc::mma_f16(tmem + (j & 1) * kTcKeys, tc::sdesc_sw128(aQ + off, 16, 1024),
+                      tc::sdesc_sw128(kb + off, 16, 1024), idS, kk > 0);
+        }
+        tc::commit(bar_s + (j & 1));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; j < ntiles && ok; ++j) {
+        if (j + 1 < ntiles && !issue_s(j + 1)) break;
+        if (!mbar_wait_bounded(bar_p, j & 1)) break;
+        tc::fence_after();
+        const uint32_t vb = smem_u32(sm + Lay::kOffKV + (j % kTcStages) * 2 * Lay::kKV + Lay::kKV);
+#pragma unroll
+        for (int kk = 0; kk < kTcKeys / 16; ++kk)
+          tc::mma_f16(tPV, tc::sdesc_sw128(aP + (kk >> 2) * Lay::kSlab + (kk & 3) * 32, 16, 1024),
+                      tc::sdesc_sw128(vb + kk * 16 * 128, Lay::kSlab, 1024), idPV, kk > 0);
+        tc::commit(bar_pv);
+        tc::commit(bar_empty + (j % kTcStages));
+      }
+    }
+  } else {
+    // ---- softmax: thread = row
+    const int r = threadIdx.x;  // 0..127
+    const int tok = r >> p.hg_log2, hh = r & (hg - 1);
+    const int lim_abs = min(ctx + tok0 + tok, nkeys - 1);  // last key this row sees
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const float c2 = p.scale_log2;
+    float o[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) o[i] = 0.f;
+    float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
+    uint8_t* pt = sm + Lay::kOffP;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      if (!mbar_wait_bounded(bar_s + (j & 1), (j >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after();
+      const uint32_t ts = tmem + lane_base + (j & 1) * kTcKeys;
+      const int lim = lim_abs - j * kTcKeys;  // columns c <= lim are keys of this row
+      float mx = -INFINITY;
+#pragma unroll
+      for (int cc = 0; cc < kTcKeys / 32; ++cc) {
+        uint32_t v[32];
+        tc::ld32(ts + cc * 32, v);
+        tc::wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (cc * 32 + i <= lim) mx = fmaxf(mx, __uint_as_float(v[i]) * c2);
+      }
+      const float m_new = fmaxf(m, mx);
+      const float alpha = fast_exp2(m - m_new);
+      if (j > 0) {  // O += the previous tile's P V, rescaled to its max
+        if (!mbar_wait_bounded(bar_pv, (j - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+#pragma unroll
+        for (int dc = 0; dc < D / 32; ++dc) {
+          uint32_t v[32];
+          tc::ld32(tmem + lane_base + 2 * kTcKeys + dc * 32, v);
+          tc::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[dc * 32 + i] = fmaf(o[dc * 32 + i], alpha_prev, __uint_as_float(v[i]));
+        }
+      }
+      if (j == ntiles - 1 && (nkeys % kTcKeys) != 0) {
+        // zero V rows past the last key (tail slots and blocks never loaded)
+        const int st = j % kTcStages;
+        if (!mbar_wait_bounded(bar_full + st, (j / kTcStages) & 1)) {
+          ok = false;
+          break;
+        }
+        if (r >= nkeys - j * kTcKeys) {
+          uint8_t* vrow = sm + Lay::kOffKV + st * 2 * Lay::kKV + Lay::kKV + r * 128;
+#pragma unroll
+          for (int s = 0; s < kSlabs; ++s)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + s * Lay::kSlab + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      // P = exp2(S * c2 - m_new), rounded to T, into the swizzled P tile
+      float sum = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < kTcKeys / 32; ++cc) {
+        uint32_t v[32];
+        tc::ld32(ts + cc * 32, v);
+        tc::wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float p0 = cc * 32 + i <= lim ? fast_exp2(fmaf(__uint_as_float(v[i]), c2, -m_new)) : 0.f;
+          const float p1 = cc * 32 + i + 1 <= lim ? fast_exp2(fmaf(__uint_as_float(v[i + 1]), c2, -m_new)) : 0.f;
+          sum += p0 + p1;
+          pk[i / 2] = Mma<T>::pack(p0, p1);
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int chunk = cc * 4 + q4;  // 16-byte chunk of the row: 8 keys
+          uint8_t* dst = pt + (chunk >> 3) * Lay::kSlab + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[q4 * 4], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
+        }
+      }
+      l = fmaf(l, alpha, sum);
+      m = m_new;
+      alpha_prev = alpha;
+      fence_proxy_async_smem();  // P is read by the tensor cores
+      tc::fence_before();
+      mbar_arrive(bar_p);
+    }
+    if (ok && mbar_wait_bounded(bar_pv, (ntiles - 1) & 1)) {
+      tc::fence_after();
+#pragma unroll
+      for (int dc = 0; dc < D / 32; ++dc) {
+        uint32_t v[32];
+        tc::ld32(tmem + lane_base + 2 * kTcKeys + dc * 32, v);
+        tc::wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[dc * 32 + i] = fmaf(o[dc * 32 + i], alpha_prev, __uint_as_float(v[i]));
+      }
+      if (tok < rows_here) {
+        const float inv = l > 0.f ? __fdiv_rn(1.f, l) : 0.f;
+        T* orow = static_cast<T*>(p.out) +
+                  (static_cast<int64_t>(qs + tok0 + tok) * p.num_heads + h0 + hh) * D;
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c)
+          *reinterpret_cast<uint4*>(orow + c * 8) =
+              make_uint4(Mma<T>::pack(o[c * 8] * inv, o[c * 8 + 1] * inv), Mma<T>::pack(o[c * 8 + 2] * inv, o[c * 8 + 3] * inv),
+                         Mma<T>::pack(o[c * 8 + 4] * inv, o[c * 8 + 5] * inv), Mma<T>::pack(o[c * 8 + 6] * inv, o[c * 8 + 7] * inv));
+      }
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    __syncwarp();
+    tc::fence_after();
+    tc::dealloc(tmem, kTcCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// A 3-D tensor {n0, n1, n2} of 16-bit elements (dim 0 contiguous, dim 1
+// `n0` apart, dim 2 `n0 * n1` apart) with 128-byte-swizzled boxes
+// {64, box1, box2}.
+bool tc_map(const void* base, int64_t n0, int64_t n1, int64_t n2, int box1, int box2, CUtensorMap* out) {
+  auto fn = tc_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(n0), static_cast<cuuint64_t>(n1), static_cast<cuuint64_t>(n2)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(n0) * 2, static_cast<cuuint64_t>(n0 * n1) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box1), static_cast<cuuint32_t>(box2)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tc_supported(int block_size) { return block_size >= 16 && block_size % 16 == 0 && kTcKeys % block_size == 0; }
+
+template <typename T, int D>
+cudaError_t launch_prefill_tc(const PrefillParams& p, int max_query_len, const CUtensorMap& mq, const CUtensorMap& mk,
+                              const CUtensorMap& mv, cudaStream_t st) {
+  constexpr int kSmem = TcLayout<D>::kSmem;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(prefill_tc_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const int tpt = kTcRows >> p.hg_log2;
+  const dim3 grid((max_query_len + tpt - 1) / tpt, p.num_heads >> p.hg_log2, p.num_seqs);
+  prefill_tc_kernel<T, D><<<grid, kTcThreads, kSmem, st>>>(p, mq, mk, mv);
+  return cudaGetLastError();
+}
+
 bool aligned16(const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; }
 
 }  // namespace
@@ -251,7 +610,8 @@ using namespace pagedkv;
 
 extern "C" int paged_prefill_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
                                        const int32_t* block_tables, const int32_t* seq_lens,
-                                       const int32_t* query_start_loc, int32_t num_seqs, int32_t num_heads,
+                                       const int32_t* query_start_loc, int64_t num_query_tokens, int32_t num_seqs,
+                                       int32_t num_heads,
                                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t num_blocks,
                                        int32_t max_blocks_per_seq, int32_t max_query_len, float scale, int dtype,
                                        void* stream) {
@@ -261,7 +621,8 @@ extern "C" int paged_prefill_attention(void* out, const void* q, const void* k_c
     return KV_ERR_INVALID_ARG;
   if (num_blocks > INT32_MAX / block_size || num_heads > 65535 || num_seqs > 65535) return KV_ERR_INVALID_ARG;
   if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return KV_ERR_INVALID_ARG;
-  if (num_seqs == 0 || max_query_len == 0) return KV_OK;
+  if (num_query_tokens < 0 || num_query_tokens > INT32_MAX) return KV_ERR_INVALID_ARG;
+  if (num_seqs == 0 || max_query_len == 0 || num_query_tokens == 0) return KV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start_loc) return KV_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return KV_ERR_INVALID_ARG;
   PrefillParams p{};
@@ -280,9 +641,28 @@ extern "C" int paged_prefill_attention(void* out, const void* q, const void* k_c
   p.num_blocks = num_blocks;
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.num_tokens = num_query_tokens;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = dtype == KV_DTYPE_F16 ? launch_prefill<__half>(p, head_dim, max_query_len, st)
-                                              : launch_prefill<__nv_bfloat16>(p, head_dim, max_query_len, st);
+  if (!tc_supported(block_size)) {
+    const cudaError_t e = dtype == KV_DTYPE_F16 ? launch_prefill<__half>(p, head_dim, max_query_len, st)
+                                                : launch_prefill<__nv_bfloat16>(p, head_dim, max_query_len, st);
+    return cuda_status(e);
+  }
+  // tensor-core kernel: HG = the largest power of two (at most 8) dividing the group
+  while (p.hg_log2 < 3 && p.group % (2 << p.hg_log2) == 0) ++p.hg_log2;
+  CUtensorMap mq, mk, mv;
+  const int64_t rows = num_blocks * block_size;
+  if (!tc_map(q, head_dim, num_heads, num_query_tokens, 1 << p.hg_log2, kTcRows >> p.hg_log2, &mq) ||
+      !tc_map(k_cache, head_dim, num_kv_heads, rows, 1, block_size, &mk) ||
+      !tc_map(v_cache, head_dim, num_kv_heads, rows, 1, block_size, &mv))
+    return cuda_status(cudaErrorInvalidValue, "cuTensorMapEncodeTiled failed");
+  cudaError_t e;
+  if (dtype == KV_DTYPE_F16)
+    e = head_dim == 64 ? launch_prefill_tc<__half, 64>(p, max_query_len, mq, mk, mv, st)
+                       : launch_prefill_tc<__half, 128>(p, max_query_len, mq, mk, mv, st);
+  else
+    e = head_dim == 64 ? launch_prefill_tc<__nv_bfloat16, 64>(p, max_query_len, mq, mk, mv, st)
+                       : launch_prefill_tc<__nv_bfloat16, 128>(p, max_query_len, mq, mk, mv, st);
   return cuda_status(e);
 }
 

@@ -205,8 +205,8 @@ def paged_prefill_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.T
     if block_tables.dim() != 2 or block_tables.shape[0] != B or query_start_loc.numel() != B + 1:
         raise KVError(1, "block_tables [B, max_blocks], seq_lens [B], query_start_loc [B + 1]")
     check(lib().paged_prefill_attention(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                                        block_tables.data_ptr(), seq_lens.data_ptr(), query_start_loc.data_ptr(), B,
-                                        hq, hkv, d, bs, nb, block_tables.shape[1], max_query_len, float(scale),
+                                        block_tables.data_ptr(), seq_lens.data_ptr(), query_start_loc.data_ptr(), T,
+                                        B, hq, hkv, d, bs, nb, block_tables.shape[1], max_query_len, float(scale),
                                         dtype_code(q.dtype), _stream_ptr(stream)), "paged_prefill_attention")
     return out
 

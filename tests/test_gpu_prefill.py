@@ -5,9 +5,12 @@ last n positions; all L = ctx + n tokens are written through the cache
 write first).  Every chunk row must match the float64 oracle
 (oracle.attention.chunked_prefill_attention) on the sequence's logical K/V,
 within the dtype's tolerance: chunks with and without history, chunks
-crossing 64-token query tiles and 32-token key tiles, one-token chunks
-(decode), GQA ratios 1 to 8, head_dim 64 and 128, block sizes 16 and 32,
-and the mixed-batch workload's 4096-token prefill chunk (sampled rows).
+crossing query tiles and 128-key tiles, one-token chunks (decode), GQA
+ratios 1 to 8 (the tensor-core kernel packs 1, 2, 4 or 8 heads of a group
+into one 128-row tile), head_dim 64 and 128, block sizes 16 to 128 (tcgen05
+kernel) and 4 and 8 (mma.sync kernel), and the mixed-batch workload's
+4096-token prefill chunk (sampled rows).  Unused cache slots hold a NaN
+sentinel, so a tail slot that reached the output would show.
 """
 
 import math
@@ -74,6 +77,10 @@ CASES = [
     ("f16", 14, 2, 64, 16, [(0, 63), (5, 64), (40, 129), (0, 1)]),
     ("bf16", 32, 8, 128, 32, [(0, 256), (17, 95), (64, 64)]),
     ("f16", 4, 4, 128, 32, [(7, 40), (0, 3), (500, 70)]),
+    ("bf16", 16, 2, 128, 64, [(0, 300), (257, 129), (1000, 17)]),
+    ("f16", 4, 2, 64, 128, [(5, 250), (128, 128), (0, 1)]),
+    ("bf16", 8, 2, 128, 8, [(0, 70), (20, 45), (0, 1)]),
+    ("f16", 6, 3, 64, 4, [(3, 33), (0, 9)]),
 ]
 
 
@@ -109,3 +116,19 @@ def test_prefill_chunk_longer_than_sequence_is_reported():
     pk.paged_prefill_attention(out, q, kc, vc, tables, lens, qsl, 0.125, 12)
     assert pk.device_error() == 8
     assert torch.all(out == 7.0)                                   # nothing written
+
+
+def test_prefill_chunk_past_the_query_rows_is_reported():
+    dev = torch.device("cuda")
+    nb, bs, hkv, d, hq = 8, 16, 2, 64, 4
+    kc = torch.zeros(nb, bs, hkv, d, dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    tables = torch.tensor([[0, 1, 2, -1]], dtype=torch.int32, device=dev)
+    lens = torch.tensor([40], dtype=torch.int32, device=dev)
+    qsl = torch.tensor([0, 20], dtype=torch.int32, device=dev)    # 20 chunk rows, q holds 12
+    q = torch.randn(12, hq, d, device=dev).bfloat16()
+    out = torch.full((12, hq, d), 7.0, dtype=torch.bfloat16, device=dev)
+    pk.device_error()
+    pk.paged_prefill_attention(out, q, kc, vc, tables, lens, qsl, 0.125, 20)
+    assert pk.device_error() == 8
+    assert torch.all(out == 7.0)
