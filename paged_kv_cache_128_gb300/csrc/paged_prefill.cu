@@ -264,16 +264,20 @@ cudaError_t launch_prefill(const PrefillParams& p, int head_dim, int max_query_l
 // query heads of one kv head times 128 / HG chunk tokens (row r = token
 // r / HG, head r % HG), so every K/V tile serves all the tile's heads.  Key
 // tiles hold 128 positions.
-//   warp 5: TMA producer -- Q once, then each key tile's K and V, one box per
-//     (block, 64-dim slab), through the block table, into a two-stage ring;
-//   warp 4: owns 512 tensor-memory columns; one lane issues the MMAs:
+//   warp 17: TMA producer -- Q once, then each key tile's K and V, one box
+//     per (block, 64-dim slab), through the block table, into a two-stage ring;
+//   warp 16: owns 512 tensor-memory columns; one lane issues the MMAs:
 //     S_j = Q K_j^T (M 128, N 128, K head_dim) into one of two S buffers,
 //     one tile ahead, and O_j = P_j V_j (M 128, N head_dim, K 128) into the
 //     PV buffer once P_j is in shared memory;
-//   warps 0-3: one thread per row: read its S row from tensor memory, mask
-//     keys past the row's position, keep the running max and sum in the exp2
-//     domain, write P (rounded to the q dtype) to a 128-byte-swizzled shared
-//     tile, and accumulate O_j into fp32 registers with the rescale factor.
+//   warps 0-15: four threads per row (warp w reads tensor-memory lanes
+//     32 (w % 4) .. + 31, column group w / 4): each reads its 32 S columns,
+//     masks keys past the row's position, exchanges its partial max with the
+//     row's other three threads through shared memory, keeps the running max
+//     and its partial sum in the exp2 domain, writes its 32 P values (rounded
+//     to the q dtype) to a 128-byte-swizzled shared tile, and accumulates its
+//     head_dim / 4 columns of O_j into fp32 registers with the rescale
+//     factor.  The partial sums are added once, at the end.
 // Slots past the last key of the last tile (the tail of its last block and
 // blocks never loaded) are zeroed in the V tile before P V reads it, so a
 // sentinel there cannot reach the output.
@@ -281,7 +285,10 @@ cudaError_t launch_prefill(const PrefillParams& p, int head_dim, int max_query_l
 constexpr int kTcRows = 128;     // MMA M: query rows per CTA
 constexpr int kTcKeys = 128;     // keys per tile: N of S, K of P V
 constexpr int kTcStages = 2;     // K/V ring depth
-constexpr int kTcThreads = 192;  // warps 0-3 softmax, 4 MMA + tensor memory, 5 TMA
+constexpr int kTcSplit = 4;                // threads per row in the softmax
+constexpr int kTcSoftWarps = 4 * kTcSplit;  // warps 0-15
+constexpr int kTcMmaWarp = kTcSoftWarps, kTcTmaWarp = kTcSoftWarps + 1;
+constexpr int kTcThreads = 32 * (kTcSoftWarps + 2);
 constexpr uint32_t kTcCols = 512;
 
 template <int D>
@@ -293,7 +300,8 @@ struct TcLayout {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kQ;                 // stage s: K at + 2 s kKV, V at + (2 s + 1) kKV
   static constexpr int kOffP = kOffKV + kTcStages * 2 * kKV;
-  static constexpr int kOffBar = kOffP + kP;
+  static constexpr int kOffX = kOffP + kP;           // [2][kTcSplit][128] partial maxima, then [kTcSplit][128] sums
+  static constexpr int kOffBar = kOffX + 3 * kTcSplit * 128 * 4;
   static constexpr int kBytes = kOffBar + 128;
   static constexpr int kSmem = kBytes + 1024;  // slack for 1024-byte alignment
 };
@@ -308,9 +316,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar_q = reinterpret_cast<uint64_t*>(sm + Lay::kOffBar);
-  uint64_t* bar_full = bar_q + 1;               // [kTcStages] K/V tile landed
-  uint64_t* bar_empty = bar_full + kTcStages;   // [kTcStages] P V of the tile done
-  uint64_t* bar_s = bar_empty + kTcStages;      // [2] S buffer written
+  uint64_t* bar_kfull = bar_q + 1;                // [kTcStages] K tile landed
+  uint64_t* bar_vfull = bar_kfull + kTcStages;    // [kTcStages] V tile landed
+  uint64_t* bar_kempty = bar_vfull + kTcStages;   // [kTcStages] S of the tile done
+  uint64_t* bar_vempty = bar_kempty + kTcStages;  // [kTcStages] P V of the tile done
+  uint64_t* bar_s = bar_vempty + kTcStages;       // [2] S buffer written
   uint64_t* bar_p = bar_s + 2;                  // P written (128 arrivals)
   uint64_t* bar_pv = bar_p + 1;                 // P V written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_pv + 1);
@@ -340,23 +350,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
     for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(bar_full + s, 1);
-      mbar_init(bar_empty + s, 1);
+      mbar_init(bar_kfull + s, 1);
+      mbar_init(bar_vfull + s, 1);
+      mbar_init(bar_kempty + s, 1);
+      mbar_init(bar_vempty + s, 1);
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_s + 1, 1);
-    mbar_init(bar_p, 4 * 32);
+    mbar_init(bar_p, kTcSoftWarps * 32);
     mbar_init(bar_pv, 1);
     fence_mbar_init();
   }
-  if (warp == 4) tc::alloc(tmem_slot, kTcCols);
+  if (warp == kTcMmaWarp) tc::alloc(tmem_slot, kTcCols);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tPV = tmem + 2 * kTcKeys;
 
-  if (warp == 5) {
+  if (warp == kTcTmaWarp) {
     if (lane == 0) {
       // ---- TMA producer
       prefetch_tensormap(&tmQ);
@@ -367,15 +379,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_load_3d(sm + Lay::kOffQ + s * Lay::kSlab, &tmQ, bar_q, s * 64, h0, qs + tok0);
       const int32_t* table = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
       const int bs = p.block_size;
-      bool ok = true;
-      for (int j = 0; j < ntiles && ok; ++j) {
+      // K (V) of tile j into stage j % kTcStages once S (P V) of tile
+      // j - kTcStages is done; K runs one tile ahead of V, since S of a tile
+      // completes before its P V
+      auto load = [&](int j, bool is_v) -> bool {
         const int st = j % kTcStages;
-        if (j >= kTcStages) ok = mbar_wait_bounded(bar_empty + st, ((j / kTcStages) - 1) & 1);
-        if (!ok) break;
+        uint64_t* full = (is_v ? bar_vfull : bar_kfull) + st;
+        if (j >= kTcStages &&
+            !mbar_wait_bounded((is_v ? bar_vempty : bar_kempty) + st, ((j / kTcStages) - 1) & 1))
+          return false;
         const int k0 = j * kTcKeys, k1 = min(k0 + kTcKeys, nkeys);
         const int blk0 = k0 / bs, blk1 = (k1 + bs - 1) / bs;
-        mbar_arrive_expect_tx(bar_full + st, static_cast<uint32_t>((blk1 - blk0) * bs * D * 2 * 2));
-        uint8_t* kt = sm + Lay::kOffKV + st * 2 * Lay::kKV;
+        mbar_arrive_expect_tx(full, static_cast<uint32_t>((blk1 - blk0) * bs * D * 2));
+        uint8_t* dst = sm + Lay::kOffKV + (2 * st + (is_v ? 1 : 0)) * Lay::kKV;
+        const CUtensorMap* map = is_v ? &tmV : &tmK;
         for (int bi = blk0; bi < blk1; ++bi) {
           int pb = __ldg(table + bi);
           if (pb < 0 || pb >= p.num_blocks) {
@@ -383,17 +400,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             pb = 0;
           }
           const int r = (bi - blk0) * bs;
-          for (int s = 0; s < kSlabs; ++s) {
-            tma_load_3d(kt + s * Lay::kSlab + r * 128, &tmK, bar_full + st, s * 64, kvh, pb * bs);
-            tma_load_3d(kt + Lay::kKV + s * Lay::kSlab + r * 128, &tmV, bar_full + st, s * 64, kvh, pb * bs);
-          }
+          for (int s = 0; s < kSlabs; ++s) tma_load_3d(dst + s * Lay::kSlab + r * 128, map, full, s * 64, kvh, pb * bs);
         }
+        return true;
+      };
+      bool ok = load(0, false);
+      for (int j = 0; j < ntiles && ok; ++j) {
+        if (j + 1 < ntiles) ok = load(j + 1, false);
+        if (ok) ok = load(j, true);
       }
-      // every stage's last P V has completed (no copy or commit in flight at exit)
-      for (int j = max(0, ntiles - kTcStages); j < ntiles; ++j)
-        mbar_wait_bounded(bar_empty + (j % kTcStages), (j / kTcStages) & 1);
+      // every stage's last S and P V have completed (no copy or commit in flight at exit)
+      for (int j = max(0, ntiles - kTcStages); j < ntiles; ++j) {
+        mbar_wait_bounded(bar_kempty + (j % kTcStages), (j / kTcStages) & 1);
+        mbar_wait_bounded(bar_vempty + (j % kTcStages), (j / kTcStages) & 1);
+      }
     }
-  } else if (warp == 4) {
+  } else if (warp == kTcMmaWarp) {
     if (lane == 0) {
       // ---- MMA issue
       constexpr uint32_t idS = tc::idesc_f16(kBf16, kTcRows, kTcKeys, false);
@@ -402,7 +424,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = mbar_wait_bounded(bar_q, 0);
       auto issue_s = [&](int j) -> bool {
         const int st = j % kTcStages;
-        if (!mbar_wait_bounded(bar_full + st, (j / kTcStages) & 1)) return false;
+        if (!mbar_wait_bounded(bar_kfull + st, (j / kTcStages) & 1)) return false;
         tc::fence_after();
         const uint32_t kb = smem_u32(sm + Lay::kOffKV + st * 2 * Lay::kKV);
 #pragma unroll
@@ -412,12 +434,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       tc::sdesc_sw128(kb + off, 16, 1024), idS, kk > 0);
         }
         tc::commit(bar_s + (j & 1));
+        tc::commit(bar_kempty + st);
         return true;
       };
       if (ok) ok = issue_s(0);
       for (int j = 0; j < ntiles && ok; ++j) {
         if (j + 1 < ntiles && !issue_s(j + 1)) break;
         if (!mbar_wait_bounded(bar_p, j & 1)) break;
+        if (!mbar_wait_bounded(bar_vfull + (j % kTcStages), (j / kTcStages) & 1)) break;
         tc::fence_after();
         const uint32_t vb = smem_u32(sm + Lay::kOffKV + (j % kTcStages) * 2 * Lay::kKV + Lay::kKV);
 #pragma unroll
@@ -425,93 +449,87 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::mma_f16(tPV, tc::sdesc_sw128(aP + (kk >> 2) * Lay::kSlab + (kk & 3) * 32, 16, 1024),
                       tc::sdesc_sw128(vb + kk * 16 * 128, Lay::kSlab, 1024), idPV, kk > 0);
         tc::commit(bar_pv);
-        tc::commit(bar_empty + (j % kTcStages));
+        tc::commit(bar_vempty + (j % kTcStages));
       }
     }
   } else {
-    // ---- softmax: thread = row
-    const int r = threadIdx.x;  // 0..127
+    // ---- softmax: four threads per row, 32 S columns and D / 4 O columns each
+    constexpr int kOc = D / kTcSplit;  // O columns of this thread
+    const int quarter = warp & 3, cg = warp >> 2;
+    const int r = quarter * 32 + lane;  // row of the tile
     const int tok = r >> p.hg_log2, hh = r & (hg - 1);
     const int lim_abs = min(ctx + tok0 + tok, nkeys - 1);  // last key this row sees
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c2 = p.scale_log2;
-    float o[D];
+    float* xmax = reinterpret_cast<float*>(sm + Lay::kOffX);  // [2][kTcSplit][128]
+    float* xsum = xmax + 2 * kTcSplit * 128;                   // [kTcSplit][128]
+    float o[kOc];
 #pragma unroll
-    for (int i = 0; i < D; ++i) o[i] = 0.f;
+    for (int i = 0; i < kOc; ++i) o[i] = 0.f;
     float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
     uint8_t* pt = sm + Lay::kOffP;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
-      if (!mbar_wait_bounded(bar_s + (j & 1), (j >> 1) & 1)) {
-        ok = false;
-        break;
-      }
+      // after a timeout (recorded) the remaining waits are skipped, but every
+      // thread still runs every tile, so the named barriers stay matched
+      if (ok && !mbar_wait_bounded(bar_s + (j & 1), (j >> 1) & 1)) ok = false;
       tc::fence_after();
-      const uint32_t ts = tmem + lane_base + (j & 1) * kTcKeys;
-      const int lim = lim_abs - j * kTcKeys;  // columns c <= lim are keys of this row
+      uint32_t v[32];
+      tc::ld32(trow + (j & 1) * kTcKeys + cg * 32, v);
+      tc::wait_ld();
+      const int lim = lim_abs - j * kTcKeys - cg * 32;  // columns i <= lim of this group are keys of the row
       float mx = -INFINITY;
 #pragma unroll
-      for (int cc = 0; cc < kTcKeys / 32; ++cc) {
-        uint32_t v[32];
-        tc::ld32(ts + cc * 32, v);
-        tc::wait_ld();
+      for (int i = 0; i < 32; ++i)
+        if (i <= lim) mx = fmaxf(mx, __uint_as_float(v[i]) * c2);
+      float* xm = xmax + (j & 1) * kTcSplit * 128;
+      xm[cg * 128 + r] = mx;
+      named_barrier_sync(1, kTcSoftWarps * 32);
+      float m_new = m;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (cc * 32 + i <= lim) mx = fmaxf(mx, __uint_as_float(v[i]) * c2);
-      }
-      const float m_new = fmaxf(m, mx);
+      for (int g = 0; g < kTcSplit; ++g) m_new = fmaxf(m_new, xm[g * 128 + r]);
       const float alpha = fast_exp2(m - m_new);
-      if (j > 0) {  // O += the previous tile's P V, rescaled to its max
-        if (!mbar_wait_bounded(bar_pv, (j - 1) & 1)) {
-          ok = false;
-          break;
-        }
+      if (j > 0) {  // the previous tile's P V has read the P tile and written the PV buffer
+        if (ok && !mbar_wait_bounded(bar_pv, (j - 1) & 1)) ok = false;
         tc::fence_after();
-#pragma unroll
-        for (int dc = 0; dc < D / 32; ++dc) {
-          uint32_t v[32];
-          tc::ld32(tmem + lane_base + 2 * kTcKeys + dc * 32, v);
-          tc::wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[dc * 32 + i] = fmaf(o[dc * 32 + i], alpha_prev, __uint_as_float(v[i]));
-        }
       }
       if (j == ntiles - 1 && (nkeys % kTcKeys) != 0) {
         // zero V rows past the last key (tail slots and blocks never loaded)
         const int st = j % kTcStages;
-        if (!mbar_wait_bounded(bar_full + st, (j / kTcStages) & 1)) {
-          ok = false;
-          break;
-        }
+        if (ok && !mbar_wait_bounded(bar_vfull + st, (j / kTcStages) & 1)) ok = false;
         if (r >= nkeys - j * kTcKeys) {
           uint8_t* vrow = sm + Lay::kOffKV + st * 2 * Lay::kKV + Lay::kKV + r * 128;
 #pragma unroll
           for (int s = 0; s < kSlabs; ++s)
 #pragma unroll
-            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + s * Lay::kSlab + c * 16) = make_uint4(0, 0, 0, 0);
+            for (int c = 0; c < 8 / kTcSplit; ++c)
+              *reinterpret_cast<uint4*>(vrow + s * Lay::kSlab + (cg * (8 / kTcSplit) + c) * 16) = make_uint4(0, 0, 0, 0);
         }
       }
       // P = exp2(S * c2 - m_new), rounded to T, into the swizzled P tile
       float sum = 0.f;
 #pragma unroll
-      for (int cc = 0; cc < kTcKeys / 32; ++cc) {
-        uint32_t v[32];
-        tc::ld32(ts + cc * 32, v);
-        tc::wait_ld();
-        uint32_t pk[16];
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t pk[4];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float p0 = cc * 32 + i <= lim ? fast_exp2(fmaf(__uint_as_float(v[i]), c2, -m_new)) : 0.f;
-          const float p1 = cc * 32 + i + 1 <= lim ? fast_exp2(fmaf(__uint_as_float(v[i + 1]), c2, -m_new)) : 0.f;
+        for (int e = 0; e < 4; ++e) {
+          const int i = q4 * 8 + e * 2;
+          const float p0 = i <= lim ? fast_exp2(fmaf(__uint_as_float(v[i]), c2, -m_new)) : 0.f;
+          const float p1 = i + 1 <= lim ? fast_exp2(fmaf(__uint_as_float(v[i + 1]), c2, -m_new)) : 0.f;
           sum += p0 + p1;
-          pk[i / 2] = Mma<T>::pack(p0, p1);
+          pk[e] = Mma<T>::pack(p0, p1);
         }
+        const int chunk = cg * 4 + q4;  // 16-byte chunk of the row: 8 keys
+        uint8_t* dst = pt + (chunk >> 3) * Lay::kSlab + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      if (j > 0) {  // O += the previous tile's P V, rescaled to its max
+        uint32_t w[kOc];
+        if constexpr (kOc == 32) tc::ld32(trow + 2 * kTcKeys + cg * kOc, w);
+        else tc::ld16(trow + 2 * kTcKeys + cg * kOc, w);
+        tc::wait_ld();
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int chunk = cc * 4 + q4;  // 16-byte chunk of the row: 8 keys
-          uint8_t* dst = pt + (chunk >> 3) * Lay::kSlab + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[q4 * 4], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
-        }
+        for (int i = 0; i < kOc; ++i) o[i] = fmaf(o[i], alpha_prev, __uint_as_float(w[i]));
       }
       l = fmaf(l, alpha, sum);
       m = m_new;
@@ -520,31 +538,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::fence_before();
       mbar_arrive(bar_p);
     }
-    if (ok && mbar_wait_bounded(bar_pv, (ntiles - 1) & 1)) {
+    if (ok && !mbar_wait_bounded(bar_pv, (ntiles - 1) & 1)) ok = false;
+    if (ok) {
       tc::fence_after();
+      uint32_t w[kOc];
+      if constexpr (kOc == 32) tc::ld32(trow + 2 * kTcKeys + cg * kOc, w);
+      else tc::ld16(trow + 2 * kTcKeys + cg * kOc, w);
+      tc::wait_ld();
 #pragma unroll
-      for (int dc = 0; dc < D / 32; ++dc) {
-        uint32_t v[32];
-        tc::ld32(tmem + lane_base + 2 * kTcKeys + dc * 32, v);
-        tc::wait_ld();
+      for (int i = 0; i < kOc; ++i) o[i] = fmaf(o[i], alpha_prev, __uint_as_float(w[i]));
+    }
+    // the row's sum: its four partial sums (all relative to the same max)
+    xsum[cg * 128 + r] = l;
+    named_barrier_sync(1, kTcSoftWarps * 32);
+    if (ok) {
+      float lt = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[dc * 32 + i] = fmaf(o[dc * 32 + i], alpha_prev, __uint_as_float(v[i]));
-      }
+      for (int g = 0; g < kTcSplit; ++g) lt += xsum[g * 128 + r];
       if (tok < rows_here) {
-        const float inv = l > 0.f ? __fdiv_rn(1.f, l) : 0.f;
-        T* orow = static_cast<T*>(p.out) +
-                  (static_cast<int64_t>(qs + tok0 + tok) * p.num_heads + h0 + hh) * D;
+        const float inv = lt > 0.f ? __fdiv_rn(1.f, lt) : 0.f;
+        T* orow = static_cast<T*>(p.out) + (static_cast<int64_t>(qs + tok0 + tok) * p.num_heads + h0 + hh) * D +
+                  cg * kOc;
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c)
+        for (int c = 0; c < kOc / 8; ++c)
           *reinterpret_cast<uint4*>(orow + c * 8) =
-              make_uint4(Mma<T>::pack(o[c * 8] * inv, o[c * 8 + 1] * inv), Mma<T>::pack(o[c * 8 + 2] * inv, o[c * 8 + 3] * inv),
-                         Mma<T>::pack(o[c * 8 + 4] * inv, o[c * 8 + 5] * inv), Mma<T>::pack(o[c * 8 + 6] * inv, o[c * 8 + 7] * inv));
+              make_uint4(Mma<T>::pack(o[c * 8] * inv, o[c * 8 + 1] * inv),
+                         Mma<T>::pack(o[c * 8 + 2] * inv, o[c * 8 + 3] * inv),
+                         Mma<T>::pack(o[c * 8 + 4] * inv, o[c * 8 + 5] * inv),
+                         Mma<T>::pack(o[c * 8 + 6] * inv, o[c * 8 + 7] * inv));
       }
     }
   }
   tc::fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kTcMmaWarp) {
     __syncwarp();
     tc::fence_after();
     tc::dealloc(tmem, kTcCols);
