@@ -55,6 +55,11 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="--impl reference: seconds of oracle time for the whole run (steps + warm-up)")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time chunked-prefill attention instead of the decode step: the mixed-batch workload's "
+                         "4096-token prefill chunk, one JSON line per --prefill-context")
+    ap.add_argument("--prefill-context", default="0,2048",
+                    help="--prefill: comma-separated history lengths (tokens already cached per sequence)")
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="only set the workload up and run this many attention calls (L2 flushed before each); "
                          "the small case used under ncu")
@@ -543,8 +548,116 @@ def run_profile_calls(args):
         sys.exit(1)
 
 
+# ------------------------------------------------------ chunked prefill
+
+def prefill_setup(ctx, dev, seed=5):
+    """The mixed-batch workload's prefill chunk (8 new sequences, 4096 tokens
+    split U[256, 768]-like by the workload generator; bf16, Hq 32, Hkv 8,
+    D 128, bs 32), each sequence with ``ctx`` tokens of history before its
+    chunk.  K/V of every position go through the cache write into pool
+    blocks taken in a seeded shuffled order; values N(0, 1)."""
+    import numpy as np
+    import torch
+    import paged_kv_cache_128_gb300 as pk
+    from paged_kv_cache_128_gb300.inputs import make_workload
+    wl = make_workload("mixed_batch_bf16")
+    chunks = [int(n) for n in wl.prefill_lens]
+    lens = [ctx + n for n in chunks]
+    bs, hkv, d, hq = wl.block_size, wl.num_kv_heads, wl.head_dim, wl.num_heads
+    nb = sum(-(-L // bs) for L in lens) + 8
+    rng = np.random.default_rng(seed)
+    mgr = pk.KVBlockManager(nb, bs, rng.permutation(nb).tolist())
+    g = torch.Generator(device=dev).manual_seed(seed)
+    kc = torch.empty(nb, bs, hkv, d, dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    for sid, L in enumerate(lens):
+        slots = torch.from_numpy(mgr.allocate_for_prefill(sid, L)).to(dev)
+        k = torch.randn(L, hkv, d, generator=g, device=dev).to(torch.bfloat16)
+        v = torch.randn(L, hkv, d, generator=g, device=dev).to(torch.bfloat16)
+        pk.reshape_and_cache(k, v, kc, vc, slots)
+    tables, seq_lens = mgr.export(list(range(len(lens))), max(-(-L // bs) for L in lens))
+    qsl = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    T = int(qsl[-1])
+    q = torch.randn(T, hq, d, generator=g, device=dev).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    args = (out, q, kc, vc, torch.from_numpy(tables).to(dev), torch.from_numpy(seq_lens).to(dev),
+            torch.from_numpy(qsl).to(dev), 1.0 / d ** 0.5, max(chunks))
+    # causal work: chunk token t of a sequence attends ctx + t + 1 keys; 4 D
+    # flops per (query head, key): 2 D for q.k and 2 D for p v
+    keys = sum(ctx + t + 1 for n in chunks for t in range(n))
+    return {"args": args, "flops": keys * hq * d * 4, "tokens": T, "seqs": len(chunks), "hq": hq, "hkv": hkv,
+            "d": d, "bs": bs, "kv_bytes": 2 * sum(lens) * hkv * d * 2}
+
+
+def run_prefill(args):
+    """Chunked-prefill attention (one launch per call) on the mixed-batch
+    prefill chunk, L2 flushed before each timed call, events on the launching
+    stream around the launch only (queued behind a GPU-side delay)."""
+    import torch
+    import paged_kv_cache_128_gb300 as pk
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, peak_kind = float(json.load(f)["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
+    except Exception:
+        peak, peak_kind = 1900.0, "fallback"
+    for ctx in [int(c) for c in args.prefill_context.split(",")]:
+        w = prefill_setup(ctx, dev)
+        pk.device_error()
+        if args.profile_calls:
+            for _ in range(args.profile_calls):
+                flush.zero_()
+                pk.paged_prefill_attention(*w["args"])
+            torch.cuda.synchronize()
+            print(json.dumps({"profile_calls": args.profile_calls, "history_tokens": ctx,
+                              "device_error": pk.device_error()}))
+            continue
+        for _ in range(max(args.warmup, 3)):
+            pk.paged_prefill_attention(*w["args"])
+        torch.cuda.synchronize()
+        clocks = ClockSampler(0)
+        clocks.start()
+        ms = []
+        stream = torch.cuda.current_stream()
+        for _ in range(args.steps):
+            flush.zero_()
+            if hasattr(torch.cuda, "_sleep"):
+                torch.cuda._sleep(100000)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            pk.paged_prefill_attention(*w["args"], stream=stream)
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        clk = clocks.stop()
+        t = statistics.fmean(ms) / 1e3
+        tflops = w["flops"] / t / 1e12
+        status = pk.device_error()
+        print(json.dumps({
+            "metric": "chunked-prefill paged attention TFLOP/s (causal flops) at 1 GB300",
+            "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": round(t * 1e3, 5), "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "mixed_batch_bf16 prefill chunk", "sequences": w["seqs"],
+                       "chunk_tokens": w["tokens"], "history_tokens": ctx, "num_heads": w["hq"],
+                       "num_kv_heads": w["hkv"], "head_dim": w["d"], "block_size": w["bs"],
+                       "kv_bytes": w["kv_bytes"], "l2": "flushed before each call"},
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(tflops / peak, 4), "peak_kind": peak_kind, "flops_per_call": w["flops"],
+                         "traffic": None},
+            "gpu_launches": args.steps, "clocks": clk, "device_error": status}))
+        if status:
+            sys.exit(1)
+
+
 def main():
     args = parse_args()
+    if args.prefill:
+        run_prefill(args)
+        return
     if args.profile_calls:
         run_profile_calls(args)
         return

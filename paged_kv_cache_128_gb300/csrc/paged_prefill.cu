@@ -265,19 +265,22 @@ cudaError_t launch_prefill(const PrefillParams& p, int head_dim, int max_query_l
 // r / HG, head r % HG), so every K/V tile serves all the tile's heads.  Key
 // tiles hold 128 positions.
 //   warp 17: TMA producer -- Q once, then each key tile's K and V, one box
-//     per (block, 64-dim slab), through the block table, into a two-stage ring;
+//     per (block, 64-dim slab), through the block table, into two-stage K and
+//     V rings (a K stage is free once its S is done, a V stage once its P V is);
 //   warp 16: owns 512 tensor-memory columns; one lane issues the MMAs:
 //     S_j = Q K_j^T (M 128, N 128, K head_dim) into one of two S buffers,
-//     one tile ahead, and O_j = P_j V_j (M 128, N head_dim, K 128) into the
-//     PV buffer once P_j is in shared memory;
+//     one tile ahead, and O += P_j V_j (M 128, N head_dim, K 128) into the O
+//     columns once P_j is in shared memory;
 //   warps 0-15: four threads per row (warp w reads tensor-memory lanes
 //     32 (w % 4) .. + 31, column group w / 4): each reads its 32 S columns,
 //     masks keys past the row's position, exchanges its partial max with the
-//     row's other three threads through shared memory, keeps the running max
-//     and its partial sum in the exp2 domain, writes its 32 P values (rounded
-//     to the q dtype) to a 128-byte-swizzled shared tile, and accumulates its
-//     head_dim / 4 columns of O_j into fp32 registers with the rescale
-//     factor.  The partial sums are added once, at the end.
+//     row's other three threads through shared memory, and writes its 32 P
+//     values (rounded to the q dtype) to a 128-byte-swizzled shared tile.
+//     P, the partial sums and O are relative to a reference max that moves
+//     only when a tile's max exceeds it by more than 2^8 (then the thread
+//     rescales its partial sum and its head_dim / 4 columns of O in tensor
+//     memory before the next P V); P stays <= 256.  The partial sums are
+//     added once, at the end, and O is read from tensor memory once.
 // Slots past the last key of the last tile (the tail of its last block and
 // blocks never loaded) are zeroed in the V tile before P V reads it, so a
 // sentinel there cannot reach the output.
@@ -296,13 +299,11 @@ struct TcLayout {
   static constexpr int kSlab = 128 * 128;           // one 64-column slab of 128 rows
   static constexpr int kQ = (D / 64) * kSlab;       // Q tile
   static constexpr int kKV = (D / 64) * kSlab;      // K or V tile
-  static constexpr int kP = (kTcKeys / 64) * kSlab;  // P tile
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kQ;                 // stage s: K at + 2 s kKV, V at + (2 s + 1) kKV
-  static constexpr int kOffP = kOffKV + kTcStages * 2 * kKV;
-  static constexpr int kOffX = kOffP + kP;           // [2][kTcSplit][128] partial maxima, then [kTcSplit][128] sums
+  static constexpr int kOffX = kOffKV + kTcStages * 2 * kKV;  // [2][kTcSplit][128] partial maxima, [kTcSplit][128] sums
   static constexpr int kOffBar = kOffX + 3 * kTcSplit * 128 * 4;
-  static constexpr int kBytes = kOffBar + 128;
+  static constexpr int kBytes = kOffBar + 256;
   static constexpr int kSmem = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
@@ -321,9 +322,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* bar_kempty = bar_vfull + kTcStages;   // [kTcStages] S of the tile done
   uint64_t* bar_vempty = bar_kempty + kTcStages;  // [kTcStages] P V of the tile done
   uint64_t* bar_s = bar_vempty + kTcStages;       // [2] S buffer written
-  uint64_t* bar_p = bar_s + 2;                  // P written (128 arrivals)
-  uint64_t* bar_pv = bar_p + 1;                 // P V written
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_pv + 1);
+  uint64_t* bar_p = bar_s + 2;                    // [2] P buffer written (every softmax thread arrives)
+  uint64_t* bar_pv = bar_p + 2;                   // [2] P V from that P buffer done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_pv + 2);
 
   const int hg = 1 << p.hg_log2, tpt = kTcRows >> p.hg_log2;
   const int qt = gridDim.x - 1 - blockIdx.x;  // tiles with the most keys start first
@@ -357,8 +358,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_s + 1, 1);
-    mbar_init(bar_p, kTcSoftWarps * 32);
-    mbar_init(bar_pv, 1);
+    for (int b2 = 0; b2 < 2; ++b2) {
+      mbar_init(bar_p + b2, kTcSoftWarps * 32);
+      mbar_init(bar_pv + b2, 1);
+    }
     fence_mbar_init();
   }
   if (warp == kTcMmaWarp) tc::alloc(tmem_slot, kTcCols);
@@ -366,7 +369,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
+  // tensor memory: S buffers at columns 0 and 128, O at 256, P buffers (two
+  // 16-bit values per column) at 384 and 448
   const uint32_t tPV = tmem + 2 * kTcKeys;
+  const uint32_t tP = tmem + 2 * kTcKeys + 128;
 
   if (warp == kTcTmaWarp) {
     if (lane == 0) {
@@ -420,11 +426,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // ---- MMA issue
       constexpr uint32_t idS = tc::idesc_f16(kBf16, kTcRows, kTcKeys, false);
       constexpr uint32_t idPV = tc::idesc_f16(kBf16, kTcRows, D, true);
-      const uint32_t aQ = smem_u32(sm + Lay::kOffQ), aP = smem_u32(sm + Lay::kOffP);
+      const uint32_t aQ = smem_u32(sm + Lay::kOffQ);
       bool ok = mbar_wait_bounded(bar_q, 0);
-      auto issue_s = [&](int j) -> bool {
+      auto issue_s = [&](int j) {  // K tile j has landed
         const int st = j % kTcStages;
-        if (!mbar_wait_bounded(bar_kfull + st, (j / kTcStages) & 1)) return false;
         tc::fence_after();
         const uint32_t kb = smem_u32(sm + Lay::kOffKV + st * 2 * Lay::kKV);
 #pragma unroll
@@ -435,20 +440,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc::commit(bar_s + (j & 1));
         tc::commit(bar_kempty + st);
-        return true;
       };
-      if (ok) ok = issue_s(0);
+      if (ok) ok = mbar_wait_bounded(bar_kfull, 0);
+      if (ok) issue_s(0);
+      int js = 1;  // next S to issue
       for (int j = 0; j < ntiles && ok; ++j) {
-        if (j + 1 < ntiles && !issue_s(j + 1)) break;
-        if (!mbar_wait_bounded(bar_p, j & 1)) break;
-        if (!mbar_wait_bounded(bar_vfull + (j % kTcStages), (j / kTcStages) & 1)) break;
+        // P V of tile j as soon as P_j is written; until then, S of the next
+        // tile as soon as its K lands (its S buffer was freed by P_{js-2})
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+          if (js < ntiles && js <= j + 1 && mbar_try_wait(bar_kfull + js % kTcStages, (js / kTcStages) & 1)) {
+            issue_s(js++);
+            continue;
+          }
+          if (mbar_try_wait(bar_p + (j & 1), (j >> 1) & 1)) break;
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            record_error(KV_ERR_DEVICE_TIMEOUT);
+            ok = false;
+            break;
+          }
+        }
+        if (!ok || !mbar_wait_bounded(bar_vfull + (j % kTcStages), (j / kTcStages) & 1)) break;
         tc::fence_after();
         const uint32_t vb = smem_u32(sm + Lay::kOffKV + (j % kTcStages) * 2 * Lay::kKV + Lay::kKV);
 #pragma unroll
         for (int kk = 0; kk < kTcKeys / 16; ++kk)
-          tc::mma_f16(tPV, tc::sdesc_sw128(aP + (kk >> 2) * Lay::kSlab + (kk & 3) * 32, 16, 1024),
-                      tc::sdesc_sw128(vb + kk * 16 * 128, Lay::kSlab, 1024), idPV, kk > 0);
-        tc::commit(bar_pv);
+          tc::mma_f16_ts(tPV, tP + (j & 1) * 64 + kk * 8, tc::sdesc_sw128(vb + kk * 16 * 128, Lay::kSlab, 1024),
+                         idPV, (j > 0 || kk > 0) ? 1u : 0u);
+        tc::commit(bar_pv + (j & 1));
         tc::commit(bar_vempty + (j % kTcStages));
       }
     }
@@ -460,14 +479,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int tok = r >> p.hg_log2, hh = r & (hg - 1);
     const int lim_abs = min(ctx + tok0 + tok, nkeys - 1);  // last key this row sees
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t to = trow + 2 * kTcKeys + cg * kOc;  // this thread's O columns
     const float c2 = p.scale_log2;
+    const uint64_t c2x2 = tc::f2(c2, c2);
     float* xmax = reinterpret_cast<float*>(sm + Lay::kOffX);  // [2][kTcSplit][128]
     float* xsum = xmax + 2 * kTcSplit * 128;                   // [kTcSplit][128]
-    float o[kOc];
-#pragma unroll
-    for (int i = 0; i < kOc; ++i) o[i] = 0.f;
-    float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
-    uint8_t* pt = sm + Lay::kOffP;
+    // m_ref: the max that P, the sum l and O are taken relative to; it only
+    // moves (rescaling l and O) when a tile's max exceeds it by more than
+    // 2^kSlack, so P stays <= 2^kSlack
+    constexpr float kSlack = 8.f;
+    float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       // after a timeout (recorded) the remaining waits are skipped, but every
@@ -478,20 +499,57 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::ld32(trow + (j & 1) * kTcKeys + cg * 32, v);
       tc::wait_ld();
       const int lim = lim_abs - j * kTcKeys - cg * 32;  // columns i <= lim of this group are keys of the row
+      const bool full = lim >= 31;
       float mx = -INFINITY;
+      if (full && c2 >= 0.f) {
+        float a = __uint_as_float(v[0]), b = __uint_as_float(v[1]);
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i <= lim) mx = fmaxf(mx, __uint_as_float(v[i]) * c2);
+        for (int i = 2; i < 32; i += 2) {
+          a = fmaxf(a, __uint_as_float(v[i]));
+          b = fmaxf(b, __uint_as_float(v[i + 1]));
+        }
+        mx = fmaxf(a, b) * c2;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i <= lim) mx = fmaxf(mx, __uint_as_float(v[i]) * c2);
+      }
       float* xm = xmax + (j & 1) * kTcSplit * 128;
       xm[cg * 128 + r] = mx;
       named_barrier_sync(1, kTcSoftWarps * 32);
-      float m_new = m;
+      float m_new = m_ref;
 #pragma unroll
       for (int g = 0; g < kTcSplit; ++g) m_new = fmaxf(m_new, xm[g * 128 + r]);
-      const float alpha = fast_exp2(m - m_new);
-      if (j > 0) {  // the previous tile's P V has read the P tile and written the PV buffer
-        if (ok && !mbar_wait_bounded(bar_pv, (j - 1) & 1)) ok = false;
+      if (j >= 2) {  // P V of tile j - 2 has read this tile's P buffer
+        if (ok && !mbar_wait_bounded(bar_pv + (j & 1), ((j >> 1) - 1) & 1)) ok = false;
         tc::fence_after();
+      }
+      // decided per warp, since the tensor-memory loads and stores below are
+      // warp-collective; the four warps holding a row hold the same 32 rows,
+      // so they decide alike, and a lane whose max moved less rescales by its
+      // own (exact) factor
+      if (__any_sync(0xffffffffu, m_new > m_ref + kSlack)) {
+        const float alpha = fast_exp2(m_ref - m_new);
+        l *= alpha;
+        if (j > 0) {  // O is complete through tile j - 1 and P V of tile j waits for this thread
+          if (ok && !mbar_wait_bounded(bar_pv + ((j - 1) & 1), ((j - 1) >> 1) & 1)) ok = false;
+          tc::fence_after();
+          const uint64_t a2 = tc::f2(alpha, alpha);
+          uint32_t w[kOc];
+          if constexpr (kOc == 32) tc::ld32(to, w);
+          else tc::ld16(to, w);
+          tc::wait_ld();
+#pragma unroll
+          for (int i = 0; i < kOc; i += 2) {
+            const float2 x = tc::f2_split(tc::fmul2(tc::f2(__uint_as_float(w[i]), __uint_as_float(w[i + 1])), a2));
+            w[i] = __float_as_uint(x.x);
+            w[i + 1] = __float_as_uint(x.y);
+          }
+          if constexpr (kOc == 32) tc::st32(to, w);
+          else tc::st16(to, w);
+          tc::wait_st();
+        }
+        m_ref = m_new;
       }
       if (j == ntiles - 1 && (nkeys % kTcKeys) != 0) {
         // zero V rows past the last key (tail slots and blocks never loaded)
@@ -505,49 +563,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int c = 0; c < 8 / kTcSplit; ++c)
               *reinterpret_cast<uint4*>(vrow + s * Lay::kSlab + (cg * (8 / kTcSplit) + c) * 16) = make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();  // the zeros are read by the tensor cores
       }
-      // P = exp2(S * c2 - m_new), rounded to T, into the swizzled P tile
-      float sum = 0.f;
+      // P = exp2(S * c2 - m_ref), rounded to T, into the tile's P buffer in tensor memory
+      const uint64_t nm2 = tc::f2(-m_ref, -m_ref);
+      uint64_t sum2 = tc::f2(0.f, 0.f);
+      uint32_t pk[16];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t pk[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int i = q4 * 8 + e * 2;
-          const float p0 = i <= lim ? fast_exp2(fmaf(__uint_as_float(v[i]), c2, -m_new)) : 0.f;
-          const float p1 = i + 1 <= lim ? fast_exp2(fmaf(__uint_as_float(v[i + 1]), c2, -m_new)) : 0.f;
-          sum += p0 + p1;
-          pk[e] = Mma<T>::pack(p0, p1);
+          const float2 x = tc::f2_split(tc::ffma2(tc::f2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), c2x2, nm2));
+          float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+          if (!full) {
+            p0 = i <= lim ? p0 : 0.f;
+            p1 = i + 1 <= lim ? p1 : 0.f;
+          }
+          sum2 = tc::fadd2(sum2, tc::f2(p0, p1));
+          pk[q4 * 4 + e] = Mma<T>::pack(p0, p1);
         }
-        const int chunk = cg * 4 + q4;  // 16-byte chunk of the row: 8 keys
-        uint8_t* dst = pt + (chunk >> 3) * Lay::kSlab + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      if (j > 0) {  // O += the previous tile's P V, rescaled to its max
-        uint32_t w[kOc];
-        if constexpr (kOc == 32) tc::ld32(trow + 2 * kTcKeys + cg * kOc, w);
-        else tc::ld16(trow + 2 * kTcKeys + cg * kOc, w);
-        tc::wait_ld();
-#pragma unroll
-        for (int i = 0; i < kOc; ++i) o[i] = fmaf(o[i], alpha_prev, __uint_as_float(w[i]));
-      }
-      l = fmaf(l, alpha, sum);
-      m = m_new;
-      alpha_prev = alpha;
-      fence_proxy_async_smem();  // P is read by the tensor cores
+      tc::st16(tP + (static_cast<uint32_t>(quarter * 32) << 16) + (j & 1) * 64 + cg * 16, pk);
+      tc::wait_st();
+      const float2 sp = tc::f2_split(sum2);
+      l += sp.x + sp.y;
       tc::fence_before();
-      mbar_arrive(bar_p);
+      mbar_arrive(bar_p + (j & 1));
     }
-    if (ok && !mbar_wait_bounded(bar_pv, (ntiles - 1) & 1)) ok = false;
-    if (ok) {
-      tc::fence_after();
-      uint32_t w[kOc];
-      if constexpr (kOc == 32) tc::ld32(trow + 2 * kTcKeys + cg * kOc, w);
-      else tc::ld16(trow + 2 * kTcKeys + cg * kOc, w);
-      tc::wait_ld();
-#pragma unroll
-      for (int i = 0; i < kOc; ++i) o[i] = fmaf(o[i], alpha_prev, __uint_as_float(w[i]));
-    }
+    uint32_t w[kOc];
+    if (ok && !mbar_wait_bounded(bar_pv + ((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1)) ok = false;
+    tc::fence_after();
+    if constexpr (kOc == 32) tc::ld32(to, w);
+    else tc::ld16(to, w);
+    tc::wait_ld();
     // the row's sum: its four partial sums (all relative to the same max)
     xsum[cg * 128 + r] = l;
     named_barrier_sync(1, kTcSoftWarps * 32);
@@ -560,12 +609,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         T* orow = static_cast<T*>(p.out) + (static_cast<int64_t>(qs + tok0 + tok) * p.num_heads + h0 + hh) * D +
                   cg * kOc;
 #pragma unroll
-        for (int c = 0; c < kOc / 8; ++c)
-          *reinterpret_cast<uint4*>(orow + c * 8) =
-              make_uint4(Mma<T>::pack(o[c * 8] * inv, o[c * 8 + 1] * inv),
-                         Mma<T>::pack(o[c * 8 + 2] * inv, o[c * 8 + 3] * inv),
-                         Mma<T>::pack(o[c * 8 + 4] * inv, o[c * 8 + 5] * inv),
-                         Mma<T>::pack(o[c * 8 + 6] * inv, o[c * 8 + 7] * inv));
+        for (int c = 0; c < kOc / 8; ++c) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            pk[e] = Mma<T>::pack(__uint_as_float(w[c * 8 + 2 * e]) * inv, __uint_as_float(w[c * 8 + 2 * e + 1]) * inv);
+          *reinterpret_cast<uint4*>(orow + c * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
       }
     }
   }
