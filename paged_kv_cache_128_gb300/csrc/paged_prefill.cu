@@ -259,72 +259,76 @@ cudaError_t launch_prefill(const PrefillParams& p, int head_dim, int max_query_l
 // Tensor-core (tcgen05) kernel, used when block_size divides 128 and is a
 // multiple of 16.
 //
-// One CTA per 128 query rows.  With group G a multiple of a power of two HG
-// (HG = the largest power of two dividing G, at most 8), the rows are HG
-// query heads of one kv head times 128 / HG chunk tokens (row r = token
-// r / HG, head r % HG), so every K/V tile serves all the tile's heads.  Key
-// tiles hold 128 positions.
-//   warp 17: TMA producer -- Q once, then each key tile's K and V, one box
-//     per (block, 64-dim slab), through the block table, into two-stage K and
-//     V rings (a K stage is free once its S is done, a V stage once its P V is);
-//   warp 16: owns 512 tensor-memory columns; one lane issues the MMAs:
-//     S_j = Q K_j^T (M 128, N 128, K head_dim) into one of two S buffers,
-//     one tile ahead, and O += P_j V_j (M 128, N head_dim, K 128) into the O
-//     columns once P_j is in shared memory;
-//   warps 0-15: four threads per row (warp w reads tensor-memory lanes
-//     32 (w % 4) .. + 31, column group w / 4): each reads its 32 S columns,
-//     masks keys past the row's position, exchanges its partial max with the
-//     row's other three threads through shared memory, and writes its 32 P
-//     values (rounded to the q dtype) to a 128-byte-swizzled shared tile.
-//     P, the partial sums and O are relative to a reference max that moves
-//     only when a tile's max exceeds it by more than 2^8 (then the thread
-//     rescales its partial sum and its head_dim / 4 columns of O in tensor
-//     memory before the next P V); P stays <= 256.  The partial sums are
-//     added once, at the end, and O is read from tensor memory once.
+// One CTA per 128 query rows, two CTAs per SM: each CTA's MMAs run while
+// the other CTA's softmax works, and one CTA's start-up overlaps the
+// other's tiles.  With group G a multiple of a power of two HG (HG = the
+// largest power of two dividing G, at most 8), the rows are HG query heads
+// of one kv head times 128 / HG chunk tokens (row r = token r / HG, head
+// r % HG), so every K/V tile serves all the tile's heads.  Key tiles hold
+// 128 positions.
+//   warp 9: TMA producer -- Q once, then each key tile's K and V, one box per
+//     (block, 64-dim slab), through the block table (a K stage is free once
+//     its S is done, a V stage once its P V is);
+//   warp 8: owns 256 tensor-memory columns (S at 0-127, O at 128-255); one
+//     lane issues the MMAs: S_j = Q K_j^T (M 128, N 128, K head_dim) once
+//     P V of tile j - 1 has read the previous P, and O += P_j V_j (M 128,
+//     N head_dim, K 128) with P_j from tensor memory once it is written;
+//   warps 0-7: two threads per row (warp w reads tensor-memory lanes
+//     32 (w % 4) .. + 31, key half w / 4): each reads its 64 S columns, masks
+//     keys past the row's position, exchanges its partial max with the row's
+//     other thread through shared memory, and writes its 64 P values
+//     (rounded to the q dtype, two per column) over the first 32 of its own
+//     S columns.  P, the partial sums and O are relative to a reference max
+//     that moves only when a tile's max exceeds it by more than 2^8 (then
+//     the thread rescales its partial sum and its head_dim / 2 columns of O
+//     in tensor memory); P stays <= 256.  The partial sums are added once,
+//     at the end, and O is read from tensor memory once.
 // Slots past the last key of the last tile (the tail of its last block and
 // blocks never loaded) are zeroed in the V tile before P V reads it, so a
 // sentinel there cannot reach the output.
 
-constexpr int kTcRows = 128;     // MMA M: query rows per CTA
-constexpr int kTcKeys = 128;     // keys per tile: N of S, K of P V
-constexpr int kTcStages = 2;     // K/V ring depth
-constexpr int kTcSplit = 4;                // threads per row in the softmax
-constexpr int kTcSoftWarps = 4 * kTcSplit;  // warps 0-15
+constexpr int kTcRows = 128;                 // MMA M: query rows per CTA
+constexpr int kTcKeys = 128;                 // keys per tile: N of S, K of P V
+constexpr int kTcSplit = 2;                  // threads per row in the softmax
+constexpr int kTcSoftWarps = 4 * kTcSplit;   // warps 0-7
 constexpr int kTcMmaWarp = kTcSoftWarps, kTcTmaWarp = kTcSoftWarps + 1;
 constexpr int kTcThreads = 32 * (kTcSoftWarps + 2);
-constexpr uint32_t kTcCols = 512;
+constexpr int kTcHalf = kTcKeys / kTcSplit;  // S columns (keys) per softmax thread
+constexpr uint32_t kTcCols = 256;            // tensor-memory columns per CTA
 
 template <int D>
 struct TcLayout {
+  static constexpr int kStages = D == 64 ? 2 : 1;   // K and V ring depth (two CTAs per SM)
   static constexpr int kSlab = 128 * 128;           // one 64-column slab of 128 rows
   static constexpr int kQ = (D / 64) * kSlab;       // Q tile
   static constexpr int kKV = (D / 64) * kSlab;      // K or V tile
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kQ;                 // stage s: K at + 2 s kKV, V at + (2 s + 1) kKV
-  static constexpr int kOffX = kOffKV + kTcStages * 2 * kKV;  // [2][kTcSplit][128] partial maxima, [kTcSplit][128] sums
+  static constexpr int kOffX = kOffKV + kStages * 2 * kKV;  // [2][kTcSplit][128] maxima, [kTcSplit][128] sums
   static constexpr int kOffBar = kOffX + 3 * kTcSplit * 128 * 4;
   static constexpr int kBytes = kOffBar + 256;
   static constexpr int kSmem = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 2)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using Lay = TcLayout<D>;
-  constexpr int kSlabs = D / 64;
+  constexpr int kSlabs = D / 64, kStages = Lay::kStages;
+  constexpr int kOc = D / kTcSplit;  // O columns per softmax thread
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar_q = reinterpret_cast<uint64_t*>(sm + Lay::kOffBar);
-  uint64_t* bar_kfull = bar_q + 1;                // [kTcStages] K tile landed
-  uint64_t* bar_vfull = bar_kfull + kTcStages;    // [kTcStages] V tile landed
-  uint64_t* bar_kempty = bar_vfull + kTcStages;   // [kTcStages] S of the tile done
-  uint64_t* bar_vempty = bar_kempty + kTcStages;  // [kTcStages] P V of the tile done
-  uint64_t* bar_s = bar_vempty + kTcStages;       // [2] S buffer written
-  uint64_t* bar_p = bar_s + 2;                    // [2] P buffer written (every softmax thread arrives)
-  uint64_t* bar_pv = bar_p + 2;                   // [2] P V from that P buffer done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_pv + 2);
+  uint64_t* bar_kfull = bar_q + 1;              // [kStages] K tile landed
+  uint64_t* bar_vfull = bar_kfull + kStages;    // [kStages] V tile landed
+  uint64_t* bar_kempty = bar_vfull + kStages;   // [kStages] S of the tile done
+  uint64_t* bar_vempty = bar_kempty + kStages;  // [kStages] P V of the tile done
+  uint64_t* bar_s = bar_vempty + kStages;       // S written
+  uint64_t* bar_p = bar_s + 1;                  // P written (every softmax thread arrives)
+  uint64_t* bar_pv = bar_p + 1;                 // P V done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_pv + 1);
 
   const int hg = 1 << p.hg_log2, tpt = kTcRows >> p.hg_log2;
   const int qt = gridDim.x - 1 - blockIdx.x;  // tiles with the most keys start first
@@ -350,18 +354,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int s = 0; s < kTcStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_kfull + s, 1);
       mbar_init(bar_vfull + s, 1);
       mbar_init(bar_kempty + s, 1);
       mbar_init(bar_vempty + s, 1);
     }
     mbar_init(bar_s, 1);
-    mbar_init(bar_s + 1, 1);
-    for (int b2 = 0; b2 < 2; ++b2) {
-      mbar_init(bar_p + b2, kTcSoftWarps * 32);
-      mbar_init(bar_pv + b2, 1);
-    }
+    mbar_init(bar_p, kTcSoftWarps * 32);
+    mbar_init(bar_pv, 1);
     fence_mbar_init();
   }
   if (warp == kTcMmaWarp) tc::alloc(tmem_slot, kTcCols);
@@ -369,10 +370,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
-  // tensor memory: S buffers at columns 0 and 128, O at 256, P buffers (two
-  // 16-bit values per column) at 384 and 448
-  const uint32_t tPV = tmem + 2 * kTcKeys;
-  const uint32_t tP = tmem + 2 * kTcKeys + 128;
+  const uint32_t tS = tmem, tO = tmem + kTcKeys;  // S (P over its first half-columns), O
 
   if (warp == kTcTmaWarp) {
     if (lane == 0) {
@@ -385,14 +383,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_load_3d(sm + Lay::kOffQ + s * Lay::kSlab, &tmQ, bar_q, s * 64, h0, qs + tok0);
       const int32_t* table = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
       const int bs = p.block_size;
-      // K (V) of tile j into stage j % kTcStages once S (P V) of tile
-      // j - kTcStages is done; K runs one tile ahead of V, since S of a tile
-      // completes before its P V
+      // K (V) of tile j into stage j % kStages once S (P V) of tile
+      // j - kStages is done.  K runs one tile ahead of V; V of tile j is
+      // issued first, since P V of tile j - 1 completes before S of tile j
+      // is issued
       auto load = [&](int j, bool is_v) -> bool {
-        const int st = j % kTcStages;
+        const int st = j % kStages;
         uint64_t* full = (is_v ? bar_vfull : bar_kfull) + st;
-        if (j >= kTcStages &&
-            !mbar_wait_bounded((is_v ? bar_vempty : bar_kempty) + st, ((j / kTcStages) - 1) & 1))
+        if (j >= kStages && !mbar_wait_bounded((is_v ? bar_vempty : bar_kempty) + st, ((j / kStages) - 1) & 1))
           return false;
         const int k0 = j * kTcKeys, k1 = min(k0 + kTcKeys, nkeys);
         const int blk0 = k0 / bs, blk1 = (k1 + bs - 1) / bs;
@@ -412,13 +410,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       };
       bool ok = load(0, false);
       for (int j = 0; j < ntiles && ok; ++j) {
-        if (j + 1 < ntiles) ok = load(j + 1, false);
-        if (ok) ok = load(j, true);
+        ok = load(j, true);
+        if (ok && j + 1 < ntiles) ok = load(j + 1, false);
       }
       // every stage's last S and P V have completed (no copy or commit in flight at exit)
-      for (int j = max(0, ntiles - kTcStages); j < ntiles; ++j) {
-        mbar_wait_bounded(bar_kempty + (j % kTcStages), (j / kTcStages) & 1);
-        mbar_wait_bounded(bar_vempty + (j % kTcStages), (j / kTcStages) & 1);
+      for (int j = max(0, ntiles - kStages); j < ntiles; ++j) {
+        mbar_wait_bounded(bar_kempty + (j % kStages), (j / kStages) & 1);
+        mbar_wait_bounded(bar_vempty + (j % kStages), (j / kStages) & 1);
       }
     }
   } else if (warp == kTcMmaWarp) {
@@ -428,91 +426,77 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t idPV = tc::idesc_f16(kBf16, kTcRows, D, true);
       const uint32_t aQ = smem_u32(sm + Lay::kOffQ);
       bool ok = mbar_wait_bounded(bar_q, 0);
-      auto issue_s = [&](int j) {  // K tile j has landed
-        const int st = j % kTcStages;
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int st = j % kStages;
+        // S_j overwrites the S columns, which hold P_{j-1} until P V of tile j - 1 is done
+        if (j > 0 && !mbar_wait_bounded(bar_pv, (j - 1) & 1)) break;
+        if (!mbar_wait_bounded(bar_kfull + st, (j / kStages) & 1)) break;
         tc::fence_after();
         const uint32_t kb = smem_u32(sm + Lay::kOffKV + st * 2 * Lay::kKV);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * Lay::kSlab + (kk & 3) * 32;  // 64-dim slab, 16-dim step inside it
-          tc::mma_f16(tmem + (j & 1) * kTcKeys, tc::sdesc_sw128(aQ + off, 16, 1024),
-                      tc::sdesc_sw128(kb + off, 16, 1024), idS, kk > 0);
+          tc::mma_f16(tS, tc::sdesc_sw128(aQ + off, 16, 1024), tc::sdesc_sw128(kb + off, 16, 1024), idS, kk > 0);
         }
-        tc::commit(bar_s + (j & 1));
+        tc::commit(bar_s);
         tc::commit(bar_kempty + st);
-      };
-      if (ok) ok = mbar_wait_bounded(bar_kfull, 0);
-      if (ok) issue_s(0);
-      int js = 1;  // next S to issue
-      for (int j = 0; j < ntiles && ok; ++j) {
-        // P V of tile j as soon as P_j is written; until then, S of the next
-        // tile as soon as its K lands (its S buffer was freed by P_{js-2})
-        const uint64_t t0 = globaltimer_ns();
-        for (;;) {
-          if (js < ntiles && js <= j + 1 && mbar_try_wait(bar_kfull + js % kTcStages, (js / kTcStages) & 1)) {
-            issue_s(js++);
-            continue;
-          }
-          if (mbar_try_wait(bar_p + (j & 1), (j >> 1) & 1)) break;
-          if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            record_error(KV_ERR_DEVICE_TIMEOUT);
-            ok = false;
-            break;
-          }
-        }
-        if (!ok || !mbar_wait_bounded(bar_vfull + (j % kTcStages), (j / kTcStages) & 1)) break;
+        if (!mbar_wait_bounded(bar_p, j & 1)) break;
+        if (!mbar_wait_bounded(bar_vfull + st, (j / kStages) & 1)) break;
         tc::fence_after();
-        const uint32_t vb = smem_u32(sm + Lay::kOffKV + (j % kTcStages) * 2 * Lay::kKV + Lay::kKV);
+        const uint32_t vb = smem_u32(sm + Lay::kOffKV + st * 2 * Lay::kKV + Lay::kKV);
 #pragma unroll
-        for (int kk = 0; kk < kTcKeys / 16; ++kk)
-          tc::mma_f16_ts(tPV, tP + (j & 1) * 64 + kk * 8, tc::sdesc_sw128(vb + kk * 16 * 128, Lay::kSlab, 1024),
-                         idPV, (j > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(bar_pv + (j & 1));
-        tc::commit(bar_vempty + (j % kTcStages));
+        for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+          // keys 16 kk .. + 15: P of key half kk / 4, two keys per column
+          const uint32_t pa = tS + (kk / 4) * kTcHalf + (kk % 4) * 8;
+          tc::mma_f16_ts(tO, pa, tc::sdesc_sw128(vb + kk * 16 * 128, Lay::kSlab, 1024), idPV,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc::commit(bar_pv);
+        tc::commit(bar_vempty + st);
       }
     }
   } else {
-    // ---- softmax: four threads per row, 32 S columns and D / 4 O columns each
-    constexpr int kOc = D / kTcSplit;  // O columns of this thread
+    // ---- softmax: two threads per row, 64 S columns and D / 2 O columns each
     const int quarter = warp & 3, cg = warp >> 2;
     const int r = quarter * 32 + lane;  // row of the tile
     const int tok = r >> p.hg_log2, hh = r & (hg - 1);
     const int lim_abs = min(ctx + tok0 + tok, nkeys - 1);  // last key this row sees
-    const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t to = trow + 2 * kTcKeys + cg * kOc;  // this thread's O columns
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t ts = tS + lane_base + cg * kTcHalf;  // this thread's S columns
+    const uint32_t to = tO + lane_base + cg * kOc;      // this thread's O columns
     const float c2 = p.scale_log2;
     const uint64_t c2x2 = tc::f2(c2, c2);
     float* xmax = reinterpret_cast<float*>(sm + Lay::kOffX);  // [2][kTcSplit][128]
     float* xsum = xmax + 2 * kTcSplit * 128;                   // [kTcSplit][128]
-    // m_ref: the max that P, the sum l and O are taken relative to; it only
-    // moves (rescaling l and O) when a tile's max exceeds it by more than
-    // 2^kSlack, so P stays <= 2^kSlack
     constexpr float kSlack = 8.f;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       // after a timeout (recorded) the remaining waits are skipped, but every
       // thread still runs every tile, so the named barriers stay matched
-      if (ok && !mbar_wait_bounded(bar_s + (j & 1), (j >> 1) & 1)) ok = false;
+      if (ok && !mbar_wait_bounded(bar_s, j & 1)) ok = false;
       tc::fence_after();
-      uint32_t v[32];
-      tc::ld32(trow + (j & 1) * kTcKeys + cg * 32, v);
-      tc::wait_ld();
-      const int lim = lim_abs - j * kTcKeys - cg * 32;  // columns i <= lim of this group are keys of the row
-      const bool full = lim >= 31;
+      const int lim = lim_abs - j * kTcKeys - cg * kTcHalf;  // columns i <= lim of this half are keys of the row
+      const bool full = lim >= kTcHalf - 1;
       float mx = -INFINITY;
-      if (full && c2 >= 0.f) {
-        float a = __uint_as_float(v[0]), b = __uint_as_float(v[1]);
 #pragma unroll
-        for (int i = 2; i < 32; i += 2) {
-          a = fmaxf(a, __uint_as_float(v[i]));
-          b = fmaxf(b, __uint_as_float(v[i + 1]));
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t v[32];
+        tc::ld32(ts + hf * 32, v);
+        tc::wait_ld();
+        if (full && c2 >= 0.f) {
+          float a = __uint_as_float(v[0]), bq = __uint_as_float(v[1]);
+#pragma unroll
+          for (int i = 2; i < 32; i += 2) {
+            a = fmaxf(a, __uint_as_float(v[i]));
+            bq = fmaxf(bq, __uint_as_float(v[i + 1]));
+          }
+          mx = fmaxf(mx, fmaxf(a, bq) * c2);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (hf * 32 + i <= lim) mx = fmaxf(mx, __uint_as_float(v[i]) * c2);
         }
-        mx = fmaxf(a, b) * c2;
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i <= lim) mx = fmaxf(mx, __uint_as_float(v[i]) * c2);
       }
       float* xm = xmax + (j & 1) * kTcSplit * 128;
       xm[cg * 128 + r] = mx;
@@ -520,41 +504,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float m_new = m_ref;
 #pragma unroll
       for (int g = 0; g < kTcSplit; ++g) m_new = fmaxf(m_new, xm[g * 128 + r]);
-      if (j >= 2) {  // P V of tile j - 2 has read this tile's P buffer
-        if (ok && !mbar_wait_bounded(bar_pv + (j & 1), ((j >> 1) - 1) & 1)) ok = false;
-        tc::fence_after();
-      }
       // decided per warp, since the tensor-memory loads and stores below are
-      // warp-collective; the four warps holding a row hold the same 32 rows,
+      // warp-collective; the two warps holding a row hold the same 32 rows,
       // so they decide alike, and a lane whose max moved less rescales by its
       // own (exact) factor
       if (__any_sync(0xffffffffu, m_new > m_ref + kSlack)) {
         const float alpha = fast_exp2(m_ref - m_new);
         l *= alpha;
-        if (j > 0) {  // O is complete through tile j - 1 and P V of tile j waits for this thread
-          if (ok && !mbar_wait_bounded(bar_pv + ((j - 1) & 1), ((j - 1) >> 1) & 1)) ok = false;
+        if (j > 0) {  // O holds tiles 0 .. j - 1 (P V of tile j - 1 is done: S_j was issued after it)
+          if (ok && !mbar_wait_bounded(bar_pv, (j - 1) & 1)) ok = false;
           tc::fence_after();
           const uint64_t a2 = tc::f2(alpha, alpha);
-          uint32_t w[kOc];
-          if constexpr (kOc == 32) tc::ld32(to, w);
-          else tc::ld16(to, w);
-          tc::wait_ld();
 #pragma unroll
-          for (int i = 0; i < kOc; i += 2) {
-            const float2 x = tc::f2_split(tc::fmul2(tc::f2(__uint_as_float(w[i]), __uint_as_float(w[i + 1])), a2));
-            w[i] = __float_as_uint(x.x);
-            w[i + 1] = __float_as_uint(x.y);
+          for (int oc = 0; oc < kOc; oc += 32) {
+            uint32_t w[32];
+            tc::ld32(to + oc, w);
+            tc::wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float2 x = tc::f2_split(tc::fmul2(tc::f2(__uint_as_float(w[i]), __uint_as_float(w[i + 1])), a2));
+              w[i] = __float_as_uint(x.x);
+              w[i + 1] = __float_as_uint(x.y);
+            }
+            tc::st32(to + oc, w);
           }
-          if constexpr (kOc == 32) tc::st32(to, w);
-          else tc::st16(to, w);
           tc::wait_st();
         }
         m_ref = m_new;
       }
       if (j == ntiles - 1 && (nkeys % kTcKeys) != 0) {
         // zero V rows past the last key (tail slots and blocks never loaded)
-        const int st = j % kTcStages;
-        if (ok && !mbar_wait_bounded(bar_vfull + st, (j / kTcStages) & 1)) ok = false;
+        const int st = j % kStages;
+        if (ok && !mbar_wait_bounded(bar_vfull + st, (j / kStages) & 1)) ok = false;
         if (r >= nkeys - j * kTcKeys) {
           uint8_t* vrow = sm + Lay::kOffKV + st * 2 * Lay::kKV + Lay::kKV + r * 128;
 #pragma unroll
@@ -565,56 +546,59 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         fence_proxy_async_smem();  // the zeros are read by the tensor cores
       }
-      // P = exp2(S * c2 - m_ref), rounded to T, into the tile's P buffer in tensor memory
+      // P = exp2(S * c2 - m_ref), rounded to T, two per column over the first
+      // 32 of this thread's S columns (its S values were read first: the
+      // second half is read again before its P lands over the first half)
       const uint64_t nm2 = tc::f2(-m_ref, -m_ref);
       uint64_t sum2 = tc::f2(0.f, 0.f);
-      uint32_t pk[16];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t v[32];
+        tc::ld32(ts + hf * 32, v);
+        tc::wait_ld();
+        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = q4 * 8 + e * 2;
+        for (int i = 0; i < 32; i += 2) {
           const float2 x = tc::f2_split(tc::ffma2(tc::f2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), c2x2, nm2));
           float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
           if (!full) {
-            p0 = i <= lim ? p0 : 0.f;
-            p1 = i + 1 <= lim ? p1 : 0.f;
+            p0 = hf * 32 + i <= lim ? p0 : 0.f;
+            p1 = hf * 32 + i + 1 <= lim ? p1 : 0.f;
           }
           sum2 = tc::fadd2(sum2, tc::f2(p0, p1));
-          pk[q4 * 4 + e] = Mma<T>::pack(p0, p1);
+          pk[i / 2] = Mma<T>::pack(p0, p1);
         }
+        tc::st16(ts + hf * 16, pk);
       }
-      tc::st16(tP + (static_cast<uint32_t>(quarter * 32) << 16) + (j & 1) * 64 + cg * 16, pk);
       tc::wait_st();
       const float2 sp = tc::f2_split(sum2);
       l += sp.x + sp.y;
       tc::fence_before();
-      mbar_arrive(bar_p + (j & 1));
+      mbar_arrive(bar_p);
     }
-    uint32_t w[kOc];
-    if (ok && !mbar_wait_bounded(bar_pv + ((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1)) ok = false;
+    if (ok && !mbar_wait_bounded(bar_pv, (ntiles - 1) & 1)) ok = false;
     tc::fence_after();
-    if constexpr (kOc == 32) tc::ld32(to, w);
-    else tc::ld16(to, w);
-    tc::wait_ld();
-    // the row's sum: its four partial sums (all relative to the same max)
+    // the row's sum: its two partial sums (both relative to the same max)
     xsum[cg * 128 + r] = l;
     named_barrier_sync(1, kTcSoftWarps * 32);
-    if (ok) {
-      float lt = 0.f;
+    float lt = 0.f;
 #pragma unroll
-      for (int g = 0; g < kTcSplit; ++g) lt += xsum[g * 128 + r];
-      if (tok < rows_here) {
-        const float inv = lt > 0.f ? __fdiv_rn(1.f, lt) : 0.f;
-        T* orow = static_cast<T*>(p.out) + (static_cast<int64_t>(qs + tok0 + tok) * p.num_heads + h0 + hh) * D +
-                  cg * kOc;
+    for (int g = 0; g < kTcSplit; ++g) lt += xsum[g * 128 + r];
+    const float inv = lt > 0.f ? __fdiv_rn(1.f, lt) : 0.f;
+    T* orow = static_cast<T*>(p.out) + (static_cast<int64_t>(qs + tok0 + tok) * p.num_heads + h0 + hh) * D + cg * kOc;
 #pragma unroll
-        for (int c = 0; c < kOc / 8; ++c) {
+    for (int oc = 0; oc < kOc; oc += 32) {
+      uint32_t w[32];
+      tc::ld32(to + oc, w);
+      tc::wait_ld();
+      if (ok && tok < rows_here) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
           uint32_t pk[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             pk[e] = Mma<T>::pack(__uint_as_float(w[c * 8 + 2 * e]) * inv, __uint_as_float(w[c * 8 + 2 * e + 1]) * inv);
-          *reinterpret_cast<uint4*>(orow + c * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(orow + oc + c * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
     }
@@ -669,6 +653,9 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int max_query_len, const C
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
     e = cudaFuncSetAttribute(prefill_tc_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    // the largest shared-memory carve-out, so two CTAs fit on an SM
+    e = cudaFuncSetAttribute(prefill_tc_kernel<T, D>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
