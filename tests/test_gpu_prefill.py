@@ -27,8 +27,9 @@ from tests.helpers import TOL, TORCH, sentinel_tensor, to_f64
 pytestmark = pytest.mark.gpu
 
 
-def _run(dtype, hq, hkv, d, bs, seqs, seed, value_scale=0.5, sample_rows=None):
-    """seqs: list of (history length, chunk length)."""
+def _run(dtype, hq, hkv, d, bs, seqs, seed, value_scale=0.5, sample_rows=None, max_query_len=None):
+    """seqs: list of (history length, chunk length); every sequence has at
+    least one token.  max_query_len defaults to the longest chunk."""
     rng = np.random.default_rng(seed)
     g = torch.Generator().manual_seed(seed)
     dt = TORCH[dtype]
@@ -56,7 +57,7 @@ def _run(dtype, hq, hkv, d, bs, seqs, seed, value_scale=0.5, sample_rows=None):
     pk.device_error()
     pk.paged_prefill_attention(out, q.to(dev), kc, vc, torch.from_numpy(tables).to(dev),
                                torch.from_numpy(seq_lens).to(dev), torch.from_numpy(qsl).to(dev), scale,
-                               max(n for _, n in seqs))
+                               max_query_len if max_query_len is not None else max(n for _, n in seqs))
     assert pk.device_error() == 0
     got = to_f64(out, dtype)
     assert np.all(np.isfinite(got))
@@ -132,3 +133,36 @@ def test_prefill_chunk_past_the_query_rows_is_reported():
     pk.paged_prefill_attention(out, q, kc, vc, tables, lens, qsl, 0.125, 20)
     assert pk.device_error() == 8
     assert torch.all(out == 7.0)
+
+
+@pytest.mark.parametrize("bs", [16, 8], ids=["tcgen05", "mma_sync"])
+def test_prefill_empty_chunks_between_others(bs):
+    """Sequences whose chunk is empty (n = 0) sit between others: they own
+    no rows of q/out, and every other chunk still matches the oracle."""
+    seqs = [(5, 0), (30, 17), (3, 0), (100, 1), (0, 40), (7, 0)]
+    worst = _run("bf16", 8, 2, 128, bs, seqs, seed=21)
+    assert worst <= TOL["bf16"], f"max abs err {worst:.3e}"
+
+
+@pytest.mark.parametrize("bs", [32, 4], ids=["tcgen05", "mma_sync"])
+def test_prefill_grid_larger_than_the_chunks(bs):
+    """max_query_len is only an upper bound: a grid sized for 4x the longest
+    chunk gives the same rows."""
+    seqs = [(12, 70), (0, 129)]
+    worst = _run("f16", 4, 2, 64, bs, seqs, seed=22, max_query_len=4 * 129)
+    assert worst <= TOL["f16"], f"max abs err {worst:.3e}"
+
+
+def test_prefill_without_query_rows_launches_nothing():
+    dev = torch.device("cuda")
+    kc = torch.zeros(4, 16, 2, 64, dtype=torch.float16, device=dev)
+    vc = torch.zeros_like(kc)
+    tables = torch.tensor([[0, 1]], dtype=torch.int32, device=dev)
+    lens = torch.tensor([20], dtype=torch.int32, device=dev)
+    qsl = torch.tensor([0, 0], dtype=torch.int32, device=dev)
+    q = torch.empty(0, 4, 64, dtype=torch.float16, device=dev)
+    out = torch.empty_like(q)
+    pk.device_error()
+    pk.paged_prefill_attention(out, q, kc, vc, tables, lens, qsl, 0.125, 0)
+    torch.cuda.synchronize()
+    assert pk.device_error() == 0
