@@ -273,27 +273,25 @@ cudaError_t launch_prefill(const PrefillParams& p, int head_dim, int max_query_l
 //     lane issues the MMAs: S_j = Q K_j^T (M 128, N 128, K head_dim) once
 //     P V of tile j - 1 has read the previous P, and O += P_j V_j (M 128,
 //     N head_dim, K 128) with P_j from tensor memory once it is written;
-//   warps 0-7: two threads per row (warp w reads tensor-memory lanes
-//     32 (w % 4) .. + 31, key half w / 4): each reads its 64 S columns, masks
-//     keys past the row's position, exchanges its partial max with the row's
-//     other thread through shared memory, and writes its 64 P values
-//     (rounded to the q dtype, two per column) over the first 32 of its own
-//     S columns.  P, the partial sums and O are relative to a reference max
+//   warps 0-7: warp w owns the 16 rows 32 (w % 4) + 16 (w / 4) .. + 15 and
+//     reads them with the 16x256b tensor-memory shape: a quad of threads
+//     holds two rows, each thread a quarter of their columns, so the row max
+//     and sum are two quad shuffles and the warps never wait for one
+//     another.  Each warp masks keys past each row's position and writes P
+//     (rounded to the q dtype, two keys per column) over S columns 0-63 with
+//     the 16x128b shape.  P, the sums and O are relative to a reference max
 //     that moves only when a tile's max exceeds it by more than 2^8 (then
-//     the thread rescales its partial sum and its head_dim / 2 columns of O
-//     in tensor memory); P stays <= 256.  The partial sums are added once,
-//     at the end, and O is read from tensor memory once.
+//     the warp rescales the rows' sums and O columns in tensor memory); P
+//     stays <= 256.  O is read from tensor memory once, at the end.
 // Slots past the last key of the last tile (the tail of its last block and
 // blocks never loaded) are zeroed in the V tile before P V reads it, so a
 // sentinel there cannot reach the output.
 
 constexpr int kTcRows = 128;                 // MMA M: query rows per CTA
 constexpr int kTcKeys = 128;                 // keys per tile: N of S, K of P V
-constexpr int kTcSplit = 2;                  // threads per row in the softmax
-constexpr int kTcSoftWarps = 4 * kTcSplit;   // warps 0-7
+constexpr int kTcSoftWarps = 8;              // softmax warps 0-7
 constexpr int kTcMmaWarp = kTcSoftWarps, kTcTmaWarp = kTcSoftWarps + 1;
 constexpr int kTcThreads = 32 * (kTcSoftWarps + 2);
-constexpr int kTcHalf = kTcKeys / kTcSplit;  // S columns (keys) per softmax thread
 constexpr uint32_t kTcCols = 256;            // tensor-memory columns per CTA
 
 template <int D>
@@ -304,8 +302,7 @@ struct TcLayout {
   static constexpr int kKV = (D / 64) * kSlab;      // K or V tile
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kQ;                 // stage s: K at + 2 s kKV, V at + (2 s + 1) kKV
-  static constexpr int kOffX = kOffKV + kStages * 2 * kKV;  // [2][kTcSplit][128] maxima, [kTcSplit][128] sums
-  static constexpr int kOffBar = kOffX + 3 * kTcSplit * 128 * 4;
+  static constexpr int kOffBar = kOffKV + kStages * 2 * kKV;
   static constexpr int kBytes = kOffBar + 256;
   static constexpr int kSmem = kBytes + 1024;  // slack for 1024-byte alignment
 };
@@ -316,7 +313,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                       const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using Lay = TcLayout<D>;
   constexpr int kSlabs = D / 64, kStages = Lay::kStages;
-  constexpr int kOc = D / kTcSplit;  // O columns per softmax thread
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -446,8 +442,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const uint32_t vb = smem_u32(sm + Lay::kOffKV + st * 2 * Lay::kKV + Lay::kKV);
 #pragma unroll
         for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-          // keys 16 kk .. + 15: P of key half kk / 4, two keys per column
-          const uint32_t pa = tS + (kk / 4) * kTcHalf + (kk % 4) * 8;
+          // keys 16 kk .. + 15: P, two keys per column
+          const uint32_t pa = tS + kk * 8;
           tc::mma_f16_ts(tO, pa, tc::sdesc_sw128(vb + kk * 16 * 128, Lay::kSlab, 1024), idPV,
                          (j > 0 || kk > 0) ? 1u : 0u);
         }
@@ -456,150 +452,178 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       }
     }
   } else {
-    // ---- softmax: two threads per row, 64 S columns and D / 2 O columns each
-    const int quarter = warp & 3, cg = warp >> 2;
-    const int r = quarter * 32 + lane;  // row of the tile
-    const int tok = r >> p.hg_log2, hh = r & (hg - 1);
-    const int lim_abs = min(ctx + tok0 + tok, nkeys - 1);  // last key this row sees
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t ts = tS + lane_base + cg * kTcHalf;  // this thread's S columns
-    const uint32_t to = tO + lane_base + cg * kOc;      // this thread's O columns
+    // ---- softmax: warp w owns the 16 rows 32 (w % 4) + 16 (w / 4) .. + 15;
+    // a quad of threads holds two rows (lane / 4 and lane / 4 + 8), each
+    // thread a quarter of their columns, so row maxima and sums are quad
+    // shuffles and the warps run independently
+    const int quarter = warp & 3, half = warp >> 2;
+    const int rbase = quarter * 32 + half * 16;
+    const int g = lane >> 2, c4 = lane & 3;
+    const uint32_t lanes = static_cast<uint32_t>(rbase) << 16;
+    const uint32_t tsw = tS + lanes, tow = tO + lanes;
+    int tok[2], hh[2], lim_abs[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = rbase + g + 8 * e;
+      tok[e] = r >> p.hg_log2;
+      hh[e] = r & (hg - 1);
+      lim_abs[e] = min(ctx + tok0 + tok[e], nkeys - 1);  // last key row r sees
+    }
     const float c2 = p.scale_log2;
     const uint64_t c2x2 = tc::f2(c2, c2);
-    float* xmax = reinterpret_cast<float*>(sm + Lay::kOffX);  // [2][kTcSplit][128]
-    float* xsum = xmax + 2 * kTcSplit * 128;                   // [kTcSplit][128]
     constexpr float kSlack = 8.f;
-    float m_ref = -INFINITY, l = 0.f;
+    float m_ref[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
-      // after a timeout (recorded) the remaining waits are skipped, but every
-      // thread still runs every tile, so the named barriers stay matched
+      // after a timeout (recorded) the remaining waits are skipped
       if (ok && !mbar_wait_bounded(bar_s, j & 1)) ok = false;
       tc::fence_after();
-      const int lim = lim_abs - j * kTcKeys - cg * kTcHalf;  // columns i <= lim of this half are keys of the row
-      const bool full = lim >= kTcHalf - 1;
-      float mx = -INFINITY;
+      int lim[2];
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
+      for (int e = 0; e < 2; ++e) lim[e] = lim_abs[e] - j * kTcKeys;  // columns <= lim[e] are keys of row e
+      const bool full = __all_sync(0xffffffffu, min(lim[0], lim[1]) >= kTcKeys - 1) && c2 > 0.f;
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
         uint32_t v[32];
-        tc::ld32(ts + hf * 32, v);
+        tc::ld_16x256b_x8(tsw + ch * 64, v);
         tc::wait_ld();
-        if (full && c2 >= 0.f) {
-          float a = __uint_as_float(v[0]), bq = __uint_as_float(v[1]);
+        if (full) {
 #pragma unroll
-          for (int i = 2; i < 32; i += 2) {
-            a = fmaxf(a, __uint_as_float(v[i]));
-            bq = fmaxf(bq, __uint_as_float(v[i + 1]));
-          }
-          mx = fmaxf(mx, fmaxf(a, bq) * c2);
+          for (int k = 0; k < 8; ++k)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+              mx[e] = fmaxf(mx[e], fmaxf(__uint_as_float(v[4 * k + 2 * e]), __uint_as_float(v[4 * k + 2 * e + 1])));
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (hf * 32 + i <= lim) mx = fmaxf(mx, __uint_as_float(v[i]) * c2);
+          for (int k = 0; k < 8; ++k)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+#pragma unroll
+              for (int bb = 0; bb < 2; ++bb)
+                if (ch * 64 + 8 * k + 2 * c4 + bb <= lim[e])
+                  mx[e] = fmaxf(mx[e], __uint_as_float(v[4 * k + 2 * e + bb]) * c2);
         }
       }
-      float* xm = xmax + (j & 1) * kTcSplit * 128;
-      xm[cg * 128 + r] = mx;
-      named_barrier_sync(1, kTcSoftWarps * 32);
-      float m_new = m_ref;
+      float m_new[2];
+      bool need = false;
 #pragma unroll
-      for (int g = 0; g < kTcSplit; ++g) m_new = fmaxf(m_new, xm[g * 128 + r]);
+      for (int e = 0; e < 2; ++e) {
+        if (full) mx[e] *= c2;
+        mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 1));
+        mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 2));
+        m_new[e] = fmaxf(m_ref[e], mx[e]);
+        need = need || m_new[e] > m_ref[e] + kSlack;
+      }
       // decided per warp, since the tensor-memory loads and stores below are
-      // warp-collective; the two warps holding a row hold the same 32 rows,
-      // so they decide alike, and a lane whose max moved less rescales by its
-      // own (exact) factor
-      if (__any_sync(0xffffffffu, m_new > m_ref + kSlack)) {
-        const float alpha = fast_exp2(m_ref - m_new);
-        l *= alpha;
+      // warp-collective; a row whose max moved less rescales by its own
+      // (exact) factor
+      if (__any_sync(0xffffffffu, need)) {
+        float alpha[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          alpha[e] = fast_exp2(m_ref[e] - m_new[e]);
+          l[e] *= alpha[e];
+          m_ref[e] = m_new[e];
+        }
         if (j > 0) {  // O holds tiles 0 .. j - 1 (P V of tile j - 1 is done: S_j was issued after it)
           if (ok && !mbar_wait_bounded(bar_pv, (j - 1) & 1)) ok = false;
           tc::fence_after();
-          const uint64_t a2 = tc::f2(alpha, alpha);
 #pragma unroll
-          for (int oc = 0; oc < kOc; oc += 32) {
+          for (int oc = 0; oc < D; oc += 64) {
             uint32_t w[32];
-            tc::ld32(to + oc, w);
+            tc::ld_16x256b_x8(tow + oc, w);
             tc::wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float2 x = tc::f2_split(tc::fmul2(tc::f2(__uint_as_float(w[i]), __uint_as_float(w[i + 1])), a2));
-              w[i] = __float_as_uint(x.x);
-              w[i + 1] = __float_as_uint(x.y);
-            }
-            tc::st32(to + oc, w);
+            for (int k = 0; k < 8; ++k)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float2 x = tc::f2_split(tc::fmul2(
+                    tc::f2(__uint_as_float(w[4 * k + 2 * e]), __uint_as_float(w[4 * k + 2 * e + 1])),
+                    tc::f2(alpha[e], alpha[e])));
+                w[4 * k + 2 * e] = __float_as_uint(x.x);
+                w[4 * k + 2 * e + 1] = __float_as_uint(x.y);
+              }
+            tc::st_16x256b_x8(tow + oc, w);
           }
           tc::wait_st();
         }
-        m_ref = m_new;
       }
       if (j == ntiles - 1 && (nkeys % kTcKeys) != 0) {
         // zero V rows past the last key (tail slots and blocks never loaded)
         const int st = j % kStages;
         if (ok && !mbar_wait_bounded(bar_vfull + st, (j / kStages) & 1)) ok = false;
-        if (r >= nkeys - j * kTcKeys) {
-          uint8_t* vrow = sm + Lay::kOffKV + st * 2 * Lay::kKV + Lay::kKV + r * 128;
-#pragma unroll
-          for (int s = 0; s < kSlabs; ++s)
-#pragma unroll
-            for (int c = 0; c < 8 / kTcSplit; ++c)
-              *reinterpret_cast<uint4*>(vrow + s * Lay::kSlab + (cg * (8 / kTcSplit) + c) * 16) = make_uint4(0, 0, 0, 0);
+        const int first = nkeys - j * kTcKeys;
+        uint8_t* vt = sm + Lay::kOffKV + st * 2 * Lay::kKV + Lay::kKV;
+        for (int i = threadIdx.x; i < kTcKeys * kSlabs * 8; i += kTcSoftWarps * 32) {
+          const int row = i / (kSlabs * 8), rest = i % (kSlabs * 8);
+          if (row >= first)
+            *reinterpret_cast<uint4*>(vt + (rest >> 3) * Lay::kSlab + row * 128 + (rest & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();  // the zeros are read by the tensor cores
       }
-      // P = exp2(S * c2 - m_ref), rounded to T, two per column over the first
-      // 32 of this thread's S columns (its S values were read first: the
-      // second half is read again before its P lands over the first half)
-      const uint64_t nm2 = tc::f2(-m_ref, -m_ref);
-      uint64_t sum2 = tc::f2(0.f, 0.f);
+      // P = exp2(S * c2 - m_ref), rounded to T, two keys per column over the
+      // first 64 S columns (chunk 0's S is read before its P lands there, and
+      // chunk 1's S lies in columns 64-127)
+      uint64_t sum2[2] = {tc::f2(0.f, 0.f), tc::f2(0.f, 0.f)};
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
+      for (int ch = 0; ch < 2; ++ch) {
         uint32_t v[32];
-        tc::ld32(ts + hf * 32, v);
+        tc::ld_16x256b_x8(tsw + ch * 64, v);
         tc::wait_ld();
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float2 x = tc::f2_split(tc::ffma2(tc::f2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), c2x2, nm2));
-          float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-          if (!full) {
-            p0 = hf * 32 + i <= lim ? p0 : 0.f;
-            p1 = hf * 32 + i + 1 <= lim ? p1 : 0.f;
+        for (int k = 0; k < 8; ++k)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float2 x = tc::f2_split(tc::ffma2(
+                tc::f2(__uint_as_float(v[4 * k + 2 * e]), __uint_as_float(v[4 * k + 2 * e + 1])), c2x2,
+                tc::f2(-m_ref[e], -m_ref[e])));
+            float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+            if (!full) {
+              const int col = ch * 64 + 8 * k + 2 * c4;
+              p0 = col <= lim[e] ? p0 : 0.f;
+              p1 = col + 1 <= lim[e] ? p1 : 0.f;
+            }
+            sum2[e] = tc::fadd2(sum2[e], tc::f2(p0, p1));
+            pk[2 * k + e] = Mma<T>::pack(p0, p1);
           }
-          sum2 = tc::fadd2(sum2, tc::f2(p0, p1));
-          pk[i / 2] = Mma<T>::pack(p0, p1);
-        }
-        tc::st16(ts + hf * 16, pk);
+        tc::st_16x128b_x8(tsw + ch * 32, pk);
       }
       tc::wait_st();
-      const float2 sp = tc::f2_split(sum2);
-      l += sp.x + sp.y;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float2 sp = tc::f2_split(sum2[e]);
+        l[e] += sp.x + sp.y;
+      }
       tc::fence_before();
       mbar_arrive(bar_p);
     }
     if (ok && !mbar_wait_bounded(bar_pv, (ntiles - 1) & 1)) ok = false;
     tc::fence_after();
-    // the row's sum: its two partial sums (both relative to the same max)
-    xsum[cg * 128 + r] = l;
-    named_barrier_sync(1, kTcSoftWarps * 32);
-    float lt = 0.f;
+    float inv[2];
 #pragma unroll
-    for (int g = 0; g < kTcSplit; ++g) lt += xsum[g * 128 + r];
-    const float inv = lt > 0.f ? __fdiv_rn(1.f, lt) : 0.f;
-    T* orow = static_cast<T*>(p.out) + (static_cast<int64_t>(qs + tok0 + tok) * p.num_heads + h0 + hh) * D + cg * kOc;
+    for (int e = 0; e < 2; ++e) {  // the row's sum over its quad (all relative to the same max)
+      float lt = l[e];
+      lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+      lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+      inv[e] = lt > 0.f ? __fdiv_rn(1.f, lt) : 0.f;
+    }
 #pragma unroll
-    for (int oc = 0; oc < kOc; oc += 32) {
+    for (int oc = 0; oc < D; oc += 64) {
       uint32_t w[32];
-      tc::ld32(to + oc, w);
+      tc::ld_16x256b_x8(tow + oc, w);
       tc::wait_ld();
-      if (ok && tok < rows_here) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[4];
+      for (int e = 0; e < 2; ++e) {
+        if (!ok || tok[e] >= rows_here) continue;
+        T* orow = static_cast<T*>(p.out) + (static_cast<int64_t>(qs + tok0 + tok[e]) * p.num_heads + h0 + hh[e]) * D +
+                  oc + 2 * c4;
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            pk[e] = Mma<T>::pack(__uint_as_float(w[c * 8 + 2 * e]) * inv, __uint_as_float(w[c * 8 + 2 * e + 1]) * inv);
-          *reinterpret_cast<uint4*>(orow + oc + c * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<uint32_t*>(orow + 8 * k) =
+              Mma<T>::pack(__uint_as_float(w[4 * k + 2 * e]) * inv[e], __uint_as_float(w[4 * k + 2 * e + 1]) * inv[e]);
       }
     }
   }
