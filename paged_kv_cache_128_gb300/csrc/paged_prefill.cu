@@ -652,17 +652,45 @@ PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn() {
 
 // A 3-D tensor {n0, n1, n2} of 16-bit elements (dim 0 contiguous, dim 1
 // `n0` apart, dim 2 `n0 * n1` apart) with 128-byte-swizzled boxes
-// {64, box1, box2}.
+// {64, box1, box2}.  Encoded maps are kept in a small table keyed by all the
+// arguments, so a caller that reuses its buffers pays the encoding once.
 bool tc_map(const void* base, int64_t n0, int64_t n1, int64_t n2, int box1, int box2, CUtensorMap* out) {
+  struct Key {
+    const void* base;
+    int64_t n0, n1, n2;
+    int box1, box2;
+    bool operator==(const Key& o) const {
+      return base == o.base && n0 == o.n0 && n1 == o.n1 && n2 == o.n2 && box1 == o.box1 && box2 == o.box2;
+    }
+  };
+  constexpr int kSlots = 32;
+  static std::mutex mu;
+  static Key keys[kSlots];
+  static CUtensorMap maps[kSlots];
+  static int used = 0, next = 0;
+  const Key key{base, n0, n1, n2, box1, box2};
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (keys[i] == key) {
+      *out = maps[i];
+      return true;
+    }
   auto fn = tc_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(n0), static_cast<cuuint64_t>(n1), static_cast<cuuint64_t>(n2)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(n0) * 2, static_cast<cuuint64_t>(n0 * n1) * 2};
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box1), static_cast<cuuint32_t>(box2)};
   cuuint32_t estr[3] = {1, 1, 1};
-  return fn(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  CUtensorMap m;
+  if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  const int slot = used < kSlots ? used++ : (next++ % kSlots);
+  keys[slot] = key;
+  maps[slot] = m;
+  *out = m;
+  return true;
 }
 
 bool tc_supported(int block_size) { return block_size >= 16 && block_size % 16 == 0 && kTcKeys % block_size == 0; }
