@@ -166,3 +166,54 @@ def test_prefill_without_query_rows_launches_nothing():
     pk.paged_prefill_attention(out, q, kc, vc, tables, lens, qsl, 0.125, 0)
     torch.cuda.synchronize()
     assert pk.device_error() == 0
+
+
+def test_prefill_attention_over_a_runner_step():
+    """One mixed-batch serving step through the native step runner allocates
+    the step's 8 new sequences and writes their chunk K/V.  Chunked-prefill
+    attention over the runner's own block tables then matches the oracle,
+    whose K/V are the step's original rows, found through the step's slot
+    mapping on the host (sampled chunk rows of every sequence)."""
+    from paged_kv_cache_128_gb300.engine import PagedDecodeEngine
+
+    wl = make_workload("mixed_batch_bf16")
+    dev = torch.device("cuda")
+    vals = make_values(wl, device="cuda")
+    eng = PagedDecodeEngine(wl, dev, max_steps=2)
+    eng.setup(vals)
+    eng.make_runner()
+    out = torch.empty_like(vals.q)
+    eng.runner_step(vals.q, vals.k_step, vals.v_step, out)
+    eng.runner_join()
+    torch.cuda.synchronize()
+    slots, _, _, _ = eng.runner_last_metadata()
+    ids = eng._prefill_ids.copy()
+    lens = np.asarray(eng._prefill_lens, dtype=np.int64)
+    bs = wl.block_size
+    tables, seq_lens = eng.mgr.export(ids.tolist(), int(max(-(-lens // bs))))
+    assert np.array_equal(seq_lens, lens)
+    row_of_slot = {int(s): r for r, s in enumerate(slots) if s >= 0}
+    qsl = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    g = torch.Generator().manual_seed(31)
+    q = torch.randn(int(qsl[-1]), wl.num_heads, wl.head_dim, generator=g).to(wl.torch_dtype)
+    got = torch.full(q.shape, float("nan"), dtype=wl.torch_dtype, device=dev)
+    scale = float(wl.scale)
+    pk.device_error()
+    pk.paged_prefill_attention(got, q.to(dev), eng.k_cache, eng.v_cache, torch.from_numpy(tables).to(dev),
+                               torch.from_numpy(seq_lens).to(dev), torch.from_numpy(qsl).to(dev), scale,
+                               int(lens.max()))
+    torch.cuda.synchronize()
+    assert pk.device_error() == 0
+    got64, q64 = to_f64(got, "bf16"), to_f64(q, "bf16")
+    k_rows, v_rows = to_f64(vals.k_step, "bf16"), to_f64(vals.v_step, "bf16")
+    rng = np.random.default_rng(32)
+    worst = 0.0
+    for b in range(ids.size):
+        n = int(lens[b])
+        rows = [row_of_slot[int(tables[b, i // bs]) * bs + i % bs] for i in range(n)]
+        K, V = k_rows[rows], v_rows[rows]
+        for t in sorted(set(rng.integers(0, n, 10).tolist()) | {0, n - 1}):
+            ref = chunked_prefill_attention(q64[qsl[b] + t:qsl[b] + t + 1], K[:t + 1], V[:t + 1], scale)[0]
+            worst = max(worst, float(np.max(np.abs(got64[qsl[b] + t] - ref))))
+    assert worst <= TOL["bf16"], f"max abs err {worst:.3e}"
+    eng.close_runner()
