@@ -586,7 +586,46 @@ def prefill_setup(ctx, dev, seed=5):
     # flops per (query head, key): 2 D for q.k and 2 D for p v
     keys = sum(ctx + t + 1 for n in chunks for t in range(n))
     return {"args": args, "flops": keys * hq * d * 4, "tokens": T, "seqs": len(chunks), "hq": hq, "hkv": hkv,
-            "d": d, "bs": bs, "kv_bytes": 2 * sum(lens) * hkv * d * 2}
+            "d": d, "bs": bs, "kv_bytes": 2 * sum(lens) * hkv * d * 2, "lens": lens, "chunks": chunks,
+            "tables": tables, "qsl": qsl}
+
+
+def prefill_cpu_baseline(w, budget_s=6.0):
+    """The float64 oracle (one host thread) on a bounded sample of the same
+    call: the first sequence's K/V gathered through its block table, then
+    chunk rows from its last one backwards until about ``budget_s`` pass;
+    causal TFLOP/s of the rows done."""
+    import numpy as np
+    import torch
+    from oracle.attention import chunked_prefill_attention
+    from oracle.paged_cache import gather, to_float64
+
+    out, q, kc, vc = w["args"][:4]
+    scale, bs = w["args"][7], w["bs"]
+    L, n = int(w["lens"][0]), int(w["chunks"][0])
+
+    def f64(t):
+        return to_float64(t.contiguous().view(torch.int16).numpy().view(np.uint16), "bf16")
+
+    nblk = -(-L // bs)
+    table = [int(x) for x in w["tables"][0, :nblk]]
+    idx = torch.tensor(table, dtype=torch.long, device=kc.device)
+    K = gather(f64(kc.index_select(0, idx).cpu()), list(range(nblk)), L)
+    V = gather(f64(vc.index_select(0, idx).cpu()), list(range(nblk)), L)
+    q64 = f64(q[: n].cpu())
+    t0 = time.perf_counter()
+    flops, rows = 0, 0
+    for t in range(n - 1, -1, -1):
+        p_pos = L - n + t
+        chunked_prefill_attention(q64[t:t + 1], K[:p_pos + 1], V[:p_pos + 1], scale)
+        flops += (p_pos + 1) * w["hq"] * w["d"] * 4
+        rows += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"float64 numpy oracle, one host thread: the last {rows} chunk rows of the first sequence "
+                      f"(history + chunk {L} tokens, all {w['hq']} query heads), {dt:.1f} s"}
 
 
 def run_prefill(args):
@@ -635,7 +674,25 @@ def run_prefill(args):
         clk = clocks.stop()
         t = statistics.fmean(ms) / 1e3
         tflops = w["flops"] / t / 1e12
+        # end to end: q copied in from page-locked host memory and the output
+        # copied back, every call, inside the timed region
+        out_d, q_d = w["args"][0], w["args"][1]
+        q_h = q_d.cpu().pin_memory()
+        out_h = torch.empty(out_d.shape, dtype=out_d.dtype, pin_memory=True)
+        e2e_steps = max(10, args.steps // 4)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            q_d.copy_(q_h, non_blocking=True)
+            pk.paged_prefill_attention(*w["args"], stream=stream)
+            out_h.copy_(out_d, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        t_e2e = a.elapsed_time(b) / 1e3 / e2e_steps
         status = pk.device_error()
+        cpu = None if args.no_cpu_baseline else prefill_cpu_baseline(w)
         print(json.dumps({
             "metric": "chunked-prefill paged attention TFLOP/s (causal flops) at 1 GB300",
             "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
@@ -648,6 +705,11 @@ def run_prefill(args):
             "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(tflops / peak, 4), "peak_kind": peak_kind, "flops_per_call": w["flops"],
                          "traffic": None},
+            "e2e": {"value": round(w["flops"] / t_e2e / 1e12, 2), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": q_d.numel() * q_d.element_size(),
+                    "d2h_bytes_per_step": out_d.numel() * out_d.element_size(),
+                    "ms_per_step": round(t_e2e * 1e3, 5), "l2": "not flushed between calls"},
+            "cpu_baseline": cpu,
             "gpu_launches": args.steps, "clocks": clk, "device_error": status}))
         if status:
             sys.exit(1)
