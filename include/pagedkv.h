@@ -541,7 +541,10 @@ typedef struct {
   size_t workspace_bytes;
   void* stream;                /* compute stream (cudaStream_t) */
   int32_t host_io;             /* 0: q/k/v/out given to kvstep_run are device buffers;
-                                  1: page-locked host buffers, copied in and out by the runner */
+                                  1: page-locked host buffers, copied in and out by the runner;
+                                  2: q/k/v staged by the caller in the runner's page-locked
+                                     buffers (kvstep_stage_buffer) and copied in with the step's
+                                     metadata in one copy; out a page-locked host buffer */
   int32_t num_layers;          /* layers sharing the block tables (0 or 1: one) */
   int64_t cache_layer_stride;  /* elements between consecutive layers' caches (num_layers > 1) */
   int32_t cache_fp8;           /* 1: k_cache/v_cache hold E4M3 codes with the scales below; each step
@@ -561,9 +564,11 @@ int kvstep_destroy(kvstep_t h);
  * layers, each of the four is that many such tensors back to back, and the
  * step's metadata, built and copied once, serves one fused launch per
  * layer over that layer's cache): device buffers
- * (host_io = 0; read and written in cfg.stream order) or page-locked host
+ * (host_io = 0; read and written in cfg.stream order), page-locked host
  * buffers (host_io = 1; q/k/v are read by the copy issued here, out is
- * written when the step's device-to-host copy completes, see kvstep_join).
+ * written when the step's device-to-host copy completes, see kvstep_join),
+ * or, with host_io = 2, q/k/v NULL (the inputs were staged with
+ * kvstep_stage_buffer) and out a page-locked host buffer as for host_io = 1.
  * The id arguments are those of kvbm_prepare_step; n_decode must equal
  * cfg.num_seqs, the pads must be strictly increasing and in range, and the
  * step's rows must add up to cfg.num_step_tokens (else KV_ERR_INVALID_ARG,
@@ -575,6 +580,18 @@ int kvstep_run(kvstep_t h, const void* q, const void* k, const void* v, void* ou
                const int64_t* free_ids, int64_t n_free, const int64_t* prefill_ids,
                const int64_t* prefill_lens, int64_t n_prefill, const int64_t* decode_ids,
                int64_t n_decode, const int64_t* pad_positions, int64_t n_pad);
+
+/* host_io = 2: page-locked host addresses where a step's q, k and v are to
+ * be written (layouts as for kvstep_run; 256-byte aligned).  The runner
+ * rotates four such slots, one per step in turn.  slot = -1: the slot the
+ * next kvstep_run copies from, after waiting for the copy that last read
+ * it; the caller writes its inputs there, then calls kvstep_run with q, k
+ * and v NULL.  slot = 0..3: that slot, without waiting (for filling slots
+ * before any step; the caller must not write a slot whose copy may still be
+ * running).  slot_out (nullable) receives the slot index.  Any pointer
+ * output may be NULL.  KV_ERR_INVALID_ARG for another host_io mode or a
+ * slot out of range. */
+int kvstep_stage_buffer(kvstep_t h, int32_t slot, void** q, void** k, void** v, int32_t* slot_out);
 
 /* Make `stream` wait for every copy and kernel the runner has issued. */
 int kvstep_join(kvstep_t h, void* stream);

@@ -115,6 +115,8 @@ SIGNATURES = {
     "kvstep_run": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_void_p,
                            c_int64, c_void_p, c_int64, c_void_p, c_int64]),
     "kvstep_join": (c_int, [c_void_p, c_void_p]),
+    "kvstep_stage_buffer": (c_int, [c_void_p, c_int32, POINTER(c_void_p), POINTER(c_void_p), POINTER(c_void_p),
+                                    POINTER(c_int32)]),
     "kvstep_last_buffers": (c_int, [c_void_p, POINTER(c_void_p), POINTER(c_void_p), POINTER(c_void_p),
                                     POINTER(c_void_p)]),
     "kv_mapped_device_pointer": (c_int, [c_void_p, POINTER(c_void_p)]),

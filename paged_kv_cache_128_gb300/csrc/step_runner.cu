@@ -57,6 +57,7 @@ struct kvstep_s {
   pagedkv::Side side[kNumBufs];
   int32_t layers = 1;
   size_t q_bytes = 0, kv_bytes = 0;  // one layer's
+  size_t stage_q = 0, stage_k = 0, stage_v = 0, stage_bytes = 0;  // host_io = 2: byte offsets in a slot's block
   cudaStream_t compute = nullptr, h2d = nullptr, d2h = nullptr;
   cudaEvent_t copied[kNumBufs] = {};    // H2D of buffer i done
   cudaEvent_t done[kNumBufs] = {};      // kernel that read buffer i done
@@ -71,8 +72,12 @@ void release(kvstep_s* h) {
   for (int i = 0; i < kNumBufs; ++i) {
     if (h->h_meta[i]) cudaFreeHost(h->h_meta[i]);
     if (h->d_meta[i]) cudaFree(h->d_meta[i]);
-    for (void* p : {h->side[i].q, h->side[i].k, h->side[i].v, h->side[i].out})
-      if (p) cudaFree(p);
+    if (h->cfg.host_io == 2) {  // q/k/v live inside d_meta[i]
+      if (h->side[i].out) cudaFree(h->side[i].out);
+    } else {
+      for (void* p : {h->side[i].q, h->side[i].k, h->side[i].v, h->side[i].out})
+        if (p) cudaFree(p);
+    }
     for (cudaEvent_t e : {h->copied[i], h->done[i], h->out_back[i]})
       if (e) cudaEventDestroy(e);
   }
@@ -103,6 +108,7 @@ extern "C" int kvstep_create(kvbm_t mgr, const kvstep_config_t* cfg, kvstep_t* o
       c.max_seq_len <= 0 || c.num_step_tokens < c.num_seqs || !c.k_cache || !c.v_cache)
     return KV_ERR_INVALID_ARG;
   if (c.dtype != KV_DTYPE_F32 && c.dtype != KV_DTYPE_F16 && c.dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
+  if (c.host_io < 0 || c.host_io > 2) return KV_ERR_INVALID_ARG;
   const int32_t layers = c.num_layers > 1 ? c.num_layers : 1;
   if (c.cache_fp8 && (!c.k_scales || !c.v_scales || c.dtype == KV_DTYPE_F32)) return KV_ERR_INVALID_ARG;
   if (c.num_layers < 0 || c.num_layers > 65535 ||
@@ -121,14 +127,33 @@ extern "C" int kvstep_create(kvbm_t mgr, const kvstep_config_t* cfg, kvstep_t* o
   const size_t es = pagedkv::dtype_bytes(c.dtype);
   h->q_bytes = static_cast<size_t>(c.num_seqs) * c.num_heads * c.head_dim * es;
   h->kv_bytes = static_cast<size_t>(c.num_step_tokens) * c.num_kv_heads * c.head_dim * es;
+  // host_io = 2: one block per slot holds [metadata | q | k | v] (each part
+  // 256-byte aligned), the same on the host and on the device, so a step is
+  // one host-to-device copy
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  size_t block_bytes = meta_bytes;
+  if (c.host_io == 2) {
+    const size_t L = static_cast<size_t>(layers);
+    h->stage_q = up(meta_bytes);
+    h->stage_k = h->stage_q + up(h->q_bytes * L);
+    h->stage_v = h->stage_k + up(h->kv_bytes * L);
+    h->stage_bytes = h->stage_v + h->kv_bytes * L;
+    block_bytes = h->stage_bytes;
+  }
   cudaError_t e = cudaGetDevice(&h->device);
   for (int i = 0; i < kNumBufs && e == cudaSuccess; ++i) {
-    e = cudaHostAlloc(reinterpret_cast<void**>(&h->h_meta[i]), meta_bytes, cudaHostAllocDefault);
-    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&h->d_meta[i]), meta_bytes);
+    e = cudaHostAlloc(reinterpret_cast<void**>(&h->h_meta[i]), block_bytes, cudaHostAllocDefault);
+    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&h->d_meta[i]), block_bytes);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->copied[i], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->done[i], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->out_back[i], cudaEventDisableTiming);
-    if (e == cudaSuccess && c.host_io) {
+    if (e == cudaSuccess && c.host_io == 2) {
+      char* d = reinterpret_cast<char*>(h->d_meta[i]);
+      h->side[i].q = d + h->stage_q;
+      h->side[i].k = d + h->stage_k;
+      h->side[i].v = d + h->stage_v;
+      e = cudaMalloc(&h->side[i].out, h->q_bytes * layers);
+    } else if (e == cudaSuccess && c.host_io) {
       e = cudaMalloc(&h->side[i].q, h->q_bytes * layers);
       if (e == cudaSuccess) e = cudaMalloc(&h->side[i].out, h->q_bytes * layers);
       if (e == cudaSuccess) e = cudaMalloc(&h->side[i].k, h->kv_bytes * layers);
@@ -163,8 +188,9 @@ extern "C" int kvstep_run(kvstep_t h, const void* q, const void* k, const void* 
                           const int64_t* free_ids, int64_t n_free, const int64_t* prefill_ids,
                           const int64_t* prefill_lens, int64_t n_prefill, const int64_t* decode_ids,
                           int64_t n_decode, const int64_t* pad_positions, int64_t n_pad) {
-  if (!h || !q || !k || !v || !out) return KV_ERR_INVALID_ARG;
+  if (!h || !out) return KV_ERR_INVALID_ARG;
   const kvstep_config_t& c = h->cfg;
+  if (c.host_io != 2 && (!q || !k || !v)) return KV_ERR_INVALID_ARG;
   if (n_decode != c.num_seqs || n_pad < 0 || n_prefill < 0 || (n_prefill && !prefill_lens)) return KV_ERR_INVALID_ARG;
   int64_t n_pre_tokens = 0;
   for (int64_t i = 0; i < n_prefill; ++i) n_pre_tokens += prefill_lens[i] > 0 ? prefill_lens[i] : 0;
@@ -201,10 +227,17 @@ extern "C" int kvstep_run(kvstep_t h, const void* q, const void* k, const void* 
   // H2D on the side stream, after the kernel that read device buffer i
   if (h->used[i]) e = cudaStreamWaitEvent(h->h2d, h->done[i], 0);
   const size_t meta_bytes = static_cast<size_t>(h->meta_ints) * sizeof(int32_t);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(h->d_meta[i], h->h_meta[i], meta_bytes, cudaMemcpyHostToDevice, h->h2d);
+  // staged inputs travel with the metadata in one copy
+  const size_t copy_bytes = c.host_io == 2 ? h->stage_bytes : meta_bytes;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h->d_meta[i], h->h_meta[i], copy_bytes, cudaMemcpyHostToDevice, h->h2d);
   const void *dq = q, *dk = k, *dv = v;
   void* dout = out;
-  if (c.host_io) {
+  if (c.host_io == 2) {
+    dq = h->side[i].q;
+    dk = h->side[i].k;
+    dv = h->side[i].v;
+    dout = h->side[i].out;
+  } else if (c.host_io) {
     dq = h->side[i].q;
     dk = h->side[i].k;
     dv = h->side[i].v;
@@ -268,6 +301,24 @@ extern "C" int kvstep_run(kvstep_t h, const void* q, const void* k, const void* 
   }
   h->used[i] = true;
   return pagedkv::cuda_status(e);
+}
+
+extern "C" int kvstep_stage_buffer(kvstep_t h, int32_t slot, void** q, void** k, void** v, int32_t* slot_out) {
+  if (!h || h->cfg.host_io != 2 || slot < -1 || slot >= kNumBufs) return KV_ERR_INVALID_ARG;
+  int i = slot;
+  if (slot == -1) {  // the next step's slot, once the copy that last read it has run
+    i = (h->cur + 1) % kNumBufs;
+    if (h->used[i]) {
+      const cudaError_t e = cudaEventSynchronize(h->copied[i]);
+      if (e != cudaSuccess) return pagedkv::cuda_status(e);
+    }
+  }
+  char* base = reinterpret_cast<char*>(h->h_meta[i]);
+  if (q) *q = base + h->stage_q;
+  if (k) *k = base + h->stage_k;
+  if (v) *v = base + h->stage_v;
+  if (slot_out) *slot_out = i;
+  return KV_OK;
 }
 
 extern "C" int kvstep_join(kvstep_t h, void* stream) {

@@ -26,7 +26,7 @@ import torch
 
 import ctypes
 
-from ._lib import check, kvstep_config_t, lib
+from ._lib import KVError, check, kvstep_config_t, lib
 from .block_manager import KVBlockManager
 from .inputs import Values, Workload, pad_positions, sentinel_bits
 from .kernels import (alloc_workspace, decode_plan, dtype_code, paged_decode_attention, paged_decode_attention_fp8,
@@ -300,12 +300,16 @@ class PagedDecodeEngine:
         return self.out
 
     # ------------------------------------------------------- native runner
-    def make_runner(self, host_io: bool = False, stream: Optional[torch.cuda.Stream] = None) -> None:
+    def make_runner(self, host_io: int = 0, stream: Optional[torch.cuda.Stream] = None) -> None:
         """Create the native step runner (kvstep_*): afterwards each
         ``runner_step`` is ONE library call doing a1 (kvbm_prepare_step, the
         async metadata copy on a side stream) and a2-a8 (the fused launch).
-        With ``host_io`` the step's q/k/v and output are page-locked host
-        buffers that the runner copies in and out on its side streams."""
+        ``host_io`` 1 (or True): the step's q/k/v and output are page-locked
+        host buffers that the runner copies in and out on its side streams.
+        ``host_io`` 2: q/k/v are staged in the runner's own page-locked slots
+        (``runner_stage``) and travel with the metadata in one copy; the
+        output is a page-locked host buffer."""
+        host_io = int(host_io)
         wl = self.wl
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
         ws = self.workspace
@@ -315,7 +319,7 @@ class PagedDecodeEngine:
             max_seq_len=self.max_seq_len, scale=float(wl.scale), dtype=dtype_code(wl.torch_dtype),
             num_step_tokens=wl.num_step_tokens, k_cache=self.k_cache.data_ptr(), v_cache=self.v_cache.data_ptr(),
             workspace=ws.data_ptr() if ws is not None else None,
-            workspace_bytes=ws.numel() if ws is not None else 0, stream=s.cuda_stream, host_io=1 if host_io else 0,
+            workspace_bytes=ws.numel() if ws is not None else 0, stream=s.cuda_stream, host_io=host_io,
             cache_fp8=1 if self.fp8 else 0, k_scales=self.k_scales.data_ptr() if self.fp8 else None,
             v_scales=self.v_scales.data_ptr() if self.fp8 else None)
         self.close_runner()
@@ -323,16 +327,41 @@ class PagedDecodeEngine:
         check(lib().kvstep_create(self.mgr._h, ctypes.byref(cfg), ctypes.byref(h)), "kvstep_create")
         self._runner = h
         self._runner_stream = s
+        self._runner_host_io = host_io
         self._runner_args = (
             self._decode_ids.ctypes.data, self._decode_ids.size,
             self._pad_pos.ctypes.data if self._pad_pos.size else None, self._pad_pos.size)
 
-    def runner_step(self, q: torch.Tensor, k_step: torch.Tensor, v_step: torch.Tensor, out: torch.Tensor) -> None:
-        """One step through the native runner (a1-a8 in one call)."""
+    def runner_stage(self, slot: int = -1):
+        """host_io 2: page-locked CPU tensors (q, k, v) viewing a staging
+        slot of the runner -- slot -1 is the next step's (after its previous
+        copy has run), 0..3 a given one (filled before any step)."""
+        if getattr(self, "_runner_host_io", 0) != 2:
+            raise KVError(1, "runner_stage needs a runner made with host_io=2")
+        ptrs = [ctypes.c_void_p() for _ in range(3)]
+        got = ctypes.c_int32()
+        check(lib().kvstep_stage_buffer(self._runner, int(slot), *[ctypes.byref(x) for x in ptrs],
+                                        ctypes.byref(got)), "kvstep_stage_buffer")
+        wl = self.wl
+        es = torch.empty((), dtype=wl.torch_dtype).element_size()
+        shapes = [(wl.num_seqs, wl.num_heads, wl.head_dim), (wl.num_step_tokens, wl.num_kv_heads, wl.head_dim),
+                  (wl.num_step_tokens, wl.num_kv_heads, wl.head_dim)]
+        views = []
+        for ptr, shape in zip(ptrs, shapes):
+            nbytes = int(np.prod(shape)) * es
+            buf = (ctypes.c_uint8 * nbytes).from_address(ptr.value)
+            views.append(torch.frombuffer(buf, dtype=torch.uint8).view(wl.torch_dtype).view(shape))
+        return tuple(views)
+
+    def runner_step(self, q: Optional[torch.Tensor], k_step: Optional[torch.Tensor], v_step: Optional[torch.Tensor],
+                    out: torch.Tensor) -> None:
+        """One step through the native runner (a1-a8 in one call); with
+        host_io 2, q/k/v are None (staged with ``runner_stage``)."""
         self._check_room()
         n_free, n_pre = self._advance_ids()
         dec, n_dec, pads, n_pad = self._runner_args
-        check(lib().kvstep_run(self._runner, q.data_ptr(), k_step.data_ptr(), v_step.data_ptr(), out.data_ptr(),
+        ptr = lambda t: t.data_ptr() if t is not None else None
+        check(lib().kvstep_run(self._runner, ptr(q), ptr(k_step), ptr(v_step), out.data_ptr(),
                                self._free_ids.ctypes.data if n_free else None, n_free,
                                self._prefill_ids.ctypes.data if n_pre else None,
                                self._prefill_lens.ctypes.data if n_pre else None, n_pre, dec, n_dec, pads, n_pad),

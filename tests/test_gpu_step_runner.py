@@ -29,7 +29,7 @@ def bits(t):
 
 
 @pytest.mark.parametrize("name", NAMES)
-@pytest.mark.parametrize("host_io", [False, True], ids=["device_io", "host_io"])
+@pytest.mark.parametrize("host_io", [0, 1, 2], ids=["device_io", "host_io", "staged_io"])
 def test_runner_matches_python_step(name, host_io):
     wl = make_workload(name)
     dev = torch.device("cuda")
@@ -39,13 +39,19 @@ def test_runner_matches_python_step(name, host_io):
     ref.setup(vals)
     run.setup(vals)
     run.make_runner(host_io=host_io)
-    if host_io:
+    if host_io == 1:
         q, k, v = (t.cpu().pin_memory() for t in (vals.q, vals.k_step, vals.v_step))
+        out = torch.empty(vals.q.shape, dtype=vals.q.dtype, pin_memory=True)
+    elif host_io == 2:
+        q = k = v = None
         out = torch.empty(vals.q.shape, dtype=vals.q.dtype, pin_memory=True)
     else:
         q, k, v, out = vals.q, vals.k_step, vals.v_step, torch.empty_like(vals.q)
     for _ in range(4):
         a = ref.step(vals.q, vals.k_step, vals.v_step).clone()
+        if host_io == 2:  # this step's slot, written after its previous copy has run
+            for dst, src in zip(run.runner_stage(-1), (vals.q, vals.k_step, vals.v_step)):
+                dst.copy_(src.cpu())
         run.runner_step(q, k, v, out)
         run.runner_join()
         torch.cuda.synchronize()
