@@ -5,7 +5,8 @@ float64 with an explicit causal-with-offset mask (chunk token t may see keys
 0..L-n+t) and the GQA heads repeated; a chunk of one token is decode; the
 first token of a sequence with no history returns its own V row exactly;
 and changing keys or values after a token's position leaves its output
-unchanged (causality), while changing one before it does not.
+unchanged (causality), while changing one before it does not; with q = 0
+every row is the plain mean of V over its prefix (closed form).
 """
 
 import numpy as np
@@ -68,3 +69,22 @@ def test_causality():
     assert not np.allclose(chunked_prefill_attention(q, K3, V, 0.35)[t], base[t])
     with pytest.raises(ValueError):
         chunked_prefill_attention(rng.standard_normal((12, 4, 8)), K, V, 0.35)
+
+
+@pytest.mark.parametrize("ctx", [0, 9])
+def test_zero_query_gives_prefix_means(ctx):
+    """q = 0 makes every score equal, so chunk token t (position ctx + t)
+    returns the plain mean of V over keys 0 .. ctx + t, for every query head
+    of its kv head: a closed form that pins the causal bound and the history
+    offset without any attention routine."""
+    rng = np.random.default_rng(40 + ctx)
+    n, hq, hkv, d = 6, 4, 2, 8
+    L = ctx + n
+    K = rng.standard_normal((L, hkv, d))
+    V = rng.standard_normal((L, hkv, d))
+    got = chunked_prefill_attention(np.zeros((n, hq, d)), K, V, 0.3)
+    for t in range(n):
+        p = ctx + t
+        for h in range(hq):
+            want = V[:p + 1, h // (hq // hkv)].mean(axis=0)
+            np.testing.assert_allclose(got[t, h], want, rtol=0, atol=1e-13)
