@@ -67,6 +67,47 @@ class FreeList {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Set of sequence ids for one call's duplicate checks: open addressing over
+// a reused table whose slots are valid only for the current generation, so
+// clearing it is one increment and inserting allocates nothing.
+class IdSet {
+ public:
+  // Empty the set, with room for n ids.
+  void reset(int64_t n) {
+    size_t cap = 16;
+    while (cap < 2 * static_cast<size_t>(n) + 1) cap <<= 1;
+    if (cap > keys_.size()) {
+      keys_.assign(cap, 0);
+      gen_.assign(cap, 0);
+      cur_ = 0;
+    }
+    if (++cur_ == 0) {  // generation counter wrapped: every slot is stale again
+      std::fill(gen_.begin(), gen_.end(), 0u);
+      cur_ = 1;
+    }
+  }
+  // false when id was already in the set
+  bool insert(int64_t id) {
+    size_t i = find(id);
+    if (gen_[i] == cur_) return false;
+    gen_[i] = cur_;
+    keys_[i] = id;
+    return true;
+  }
+  bool contains(int64_t id) const { return gen_[find(id)] == cur_; }
+
+ private:
+  size_t find(int64_t id) const {  // the slot holding id, or the empty slot where it would go
+    const size_t mask = keys_.size() - 1;
+    size_t i = static_cast<size_t>(static_cast<uint64_t>(id) * 0x9E3779B97F4A7C15ull >> 20) & mask;
+    while (gen_[i] == cur_ && keys_[i] != id) i = (i + 1) & mask;
+    return i;
+  }
+  std::vector<int64_t> keys_;
+  std::vector<uint32_t> gen_;
+  uint32_t cur_ = 0;
+};
+
 }  // namespace
 
 struct kvbm_s {
@@ -77,8 +118,21 @@ struct kvbm_s {
   std::unordered_map<int64_t, Sequence> seqs;
   std::unordered_set<int64_t> released;
   std::vector<int32_t> copy_src, copy_dst;  // copy-on-write copies not yet taken
+  IdSet step_ids;                      // kvbm_prepare_step's duplicate checks
+  std::vector<uint32_t> block_mark;    // kvbm_free_sequence's duplicate-block check, by generation
+  uint32_t block_gen = 0;
 
-  kvbm_s(int64_t nb, int32_t bs) : num_blocks(nb), block_size(bs), free_list(nb), ref_count(nb, 0) {}
+  kvbm_s(int64_t nb, int32_t bs)
+      : num_blocks(nb), block_size(bs), free_list(nb), ref_count(nb, 0), block_mark(nb, 0) {}
+
+  // A fresh generation for block_mark (all marks stale).
+  uint32_t next_block_gen() {
+    if (++block_gen == 0) {
+      std::fill(block_mark.begin(), block_mark.end(), 0u);
+      block_gen = 1;
+    }
+    return block_gen;
+  }
 
   bool is_free(int32_t b) const { return ref_count[static_cast<size_t>(b)] == 0; }
   int32_t take_front() {
@@ -322,11 +376,11 @@ int kvbm_decode_step(kvbm_t h, const int64_t* seq_ids, int64_t n, int64_t max_bl
   if (!h || n < 0 || (n > 0 && !seq_ids) || max_blocks < 0) return KV_ERR_INVALID_ARG;
   return guarded([&] {
     std::vector<Sequence*> seqs(static_cast<size_t>(n));
-    std::unordered_set<int64_t> seen;
-    seen.reserve(static_cast<size_t>(n) * 2);
+    IdSet& seen = h->step_ids;
+    seen.reset(n);
     int64_t need = 0;
     for (int64_t i = 0; i < n; ++i) {
-      if (!seen.insert(seq_ids[i]).second) return static_cast<int>(KV_ERR_INVALID_ARG);
+      if (!seen.insert(seq_ids[i])) return static_cast<int>(KV_ERR_INVALID_ARG);
       Sequence* s = h->find(seq_ids[i]);
       if (!s) return static_cast<int>(KV_ERR_UNKNOWN_SEQ);
       int64_t grow = h->blocks_needed(*s, 1);
@@ -366,20 +420,21 @@ int kvbm_prepare_step(kvbm_t h, const int64_t* free_ids, int64_t n_free, const i
       if (st != KV_OK) return st;
     }
     // 2-3. validate the prefills and appends and their block need, before any change
-    std::unordered_set<int64_t> seen;
+    IdSet& seen = h->step_ids;
+    seen.reset(n_prefill + n_decode);
     int64_t n_prefill_tokens = 0, need = 0;
     for (int64_t i = 0; i < n_prefill; ++i) {
       if (prefill_ids[i] < 0 || prefill_lens[i] <= 0) return static_cast<int>(KV_ERR_INVALID_ARG);
       if (h->seqs.count(prefill_ids[i])) return static_cast<int>(KV_ERR_DUPLICATE_SEQ);
-      if (!seen.insert(prefill_ids[i]).second) return static_cast<int>(KV_ERR_DUPLICATE_SEQ);
+      if (!seen.insert(prefill_ids[i])) return static_cast<int>(KV_ERR_DUPLICATE_SEQ);
       n_prefill_tokens += prefill_lens[i];
       need += ceil_div(prefill_lens[i], h->block_size);
     }
     std::vector<Sequence*> dec(static_cast<size_t>(n_decode));
     for (int64_t i = 0; i < n_decode; ++i) {
       Sequence* sq = h->find(decode_ids[i]);
-      if (!sq) return static_cast<int>(seen.count(decode_ids[i]) ? KV_ERR_INVALID_ARG : KV_ERR_UNKNOWN_SEQ);
-      if (!seen.insert(decode_ids[i]).second) return static_cast<int>(KV_ERR_INVALID_ARG);
+      if (!sq) return static_cast<int>(seen.contains(decode_ids[i]) ? KV_ERR_INVALID_ARG : KV_ERR_UNKNOWN_SEQ);
+      if (!seen.insert(decode_ids[i])) return static_cast<int>(KV_ERR_INVALID_ARG);
       const int64_t grow = h->blocks_needed(*sq, 1);
       if ((block_tables || seq_lens) && ceil_div(sq->length + 1, h->block_size) > max_blocks)
         return static_cast<int>(KV_ERR_INVALID_ARG);
@@ -429,10 +484,11 @@ int kvbm_free_sequence(kvbm_t h, int64_t seq_id) {
   if (it == h->seqs.end()) return h->released.count(seq_id) ? KV_ERR_DOUBLE_FREE : KV_ERR_UNKNOWN_SEQ;
   const std::vector<int32_t>& table = it->second.table;
   // LLM-algo ch.22 release checks: in range, no duplicates, none already free.
-  std::unordered_set<int32_t> seen;
+  const uint32_t gen = h->next_block_gen();
   for (int32_t b : table) {
     if (b < 0 || b >= h->num_blocks) return KV_ERR_INVARIANT;
-    if (!seen.insert(b).second) return KV_ERR_INVARIANT;
+    if (h->block_mark[static_cast<size_t>(b)] == gen) return KV_ERR_INVARIANT;
+    h->block_mark[static_cast<size_t>(b)] = gen;
     if (h->is_free(b)) return KV_ERR_INVARIANT;
   }
   return guarded([&] {

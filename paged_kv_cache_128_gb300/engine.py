@@ -73,7 +73,8 @@ class PagedDecodeEngine:
             self.k_cache.view(iv).fill_(fill)
             self.v_cache.view(iv).fill_(fill)
         B = wl.num_seqs
-        self.max_seq_len = int(wl.cached_lens.max()) + 1 + max_steps
+        self._max_cached = int(wl.cached_lens.max())
+        self.max_seq_len = self._max_cached + 1 + max_steps
         self.max_blocks = -(-self.max_seq_len // wl.block_size)
         self.plan = decode_plan(B, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size, self.max_seq_len,
                                 dt, blocks_per_split)
@@ -250,7 +251,7 @@ class PagedDecodeEngine:
         return self.attention(q)
 
     def _check_room(self) -> None:
-        if self.steps_done + 1 > self.max_seq_len - int(self.wl.cached_lens.max()):
+        if self.steps_done + 1 > self.max_seq_len - self._max_cached:
             raise RuntimeError("engine sized for fewer steps")
 
     def step(self, q: torch.Tensor, k_step: torch.Tensor, v_step: torch.Tensor) -> torch.Tensor:
