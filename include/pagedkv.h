@@ -191,6 +191,19 @@ int kvbm_get_block_table(kvbm_t h, int64_t seq_id, int32_t* out, int64_t cap, in
 int kvbm_export(kvbm_t h, const int64_t* seq_ids, int64_t n, int64_t max_blocks,
                 int32_t* block_tables, int32_t* seq_lens);
 
+/* kvbm_export's block tables written as an update of a buffer that already
+ * holds an earlier export: for row i, prev_ids[i] and prev_nblocks[i] say
+ * which sequence the row held and how many of its entries were blocks (the
+ * rest -1), as this call left them (initialise prev_ids to -1 for a buffer
+ * never exported into).  A row that held the same sequence gets its block
+ * entries written and -1 only over entries that were blocks before; any
+ * other row is written in full.  The result equals kvbm_export's, with
+ * the same max_blocks for every call on one buffer.  prev_ids /
+ * prev_nblocks are updated.  All caller-owned host memory; validation and
+ * errors as kvbm_export (nothing written on an error). */
+int kvbm_export_update(kvbm_t h, const int64_t* seq_ids, int64_t n, int64_t max_blocks, int32_t* block_tables,
+                       int64_t* prev_ids, int32_t* prev_nblocks);
+
 /* KV_OK iff: every table entry is in range and appears once in its table,
  * each block's reference count equals the table entries referring to it,
  * the free list holds exactly the unreferenced blocks once each, referenced

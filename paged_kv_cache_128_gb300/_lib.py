@@ -68,6 +68,7 @@ SIGNATURES = {
     "kvbm_seq_len": (c_int, [c_void_p, c_int64, P64]),
     "kvbm_get_block_table": (c_int, [c_void_p, c_int64, P32, c_int64, P64]),
     "kvbm_export": (c_int, [c_void_p, P64, c_int64, c_int64, P32, P32]),
+    "kvbm_export_update": (c_int, [c_void_p, P64, c_int64, c_int64, P32, P64, P32]),
     "kvbm_check_invariants": (c_int, [c_void_p]),
     "kvbm_stats": (c_int, [c_void_p, POINTER(kvbm_stats_t)]),
     "kvbm_allocation_report": (c_int, [c_void_p, c_int64, P64, P64, P64, POINTER(c_double)]),

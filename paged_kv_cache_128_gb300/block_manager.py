@@ -184,6 +184,20 @@ class KVBlockManager:
               "kvbm_export")
         return tables, lens
 
+    def export_update(self, seq_ids, max_blocks: int, tables: np.ndarray, prev_ids: np.ndarray,
+                      prev_nblocks: np.ndarray) -> None:
+        """kvbm_export_update: refresh ``tables`` ([n, max_blocks] int32, an
+        earlier export described by ``prev_ids`` int64 / ``prev_nblocks``
+        int32, both [n] and updated in place) to the current export."""
+        ids = _ids(seq_ids)
+        for a, dt in ((tables, np.int32), (prev_ids, np.int64), (prev_nblocks, np.int32)):
+            if a.dtype != dt or not a.flags.c_contiguous:
+                raise KVError(1, "export_update buffers: contiguous int32 tables / int64 ids / int32 counts")
+        if tables.shape != (ids.size, max_blocks) or prev_ids.size != ids.size or prev_nblocks.size != ids.size:
+            raise KVError(1, "export_update buffer shapes")
+        check(self._lib.kvbm_export_update(self._h, _i64(ids), ids.size, max_blocks, _i32(tables), _i64(prev_ids),
+                                           _i32(prev_nblocks)), "kvbm_export_update")
+
     def check_invariants(self) -> bool:
         st = self._lib.kvbm_check_invariants(self._h)
         if st not in (0, 6):

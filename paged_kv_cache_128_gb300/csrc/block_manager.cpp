@@ -119,6 +119,7 @@ struct kvbm_s {
   std::unordered_set<int64_t> released;
   std::vector<int32_t> copy_src, copy_dst;  // copy-on-write copies not yet taken
   IdSet step_ids;                      // kvbm_prepare_step's duplicate checks
+  std::vector<const Sequence*> export_rows;  // kvbm_export_update's rows, validated before any write
   std::vector<uint32_t> block_mark;    // kvbm_free_sequence's duplicate-block check, by generation
   uint32_t block_gen = 0;
 
@@ -369,6 +370,36 @@ int kvbm_export(kvbm_t h, const int64_t* seq_ids, int64_t n, int64_t max_blocks,
     if (seq_lens) seq_lens[i] = static_cast<int32_t>(s.length);
   }
   return KV_OK;
+}
+
+int kvbm_export_update(kvbm_t h, const int64_t* seq_ids, int64_t n, int64_t max_blocks, int32_t* block_tables,
+                       int64_t* prev_ids, int32_t* prev_nblocks) {
+  if (!h || n < 0 || max_blocks < 0 || (n > 0 && (!seq_ids || !block_tables || !prev_ids || !prev_nblocks)))
+    return KV_ERR_INVALID_ARG;
+  return guarded([&] {
+    std::vector<const Sequence*>& rows = h->export_rows;
+    rows.resize(static_cast<size_t>(n));
+    for (int64_t i = 0; i < n; ++i) {  // validate everything before writing
+      const Sequence* s = h->find(seq_ids[i]);
+      if (!s) return static_cast<int>(KV_ERR_UNKNOWN_SEQ);
+      if (static_cast<int64_t>(s->table.size()) > max_blocks) return static_cast<int>(KV_ERR_INVALID_ARG);
+      rows[static_cast<size_t>(i)] = s;
+    }
+    for (int64_t i = 0; i < n; ++i) {
+      const Sequence& s = *rows[static_cast<size_t>(i)];
+      int32_t* row = block_tables + i * max_blocks;
+      const int64_t nb = static_cast<int64_t>(s.table.size());
+      std::copy(s.table.begin(), s.table.end(), row);
+      // entries past nb: -1 already where the row held this sequence before,
+      // up to its previous block count; everything else is written
+      const int32_t pn = prev_nblocks[i];
+      const int64_t stale = prev_ids[i] == seq_ids[i] && pn >= 0 && pn <= max_blocks ? pn : max_blocks;
+      if (stale > nb) std::fill(row + nb, row + stale, -1);
+      prev_ids[i] = seq_ids[i];
+      prev_nblocks[i] = static_cast<int32_t>(nb);
+    }
+    return static_cast<int>(KV_OK);
+  });
 }
 
 int kvbm_decode_step(kvbm_t h, const int64_t* seq_ids, int64_t n, int64_t max_blocks,

@@ -29,6 +29,8 @@
 #include <cstdint>
 #include <cstring>
 #include <new>
+#include <algorithm>
+#include <vector>
 
 #include "common.cuh"
 
@@ -58,6 +60,10 @@ struct kvstep_s {
   int32_t layers = 1;
   size_t q_bytes = 0, kv_bytes = 0;  // one layer's
   size_t stage_q = 0, stage_k = 0, stage_v = 0, stage_bytes = 0;  // host_io = 2: byte offsets in a slot's block
+  // per metadata buffer: the sequence and block count each table row held
+  // at its last export (kvbm_export_update rewrites only what changed)
+  std::vector<int64_t> row_ids[kNumBufs];
+  std::vector<int32_t> row_nblocks[kNumBufs];
   cudaStream_t compute = nullptr, h2d = nullptr, d2h = nullptr;
   cudaEvent_t copied[kNumBufs] = {};    // H2D of buffer i done
   cudaEvent_t done[kNumBufs] = {};      // kernel that read buffer i done
@@ -140,6 +146,10 @@ extern "C" int kvstep_create(kvbm_t mgr, const kvstep_config_t* cfg, kvstep_t* o
     h->stage_bytes = h->stage_v + h->kv_bytes * L;
     block_bytes = h->stage_bytes;
   }
+  for (int i = 0; i < kNumBufs; ++i) {
+    h->row_ids[i].assign(static_cast<size_t>(c.num_seqs), -1);  // never exported into
+    h->row_nblocks[i].assign(static_cast<size_t>(c.num_seqs), 0);
+  }
   cudaError_t e = cudaGetDevice(&h->device);
   for (int i = 0; i < kNumBufs && e == cudaSuccess; ++i) {
     e = cudaHostAlloc(reinterpret_cast<void**>(&h->h_meta[i]), block_bytes, cudaHostAllocDefault);
@@ -216,9 +226,17 @@ extern "C" int kvstep_run(kvstep_t h, const void* q, const void* k, const void* 
   int st = kvbm_take_copies(h->mgr, nullptr, nullptr, 0, &n_copies);
   if (st != KV_OK) return st;
   if (n_copies != 0) return KV_ERR_INVALID_ARG;  // copies queued outside the runner must be applied by their caller
+  // the lengths here (and the block-table width checked before any change);
+  // the tables as an update of what this buffer held four steps ago
   st = kvbm_prepare_step(h->mgr, free_ids, n_free, prefill_ids, prefill_lens, n_prefill, decode_ids, n_decode,
-                         pad_positions, n_pad, maxb, slots, tables, lens);
-  if (st != KV_OK) return st;
+                         pad_positions, n_pad, maxb, slots, nullptr, lens);
+  if (st == KV_OK)
+    st = kvbm_export_update(h->mgr, decode_ids, n_decode, maxb, tables, h->row_ids[i].data(),
+                            h->row_nblocks[i].data());
+  if (st != KV_OK) {
+    std::fill(h->row_ids[i].begin(), h->row_ids[i].end(), -1);  // contents unknown: rewrite in full next time
+    return st;
+  }
   st = kvbm_take_copies(h->mgr, cp_src, cp_dst, B, &n_copies);
   if (st != KV_OK) return st;
   decode_rows(pad_positions, n_pad, n_pre_tokens, n_decode, rows);

@@ -290,3 +290,58 @@ def test_prepare_step_is_atomic_and_validates():
     slots, tables, lens = nat.prepare_step([1], [5], [3], [0], [0, 4], 8)
     assert slots.size == 3 + 1 + 2 and slots[0] == -1 and slots[4] == -1
     assert lens.tolist() == [5] and nat.check_invariants()
+
+
+def test_export_update_equals_full_export():
+    """kvbm_export_update keeps a buffer equal to kvbm_export through random
+    appends, releases with new sequences in the freed rows, copy-on-write
+    forks (the shared last block replaced by the next append) and rows that
+    swap sequences, starting from a buffer of garbage."""
+    rng = np.random.default_rng(7)
+    bs, nb, maxb, R = 4, 1024, 40, 6
+    mgr = KVBlockManager(nb, bs)
+    next_id = 0
+    rows = []
+    for _ in range(R):
+        mgr.allocate_for_prefill(next_id, int(rng.integers(1, 30)))
+        rows.append(next_id)
+        next_id += 1
+    lens = {sid: mgr.seq_len(sid) for sid in rows}
+    tables = np.full((R, maxb), 12345, np.int32)
+    prev_ids = np.full(R, -1, np.int64)
+    prev_nb = np.zeros(R, np.int32)
+    for _ in range(300):
+        op = int(rng.integers(0, 5))
+        r = int(rng.integers(0, R))
+        sid = rows[r]
+        if op <= 1 and lens[sid] + 3 <= maxb * bs:              # appends (block growth, copy-on-write)
+            n = int(rng.integers(1, 4))
+            mgr.append_slots(sid, n)
+            lens[sid] += n
+        elif op == 2 or lens[sid] + 3 > maxb * bs:               # release, new sequence in the same row
+            mgr.free_sequence(sid)
+            if sid not in rows[:r] + rows[r + 1:]:
+                del lens[sid]
+            mgr.allocate_for_prefill(next_id, int(rng.integers(1, 40)))
+            rows[r] = next_id
+            lens[next_id] = mgr.seq_len(next_id)
+            next_id += 1
+        elif op == 3:                                              # fork: the child shares the parent's blocks
+            child = next_id
+            next_id += 1
+            mgr.fork(sid, child, lens[sid])
+            lens[child] = lens[sid]
+            old = rows[(r + 1) % R]
+            rows[(r + 1) % R] = child
+            if old not in rows:
+                mgr.free_sequence(old)
+                del lens[old]
+        else:                                                      # two rows swap their sequences
+            r2 = int(rng.integers(0, R))
+            rows[r], rows[r2] = rows[r2], rows[r]
+        if len(set(rows)) != R:
+            continue
+        mgr.export_update(rows, maxb, tables, prev_ids, prev_nb)
+        full, _ = mgr.export(rows, maxb)
+        assert np.array_equal(tables, full)
+    assert mgr.check_invariants()
