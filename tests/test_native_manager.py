@@ -345,3 +345,28 @@ def test_export_update_equals_full_export():
         full, _ = mgr.export(rows, maxb)
         assert np.array_equal(tables, full)
     assert mgr.check_invariants()
+
+
+def test_prepare_step_duplicate_and_unknown_ids():
+    """The step's id checks: a new id prefilled twice is DUPLICATE_SEQ; a
+    decode id that is one of the step's prefills is INVALID_ARG; a decode id
+    never seen is UNKNOWN_SEQ; nothing changes in any of them.  The same
+    checks hold call after call (the id set is reused across calls)."""
+    nat = KVBlockManager(64, 4)
+    nat.allocate_for_prefill(0, 5)
+    nat.allocate_for_prefill(1, 2)
+    before = (nat.free_list().tolist(), nat.seq_len(0), nat.seq_len(1))
+    for _ in range(3):
+        for args, code in [(([], [7, 7], [3, 3], [0], [], 8), "DUPLICATE_SEQ"),
+                           (([], [7], [3], [0, 7], [], 8), "INVALID_ARG"),
+                           (([], [], [], [0, 9], [], 8), "UNKNOWN_SEQ"),
+                           (([], [], [], [1, 0, 1], [], 8), "INVALID_ARG")]:
+            with pytest.raises(KVError) as e:
+                nat.prepare_step(*args)
+            assert e.value.code == code, args
+            assert (nat.free_list().tolist(), nat.seq_len(0), nat.seq_len(1)) == before
+        with pytest.raises(KVError) as e:
+            nat.decode_step([1, 1], 8)
+        assert e.value.code == "INVALID_ARG"
+    slots, tables, lens = nat.prepare_step([], [7], [3], [0, 1], [], 8)
+    assert lens.tolist() == [6, 3] and nat.check_invariants()
