@@ -153,6 +153,17 @@ struct kvbm_s {
   bool needs_copy(const Sequence& s) const {
     return s.length % block_size != 0 && !s.table.empty() && ref_count[static_cast<size_t>(s.table.back())] > 1;
   }
+  // The slots of positions 0 .. n - 1 of s, in order, to f: block by block,
+  // table[k] * bs + off (slot_of without a division per token).
+  template <typename F>
+  void for_each_slot(const Sequence& s, int64_t n, F&& f) const {
+    for (size_t k = 0; n > 0; ++k) {
+      const int32_t base = s.table[k] * block_size;
+      const int64_t m = n < block_size ? n : block_size;
+      for (int64_t off = 0; off < m; ++off) f(base + static_cast<int32_t>(off));
+      n -= m;
+    }
+  }
   // MiniPaged-Qwen §3: slot = table[pos / bs] * bs + pos % bs.
   int32_t slot_of(const Sequence& s, int64_t pos) const {
     return static_cast<int32_t>(static_cast<int64_t>(s.table[static_cast<size_t>(pos / block_size)]) *
@@ -269,8 +280,10 @@ int kvbm_allocate_for_prefill(kvbm_t h, int64_t seq_id, int64_t num_tokens, int3
     s.table.reserve(static_cast<size_t>(need));
     for (int64_t i = 0; i < need; ++i) s.table.push_back(h->take_front());
     s.length = num_tokens;
-    if (slots_out)
-      for (int64_t t = 0; t < num_tokens; ++t) slots_out[t] = h->slot_of(s, t);
+    if (slots_out) {
+      int32_t* out = slots_out;
+      h->for_each_slot(s, num_tokens, [&](int32_t slot) { *out++ = slot; });
+    }
     h->seqs.emplace(seq_id, std::move(s));
     h->released.erase(seq_id);
     return static_cast<int>(KV_OK);
@@ -494,7 +507,7 @@ int kvbm_prepare_step(kvbm_t h, const int64_t* free_ids, int64_t n_free, const i
       sq.table.reserve(static_cast<size_t>(nb));
       for (int64_t k = 0; k < nb; ++k) sq.table.push_back(h->take_front());
       sq.length = prefill_lens[i];
-      for (int64_t t = 0; t < prefill_lens[i]; ++t) put(h->slot_of(sq, t));
+      h->for_each_slot(sq, prefill_lens[i], put);
       h->seqs.emplace(prefill_ids[i], std::move(sq));
       h->released.erase(prefill_ids[i]);
     }
