@@ -352,7 +352,9 @@ int paged_decode_step_fp8(void* out, const void* q, const void* k, const void* v
  *     or bf16), 16-byte aligned; caches as for paged_decode_attention.
  *   query_start_loc: device int32[num_seqs + 1], non-decreasing, every
  *     entry in [0, num_query_tokens].
- *   max_query_len: host upper bound of the chunk lengths (sizes the grid).
+ *   max_query_len: host upper bound of the chunk lengths (sizes the grid;
+ *     rows of a longer chunk past it are not computed, and this is not
+ *     detected).
  *   head_dim 64 or 128.
  * A chunk longer than its sequence or reaching past num_query_tokens, or a
  * sequence longer than its table row, is recorded as KV_ERR_DEVICE_BOUNDS
