@@ -19,6 +19,14 @@ step i + 1's metadata and its copy runs while the GPU runs step i; steps
 rotate over enough replica pools that no step finds its K/V in L2.  The
 roofline object times the step's device launch alone, L2 flushed before
 each.
+
+The default workload is the mixed continuous-batching step (256 decode
+sequences, a 4096-token prefill chunk, 5 % padded slots; bf16, Hq 32,
+Hkv 8, D 128, block 32), the largest of the five.  ``roofline_by_workload``
+times the fused-step launch of the three single-layer decode batches held
+to 70 % of HBM peak in the same run.  ``cpu_baseline`` is the float64
+oracle on one host thread; ``cpu_baseline_all_cores`` runs it on every host
+core at once.
 """
 
 from __future__ import annotations
@@ -36,7 +44,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attn HBM GB/s (% of ~8 TB/s peak) and decode tokens/s at 1 GB300"
-DEFAULT_WORKLOAD = "decode_gqa14x2_d64_fp16"
+DEFAULT_WORKLOAD = "mixed_batch_bf16"
+# workloads whose fused-step launch is also timed (L2 flushed) in every
+# default run: the three single-layer decode batches held to 70 % of HBM peak
+TARGET_WORKLOADS = ("decode_gqa14x2_d64_fp16", "decode_gqa28x4_d128_bf16", "decode_long_skewed_bf16")
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 
@@ -52,6 +63,8 @@ def parse_args():
                     help="cache element type: the workload's dtype, or fp8 E4M3 codes with per-token scales "
                          "(head_dim 128 workloads)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-target-rooflines", action="store_true",
+                    help="skip the per-workload launch timings of the 70 %% target workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="--impl reference: seconds of oracle time for the whole run (steps + warm-up)")
@@ -160,21 +173,25 @@ from paged_kv_cache_128_gb300.inputs import make_workload, make_values, pad_posi
 import torch
 
 wl = make_workload({name!r})
-vals = make_values(wl)
+vals = make_values(wl, history=False)
 def st(t):
     t = t.contiguous()
     return t.view(torch.int16).numpy().view(np.uint16) if wl.dtype == "bf16" else t.numpy()
 budget = {budget}
-# sample: the first S decode sequences (a bounded slice of the same step)
-S = min(wl.num_seqs, {max_seqs})
+# sample: S decode sequences from batch position F on (a bounded slice of the same step)
+F = {first} % wl.num_seqs
+S = min(wl.num_seqs - F, {max_seqs})
 def setup():
     mgr = BlockManager(wl.num_blocks, wl.block_size, None if wl.free_order is None else wl.free_order.tolist())
     shape = (wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim)
     kc = np.zeros(shape, dtype=st(vals.k_step[:1]).dtype)
     vc = np.zeros_like(kc)
-    ids = set(int(i) for i in wl.decode_ids[:S])
-    off = vals.hist_offsets
-    pos = {{}}
+    ids = set(int(i) for i in wl.decode_ids[F:F + S])
+    # history of the sampled sequences only, seeded per sample
+    g = torch.Generator().manual_seed(wl.seed + 7919 * (F + 1))
+    def draw(n):
+        x = torch.randn(n, wl.num_kv_heads, wl.head_dim, generator=g) * wl.value_scale
+        return st(x.to(wl.torch_dtype))
     for op, sid, n in wl.setup_ops:
         if op == "prefill":
             s = mgr.allocate_for_prefill(sid, n)
@@ -183,15 +200,15 @@ def setup():
         else:
             mgr.free_sequence(sid); continue
         if sid in ids:
-            b = int(np.nonzero(wl.decode_ids == sid)[0][0])
-            a = off[b] + pos.get(sid, 0)
-            reshape_and_cache(st(vals.k_hist[a:a + n]), st(vals.v_hist[a:a + n]), kc, vc, s)
-            pos[sid] = pos.get(sid, 0) + n
+            reshape_and_cache(draw(n), draw(n), kc, vc, s)
     return mgr, kc, vc
 mgr, kc, vc = setup()
-sample_ids = wl.decode_ids[:S].tolist()
-q = st(vals.q[:S])
-k_new = st(vals.k_step[:S]); v_new = st(vals.v_step[:S])
+sample_ids = wl.decode_ids[F:F + S].tolist()
+q = st(vals.q[F:F + S])
+k_new = st(vals.k_step[F:F + S]); v_new = st(vals.v_step[F:F + S])
+if {sync}:   # several copies run at once: start timing together
+    print("READY", flush=True)
+    sys.stdin.readline()
 elapsed, steps, bytes_total = 0.0, 0, 0
 es = 4 if wl.dtype == "f32" else 2
 row = wl.num_kv_heads * wl.head_dim * es
@@ -214,17 +231,53 @@ print(json.dumps({{"seconds": elapsed, "steps": steps, "seqs": S, "bytes": bytes
 """
 
 
-def run_oracle_sample(name, budget, max_seqs):
+def _oracle_env():
     env = dict(os.environ)
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[var] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
-    code = ORACLE_SNIPPET.format(root=ROOT, name=name, budget=budget, max_seqs=max_seqs)
-    proc = subprocess.run([sys.executable, "-c", code], env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE,
-                          text=True, timeout=budget * 20 + 300)
+    return env
+
+
+def run_oracle_sample(name, budget, max_seqs, first=0):
+    code = ORACLE_SNIPPET.format(root=ROOT, name=name, budget=budget, max_seqs=max_seqs, first=first, sync=False)
+    proc = subprocess.run([sys.executable, "-c", code], env=_oracle_env(), stdout=subprocess.PIPE,
+                          stderr=subprocess.PIPE, text=True, timeout=budget * 20 + 300)
     if proc.returncode != 0:
         raise RuntimeError("oracle sample failed:\n" + proc.stderr[-2000:])
     return json.loads(proc.stdout.strip().splitlines()[-1])
+
+
+def run_oracle_parallel(name, budget, max_seqs, procs):
+    """``procs`` single-threaded oracle processes at once, process i on the
+    8 sequences from batch position 8 i (sequences are independent); they
+    set up, then start their timed loops together.  Returns the summed
+    bytes and tokens, and the longest timed loop."""
+    code = [ORACLE_SNIPPET.format(root=ROOT, name=name, budget=budget, max_seqs=max_seqs, first=i * max_seqs,
+                                  sync=True) for i in range(procs)]
+    ps = [subprocess.Popen([sys.executable, "-c", c], env=_oracle_env(), stdin=subprocess.PIPE,
+                           stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True) for c in code]
+    try:
+        for p in ps:
+            line = p.stdout.readline()
+            if not line.startswith("READY"):
+                raise RuntimeError("oracle process failed during set-up:\n" + p.stderr.read()[-2000:])
+        for p in ps:
+            p.stdin.write("go\n")
+            p.stdin.flush()
+        outs = [p.communicate(timeout=budget * 20 + 300) for p in ps]
+    finally:
+        for p in ps:
+            if p.poll() is None:
+                p.kill()
+    res = []
+    for p, (out, err) in zip(ps, outs):
+        if p.returncode != 0:
+            raise RuntimeError("oracle process failed:\n" + err[-2000:])
+        res.append(json.loads(out.strip().splitlines()[-1]))
+    return {"seconds": max(r["seconds"] for r in res), "bytes": sum(r["bytes"] for r in res),
+            "tokens": sum(r["tokens"] for r in res), "seqs": sum(r["seqs"] for r in res),
+            "steps": min(r["steps"] for r in res)}
 
 
 def cpu_baseline(name, budget):
@@ -234,6 +287,21 @@ def cpu_baseline(name, budget):
             "sample": (f"float64 numpy oracle, one host thread: {r['steps']} decode steps of the first "
                        f"{r['seqs']} sequences of {name} (manager append + export, cache write, attention), "
                        f"{r['seconds']:.1f} s"),
+            "decode_tokens_per_s": r["tokens"] / r["seconds"]}
+
+
+def cpu_baseline_all_cores(name, budget):
+    """The same oracle loop on every host core: one single-threaded process
+    per core, each over its own 8 sequences of the batch."""
+    from paged_kv_cache_128_gb300.inputs import make_workload
+    cores = os.cpu_count() or 1
+    procs = max(1, min(cores, make_workload(name).num_seqs // 8))
+    r = run_oracle_parallel(name, budget, 8, procs)
+    gbs = r["bytes"] / r["seconds"] / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": procs, "kind": "oracle",
+            "sample": (f"float64 numpy oracle, {procs} single-threaded processes at once on {cores} host cores, "
+                       f"each over its own 8 sequences of {name} ({r['seqs']} in all; manager append + export, "
+                       f"cache write, attention), at least {r['steps']} decode steps each, {r['seconds']:.1f} s"),
             "decode_tokens_per_s": r["tokens"] / r["seconds"]}
 
 
@@ -256,6 +324,70 @@ def max_over_ranks(x: float, world: int, device="cpu") -> float:
     t = torch.tensor([float(x)], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def flushed_launch_time(eng, q, k_step, v_step, calls, l2, dev):
+    """Mean device time of the step's device launch alone, and its
+    algorithmic bytes.  Launches are queued behind a GPU-side delay, so the
+    events bracket device time only.  Before each call L2 is flushed (write
+    2x L2, then read 2x L2 of other data) and the step's metadata is copied
+    host to device again, as every step does before its kernels: K/V come
+    from HBM, the block tables and lengths from where the step's copy left
+    them.  The event clock ticks in steps of about 2 us, so the mean over
+    the calls is taken (a median would snap to a tick)."""
+    import torch
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush_read = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    meta_h = eng.d_meta.cpu().pin_memory()
+    ms = []
+    for _ in range(calls):
+        flush.zero_()
+        flush_read.sum()
+        eng.d_meta.copy_(meta_h, non_blocking=True)
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(200000)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        eng.device_step(q, k_step, v_step)
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    call_s = statistics.fmean(ms[2:] if len(ms) > 4 else ms) / 1e3
+    # the step's device kernels after the metadata copy (one fused launch of
+    # the cache write + attention with the stream-K kernel), over the lengths
+    # in the metadata it was given
+    return call_s, eng.algorithmic_bytes(eng._views(meta_h)[2].numpy())["step"]
+
+
+def target_rooflines(args, dev, l2, peak, peak_kind):
+    """The fused-step launch of each 70 %-target workload, timed as the
+    headline roofline is (one pool each, L2 flushed before every call)."""
+    import torch
+    from paged_kv_cache_128_gb300.engine import PagedDecodeEngine
+    from paged_kv_cache_128_gb300.inputs import make_values, make_workload
+    out = {}
+    calls = max(args.steps, 30)
+    for name in TARGET_WORKLOADS:
+        if name == args.workload:
+            continue
+        wl = make_workload(name)
+        eng = PagedDecodeEngine(wl, dev, max_steps=2, fill_sentinel=False, kv_cache=args.kv_cache)
+        vals = make_values(wl, device="cuda")
+        eng.setup(vals)
+        eng.step(vals.q, vals.k_step, vals.v_step)
+        torch.cuda.synchronize()
+        call_s, nbytes = flushed_launch_time(eng, vals.q, vals.k_step, vals.v_step, calls, l2, dev)
+        achieved = nbytes / call_s / 1e9
+        out[name] = {"bound": "hbm", "achieved": achieved, "peak": peak,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback", "unit": "GB/s", "frac": achieved / peak,
+                     "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                     "traffic": recorded_traffic(name if args.kv_cache == "native" else f"{name}:fp8"),
+                     "algorithmic_bytes_per_call": nbytes, "mean_call_us": call_s * 1e6, "calls": calls,
+                     "plan": {0: "simt_split", 1: "tma_mma_split", 2: "tma_mma_stream_k"}[eng.plan.kernel]}
+        del eng, vals
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_native(args):
@@ -297,9 +429,11 @@ def run_native(args):
         eng.setup(vals)
         engines.append(eng)
     q, k_step, v_step = vals.q, vals.k_step, vals.v_step
-    for eng in engines:            # one direct step each (lazy set-up), then the native step runner
-        eng.step(q, k_step, v_step)
+    for eng in engines:            # one direct step each (lazy set-up), then the native step runner,
+        eng.step(q, k_step, v_step)    # primed with one step so no runner's first step is timed
         eng.make_runner()
+        eng.runner_step(q, k_step, v_step, eng.out)
+        eng.runner_join()
     torch.cuda.synchronize()
 
     def run_step(i):
@@ -352,29 +486,8 @@ def run_native(args):
     # HBM, the block tables and lengths from where the step's copy left them.
     # The event clock ticks in steps of about 2 us, so the mean over many
     # calls is taken (the median would snap to a tick).
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-    flush_read = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
     eng0 = engines[0]
-    meta_h = eng0.d_meta.cpu().pin_memory()
-    attn_ms = []
-    for i in range(max(args.steps, 10)):
-        flush.zero_()
-        flush_read.sum()
-        eng0.d_meta.copy_(meta_h, non_blocking=True)
-        if hasattr(torch.cuda, "_sleep"):
-            torch.cuda._sleep(200000)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        eng0.device_step(q, k_step, v_step)
-        b.record()
-        b.synchronize()
-        attn_ms.append(a.elapsed_time(b))
-    attn_call_s = statistics.fmean(attn_ms[2:] if len(attn_ms) > 4 else attn_ms) / 1e3
-    # the step's device kernels after the metadata copy: one fused launch
-    # (cache write + attention) with the stream-K kernel, over the lengths
-    # in the metadata it was given
-    roof_bytes = eng0.algorithmic_bytes(eng0._views(meta_h)[2].numpy())
-    attn_bytes = roof_bytes["step"]
+    attn_call_s, attn_bytes = flushed_launch_time(eng0, q, k_step, v_step, max(args.steps, 10), l2, dev)
 
     # ---------------- end to end through host buffers ----------------
     # The step's q/k/v sit in the runners' page-locked staging slots (host_io
@@ -386,11 +499,13 @@ def run_native(args):
     k_h = k_step.cpu()
     v_h = v_step.cpu()
     outs_h = [torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in engines]
-    for eng in engines:
+    for r, eng in enumerate(engines):
         eng.make_runner(host_io=2)
         for slot in range(4):
             for dst, src in zip(eng.runner_stage(slot), (q_h, k_h, v_h)):
                 dst.copy_(src)
+        eng.runner_step(None, None, None, outs_h[r])   # primed: no runner's first step is timed
+        eng.runner_join()
 
     def run_e2e(i):
         eng = engines[i % replicas]
@@ -479,11 +594,27 @@ def run_native(args):
         "device_error": status,
         "wall_s_timed_region": wall,
     }
+    # ---------------- the fused-step launch of the 70 % target workloads ----------------
+    if not args.no_target_rooflines:
+        for e in engines:
+            e.close_runner()
+        engines.clear()
+        marks.clear()
+        e_marks.clear()
+        eng = eng0 = None
+        torch.cuda.empty_cache()
+        result["roofline_by_workload"] = target_rooflines(args, dev, l2, peak, peak_kind)
+        status = status or pk.device_error()
+        result["device_error"] = status
     if rank == 0 and not args.no_cpu_baseline:
         try:
             result["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_budget)
         except Exception as exc:  # reported, not fatal
             result["cpu_baseline"] = {"value": None, "error": str(exc)[-300:]}
+        try:
+            result["cpu_baseline_all_cores"] = cpu_baseline_all_cores(args.workload, args.cpu_budget)
+        except Exception as exc:  # reported, not fatal
+            result["cpu_baseline_all_cores"] = {"value": None, "error": str(exc)[-300:]}
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:

@@ -352,9 +352,9 @@ int paged_decode_step_fp8(void* out, const void* q, const void* k, const void* v
  *     or bf16), 16-byte aligned; caches as for paged_decode_attention.
  *   query_start_loc: device int32[num_seqs + 1], non-decreasing, every
  *     entry in [0, num_query_tokens].
- *   max_query_len: host upper bound of the chunk lengths (sizes the grid;
- *     rows of a longer chunk past it are not computed, and this is not
- *     detected).
+ *   max_query_len: host upper bound of the chunk lengths (sizes the grid).
+ *     A longer chunk's rows past the grid's reach are not computed, and the
+ *     launch records KV_ERR_DEVICE_BOUNDS.
  *   head_dim 64 or 128.
  * A chunk longer than its sequence or reaching past num_query_tokens, or a
  * sequence longer than its table row, is recorded as KV_ERR_DEVICE_BOUNDS
@@ -489,8 +489,11 @@ int paged_decode_step(void* out, const void* q, const void* k, const void* v,
  * (paged_decode_workspace_size) exceeds the array return KV_ERR_WORKSPACE
  * and launch nothing.  All calls on a device share the array: calls that
  * overlap on the GPU (other streams, other threads) race; order them on one
- * stream.  Nothing in it needs clearing between calls.  Other arguments,
- * results and errors are those of paged_decode_attention. */
+ * stream.  Nothing in it needs clearing between calls.  The address found
+ * by the first call is kept for the life of the process: do not use this
+ * entry point after cudaDeviceReset (or any other teardown of the device's
+ * primary context) in the same process.  Other arguments, results and
+ * errors are those of paged_decode_attention. */
 int paged_decode_attention_static_scratch(void* out, const void* q, const void* k_cache,
                                           const void* v_cache, const int32_t* block_tables,
                                           const int32_t* seq_lens, int32_t num_seqs,

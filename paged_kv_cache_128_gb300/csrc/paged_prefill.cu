@@ -80,6 +80,10 @@ __global__ void __launch_bounds__(kPfWarps * 32) prefill_kernel(const PrefillPar
   const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qs = __ldg(p.query_start + b), n = __ldg(p.query_start + b + 1) - qs;
+  // rows past the grid's reach (a chunk longer than max_query_len) would be
+  // left uncomputed: the last row tile of the sequence reports it
+  if (qt == gridDim.x - 1 && h == 0 && tid == 0 && n > static_cast<int>(gridDim.x) * kPfRows)
+    record_error(KV_ERR_DEVICE_BOUNDS);
   if (n <= 0 || qt * kPfRows >= n) return;
   if (qs < 0 || qs + n > p.num_tokens) {  // the chunk's rows must lie inside q
     if (tid == 0) record_error(KV_ERR_DEVICE_BOUNDS);
@@ -331,6 +335,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const int h0 = blockIdx.y * hg, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qs = __ldg(p.query_start + b), n = __ldg(p.query_start + b + 1) - qs;
+  // rows past the grid's reach (a chunk longer than max_query_len) would be
+  // left uncomputed: the last row tile of the sequence reports it
+  if (qt == gridDim.x - 1 && blockIdx.y == 0 && threadIdx.x == 0 && n > static_cast<int>(gridDim.x) * tpt)
+    record_error(KV_ERR_DEVICE_BOUNDS);
   if (n <= 0 || qt * tpt >= n) return;
   int L = __ldg(p.seq_lens + b);
   const int64_t cap = static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size;

@@ -103,6 +103,38 @@ def test_prefill_mixed_batch_chunk():
     assert worst <= TOL["bf16"], f"max abs err {worst:.3e}"
 
 
+def test_prefill_mixed_batch_chunk_with_history():
+    """The benchmark's prefill case: the mixed-batch chunk (8 sequences, 4096
+    tokens) with 2048 tokens of history before each chunk; every row of
+    every sequence against the oracle."""
+    wl = make_workload("mixed_batch_bf16")
+    seqs = [(2048, int(n)) for n in wl.prefill_lens]
+    worst = _run("bf16", wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size, seqs, seed=6, value_scale=1.0)
+    assert worst <= TOL["bf16"], f"max abs err {worst:.3e}"
+
+
+@pytest.mark.parametrize("bs", [16, 8], ids=["tcgen05", "mma_sync"])
+def test_prefill_chunk_longer_than_max_query_len_is_reported(bs):
+    """A grid sized by a max_query_len below the longest chunk cannot reach
+    that chunk's last rows: the launch records KV_ERR_DEVICE_BOUNDS."""
+    dev = torch.device("cuda")
+    nb, hkv, d, hq = 64, 2, 64, 4
+    g = torch.Generator().manual_seed(3)
+    kc = (torch.randn(nb, bs, hkv, d, generator=g) * 0.5).half().to(dev)
+    vc = (torch.randn(nb, bs, hkv, d, generator=g) * 0.5).half().to(dev)
+    maxb = 300 // bs + 1
+    tables = torch.arange(maxb, dtype=torch.int32, device=dev).view(1, -1)
+    lens = torch.tensor([300], dtype=torch.int32, device=dev)
+    qsl = torch.tensor([0, 300], dtype=torch.int32, device=dev)   # one chunk of 300 rows
+    q = (torch.randn(300, hq, d, generator=g) * 0.5).half().to(dev)
+    out = torch.zeros(300, hq, d, dtype=torch.float16, device=dev)
+    pk.device_error()
+    pk.paged_prefill_attention(out, q, kc, vc, tables, lens, qsl, 0.125, 20)   # grid for 20 rows or so
+    assert pk.device_error() == 8
+    pk.paged_prefill_attention(out, q, kc, vc, tables, lens, qsl, 0.125, 300)  # the true bound: no error
+    assert pk.device_error() == 0
+
+
 def test_prefill_chunk_longer_than_sequence_is_reported():
     dev = torch.device("cuda")
     nb, bs, hkv, d, hq = 8, 16, 2, 64, 4
