@@ -73,6 +73,10 @@ def parse_args():
                          "4096-token prefill chunk, one JSON line per --prefill-context")
     ap.add_argument("--prefill-context", default="0,2048",
                     help="--prefill: comma-separated history lengths (tokens already cached per sequence)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="time a multi-layer decode step instead: the workload's decode batch over this many "
+                         "layers' caches under one block table, through the native runner (metadata once per step, "
+                         "one fused launch per layer); decode-only workloads")
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="only set the workload up and run this many attention calls (L2 flushed before each); "
                          "the small case used under ncu")
@@ -852,8 +856,115 @@ def run_prefill(args):
             sys.exit(1)
 
 
+# ------------------------------------------------------ multi-layer steps
+
+def run_layers(args):
+    """A decode step over ``--layers`` layers' caches sharing one block
+    table ("MiniPaged-Qwen" §16.3): the native runner builds and copies the
+    step's metadata once and launches one fused cache-write + attention
+    kernel per layer.  Steps rotate over replica pools until more than 3x L2
+    streams between two uses of one; one layer alone is timed the same way
+    for comparison.  K/V values are random normal (not checked here: the
+    multi-layer GPU tests check them against the oracle)."""
+    import ctypes
+    import numpy as np
+    import torch
+    import paged_kv_cache_128_gb300 as pk
+    from paged_kv_cache_128_gb300._lib import check, kvstep_config_t, lib
+    from paged_kv_cache_128_gb300.inputs import make_workload
+    from paged_kv_cache_128_gb300.kernels import alloc_workspace, decode_plan, dtype_code
+
+    wl = make_workload(args.workload)
+    if wl.prefill_lens.size or wl.num_pad:
+        raise SystemExit("--layers takes a decode-only workload")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dt = wl.torch_dtype
+    B, hq, hkv, d, bs, nb = wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size, wl.num_blocks
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    es = torch.empty((), dtype=dt).element_size()
+    row = hkv * d * es
+    ids = np.ascontiguousarray(wl.decode_ids, dtype=np.int64)
+    steps, warm = max(args.steps, 1), max(args.warmup, 3)
+    results = {}
+    for layers in (1, args.layers):
+        per_layer = int(wl.cached_lens.sum()) * 2 * row
+        replicas = int(max(1, min(16, -(-3 * l2 // (per_layer * layers)))))
+        max_len = int(wl.cached_lens.max()) + 1 + (steps + warm) // replicas + 4
+        maxb = -(-max_len // bs)
+        runners = []
+        for _ in range(replicas):
+            mgr = pk.KVBlockManager(nb, bs, wl.free_order)
+            for sid, n in zip(wl.decode_ids.tolist(), wl.cached_lens.tolist()):
+                mgr.allocate_for_prefill(int(sid), int(n))
+            kc = torch.empty(layers, nb, bs, hkv, d, dtype=dt, device=dev).normal_()
+            vc = torch.empty_like(kc).normal_()
+            ws = alloc_workspace(decode_plan(B, hq, hkv, d, bs, max_len, dt), dev)
+            cfg = kvstep_config_t(num_seqs=B, num_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=bs,
+                                  num_blocks=nb, max_blocks_per_seq=maxb, max_seq_len=max_len, scale=float(wl.scale),
+                                  dtype=dtype_code(dt), num_step_tokens=B, k_cache=kc.data_ptr(),
+                                  v_cache=vc.data_ptr(), workspace=ws.data_ptr() if ws is not None else None,
+                                  workspace_bytes=ws.numel() if ws is not None else 0,
+                                  stream=torch.cuda.current_stream().cuda_stream, host_io=0, num_layers=layers,
+                                  cache_layer_stride=kc.stride(0))
+            h = ctypes.c_void_p()
+            check(lib().kvstep_create(mgr._h, ctypes.byref(cfg), ctypes.byref(h)), "kvstep_create")
+            q = torch.randn(layers, B, hq, d, device=dev, dtype=dt)
+            k = torch.randn(layers, B, hkv, d, device=dev, dtype=dt)
+            v = torch.randn(layers, B, hkv, d, device=dev, dtype=dt)
+            runners.append([h, q, k, v, torch.empty_like(q), mgr, kc, vc, ws, 0])
+
+        def step(i):
+            r = runners[i % replicas]
+            check(lib().kvstep_run(r[0], r[1].data_ptr(), r[2].data_ptr(), r[3].data_ptr(), r[4].data_ptr(), None,
+                                   0, None, None, 0, ids.ctypes.data, B, None, 0), "kvstep_run")
+            r[9] += 1
+            return r[9]
+
+        for i in range(max(warm, replicas)):
+            step(i)
+        for r in runners:
+            check(lib().kvstep_join(r[0], torch.cuda.current_stream().cuda_stream), "kvstep_join")
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        nbytes = 0
+        wall0 = time.perf_counter()
+        a.record()
+        for i in range(steps):
+            done = step(i)
+            lens = wl.cached_lens + done   # after this step's append
+            nbytes += layers * (int(lens.sum()) * 2 * row + 2 * B * hq * d * es + 4 * (B + int((-(-lens // bs)).sum()))
+                                + 2 * 2 * B * row + 4 * B)
+        host_s = (time.perf_counter() - wall0) / steps
+        for r in runners:
+            check(lib().kvstep_join(r[0], torch.cuda.current_stream().cuda_stream), "kvstep_join")
+        b.record()
+        torch.cuda.synchronize()
+        t = a.elapsed_time(b) / 1e3
+        results[layers] = {"step_us": t / steps * 1e6, "per_layer_us": t / steps / layers * 1e6,
+                           "gbs": nbytes / t / 1e9, "host_us_per_step": host_s * 1e6,
+                           "decode_tokens_per_s": B * steps / t, "replicas": replicas}
+        for r in runners:
+            lib().kvstep_destroy(r[0])
+        del runners
+        torch.cuda.empty_cache()
+    status = pk.device_error()
+    print(json.dumps({"metric": "multi-layer decode step GB/s (algorithmic bytes of every layer) at 1 GB300",
+                      "value": results[args.layers]["gbs"], "unit": "GB/s", "n_gpus": 1, "steps": steps,
+                      "warmup": warm, "ms_per_step": results[args.layers]["step_us"] / 1e3, "higher_is_better": True,
+                      "dtype": wl.dtype, "data": "synthetic (random normal K/V)",
+                      "config": {"workload": wl.name, "layers": args.layers,
+                                 "l2": "inputs larger than L2: steps rotate over replica pools"},
+                      "layers": {str(k): v for k, v in results.items()}, "device_error": status}))
+    if status:
+        sys.exit(1)
+
+
 def main():
     args = parse_args()
+    if args.layers:
+        run_layers(args)
+        return
     if args.prefill:
         run_prefill(args)
         return

@@ -384,6 +384,24 @@ int paged_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const in
                       int32_t num_layers, int64_t layer_stride, int32_t num_kv_heads, int32_t head_dim,
                       int32_t block_size, int64_t num_blocks, int dtype, void* stream);
 
+/* paged_copy_blocks for fp8 (E4M3) caches ("paged-attention-impl-detail",
+ * copy_on_write, with the per-block quantisation of 实践建议 4): block
+ * dst[i] takes block src[i]'s codes (K and V) and its float32 scales.
+ *   k_cache, v_cache: device, num_layers code caches [num_blocks, block_size,
+ *     num_kv_heads, head_dim] of bytes, layer l at + l * layer_stride bytes
+ *     (>= one layer's codes when num_layers > 1; a multiple of 16).
+ *   k_scales, v_scales: device, num_layers scale arrays [num_blocks,
+ *     num_kv_heads, block_size] of float32, layer l at
+ *     + l * num_blocks * num_kv_heads * block_size floats.
+ *   src, dst, n: as for paged_copy_blocks.
+ * Each block's codes and scales must be whole 16-byte multiples (else
+ * KV_ERR_INVALID_ARG).  Two launches on `stream`; indices outside the pool
+ * are recorded as KV_ERR_DEVICE_BOUNDS and skipped. */
+int paged_copy_blocks_fp8(void* k_cache, void* v_cache, float* k_scales, float* v_scales, const int32_t* src,
+                          const int32_t* dst, int64_t n, int32_t num_layers, int64_t layer_stride,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                          void* stream);
+
 /* Split-K plan for a decode call with these sizes.  blocks_per_split: 0
  * chooses automatically (from the SM count of the current device, the
  * number of (sequence, kv head) pairs and max_seq_len); > 0 forces that many
@@ -425,6 +443,12 @@ int paged_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num
  *   workspace: device, >= paged_decode_workspace_size() bytes, 256-byte
  *     aligned, or NULL when that size is 0 (else KV_ERR_WORKSPACE).
  *     Clobbered; calls that share a workspace must be ordered on one stream.
+ *     Its contents need no initialisation: the stream-K kernel's ready flags
+ *     carry a tag unique to each call (a random base plus a call counter),
+ *     and each flag is cleared by its one reader.  A CUDA graph replays the
+ *     tag it captured; after a call reports KV_ERR_DEVICE_TIMEOUT, a late
+ *     flag can be left set, so zero the workspace (or capture the graph
+ *     again) before replaying a graph that uses it.
  * num_heads must be a multiple of num_kv_heads.  head_dim: fp32 a multiple
  * of 4 up to 256; fp16/bf16 a multiple of 8 up to 256.
  * Bounds violations (a table entry outside [0, num_blocks), a seq_len above
@@ -619,12 +643,19 @@ int kvstep_join(kvstep_t h, void* stream);
 int kvstep_last_buffers(kvstep_t h, const int32_t** slot_mapping, const int32_t** block_tables,
                         const int32_t** seq_lens, const int32_t** new_token_row);
 
-/* Device address of page-locked host memory that is mapped into the device
- * address space (cudaHostAlloc'd or registered memory; with unified
- * addressing it equals the host address).  Kernels may read such memory in
- * place, e.g. a step's metadata written by the host.  KV_ERR_INVALID_ARG
- * when host_ptr is not mapped page-locked memory. */
-int kv_mapped_device_pointer(const void* host_ptr, void** device_ptr_out);
+/* Test controls of the stream-K decode kernel, process-wide, read at each
+ * later launch (no counterpart on the pages).  Keys:
+ *   KV_DEBUG_WAIT_LIMIT_NS: longest one bounded device wait may take before
+ *     the kernel records KV_ERR_DEVICE_TIMEOUT and gives up (value <= 0
+ *     restores the default, 1 s).
+ *   KV_DEBUG_SKIP_TILE: value >= 0: CTA 0 of each later launch never loads
+ *     tile number `value` of its range (counted from 0), so the wait for it
+ *     runs out after the wait limit; the launch still ends, records
+ *     KV_ERR_DEVICE_TIMEOUT, and its outputs are unspecified.  value < 0:
+ *     off.  For tests of the timeout path, which need no GPU fault.
+ * KV_ERR_INVALID_ARG for an unknown key. */
+enum { KV_DEBUG_WAIT_LIMIT_NS = 1, KV_DEBUG_SKIP_TILE = 2 };
+int kv_debug_set(int key, int64_t value);
 
 /* Library version string (static). */
 const char* kv_version(void);

@@ -94,6 +94,8 @@ SIGNATURES = {
                                         c_float, c_int, c_void_p]),
     "paged_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int32, c_int64, c_int32,
                                   c_int32, c_int32, c_int64, c_int, c_void_p]),
+    "paged_copy_blocks_fp8": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int32,
+                                      c_int64, c_int32, c_int32, c_int32, c_int64, c_void_p]),
     "paged_decode_plan": (c_int, [c_int32, c_int32, c_int32, c_int32, c_int32, c_int64, c_int32, c_int,
                                   P32, P32, P32, POINTER(c_size_t)]),
     "paged_decode_workspace_size": (c_int, [c_int32, c_int32, c_int32, c_int32, c_int32, c_int64, c_int32,
@@ -120,7 +122,7 @@ SIGNATURES = {
                                     POINTER(c_int32)]),
     "kvstep_last_buffers": (c_int, [c_void_p, POINTER(c_void_p), POINTER(c_void_p), POINTER(c_void_p),
                                     POINTER(c_void_p)]),
-    "kv_mapped_device_pointer": (c_int, [c_void_p, POINTER(c_void_p)]),
+    "kv_debug_set": (c_int, [c_int, c_int64]),
     "kv_version": (c_char_p, []),
 }
 

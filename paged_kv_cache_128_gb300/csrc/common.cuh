@@ -97,17 +97,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed, for at most
-// kWaitLimitNs.  Returns false (and records KV_ERR_DEVICE_TIMEOUT) on timeout.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// limit_ns.  Returns false (and records KV_ERR_DEVICE_TIMEOUT) on timeout.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       record_error(KV_ERR_DEVICE_TIMEOUT);
       return false;
     }
   }
   return true;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 
 // Order this thread's generic-proxy shared-memory writes before later
@@ -156,14 +160,6 @@ __device__ __forceinline__ uint64_t ld_acquire_gpu(const uint64_t* ptr) {
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
   return v;
 }
-
-// Programmatic dependent launch: let the next kernel in the stream start
-// launching (its CTAs wait in griddep_wait until this grid has completed and
-// its memory is visible).
-__device__ __forceinline__ void griddep_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Named barrier over a subset of the CTA's warps.
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {

@@ -71,6 +71,8 @@ struct DecodeParams {
   uint64_t* ws_flags;  // stream-K: [P] "partial in slot 0 ready" flags, holding the call's epoch
   uint64_t epoch;      // stream-K: tag unique to this call (flags from other calls never match)
   int32_t seg_cost;    // stream-K: extra tiles charged per unit when ranges are drawn
+  uint64_t wait_limit_ns;   // stream-K: longest one bounded wait may take
+  int32_t test_skip_tile;   // stream-K test control (-1: off): CTA 0 never loads this tile of its range
   // Fused step (stream-K only; new_k == nullptr otherwise): the step's new
   // tokens' rows [num_new][Hkv][D] are scattered into the caches by
   // slot_mapping, and sequence b's newest position seq_lens[b] - 1 is taken
@@ -1061,12 +1063,15 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       const int here = min(TPB, cache_nblk - blk);  // blocks of this tile inside the sequence (>= 1)
       const int s = j % NST;
       if (lane == 0) {
-        if (j >= NST) ok = mbar_wait_bounded(&empty[s], ((j / NST) - 1) & 1);
+        if (j >= NST) ok = mbar_wait_for(&empty[s], ((j / NST) - 1) & 1, p.wait_limit_ns);
         if (ok) mbar_arrive_expect_tx(&full[s], here * kBlockTx);
       }
       __syncwarp();
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (ok && lane < kCopies && cr < here) {
+      // test control: CTA 0 never loads its tile test_skip_tile, so the wait
+      // for it runs out (the timeout path, exercised without a fault)
+      const bool skip = p.test_skip_tile >= 0 && pid == 0 && j == p.test_skip_tile;
+      if (ok && !skip && lane < kCopies && cr < here) {
         if (pb < 0 || pb >= p.num_blocks) {
           record_error(KV_ERR_DEVICE_BOUNDS);
           pb = 0;
@@ -1097,7 +1102,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
         if (q <= last && static_cast<int64_t>(q) * Wc / P != static_cast<int64_t>(q + 1) * Wc / P) {
           const uint64_t t_start = globaltimer_ns();
           while (ok && ld_acquire_gpu(p.ws_flags + q) != p.epoch) {
-            if (globaltimer_ns() - t_start > kWaitLimitNs) {
+            if (globaltimer_ns() - t_start > p.wait_limit_ns) {
               record_error(KV_ERR_DEVICE_TIMEOUT);
               ok = 0;
             }
@@ -1116,7 +1121,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           mbar_arrive_expect_tx(pre_bar, npre * (part_o + part_ml));
           // the stages the pieces go to (virtual tiles n, n + 1, ...) must be free
           for (int v = n; (v - n) * per_stage < npre; ++v)
-            if (v >= NST) mbar_wait_bounded(&empty[v % NST], ((v / NST) - 1) & 1);
+            if (v >= NST) mbar_wait_for(&empty[v % NST], ((v / NST) - 1) & 1, p.wait_limit_ns);
         } else {
           mbar_arrive(pre_bar);
         }
@@ -1131,9 +1136,9 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     if (lane == 0) {  // keep the CTA alive until every issued copy has landed (bounded)
       for (int s = 0; s < NST && s < issued; ++s) {
         const int lst = s + ((issued - 1 - s) / NST) * NST;
-        mbar_wait_bounded(&full[s], (lst / NST) & 1);
+        mbar_wait_for(&full[s], (lst / NST) & 1, p.wait_limit_ns);
       }
-      if (kPrefetchParts && owner && npre > 0) mbar_wait_bounded(pre_bar, 0);
+      if (kPrefetchParts && owner && npre > 0) mbar_wait_for(pre_bar, 0, p.wait_limit_ns);
     }
     return;
   }
@@ -1232,7 +1237,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
         }
       }
       int w = 1;
-      if (lane == 0) w = mbar_wait_bounded(&full[s], (j / NST) & 1);
+      if (lane == 0) w = mbar_wait_for(&full[s], (j / NST) & 1, p.wait_limit_ns);
       ok = __shfl_sync(0xffffffffu, w, 0);
       if (ok) {
         __syncwarp();
@@ -1380,7 +1385,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       if (static_cast<int64_t>(q) * Wc / P != static_cast<int64_t>(q + 1) * Wc / P) {
         const uint64_t t_start = globaltimer_ns();
         while (ld_acquire_gpu(p.ws_flags + q) != p.epoch) {
-          if (globaltimer_ns() - t_start > kWaitLimitNs) {
+          if (globaltimer_ns() - t_start > p.wait_limit_ns) {
             record_error(KV_ERR_DEVICE_TIMEOUT);
             break;
           }
@@ -1400,7 +1405,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     part_row[k] = row;
   }
   if (kPrefetchParts) {
-    if (lane == 0) mbar_wait_bounded(pre_bar, 0);
+    if (lane == 0) mbar_wait_for(pre_bar, 0, p.wait_limit_ns);
     __syncwarp();
   }
   named_barrier_sync(1, kConsumers * 32);
@@ -1781,6 +1786,16 @@ uint64_t next_epoch() {
   return base + 2 * (counter.fetch_add(1) + 1);
 }
 
+// Stream-K test controls (kv_debug_set), read at each launch.
+struct SkControls {
+  std::atomic<int64_t> wait_limit_ns{static_cast<int64_t>(kWaitLimitNs)};
+  std::atomic<int64_t> skip_tile{-1};
+};
+SkControls& sk_controls() {
+  static SkControls c;
+  return c;
+}
+
 int sm_count() {
   static int cached[64] = {0};
   int dev = 0;
@@ -2007,6 +2022,8 @@ cudaError_t launch_sk(DecodeParams& p, const CUtensorMap& mk, const CUtensorMap&
   p.num_ctas = ctas;
   p.epoch = next_epoch();
   p.seg_cost = seg_cost_tiles(C::TL::kStageBytes);
+  p.wait_limit_ns = static_cast<uint64_t>(sk_controls().wait_limit_ns.load());
+  p.test_skip_tile = static_cast<int32_t>(sk_controls().skip_tile.load());
   // Cooperative: the driver refuses the launch unless all CTAs can be
   // resident at once, which the owners' waits on later CTAs rely on.
   cudaLaunchConfig_t cfg{};
@@ -2512,17 +2529,18 @@ extern "C" int kv_device_error(int reset, int* status_out) {
   return KV_OK;
 }
 
-extern "C" int kv_mapped_device_pointer(const void* host_ptr, void** device_ptr_out) {
-  if (!host_ptr || !device_ptr_out) return KV_ERR_INVALID_ARG;
-  void* d = nullptr;
-  const cudaError_t e = cudaHostGetDevicePointer(&d, const_cast<void*>(host_ptr), 0);
-  if (e != cudaSuccess) {
-    cudaGetLastError();  // not mapped: clear the sticky-free error and report it
-    last_cuda_error_text() = cudaGetErrorString(e);
-    return KV_ERR_INVALID_ARG;
+extern "C" int kv_debug_set(int key, int64_t value) {
+  SkControls& c = sk_controls();
+  switch (key) {
+    case KV_DEBUG_WAIT_LIMIT_NS:
+      c.wait_limit_ns = value > 0 ? value : static_cast<int64_t>(kWaitLimitNs);
+      return KV_OK;
+    case KV_DEBUG_SKIP_TILE:
+      c.skip_tile = value >= 0 ? value : -1;
+      return KV_OK;
+    default:
+      return KV_ERR_INVALID_ARG;
   }
-  *device_ptr_out = d;
-  return KV_OK;
 }
 
 extern "C" const char* kv_version(void) { return "pagedkv-gb300 0.1 (sm_103a)"; }

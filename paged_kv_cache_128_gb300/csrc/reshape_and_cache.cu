@@ -243,6 +243,35 @@ extern "C" int paged_copy_blocks(void* k_cache, void* v_cache, const int32_t* sr
   return cuda_status(cudaGetLastError());
 }
 
+extern "C" int paged_copy_blocks_fp8(void* k_cache, void* v_cache, float* k_scales, float* v_scales,
+                                     const int32_t* src, const int32_t* dst, int64_t n, int32_t num_layers,
+                                     int64_t layer_stride, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                     int64_t num_blocks, void* stream) {
+  using namespace pagedkv;
+  if (n < 0 || num_layers <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
+      layer_stride < 0)
+    return KV_ERR_INVALID_ARG;
+  if (n == 0) return KV_OK;
+  if (!k_cache || !v_cache || !k_scales || !v_scales || !src || !dst) return KV_ERR_INVALID_ARG;
+  // a block's codes: bs x Hkv x D bytes; its scales: Hkv x bs floats, contiguous at [block][Hkv][bs]
+  const int64_t code_bytes = static_cast<int64_t>(block_size) * num_kv_heads * head_dim;
+  const int64_t scale_bytes = static_cast<int64_t>(block_size) * num_kv_heads * 4;
+  if (num_layers > 1 && layer_stride < num_blocks * code_bytes) return KV_ERR_INVALID_ARG;  // layers would overlap
+  if (code_bytes % 16 != 0 || scale_bytes % 16 != 0 || layer_stride % 16 != 0 || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(k_scales, 16) || !aligned(v_scales, 16))
+    return KV_ERR_INVALID_ARG;
+  if (n > 0x7fffffff || num_layers > 65535) return KV_ERR_INVALID_ARG;
+  const dim3 grid(static_cast<unsigned>(n), static_cast<unsigned>(num_layers));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  copy_blocks_kernel<<<grid, kCopyThreads, 0, st>>>(static_cast<char*>(k_cache), static_cast<char*>(v_cache), src,
+                                                    dst, n, layer_stride, code_bytes, num_blocks);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_status(e);
+  copy_blocks_kernel<<<grid, kCopyThreads, 0, st>>>(reinterpret_cast<char*>(k_scales), reinterpret_cast<char*>(v_scales),
+                                                    src, dst, n, num_blocks * scale_bytes, scale_bytes, num_blocks);
+  return cuda_status(cudaGetLastError());
+}
+
 // ---------------------------------------------------------------------------
 // fp8 (E4M3) cache write ("paged-attention-impl-detail", 实践建议 4: the KV
 // cache inside a block can be quantised on its own).  Each (token, kv head)

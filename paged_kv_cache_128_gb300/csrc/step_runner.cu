@@ -275,11 +275,14 @@ extern "C" int kvstep_run(kvstep_t h, const void* q, const void* k, const void* 
   int32_t* d_tables = d_slots + c.num_step_tokens;
   int32_t* d_lens = d_tables + B * maxb;
   int32_t* d_rows = d_lens + B;
-  if (n_copies > 0 && c.cache_fp8) return KV_ERR_INVALID_ARG;  // the fp8 runner has no block copy
   if (n_copies > 0) {  // copy-on-write copies (every layer) before the step's writes and reads
-    st = paged_copy_blocks(c.k_cache, c.v_cache, d_rows + B, d_rows + 2 * B, n_copies, h->layers,
-                           h->layers > 1 ? c.cache_layer_stride : 0, c.num_kv_heads, c.head_dim, c.block_size,
-                           c.num_blocks, c.dtype, h->compute);
+    st = c.cache_fp8
+             ? paged_copy_blocks_fp8(c.k_cache, c.v_cache, c.k_scales, c.v_scales, d_rows + B, d_rows + 2 * B,
+                                     n_copies, h->layers, h->layers > 1 ? c.cache_layer_stride : 0, c.num_kv_heads,
+                                     c.head_dim, c.block_size, c.num_blocks, h->compute)
+             : paged_copy_blocks(c.k_cache, c.v_cache, d_rows + B, d_rows + 2 * B, n_copies, h->layers,
+                                 h->layers > 1 ? c.cache_layer_stride : 0, c.num_kv_heads, c.head_dim, c.block_size,
+                                 c.num_blocks, c.dtype, h->compute);
     if (st != KV_OK) return st;
   }
   const int64_t row = static_cast<int64_t>(c.num_kv_heads) * c.head_dim;

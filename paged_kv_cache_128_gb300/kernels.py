@@ -237,6 +237,33 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src: torch.Tensor,
                                   _stream_ptr(stream)), "paged_copy_blocks")
 
 
+def copy_blocks_fp8(k_cache: torch.Tensor, v_cache: torch.Tensor, k_scales: torch.Tensor, v_scales: torch.Tensor,
+                    src: torch.Tensor, dst: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Copy-on-write copies for fp8 caches: block ``dst[i]`` takes block
+    ``src[i]``'s K and V codes (uint8 ``[NB, BS, Hkv, D]``, or with a leading
+    layer axis) and scales (float32 ``[NB, Hkv, BS]``, likewise)."""
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (k_scales, "k_scales"), (v_scales, "v_scales"),
+                 (src, "src"), (dst, "dst")):
+        _cuda(t, n)
+    if k_cache.dtype != torch.uint8 or v_cache.shape != k_cache.shape or k_scales.dtype != torch.float32 \
+            or v_scales.shape != k_scales.shape or not all(t.is_contiguous() for t in (k_cache, v_cache, k_scales,
+                                                                                       v_scales)):
+        raise KVError(1, "fp8 caches: contiguous uint8 codes and float32 scales")
+    if src.dtype != torch.int32 or dst.dtype != torch.int32 or src.numel() != dst.numel():
+        raise KVError(1, "src and dst must be contiguous int32 of one length")
+    if k_cache.dim() == 4:
+        layers, (nb, bs, hkv, d) = 1, k_cache.shape
+        stride = 0
+    elif k_cache.dim() == 5:
+        layers, nb, bs, hkv, d = k_cache.shape
+        stride = k_cache.stride(0)
+    else:
+        raise KVError(1, "caches must be 4-D or 5-D")
+    check(lib().paged_copy_blocks_fp8(k_cache.data_ptr(), v_cache.data_ptr(), k_scales.data_ptr(),
+                                      v_scales.data_ptr(), src.data_ptr(), dst.data_ptr(), src.numel(), layers,
+                                      stride, hkv, d, bs, nb, _stream_ptr(stream)), "paged_copy_blocks_fp8")
+
+
 @dataclass
 class DecodePlan:
     kernel: int            # 0 = SIMT, 1 = split TMA + tensor cores, 2 = stream-K TMA + tensor cores
@@ -264,7 +291,7 @@ def decode_plan(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
 def alloc_workspace(plan: DecodePlan, device) -> Optional[torch.Tensor]:
     if plan.workspace_bytes == 0:
         return None
-    return torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=device)
+    return torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device=device)
 
 
 def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
@@ -387,6 +414,23 @@ def paged_decode_attention_static_scratch(out: torch.Tensor, q: torch.Tensor, k_
         seq_lens.data_ptr(), B, hq, hkv, d, bs, nb, block_tables.shape[1], max_seq_len, float(scale),
         blocks_per_split, dtype_code(q.dtype), _stream_ptr(stream)), "paged_decode_attention_static_scratch")
     return out
+
+
+# Stream-K test controls (kv_debug_set keys), process-wide.
+DEBUG_WAIT_LIMIT_NS = 1
+DEBUG_SKIP_TILE = 2
+DEBUG_DEFAULTS = {DEBUG_WAIT_LIMIT_NS: 0, DEBUG_SKIP_TILE: -1}
+
+
+def debug_set(key: int, value: int) -> None:
+    """Set one stream-K test control (see kv_debug_set)."""
+    check(lib().kv_debug_set(int(key), int(value)), "kv_debug_set")
+
+
+def debug_reset() -> None:
+    """Every stream-K control back to its default."""
+    for key, value in DEBUG_DEFAULTS.items():
+        debug_set(key, value)
 
 
 def static_scratch_bytes() -> int:

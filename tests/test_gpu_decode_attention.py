@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 
 def run_case(dtype, hq, hkv, d, bs, lens, seed, bps=0, nb=None, scale=None, value_scale=1.0, max_seq_len=None,
-             repeat=1):
+             repeat=1, workspace=None, expect_error=0):
     rng = np.random.default_rng(seed)
     B = len(lens)
     nb = nb or sum(-(-L // bs) for L in lens) + 3
@@ -53,15 +53,19 @@ def run_case(dtype, hq, hkv, d, bs, lens, seed, bps=0, nb=None, scale=None, valu
         seq_lens[live] = l
     out = torch.empty(B, hq, d, dtype=dt, device=dev)
     pk.paged_decode_attention(out, q.to(dev), kc, vc, torch.from_numpy(tables).to(dev),
-                              torch.from_numpy(seq_lens).to(dev), scale, max_seq_len or max(max(lens), 1), bps)
-    assert pk.device_error() == 0
+                              torch.from_numpy(seq_lens).to(dev), scale, max_seq_len or max(max(lens), 1), bps,
+                              workspace=workspace)
+    assert pk.device_error() == expect_error
+    if expect_error:
+        return None, None
     if repeat > 1:
         # the partition fixes the combine order: every call is bit-identical
         d_q, d_t, d_l = q.to(dev), torch.from_numpy(tables).to(dev), torch.from_numpy(seq_lens).to(dev)
         again = torch.empty_like(out)
         for _ in range(repeat - 1):
             again.fill_(0)
-            pk.paged_decode_attention(again, d_q, kc, vc, d_t, d_l, scale, max_seq_len or max(max(lens), 1), bps)
+            pk.paged_decode_attention(again, d_q, kc, vc, d_t, d_l, scale, max_seq_len or max(max(lens), 1), bps,
+                                      workspace=workspace)
             assert torch.equal(again, out)
         assert pk.device_error() == 0
 

@@ -17,6 +17,7 @@ import pytest
 import torch
 
 import paged_kv_cache_128_gb300 as pk
+from paged_kv_cache_128_gb300 import kernels as pk_kernels
 from oracle.attention import decode_attention_contiguous
 from tests.helpers import TOL, TORCH, sentinel_tensor, to_f64
 
@@ -204,6 +205,111 @@ def test_step_runner_applies_copies():
             assert torch.equal(bits(out_p), bits(out_r))
         assert copies > 0
         assert torch.equal(bits(kc_p), bits(kc_r)) and torch.equal(bits(vc_p), bits(vc_r))
+        assert pk.device_error() == 0
+    finally:
+        lib().kvstep_destroy(h)
+
+
+def test_copy_blocks_fp8_bit_exact():
+    """fp8 caches: each copied block's codes and scales equal the source's,
+    and every other block is untouched."""
+    dev = torch.device("cuda")
+    nb, bs, hkv, d = 40, 16, 2, 128
+    g = torch.Generator(device=dev).manual_seed(3)
+    kc = torch.randint(0, 256, (nb, bs, hkv, d), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+    vc = torch.randint(0, 256, (nb, bs, hkv, d), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+    ks = torch.rand(nb, hkv, bs, generator=g, device=dev)
+    vs = torch.rand(nb, hkv, bs, generator=g, device=dev)
+    src = torch.tensor([3, 7, 0, 39], dtype=torch.int32, device=dev)
+    dst = torch.tensor([10, 20, 21, 5], dtype=torch.int32, device=dev)
+    want = [t.clone() for t in (kc, vc, ks, vs)]
+    for t in want:
+        t[dst.long()] = t[src.long()]
+    pk_kernels.copy_blocks_fp8(kc, vc, ks, vs, src, dst)
+    torch.cuda.synchronize()
+    assert pk.device_error() == 0
+    for got, w in zip((kc, vc, ks.view(torch.int32), vs.view(torch.int32)),
+                      (want[0], want[1], want[2].view(torch.int32), want[3].view(torch.int32))):
+        assert torch.equal(got, w)
+
+
+def test_fp8_step_runner_applies_copies():
+    """The step runner with fp8 caches over forked sequences: the copies its
+    appends queue are applied (codes and scales) before its launch, and its
+    outputs, codes and scales equal the same steps driven from Python."""
+    import ctypes
+
+    from paged_kv_cache_128_gb300._lib import check, kvstep_config_t, lib
+    from paged_kv_cache_128_gb300.kernels import alloc_workspace, decode_plan, dtype_code
+
+    hq, hkv, d, bs, nb = 8, 2, 128, 16, 300
+    dt = torch.bfloat16
+    dev = torch.device("cuda")
+    sides = []
+    for _ in range(2):
+        rng = np.random.default_rng(19)
+        g = torch.Generator().manual_seed(19)
+        mgr = pk.KVBlockManager(nb, bs, rng.permutation(nb).tolist())
+        kc = torch.full((nb, bs, hkv, d), 0x7F, dtype=torch.uint8, device=dev)
+        vc = torch.full_like(kc, 0x7F)
+        ks = torch.full((nb, hkv, bs), float("nan"), device=dev)
+        vs = torch.full_like(ks, float("nan"))
+        sid = 0
+        for _ in range(4):
+            L = int(rng.integers(10, 200))
+            slots = mgr.allocate_for_prefill(sid, L)
+            pk.reshape_and_cache_fp8(torch.randn(L, hkv, d, generator=g).to(dt).to(dev),
+                                     torch.randn(L, hkv, d, generator=g).to(dt).to(dev), kc, vc, ks, vs,
+                                     torch.from_numpy(slots).to(dev))
+            parent = sid
+            sid += 1
+            for _ in range(2):
+                mgr.fork(parent, sid, int(rng.integers(1, L + 1)))
+                sid += 1
+        sides.append((mgr, kc, vc, ks, vs))
+    B = sid
+    ids = np.arange(B, dtype=np.int64)
+    max_blocks, max_len = 200 // bs + 8, 200 + 16
+    scale = 1.0 / math.sqrt(d)
+    g = torch.Generator().manual_seed(2)
+    q = torch.randn(B, hq, d, generator=g).to(dt).to(dev)
+    plan = decode_plan(B, hq, hkv, d, bs, max_len, dt)
+    ws = alloc_workspace(plan, dev)
+    mgr_r, kc_r, vc_r, ks_r, vs_r = sides[1]
+    cfg = kvstep_config_t(num_seqs=B, num_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=bs, num_blocks=nb,
+                          max_blocks_per_seq=max_blocks, max_seq_len=max_len, scale=scale, dtype=dtype_code(dt),
+                          num_step_tokens=B, k_cache=kc_r.data_ptr(), v_cache=vc_r.data_ptr(),
+                          workspace=ws.data_ptr(), workspace_bytes=ws.numel(),
+                          stream=torch.cuda.current_stream().cuda_stream, host_io=0, cache_fp8=1,
+                          k_scales=ks_r.data_ptr(), v_scales=vs_r.data_ptr())
+    h = ctypes.c_void_p()
+    check(lib().kvstep_create(mgr_r._h, ctypes.byref(cfg), ctypes.byref(h)), "kvstep_create")
+    mgr_p, kc_p, vc_p, ks_p, vs_p = sides[0]
+    rows = torch.arange(B, dtype=torch.int32, device=dev)
+    copies = 0
+    try:
+        for _ in range(5):
+            kn = torch.randn(B, hkv, d, generator=g).to(dt).to(dev)
+            vn = torch.randn(B, hkv, d, generator=g).to(dt).to(dev)
+            slots, tables, lens = mgr_p.decode_step(ids, max_blocks)
+            src, dst = mgr_p.take_copies()
+            copies += src.size
+            if src.size:
+                pk_kernels.copy_blocks_fp8(kc_p, vc_p, ks_p, vs_p, torch.from_numpy(src).to(dev),
+                                           torch.from_numpy(dst).to(dev))
+            out_p = torch.empty(B, hq, d, dtype=dt, device=dev)
+            pk.paged_decode_step_fp8(out_p, q, kn, vn, torch.from_numpy(slots).to(dev), rows, kc_p, vc_p, ks_p, vs_p,
+                                     torch.from_numpy(tables).to(dev), torch.from_numpy(lens).to(dev), scale, max_len)
+            out_r = torch.empty_like(out_p)
+            check(lib().kvstep_run(h, q.data_ptr(), kn.data_ptr(), vn.data_ptr(), out_r.data_ptr(), None, 0, None,
+                                   None, 0, ids.ctypes.data, B, None, 0), "kvstep_run")
+            check(lib().kvstep_join(h, torch.cuda.current_stream().cuda_stream), "kvstep_join")
+            torch.cuda.synchronize()
+            assert torch.equal(bits(out_p), bits(out_r))
+        assert copies > 0
+        assert torch.equal(kc_p, kc_r) and torch.equal(vc_p, vc_r)
+        assert torch.equal(ks_p.view(torch.int32), ks_r.view(torch.int32))
+        assert torch.equal(vs_p.view(torch.int32), vs_r.view(torch.int32))
         assert pk.device_error() == 0
     finally:
         lib().kvstep_destroy(h)
