@@ -168,10 +168,14 @@ struct Tile {
 };
 
 // Byte offset of element (row t, column d) inside a tile written by TMA with
-// 128-byte swizzle: slab d/64, row t, 16-byte chunk (d%64)/8 XOR (t%8).
-template <int BS>
+// 128-byte swizzle.  The tile holds whole physical blocks of PB rows, block
+// by block; inside a block, 64-column slab by slab (PB rows of 128 bytes
+// each); inside a row, 16-byte chunk (d%64)/8 XOR (t%8) (PB is a multiple of
+// 8, so a row's swizzle phase is t % 8 wherever its block sits).
+template <int D, int PB>
 __device__ __forceinline__ uint32_t swz(int t, int d) {
-  return static_cast<uint32_t>((d >> 6) * (BS * 128) + t * 128 + ((((d & 63) >> 3) ^ (t & 7)) << 4));
+  return static_cast<uint32_t>(((t / PB) * (D / 64) + (d >> 6)) * (PB * 128) + (t % PB) * 128 +
+                               ((((d & 63) >> 3) ^ (t & 7)) << 4));
 }
 
 template <int D, int NG>
@@ -227,7 +231,7 @@ __device__ __forceinline__ void reset_state(WarpState<D, NG>& st) {
 // one tile held in shared memory at kt_a (K) and vt_a (V) as one step of the
 // online softmax: the score chains of the sub-tiles are interleaved, and
 // the running max, the rescale of the accumulator and l are updated once.
-template <typename T, int D, int BS, int NG, int NS>
+template <typename T, int D, int PB, int NG, int NS>
 __device__ __forceinline__ void consume_subtiles(WarpState<D, NG>& st, uint32_t kt_a, uint32_t vt_a, int tok0, int L,
                                                  float sl2, int lane) {
   using M = Mma<T>;
@@ -245,7 +249,7 @@ __device__ __forceinline__ void consume_subtiles(WarpState<D, NG>& st, uint32_t 
     uint32_t a[NS][4];
 #pragma unroll
     for (int u = 0; u < NS; ++u)
-      ldmatrix_x4(kt_a + swz<BS>(u * 16 + k_row, kk * 16 + k_col), a[u][0], a[u][1], a[u][2], a[u][3]);
+      ldmatrix_x4(kt_a + swz<D, PB>(u * 16 + k_row, kk * 16 + k_col), a[u][0], a[u][1], a[u][2], a[u][3]);
 #pragma unroll
     for (int u = 0; u < NS; ++u)
 #pragma unroll
@@ -305,7 +309,7 @@ __device__ __forceinline__ void consume_subtiles(WarpState<D, NG>& st, uint32_t 
     uint32_t a[NS][4];
 #pragma unroll
     for (int u = 0; u < NS; ++u)
-      ldmatrix_x4_trans(vt_a + swz<BS>(u * 16 + v_row, mt * 16 + v_col), a[u][0], a[u][1], a[u][2], a[u][3]);
+      ldmatrix_x4_trans(vt_a + swz<D, PB>(u * 16 + v_row, mt * 16 + v_col), a[u][0], a[u][1], a[u][2], a[u][3]);
 #pragma unroll
     for (int u = 0; u < NS; ++u)
 #pragma unroll
@@ -316,7 +320,9 @@ __device__ __forceinline__ void consume_subtiles(WarpState<D, NG>& st, uint32_t 
 // Accumulate one tile (tokens tok0 .. tok0 + BS - 1 of a sequence of length
 // L) held in shared memory at kt (K) and vt (V).  Sub-tiles wholly past the
 // sequence end are skipped.
-template <typename T, int D, int BS, int NG>
+// BS: tokens of the tile; PB: rows of each physical block in it (the tile's
+// layout, see swz).
+template <typename T, int D, int BS, int NG, int PB = BS>
 __device__ __forceinline__ void consume_tile(WarpState<D, NG>& st, uint8_t* kt, uint8_t* vt, int tok0, int L,
                                              float sl2, int lane) {
   const int valid = min(BS, L - tok0);
@@ -325,18 +331,18 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NG>& st, uint8_t* kt, 
     const int chunks = (BS - valid) * (D / 8);
     for (int c = lane; c < chunks; c += 32) {
       const int t = valid + c / (D / 8), d = (c % (D / 8)) * 8;
-      *reinterpret_cast<uint4*>(vt + swz<BS>(t, d)) = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(vt + swz<D, PB>(t, d)) = make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();  // these bytes are TMA-written again later
     __syncwarp();
   }
   const uint32_t kt_a = smem_u32(kt), vt_a = smem_u32(vt);
   if constexpr (BS == 32) {
-    if (valid > 16) consume_subtiles<T, D, BS, NG, 2>(st, kt_a, vt_a, tok0, L, sl2, lane);
-    else consume_subtiles<T, D, BS, NG, 1>(st, kt_a, vt_a, tok0, L, sl2, lane);
+    if (valid > 16) consume_subtiles<T, D, PB, NG, 2>(st, kt_a, vt_a, tok0, L, sl2, lane);
+    else consume_subtiles<T, D, PB, NG, 1>(st, kt_a, vt_a, tok0, L, sl2, lane);
   } else {
     static_assert(BS == 16, "tiles are 16 or 32 tokens");
-    consume_subtiles<T, D, BS, NG, 1>(st, kt_a, vt_a, tok0, L, sl2, lane);
+    consume_subtiles<T, D, PB, NG, 1>(st, kt_a, vt_a, tok0, L, sl2, lane);
   }
 }
 
@@ -803,13 +809,19 @@ constexpr int kMaxSkCtas = 640;
 // wait and read every piece from global memory after the last tile).
 constexpr bool kPrefetchParts = true;
 
+// Tokens a stream-K tile aims at: 32 for 16-bit caches (one block of 32, or
+// two consecutive blocks of 16: fewer, larger pipeline transactions; 16-token
+// tiles were measured slower, a consumer's fixed cost per tile outweighing
+// the second stage per warp they allow).  fp8: 64 tokens for up to 8 query
+// heads per kv head, so a stage carries as many bytes as a 16-bit one (more
+// heads: 32, to fit registers).
+constexpr int sk_want_tokens(int D, int NG, bool F8) { return F8 ? (NG == 1 ? 64 : 32) : 32; }
+
 template <typename T, int D, int BS, int NG, int NST, bool F8 = false>
 struct SkCfg {
-  // A stream-K tile is 32 tokens: one block of 32, or two consecutive
-  // blocks of 16 of the same sequence (fewer, larger pipeline transactions).
-  // fp8 tiles are 64 tokens for up to 8 query heads per kv head, so a stage
-  // carries as many bytes as a 16-bit one (more heads: 32, to fit registers).
-  static constexpr int kWantTokens = F8 && NG == 1 ? 64 : 32;
+  // A stream-K tile is sk_want_tokens tokens: one block, or consecutive
+  // blocks of the same sequence.
+  static constexpr int kWantTokens = sk_want_tokens(D, NG, F8);
   static constexpr int kBlocksPerTile = BS >= kWantTokens ? 1 : kWantTokens / BS;
   static constexpr int kTileTokens = BS * kBlocksPerTile;
   // fp8 caches: E4M3 code tiles, and per stage the tile's K and V scales
@@ -835,8 +847,10 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   using C = SkCfg<T, D, BS, NG, NST, F8>;
   using TL = typename C::TL;
   constexpr int TPB = C::kBlocksPerTile, TT = C::kTileTokens;
-  // TMA copies per block of a tile: K and V slabs, and with fp8 the K and V scales
-  constexpr int kPerBlock = 2 * TL::kSub + (F8 ? 2 : 0);
+  // TMA copies per block of a tile: 16-bit caches one each for K and V (a
+  // 4-D box covers all of a block's 64-column slabs); fp8 caches K and V
+  // slabs and the K and V scales
+  constexpr int kPerBlock = F8 ? 2 * TL::kSub + 2 : 2;
   constexpr int kCopies = kPerBlock * TPB;
   static_assert(kCopies <= 32, "one copy per producer lane");
   // bytes one block of a tile brings into its stage
@@ -1053,11 +1067,13 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
         }
       }
       // One copy per lane: lane l < kCopies loads block r = l / kPerBlock of
-      // the tile; w = l % kPerBlock < 2 kSub is column slab w / 2 of K (even
-      // w) or V (odd w) (TMA tensor copies, 1024-byte aligned destinations);
-      // with fp8, w = 2 kSub and 2 kSub + 1 are the block's K and V scales,
-      // bs contiguous floats each (a bulk copy: 16-byte aligned source and
-      // destination, bs * 4 bytes).
+      // the tile.  16-bit caches: w = l % 2 is K (0) or V (1), all of the
+      // block's column slabs in one 4-D tensor copy into the block's place
+      // in the tile (block-major, see swz).  fp8: w < 2 kSub is column slab
+      // w / 2 of K (even w) or V (odd w), and w = 2 kSub, 2 kSub + 1 the
+      // block's K and V scales, bs contiguous floats each (a bulk copy:
+      // 16-byte aligned source and destination, bs * 4 bytes).  Tensor-copy
+      // destinations are 1024-byte aligned.
       const int cr = lane / kPerBlock, cw8 = lane % kPerBlock, csl = (cw8 >> 1) % TL::kSub;
       int pb = __shfl_sync(0xffffffffu, mine, (blk + min(cr, TPB - 1)) & 31);
       const int here = min(TPB, cache_nblk - blk);  // blocks of this tile inside the sequence (>= 1)
@@ -1076,10 +1092,13 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           record_error(KV_ERR_DEVICE_BOUNDS);
           pb = 0;
         }
-        if (cw8 < 2 * TL::kSub) {
+        if constexpr (!F8) {
+          uint8_t* dst = smem + s * TL::kStageBytes + cw8 * TL::kTileBytes + cr * (TL::kSub * BS * 128);
+          tma_load_4d(dst, cw8 ? &tmV : &tmK, &full[s], 0, pb * BS, 0, c.kvh);
+        } else if (cw8 < 2 * TL::kSub) {
           uint8_t* dst = smem + s * TL::kStageBytes + (cw8 & 1) * TL::kTileBytes + csl * TL::kSlabBytes + cr * BS * 128;
-          tma_load_3d(dst, (cw8 & 1) ? &tmV : &tmK, &full[s], csl * (F8 ? 128 : 64), c.kvh, pb * BS);
-        } else if constexpr (F8) {
+          tma_load_3d(dst, (cw8 & 1) ? &tmV : &tmK, &full[s], csl * 128, c.kvh, pb * BS);
+        } else {
           const int which = cw8 - 2 * TL::kSub;  // 0: K scales, 1: V scales
           float* dst = scales + (s * 2 + which) * TT + cr * BS;
           const float* src = (which ? p.v_scales : p.k_scales) + (static_cast<int64_t>(pb) * Hkv + c.kvh) * BS;
@@ -1249,7 +1268,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
             if (ch < 2 * (D / 8)) {
               const bool isv = ch >= D / 8;
               const int d = (ch % (D / 8)) * 8;
-              *reinterpret_cast<uint4*>(kt + (isv ? TL::kTileBytes : 0) + swz<TT>(tl, d)) = pv[u];
+              *reinterpret_cast<uint4*>(kt + (isv ? TL::kTileBytes : 0) + swz<D, BS>(tl, d)) = pv[u];
             }
           }
           fence_proxy_async_smem();  // the stage is TMA-written again later
@@ -1273,7 +1292,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           consume_tile_f8<D, TT, NG>(st, kt, kt + TL::kTileBytes, scales + s * 2 * TT, scales + (s * 2 + 1) * TT,
                                      c.blk * TT, L, sl2, lane);
         else
-          consume_tile<T, D, TT, NG>(st, kt, kt + TL::kTileBytes, c.blk * TT, L, sl2, lane);
+          consume_tile<T, D, TT, NG, BS>(st, kt, kt + TL::kTileBytes, c.blk * TT, L, sl2, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
       }
@@ -1826,7 +1845,8 @@ struct Stages {
 // size 2; the stage count follows the 32-token tile).
 template <int D, int BS, int NG>
 int sk_smem_for(int B) {
-  constexpr int kTileTokens = BS >= 32 ? BS : 32;
+  constexpr int kWant = sk_want_tokens(D, NG, false);
+  constexpr int kTileTokens = BS >= kWant ? BS : kWant;
   return SkCfg<__half, D, BS, NG, Stages<D, kTileTokens>::value>::smem_bytes(B);
 }
 
@@ -1921,7 +1941,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Kinds of tensor map: 16-bit cache slabs and fp8 (E4M3) cache slabs.
-enum MapKind { kMap16 = 0, kMapFp8 = 1 };
+enum MapKind { kMap16 = 0, kMapFp8 = 1, kMap16Blocks = 2 };
 
 struct MapKey {
   const void* ptr;
@@ -1934,7 +1954,11 @@ struct MapKey {
 
 // kMap16: the cache as a 3-D tensor {D, Hkv, NB * BS} of 16-bit elements; a
 // box {64, 1, BS} is one 128-byte column slab of one block's rows for one
-// head.  kMapFp8: the same of 1-byte codes, box {128, 1, BS}.
+// head.  kMapFp8: the same of 1-byte codes, box {128, 1, BS}.  kMap16Blocks:
+// the 16-bit cache as a 4-D tensor {64, NB * BS, D / 64, Hkv} (a column in
+// a slab, a token row, a slab, a head; strides Hkv D 2, 128 and D 2 bytes),
+// box {64, BS, D / 64, 1}: all of one block's slabs for one head in one
+// copy, laid out slab by slab of BS rows of 128 bytes.
 bool get_tensor_map(const void* cache, int64_t rows, int hkv, int d, int bs, CUtensorMap* out, int kind = kMap16) {
   static std::mutex mu;
   static MapKey keys[32];
@@ -1950,20 +1974,32 @@ bool get_tensor_map(const void* cache, int64_t rows, int hkv, int d, int bs, CUt
   auto fn = encode_fn();
   if (!fn) return false;
   CUtensorMap m;
-  cuuint32_t estr[3] = {1, 1, 1};
-  const int es = kind == kMapFp8 ? 1 : 2;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es, static_cast<cuuint64_t>(hkv) * d * es};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), 1, static_cast<cuuint32_t>(bs)};
-  // L2 fill promotion: 256 bytes for 16-bit caches (one (token, head) row
-  // at head_dim 128: the tile's two slabs), 128 bytes for fp8 (one row); a
-  // 256-byte fill of an fp8 row also fetches the next head's row, which
-  // another CTA reads much later (measured: 10-33 % more DRAM reads)
-  const CUresult r = fn(&m, kind == kMapFp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
-                        const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B,
-                        kind == kMapFp8 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r;
+  if (kind == kMap16Blocks) {
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(d / 64),
+                          static_cast<cuuint64_t>(hkv)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(hkv) * d * 2, 128, static_cast<cuuint64_t>(d) * 2};
+    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(bs), static_cast<cuuint32_t>(d / 64), 1};
+    r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(cache), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint32_t estr[3] = {1, 1, 1};
+    const int es = kind == kMapFp8 ? 1 : 2;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es, static_cast<cuuint64_t>(hkv) * d * es};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), 1, static_cast<cuuint32_t>(bs)};
+    // L2 fill promotion: 256 bytes for 16-bit caches (one (token, head) row
+    // at head_dim 128: the tile's two slabs), 128 bytes for fp8 (one row); a
+    // 256-byte fill of an fp8 row also fetches the next head's row, which
+    // another CTA reads much later (measured: 10-33 % more DRAM reads)
+    r = fn(&m, kind == kMapFp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
+           const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B,
+           kind == kMapFp8 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   if (r != CUDA_SUCCESS) return false;
   const int slot = used < 32 ? used++ : (next++ % 32);
   keys[slot] = key;
@@ -1997,7 +2033,7 @@ struct Stages8 {
 
 template <typename T, int D, int BS, int NG, bool F8 = false>
 cudaError_t launch_sk(DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, int max_ctas, cudaStream_t st) {
-  constexpr int kWant = F8 && NG == 1 ? 64 : 32;
+  constexpr int kWant = sk_want_tokens(D, NG, F8);
   constexpr int kTileTokens = BS >= kWant ? BS : kWant;  // matches SkCfg::kTileTokens
   constexpr int NST =
       std::conditional<F8, Stages8<D, kTileTokens>, Stages<D, kTileTokens>>::type::value;
@@ -2247,8 +2283,11 @@ int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cac
   CUtensorMap mk, mv;
   if (pl.kind != kSimt) {
     const int64_t rows = num_blocks * block_size;
-    if (!get_tensor_map(k_cache, rows, num_kv_heads, head_dim, block_size, &mk) ||
-        !get_tensor_map(v_cache, rows, num_kv_heads, head_dim, block_size, &mv))
+    // the stream-K kernel copies whole blocks (all slabs) at once; the split
+    // kernels copy slab by slab
+    const int kind = pl.kind == kTensorCoreStreamK ? kMap16Blocks : kMap16;
+    if (!get_tensor_map(k_cache, rows, num_kv_heads, head_dim, block_size, &mk, kind) ||
+        !get_tensor_map(v_cache, rows, num_kv_heads, head_dim, block_size, &mv, kind))
       return cuda_status(cudaErrorInvalidValue, "cuTensorMapEncodeTiled failed");
   }
   if (step != nullptr && step->num_tokens > 0 && p.new_k == nullptr) {
