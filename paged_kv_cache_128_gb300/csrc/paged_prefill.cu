@@ -49,6 +49,7 @@ struct PrefillParams {
   float scale_log2;  // scale * log2(e)
   int64_t num_tokens;  // rows of q and out
   int32_t hg_log2;     // tensor-core kernel: log2 of the query heads per row tile
+  int32_t row_tiles;   // tensor-core kernel: row tiles per (sequence, head group) in the grid
 };
 
 // Byte offset of (key, dim) in a [kPfKeys][D] 16-bit tile: 128-byte slabs of
@@ -263,83 +264,128 @@ cudaError_t launch_prefill(const PrefillParams& p, int head_dim, int max_query_l
 // Tensor-core (tcgen05) kernel, used when block_size divides 128 and is a
 // multiple of 16.
 //
-// One CTA per 128 query rows, two CTAs per SM: each CTA's MMAs run while
-// the other CTA's softmax works, and one CTA's start-up overlaps the
-// other's tiles.  With group G a multiple of a power of two HG (HG = the
-// largest power of two dividing G, at most 8), the rows are HG query heads
-// of one kv head times 128 / HG chunk tokens (row r = token r / HG, head
-// r % HG), so every K/V tile serves all the tile's heads.  Key tiles hold
-// 128 positions.
-//   warp 9: TMA producer -- Q once, then each key tile's K and V, one box per
-//     (block, 64-dim slab), through the block table (a K stage is free once
-//     its S is done, a V stage once its P V is);
-//   warp 8: owns 256 tensor-memory columns (S at 0-127, O at 128-255); one
-//     lane issues the MMAs: S_j = Q K_j^T (M 128, N 128, K head_dim) once
-//     P V of tile j - 1 has read the previous P, and O += P_j V_j (M 128,
-//     N head_dim, K 128) with P_j from tensor memory once it is written;
-//   warps 0-7: warp w owns the 16 rows 32 (w % 4) + 16 (w / 4) .. + 15 and
-//     reads them with the 16x256b tensor-memory shape: a quad of threads
-//     holds two rows, each thread a quarter of their columns, so the row max
-//     and sum are two quad shuffles and the warps never wait for one
-//     another.  Each warp masks keys past each row's position and writes P
-//     (rounded to the q dtype, two keys per column) over S columns 0-63 with
-//     the 16x128b shape.  P, the sums and O are relative to a reference max
-//     that moves only when a tile's max exceeds it by more than 2^8 (then
-//     the warp rescales the rows' sums and O columns in tensor memory); P
-//     stays <= 256.  O is read from tensor memory once, at the end.
+// One CTA per 128-row query tile, two CTAs per SM: one CTA's softmax runs
+// while the tensor cores work on the other's MMAs.  With group G a multiple
+// of a power of two HG (HG = the largest power of two dividing G, at most
+// 8), a tile's rows are HG query heads of one kv head times 128 / HG chunk
+// tokens (row r = token r / HG, head r % HG), so every K/V tile serves all
+// the tile's heads.  The grid is 1-D over (head group, sequence, row tile),
+// row tile slowest and counted down: the tiles with the most keys start
+// first and the shortest close the launch.  Tensor memory (256 columns): S
+// at columns 0-127 (P over 64-127) and O at 128 + (0 .. head_dim - 1).
+//   warp 5: TMA producer -- Q once, then each 128-key tile's K and V, one
+//     box per (block, 64-dim slab), through the block table; a K stage is
+//     free once its S is done, a V stage once its P V is;
+//   warp 4: one lane issues the MMAs: S = Q K^T (M 128, N 128, K head_dim)
+//     once P V of the previous tile has completed (S overwrites P), and
+//     O += P V (M 128, N head_dim, K 128) with P from tensor memory once the
+//     softmax warps have written it;
+//   warps 0-3: thread t of warp w owns row 32 w + t and reads its S row with
+//     the 32x32b tensor-memory shape in two halves of 64 registers, so the
+//     row max and sum need no exchange.  In one pass it computes e = S c2 -
+//     m_ref (keys past the row's position: -inf), P = exp2(e) rounded to
+//     the q dtype, the sum of the rounded P, and the tile's max of e.  P,
+//     the sum and O are relative to a reference m_ref that moves only when
+//     a tile's max lies more than 2^8 above it (then the pass is repeated
+//     and the row's sum and O columns are rescaled); P stays <= 256.  O is
+//     read from tensor memory once, at the end, and written as the row's
+//     output.
 // Slots past the last key of the last tile (the tail of its last block and
 // blocks never loaded) are zeroed in the V tile before P V reads it, so a
 // sentinel there cannot reach the output.
-
-constexpr int kTcRows = 128;                 // MMA M: query rows per CTA
-constexpr int kTcKeys = 128;                 // keys per tile: N of S, K of P V
-constexpr int kTcSoftWarps = 8;              // softmax warps 0-7
+// ---------------------------------------------------------------------------
+constexpr int kTcRows = 128;                      // MMA M: rows of a query tile
+constexpr int kTcKeys = 128;                      // keys per tile: N of S, K of P V
+constexpr int kTcSoftWarps = 4;                   // softmax warps: one row per thread
 constexpr int kTcMmaWarp = kTcSoftWarps, kTcTmaWarp = kTcSoftWarps + 1;
 constexpr int kTcThreads = 32 * (kTcSoftWarps + 2);
-constexpr uint32_t kTcCols = 256;            // tensor-memory columns per CTA
+constexpr uint32_t kTcCols = 256;                 // S (128) and O (up to 128)
 
 template <int D>
 struct TcLayout {
-  static constexpr int kStages = D == 64 ? 2 : 1;   // K and V ring depth (two CTAs per SM)
+  // ring depths: two CTAs per SM share 227 KB of shared memory
+  static constexpr int kKStages = D == 64 ? 2 : 1, kVStages = kKStages;
   static constexpr int kSlab = 128 * 128;           // one 64-column slab of 128 rows
-  static constexpr int kQ = (D / 64) * kSlab;       // Q tile
-  static constexpr int kKV = (D / 64) * kSlab;      // K or V tile
+  static constexpr int kTile = (D / 64) * kSlab;    // a Q, K or V tile
   static constexpr int kOffQ = 0;
-  static constexpr int kOffKV = kQ;                 // stage s: K at + 2 s kKV, V at + (2 s + 1) kKV
-  static constexpr int kOffBar = kOffKV + kStages * 2 * kKV;
+  static constexpr int kOffK = kTile;               // stage s at + s kTile
+  static constexpr int kOffV = kOffK + kKStages * kTile;
+  static constexpr int kOffBar = kOffV + kVStages * kTile;
   static constexpr int kBytes = kOffBar + 256;
   static constexpr int kSmem = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
+// Three-input max (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// One key pair of the softmax pass: the running maxima (two chains), P =
+// exp2(e) for both keys rounded to T and packed into s[i] (the pair's S
+// values, at s[2i] and s[2i + 1], are already read), their sum into ls[i % 2].
+template <typename T>
+__device__ __forceinline__ void softmax_pair(float2 e, int i, float& ma, float& mb, uint64_t (&ls)[2],
+                                             uint32_t (&s)[64]) {
+  if (i & 1) mb = max3(mb, e.x, e.y);
+  else ma = max3(ma, e.x, e.y);
+  const uint32_t pk = Mma<T>::pack(fast_exp2(e.x), fast_exp2(e.y));
+  s[i] = pk;
+  // the sum is taken over the rounded P that P V multiplies, so that the
+  // weights the output is normalised by are the ones it was built from
+  const float2 r = Mma<T>::unpack(pk);
+  ls[i & 1] = tc::fadd2(ls[i & 1], tc::f2(r.x, r.y));
+}
+
+// Compiler barrier: the 32 packed values, the sums and the max are computed
+// here, before any later tensor-memory load is issued.
+__device__ __forceinline__ void pin_regs(uint32_t (&v)[32], uint64_t (&ls)[2], float& m) {
+  asm volatile(""
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                 "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                 "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
+                 "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]),
+                 "+r"(v[29]), "+r"(v[30]), "+r"(v[31]), "+l"(ls[0]), "+l"(ls[1]), "+f"(m));
+}
+
+// Registers: two CTAs of six warps put three warps on each of the SM's four
+// sub-partitions (16,384 registers each), so a thread holds at most 168.
 template <typename T, int D>
 __global__ void __launch_bounds__(kTcThreads, 2)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using Lay = TcLayout<D>;
-  constexpr int kSlabs = D / 64, kStages = Lay::kStages;
+  constexpr int kSlabs = D / 64, KST = Lay::kKStages, VST = Lay::kVStages;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar_q = reinterpret_cast<uint64_t*>(sm + Lay::kOffBar);
-  uint64_t* bar_kfull = bar_q + 1;              // [kStages] K tile landed
-  uint64_t* bar_vfull = bar_kfull + kStages;    // [kStages] V tile landed
-  uint64_t* bar_kempty = bar_vfull + kStages;   // [kStages] S of the tile done
-  uint64_t* bar_vempty = bar_kempty + kStages;  // [kStages] P V of the tile done
-  uint64_t* bar_s = bar_vempty + kStages;       // S written
-  uint64_t* bar_p = bar_s + 1;                  // P written (every softmax thread arrives)
-  uint64_t* bar_pv = bar_p + 1;                 // P V done
+  uint64_t* bar_kfull = bar_q + 1;             // [KST] K tile landed
+  uint64_t* bar_kempty = bar_kfull + KST;      // [KST] S of the tile done
+  uint64_t* bar_vfull = bar_kempty + KST;      // [VST] V tile landed
+  uint64_t* bar_vempty = bar_vfull + VST;      // [VST] P V of the tile done
+  uint64_t* bar_s = bar_vempty + VST;          // S written
+  uint64_t* bar_p = bar_s + 1;                 // P written (every softmax thread arrives)
+  uint64_t* bar_pv = bar_p + 1;                // P V done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_pv + 1);
 
   const int hg = 1 << p.hg_log2, tpt = kTcRows >> p.hg_log2;
-  const int qt = gridDim.x - 1 - blockIdx.x;  // tiles with the most keys start first
-  const int h0 = blockIdx.y * hg, b = blockIdx.z;
+  // 1-D grid over (head group, sequence, row tile), the row tile slowest and
+  // counted down, so the tiles with the most keys are dispatched first and
+  // the last CTAs to start are the shortest
+  const int ngroups = p.num_heads >> p.hg_log2, nrt = p.row_tiles;
+  const int gi = static_cast<int>(blockIdx.x % ngroups);
+  const int b = static_cast<int>((blockIdx.x / ngroups) % p.num_seqs);
+  const int qt = nrt - 1 - static_cast<int>(blockIdx.x / ngroups / p.num_seqs);
+  const int h0 = gi * hg;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qs = __ldg(p.query_start + b), n = __ldg(p.query_start + b + 1) - qs;
   // rows past the grid's reach (a chunk longer than max_query_len) would be
-  // left uncomputed: the last row tile of the sequence reports it
-  if (qt == gridDim.x - 1 && blockIdx.y == 0 && threadIdx.x == 0 && n > static_cast<int>(gridDim.x) * tpt)
-    record_error(KV_ERR_DEVICE_BOUNDS);
-  if (n <= 0 || qt * tpt >= n) return;
+  // left uncomputed: the sequence's last row tile in the grid reports it
+  if (qt == nrt - 1 && gi == 0 && threadIdx.x == 0 && n > nrt * tpt) record_error(KV_ERR_DEVICE_BOUNDS);
+  const int tok0 = qt * tpt;  // first chunk token of the tile
+  if (n <= 0 || tok0 >= n) return;
   int L = __ldg(p.seq_lens + b);
   const int64_t cap = static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size;
   if (L < n || qs < 0 || qs + n > p.num_tokens) {  // the chunk must lie inside its sequence and in q
@@ -352,16 +398,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (L < n) return;
   }
   const int ctx = L - n, kvh = h0 / p.group;
-  const int tok0 = qt * tpt, rows_here = min(n - tok0, tpt);
+  // the tile's chunk tokens, the keys its last row sees, its key tiles
+  const int rows_here = min(n - tok0, tpt);
   const int nkeys = min(ctx + tok0 + rows_here, L);
   const int ntiles = (nkeys + kTcKeys - 1) / kTcKeys;
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < KST; ++s) {
       mbar_init(bar_kfull + s, 1);
-      mbar_init(bar_vfull + s, 1);
       mbar_init(bar_kempty + s, 1);
+    }
+    for (int s = 0; s < VST; ++s) {
+      mbar_init(bar_vfull + s, 1);
       mbar_init(bar_vempty + s, 1);
     }
     mbar_init(bar_s, 1);
@@ -374,7 +423,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + kTcKeys;  // S (P over its first half-columns), O
 
   if (warp == kTcTmaWarp) {
     if (lane == 0) {
@@ -387,19 +435,17 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         tma_load_3d(sm + Lay::kOffQ + s * Lay::kSlab, &tmQ, bar_q, s * 64, h0, qs + tok0);
       const int32_t* table = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
       const int bs = p.block_size;
-      // K (V) of tile j into stage j % kStages once S (P V) of tile
-      // j - kStages is done.  K runs one tile ahead of V; V of tile j is
-      // issued first, since P V of tile j - 1 completes before S of tile j
-      // is issued
+      // K (V) of tile j into stage j % KST (j % VST) once S (P V) of the tile
+      // that stage held before is done.  K runs one tile ahead of V.
       auto load = [&](int j, bool is_v) -> bool {
-        const int st = j % kStages;
+        const int nst = is_v ? VST : KST, st = j % nst;
         uint64_t* full = (is_v ? bar_vfull : bar_kfull) + st;
-        if (j >= kStages && !mbar_wait_bounded((is_v ? bar_vempty : bar_kempty) + st, ((j / kStages) - 1) & 1))
+        if (j >= nst && !mbar_wait_bounded((is_v ? bar_vempty : bar_kempty) + st, ((j / nst) - 1) & 1))
           return false;
         const int k0 = j * kTcKeys, k1 = min(k0 + kTcKeys, nkeys);
         const int blk0 = k0 / bs, blk1 = (k1 + bs - 1) / bs;
         mbar_arrive_expect_tx(full, static_cast<uint32_t>((blk1 - blk0) * bs * D * 2));
-        uint8_t* dst = sm + Lay::kOffKV + (2 * st + (is_v ? 1 : 0)) * Lay::kKV;
+        uint8_t* dst = sm + (is_v ? Lay::kOffV : Lay::kOffK) + st * Lay::kTile;
         const CUtensorMap* map = is_v ? &tmV : &tmK;
         for (int bi = blk0; bi < blk1; ++bi) {
           int pb = __ldg(table + bi);
@@ -418,152 +464,147 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         if (ok && j + 1 < ntiles) ok = load(j + 1, false);
       }
       // every stage's last S and P V have completed (no copy or commit in flight at exit)
-      for (int j = max(0, ntiles - kStages); j < ntiles; ++j) {
-        mbar_wait_bounded(bar_kempty + (j % kStages), (j / kStages) & 1);
-        mbar_wait_bounded(bar_vempty + (j % kStages), (j / kStages) & 1);
-      }
+      for (int j = max(0, ntiles - KST); j < ntiles; ++j) mbar_wait_bounded(bar_kempty + (j % KST), (j / KST) & 1);
+      for (int j = max(0, ntiles - VST); j < ntiles; ++j) mbar_wait_bounded(bar_vempty + (j % VST), (j / VST) & 1);
     }
   } else if (warp == kTcMmaWarp) {
     if (lane == 0) {
       // ---- MMA issue
       constexpr uint32_t idS = tc::idesc_f16(kBf16, kTcRows, kTcKeys, false);
       constexpr uint32_t idPV = tc::idesc_f16(kBf16, kTcRows, D, true);
-      const uint32_t aQ = smem_u32(sm + Lay::kOffQ);
       bool ok = mbar_wait_bounded(bar_q, 0);
+      const uint32_t aQ = smem_u32(sm + Lay::kOffQ);
       for (int j = 0; j < ntiles && ok; ++j) {
-        const int st = j % kStages;
-        // S_j overwrites the S columns, which hold P_{j-1} until P V of tile j - 1 is done
+        const int ks = j % KST, vs = j % VST;
+        if (!mbar_wait_bounded(bar_kfull + ks, (j / KST) & 1)) break;
+        // S overwrites P of the previous tile: its P V must be done
         if (j > 0 && !mbar_wait_bounded(bar_pv, (j - 1) & 1)) break;
-        if (!mbar_wait_bounded(bar_kfull + st, (j / kStages) & 1)) break;
         tc::fence_after();
-        const uint32_t kb = smem_u32(sm + Lay::kOffKV + st * 2 * Lay::kKV);
+        const uint32_t kb = smem_u32(sm + Lay::kOffK + ks * Lay::kTile);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * Lay::kSlab + (kk & 3) * 32;  // 64-dim slab, 16-dim step inside it
-          tc::mma_f16(tS, tc::sdesc_sw128(aQ + off, 16, 1024), tc::sdesc_sw128(kb + off, 16, 1024), idS, kk > 0);
+          tc::mma_f16(tmem, tc::sdesc_sw128(aQ + off, 16, 1024), tc::sdesc_sw128(kb + off, 16, 1024), idS, kk > 0);
         }
         tc::commit(bar_s);
-        tc::commit(bar_kempty + st);
+        tc::commit(bar_kempty + ks);
+        if (!mbar_wait_bounded(bar_vfull + vs, (j / VST) & 1)) break;
+        // P lands after the softmax warps have zeroed the last tile's V tail
         if (!mbar_wait_bounded(bar_p, j & 1)) break;
-        if (!mbar_wait_bounded(bar_vfull + st, (j / kStages) & 1)) break;
         tc::fence_after();
-        const uint32_t vb = smem_u32(sm + Lay::kOffKV + st * 2 * Lay::kKV + Lay::kKV);
+        const uint32_t vb = smem_u32(sm + Lay::kOffV + vs * Lay::kTile);
 #pragma unroll
         for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-          // keys 16 kk .. + 15: P, two keys per column
-          const uint32_t pa = tS + kk * 8;
-          tc::mma_f16_ts(tO, pa, tc::sdesc_sw128(vb + kk * 16 * 128, Lay::kSlab, 1024), idPV,
+          // keys 16 kk .. + 15: P, two keys per column from S column 64
+          tc::mma_f16_ts(tmem + 128, tmem + 64 + kk * 8, tc::sdesc_sw128(vb + kk * 16 * 128, Lay::kSlab, 1024), idPV,
                          (j > 0 || kk > 0) ? 1u : 0u);
         }
         tc::commit(bar_pv);
-        tc::commit(bar_vempty + st);
+        tc::commit(bar_vempty + vs);
       }
     }
   } else {
-    // ---- softmax: warp w owns the 16 rows 32 (w % 4) + 16 (w / 4) .. + 15;
-    // a quad of threads holds two rows (lane / 4 and lane / 4 + 8), each
-    // thread a quarter of their columns, so row maxima and sums are quad
-    // shuffles and the warps run independently
-    const int quarter = warp & 3, half = warp >> 2;
-    const int rbase = quarter * 32 + half * 16;
-    const int g = lane >> 2, c4 = lane & 3;
-    const uint32_t lanes = static_cast<uint32_t>(rbase) << 16;
-    const uint32_t tsw = tS + lanes, tow = tO + lanes;
-    int tok[2], hh[2], lim_abs[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int r = rbase + g + 8 * e;
-      tok[e] = r >> p.hg_log2;
-      hh[e] = r & (hg - 1);
-      lim_abs[e] = min(ctx + tok0 + tok[e], nkeys - 1);  // last key row r sees
-    }
+    // ---- softmax: thread t of warp w owns row 32 w + t
+    const int r = warp * 32 + lane;
+    const uint32_t tS = tmem + (static_cast<uint32_t>(warp * 32) << 16), tO = tS + 128;
+    const int tok = r >> p.hg_log2, hh = r & (hg - 1);
+    const int lim_abs = min(ctx + tok0 + tok, nkeys - 1);  // last key the row sees
     const float c2 = p.scale_log2;
     const uint64_t c2x2 = tc::f2(c2, c2);
-    constexpr float kSlack = 8.f;
-    float m_ref[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    // a reference at most 2^8 below the row's max keeps P <= 256; before
+    // the row's first key it is also at most 2^8 above it, so the largest P
+    // keeps its precision in fp16 too
+    constexpr float kSlack = 8.f, kLow = 8.f;
+    // P, O and the sum are relative to m_ref, 0 until the row's scores
+    // call for another
+    float m_ref = 0.f, l = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       // after a timeout (recorded) the remaining waits are skipped
       if (ok && !mbar_wait_bounded(bar_s, j & 1)) ok = false;
       tc::fence_after();
-      int lim[2];
+      const int lim = lim_abs - j * kTcKeys;  // columns <= lim are keys of this row
+      const bool part = __any_sync(0xffffffffu, lim < kTcKeys - 1);
+      // One pass over the row's 128 S values, in two halves of 64 registers
+      // (keys 64-127, then 0-63): e = S * c2 - m_ref (keys the row does not
+      // see: -inf), P = exp2(e) rounded to T, two keys per column, and the
+      // tile's max of e.  The pass is repeated against a new reference max
+      // only where that max lies more than kSlack above the reference (P
+      // would exceed 2^kSlack), or, before the row's first key, more than
+      // kLow below it (P would lose its range).  P goes over S columns
+      // 64-127 once both halves are done: keys 0-63 to 64-95, keys 64-127
+      // to 96-127.
+      uint32_t s[64], ph[32];
+      uint64_t ls[2];
+      float me;
+      auto pass = [&]() {
+        const uint64_t negm = tc::f2(-m_ref, -m_ref);
+        ls[0] = ls[1] = tc::f2(0.f, 0.f);
+        me = -INFINITY;
+#pragma unroll 1
+        for (int h = 1; h >= 0; --h) {
+          tc::ld_32x32b_x32(tS + 64 * h, s);
+          tc::ld_32x32b_x32(tS + 64 * h + 32, s + 32);
+          tc::wait_ld();
+          float ma = -INFINITY, mb = -INFINITY;
+          if (part) {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) lim[e] = lim_abs[e] - j * kTcKeys;  // columns <= lim[e] are keys of row e
-      const bool full = __all_sync(0xffffffffu, min(lim[0], lim[1]) >= kTcKeys - 1) && c2 > 0.f;
-      float mx[2] = {-INFINITY, -INFINITY};
+            for (int i = 0; i < 32; ++i) {
+              const int c = 64 * h + 2 * i;
+              float2 e = tc::f2_split(
+                  tc::ffma2(tc::f2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2x2, negm));
+              e.x = c <= lim ? e.x : -INFINITY;
+              e.y = c + 1 <= lim ? e.y : -INFINITY;
+              softmax_pair<T>(e, i, ma, mb, ls, s);
+            }
+          } else {
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t v[32];
-        tc::ld_16x256b_x8(tsw + ch * 64, v);
-        tc::wait_ld();
-        if (full) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-#pragma unroll
-            for (int e = 0; e < 2; ++e)
-              mx[e] = fmaxf(mx[e], fmaxf(__uint_as_float(v[4 * k + 2 * e]), __uint_as_float(v[4 * k + 2 * e + 1])));
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-#pragma unroll
-            for (int e = 0; e < 2; ++e)
-#pragma unroll
-              for (int bb = 0; bb < 2; ++bb)
-                if (ch * 64 + 8 * k + 2 * c4 + bb <= lim[e])
-                  mx[e] = fmaxf(mx[e], __uint_as_float(v[4 * k + 2 * e + bb]) * c2);
-        }
-      }
-      float m_new[2];
-      bool need = false;
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        if (full) mx[e] *= c2;
-        mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 1));
-        mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 2));
-        m_new[e] = fmaxf(m_ref[e], mx[e]);
-        need = need || m_new[e] > m_ref[e] + kSlack;
-      }
-      // decided per warp, since the tensor-memory loads and stores below are
-      // warp-collective; a row whose max moved less rescales by its own
-      // (exact) factor
-      if (__any_sync(0xffffffffu, need)) {
-        float alpha[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          alpha[e] = fast_exp2(m_ref[e] - m_new[e]);
-          l[e] *= alpha[e];
-          m_ref[e] = m_new[e];
-        }
-        if (j > 0) {  // O holds tiles 0 .. j - 1 (P V of tile j - 1 is done: S_j was issued after it)
-          if (ok && !mbar_wait_bounded(bar_pv, (j - 1) & 1)) ok = false;
-          tc::fence_after();
-#pragma unroll
-          for (int oc = 0; oc < D; oc += 64) {
-            uint32_t w[32];
-            tc::ld_16x256b_x8(tow + oc, w);
-            tc::wait_ld();
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const float2 x = tc::f2_split(tc::fmul2(
-                    tc::f2(__uint_as_float(w[4 * k + 2 * e]), __uint_as_float(w[4 * k + 2 * e + 1])),
-                    tc::f2(alpha[e], alpha[e])));
-                w[4 * k + 2 * e] = __float_as_uint(x.x);
-                w[4 * k + 2 * e + 1] = __float_as_uint(x.y);
-              }
-            tc::st_16x256b_x8(tow + oc, w);
+            for (int i = 0; i < 32; ++i) {
+              const float2 e = tc::f2_split(
+                  tc::ffma2(tc::f2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2x2, negm));
+              softmax_pair<T>(e, i, ma, mb, ls, s);
+            }
           }
-          tc::wait_st();
+          me = max3(me, ma, mb);
+          if (h == 1) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ph[i] = s[i];
+            // the upper half's P and sums are complete before the lower half
+            // is read, so the two halves never hold registers at once
+            pin_regs(ph, ls, me);
+          }
         }
+      };
+      bool rescale = false;
+      float alpha = 1.f;
+#pragma unroll 1
+      for (int attempt = 0; attempt < 2; ++attempt) {
+        pass();
+        if (attempt == 1) break;
+        // me = -inf: no key of the row in the tile
+        const bool need = me > kSlack || (l == 0.f && me != -INFINITY && me < -kLow);
+        rescale = __any_sync(0xffffffffu, need);
+        if (!rescale) break;
+        // a row that does not need it keeps its reference (alpha 1)
+        const float m_new = need ? m_ref + me : m_ref;
+        alpha = fast_exp2(m_ref - m_new);
+        l *= alpha;
+        m_ref = m_new;
+      }
+      tc::st_32x32b_x32(tS + 64, s);
+      tc::st_32x32b_x32(tS + 96, ph);
+      {
+        const float2 a = tc::f2_split(ls[0]), b = tc::f2_split(ls[1]);
+        l += (a.x + a.y) + (b.x + b.y);
       }
       if (j == ntiles - 1 && (nkeys % kTcKeys) != 0) {
         // zero V rows past the last key (tail slots and blocks never loaded)
-        const int st = j % kStages;
-        if (ok && !mbar_wait_bounded(bar_vfull + st, (j / kStages) & 1)) ok = false;
+        const int vs = j % VST;
+        if (ok && !mbar_wait_bounded(bar_vfull + vs, (j / VST) & 1)) ok = false;
         const int first = nkeys - j * kTcKeys;
-        uint8_t* vt = sm + Lay::kOffKV + st * 2 * Lay::kKV + Lay::kKV;
-        for (int i = threadIdx.x; i < kTcKeys * kSlabs * 8; i += kTcSoftWarps * 32) {
+        uint8_t* vt = sm + Lay::kOffV + vs * Lay::kTile;
+#pragma unroll 1
+        for (int i = r; i < kTcKeys * kSlabs * 8; i += 128) {
           const int row = i / (kSlabs * 8), rest = i % (kSlabs * 8);
           if (row >= first)
             *reinterpret_cast<uint4*>(vt + (rest >> 3) * Lay::kSlab + row * 128 + (rest & 7) * 16) =
@@ -571,67 +612,47 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         }
         fence_proxy_async_smem();  // the zeros are read by the tensor cores
       }
-      // P = exp2(S * c2 - m_ref), rounded to T, two keys per column over the
-      // first 64 S columns (chunk 0's S is read before its P lands there, and
-      // chunk 1's S lies in columns 64-127)
-      uint64_t sum2[2] = {tc::f2(0.f, 0.f), tc::f2(0.f, 0.f)};
+      if (rescale && j > 0) {
+        // O holds tiles 0 .. j - 1: P V of tile j - 1 is done (S_j was issued after it)
+        if (ok && !mbar_wait_bounded(bar_pv, (j - 1) & 1)) ok = false;
+        tc::fence_after();
+        const uint64_t a2 = tc::f2(alpha, alpha);
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t v[32];
-        tc::ld_16x256b_x8(tsw + ch * 64, v);
-        tc::wait_ld();
-        uint32_t pk[16];
+        for (int oc = 0; oc < D; oc += 32) {
+          uint32_t w[32];
+          tc::ld_32x32b_x32(tO + oc, w);
+          tc::wait_ld();
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float2 x = tc::f2_split(tc::ffma2(
-                tc::f2(__uint_as_float(v[4 * k + 2 * e]), __uint_as_float(v[4 * k + 2 * e + 1])), c2x2,
-                tc::f2(-m_ref[e], -m_ref[e])));
-            float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-            if (!full) {
-              const int col = ch * 64 + 8 * k + 2 * c4;
-              p0 = col <= lim[e] ? p0 : 0.f;
-              p1 = col + 1 <= lim[e] ? p1 : 0.f;
-            }
-            sum2[e] = tc::fadd2(sum2[e], tc::f2(p0, p1));
-            pk[2 * k + e] = Mma<T>::pack(p0, p1);
+          for (int k = 0; k < 32; k += 2) {
+            const float2 y = tc::f2_split(tc::fmul2(tc::f2(__uint_as_float(w[k]), __uint_as_float(w[k + 1])), a2));
+            w[k] = __float_as_uint(y.x);
+            w[k + 1] = __float_as_uint(y.y);
           }
-        tc::st_16x128b_x8(tsw + ch * 32, pk);
+          tc::st_32x32b_x32(tO + oc, w);
+        }
       }
       tc::wait_st();
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float2 sp = tc::f2_split(sum2[e]);
-        l[e] += sp.x + sp.y;
-      }
       tc::fence_before();
       mbar_arrive(bar_p);
     }
     if (ok && !mbar_wait_bounded(bar_pv, (ntiles - 1) & 1)) ok = false;
     tc::fence_after();
-    float inv[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {  // the row's sum over its quad (all relative to the same max)
-      float lt = l[e];
-      lt += __shfl_xor_sync(0xffffffffu, lt, 1);
-      lt += __shfl_xor_sync(0xffffffffu, lt, 2);
-      inv[e] = lt > 0.f ? __fdiv_rn(1.f, lt) : 0.f;
-    }
-#pragma unroll
-    for (int oc = 0; oc < D; oc += 64) {
+    const float inv = l > 0.f ? __fdiv_rn(1.f, l) : 0.f;
+    T* orow = static_cast<T*>(p.out) + (static_cast<int64_t>(qs + tok0 + tok) * p.num_heads + h0 + hh) * D;
+    const bool store = ok && tok < rows_here;
+#pragma unroll 1
+    for (int oc = 0; oc < D; oc += 32) {
       uint32_t w[32];
-      tc::ld_16x256b_x8(tow + oc, w);
+      tc::ld_32x32b_x32(tO + oc, w);
       tc::wait_ld();
+      uint32_t o[16];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        if (!ok || tok[e] >= rows_here) continue;
-        T* orow = static_cast<T*>(p.out) + (static_cast<int64_t>(qs + tok0 + tok[e]) * p.num_heads + h0 + hh[e]) * D +
-                  oc + 2 * c4;
+      for (int k = 0; k < 16; ++k)
+        o[k] = Mma<T>::pack(__uint_as_float(w[2 * k]) * inv, __uint_as_float(w[2 * k + 1]) * inv);
+      if (store) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          *reinterpret_cast<uint32_t*>(orow + 8 * k) =
-              Mma<T>::pack(__uint_as_float(w[4 * k + 2 * e]) * inv[e], __uint_as_float(w[4 * k + 2 * e + 1]) * inv[e]);
+        for (int k = 0; k < 4; ++k)
+          reinterpret_cast<uint4*>(orow + oc)[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
       }
     }
   }
@@ -714,14 +735,19 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int max_query_len, const C
   if (configured_device != dev) {
     e = cudaFuncSetAttribute(prefill_tc_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    // the largest shared-memory carve-out, so two CTAs fit on an SM
+    // the largest shared-memory carve-out
     e = cudaFuncSetAttribute(prefill_tc_kernel<T, D>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  const int tpt = kTcRows >> p.hg_log2;
-  const dim3 grid((max_query_len + tpt - 1) / tpt, p.num_heads >> p.hg_log2, p.num_seqs);
-  prefill_tc_kernel<T, D><<<grid, kTcThreads, kSmem, st>>>(p, mq, mk, mv);
+  const int rows_per_cta = kTcRows >> p.hg_log2;  // chunk tokens per CTA
+  const int64_t row_tiles = (static_cast<int64_t>(max_query_len) + rows_per_cta - 1) / rows_per_cta;
+  const int64_t ctas = row_tiles * (p.num_heads >> p.hg_log2) * p.num_seqs;
+  if (ctas > INT32_MAX) return cudaErrorInvalidConfiguration;
+  PrefillParams q = p;
+  q.row_tiles = static_cast<int32_t>(row_tiles);
+  const dim3 grid(static_cast<unsigned>(ctas));
+  prefill_tc_kernel<T, D><<<grid, kTcThreads, kSmem, st>>>(q, mq, mk, mv);
   return cudaGetLastError();
 }
 

@@ -13,6 +13,20 @@ from oracle.paged_cache import to_float64
 # the tested lengths with a wide margin.
 TOL = {"f32": 1e-5, "f16": 2e-3, "bf16": 8e-3}
 TORCH = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+# significand bits (with the implicit one) of the 16-bit output types
+_SIG_BITS = {"f16": 11, "bf16": 8}
+_MIN_EXP = {"f16": -14, "bf16": -126}  # smallest normal exponent: below it the ulp stays fixed
+
+
+def rounding_allowance(ref: np.ndarray, dtype: str) -> np.ndarray:
+    """Half an ulp of each exact value in the output dtype: what rounding the
+    exact result to that dtype may cost by itself (0 for f32).  For bf16
+    outputs above 2 this alone reaches the stated 8e-3 bar, so checks whose
+    outputs are that large compare the excess over it with the bar."""
+    if dtype not in _SIG_BITS:
+        return np.zeros_like(ref)
+    e = np.floor(np.log2(np.maximum(np.abs(ref), np.finfo(np.float64).tiny)))
+    return np.exp2(np.maximum(e, _MIN_EXP[dtype]) - _SIG_BITS[dtype])
 SENTINEL = {"f32": 0x7FC00000, "f16": 0x7E00, "bf16": 0x7FC0}
 
 
