@@ -824,10 +824,15 @@ struct SkCfg {
   static constexpr int kWantTokens = sk_want_tokens(D, NG, F8);
   static constexpr int kBlocksPerTile = BS >= kWantTokens ? 1 : kWantTokens / BS;
   static constexpr int kTileTokens = BS * kBlocksPerTile;
-  // fp8 caches: E4M3 code tiles, and per stage the tile's K and V scales
+  // fp8 caches: E4M3 code tiles, and per stage the tile's K and V scales.
+  // A tile of 2 or 4 blocks gets each of its K and V scale rows with one
+  // TMA gather of four table rows (a 2-block tile repeats its last block),
+  // so a scale slot holds 4 blocks' rows; otherwise one bulk copy per block.
   using TL = typename std::conditional<F8, Tile8<D, kTileTokens>, Tile<D, kTileTokens>>::type;
+  static constexpr bool kGatherScales = F8 && (kBlocksPerTile == 2 || kBlocksPerTile == 4);
+  static constexpr int kScaleSlot = kGatherScales ? 4 * BS : kTileTokens;  // floats per (stage, K or V)
   static constexpr int kStages = NST * TL::kStageBytes;
-  static constexpr int kScales = F8 ? NST * 2 * kTileTokens * 4 : 0;
+  static constexpr int kScales = F8 ? NST * 2 * kScaleSlot * 4 : 0;
   static constexpr int kMerge = 2 * MergeArea<D, NG>::kBytes;  // double-buffered per segment
   static constexpr int kPartRows = kMaxSkCtas + 8;  // row index per part of a combined unit
   static constexpr int kFixed = 1024 + kStages + kScales + kMerge + 2 * NST * 8 + 16 + kPartRows * 4;
@@ -843,23 +848,27 @@ __device__ __forceinline__ int sk_cta_of(int64_t t, int64_t W, int P) {
 template <typename T, int D, int BS, int NG, int NST, bool F8 = false>
 __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)  // two CTAs per SM where shared memory allows
 decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
-                 const __grid_constant__ CUtensorMap tmV) {
+                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmKS,
+                 const __grid_constant__ CUtensorMap tmVS) {
   using C = SkCfg<T, D, BS, NG, NST, F8>;
   using TL = typename C::TL;
   constexpr int TPB = C::kBlocksPerTile, TT = C::kTileTokens;
   // TMA copies per block of a tile: 16-bit caches one each for K and V (a
   // 4-D box covers all of a block's 64-column slabs); fp8 caches K and V
-  // slabs and the K and V scales
-  constexpr int kPerBlock = F8 ? 2 * TL::kSub + 2 : 2;
-  constexpr int kCopies = kPerBlock * TPB;
+  // slabs, and the K and V scales unless two gathers per tile bring them
+  constexpr bool kGather = C::kGatherScales;
+  constexpr int kPerBlock = F8 ? 2 * TL::kSub + (kGather ? 0 : 2) : 2;
+  constexpr int kCopies = kPerBlock * TPB + (kGather ? 2 : 0);
   static_assert(kCopies <= 32, "one copy per producer lane");
-  // bytes one block of a tile brings into its stage
-  constexpr int kBlockTx = F8 ? 2 * BS * D + 2 * BS * 4 : TL::kStageBytes / TPB;
+  // bytes one block of a tile brings into its stage (scales by gather: per tile)
+  constexpr int kBlockTx = F8 ? 2 * BS * D + (kGather ? 0 : 2 * BS * 4) : TL::kStageBytes / TPB;
+  constexpr int kTileTx = kGather ? 2 * 4 * BS * 4 : 0;
+  constexpr int kScaleSlot = C::kScaleSlot;
   constexpr int GP = 8 * NG;
   static_assert(NST % kConsumers == 0, "stage s must always be drained by consumer s % kConsumers");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* scales = reinterpret_cast<float*>(smem + C::kStages);  // fp8: [NST][2][TT] K, V scales
+  float* scales = reinterpret_cast<float*>(smem + C::kStages);  // fp8: [NST][2][kScaleSlot] K, V scales
   float* merge_base = reinterpret_cast<float*>(smem + C::kStages + C::kScales);
   constexpr int kMergeFloats = MergeArea<D, NG>::kBytes / 4;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages + C::kScales + C::kMerge);
@@ -1026,6 +1035,10 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     if (lane == 0) {
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
+      if constexpr (kGather) {
+        prefetch_tensormap(&tmKS);
+        prefetch_tensormap(&tmVS);
+      }
     }
     Cursor c = c_first;  // c.blk counts tiles of TPB blocks
     // Block-table entries are fetched 32 at a time (one per lane; entries
@@ -1077,17 +1090,33 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       const int cr = lane / kPerBlock, cw8 = lane % kPerBlock, csl = (cw8 >> 1) % TL::kSub;
       int pb = __shfl_sync(0xffffffffu, mine, (blk + min(cr, TPB - 1)) & 31);
       const int here = min(TPB, cache_nblk - blk);  // blocks of this tile inside the sequence (>= 1)
+      // scale gathers: the table rows (block, kv head) of the tile's blocks,
+      // blocks past the sequence's end repeating its last one
+      int srow[4] = {0, 0, 0, 0};
+      if constexpr (kGather) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          int b4 = __shfl_sync(0xffffffffu, mine, (blk + min(r, here - 1)) & 31);
+          if (b4 < 0 || b4 >= p.num_blocks) b4 = 0;  // recorded by the code copy of that block
+          srow[r] = b4 * Hkv + c.kvh;
+        }
+      }
       const int s = j % NST;
       if (lane == 0) {
         if (j >= NST) ok = mbar_wait_for(&empty[s], ((j / NST) - 1) & 1, p.wait_limit_ns);
-        if (ok) mbar_arrive_expect_tx(&full[s], here * kBlockTx);
+        if (ok) mbar_arrive_expect_tx(&full[s], here * kBlockTx + kTileTx);
       }
       __syncwarp();
       ok = __shfl_sync(0xffffffffu, ok, 0);
       // test control: CTA 0 never loads its tile test_skip_tile, so the wait
       // for it runs out (the timeout path, exercised without a fault)
       const bool skip = p.test_skip_tile >= 0 && pid == 0 && j == p.test_skip_tile;
-      if (ok && !skip && lane < kCopies && cr < here) {
+      const bool gather_lane = kGather && lane >= kPerBlock * TPB && lane < kCopies;
+      if (ok && !skip && gather_lane) {
+        const int which = lane - kPerBlock * TPB;  // 0: K scales, 1: V scales
+        tma_gather4(scales + (s * 2 + which) * kScaleSlot, which ? &tmVS : &tmKS, &full[s], 0, srow[0], srow[1],
+                    srow[2], srow[3]);
+      } else if (ok && !skip && lane < kPerBlock * TPB && cr < here) {
         if (pb < 0 || pb >= p.num_blocks) {
           record_error(KV_ERR_DEVICE_BOUNDS);
           pb = 0;
@@ -1100,7 +1129,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           tma_load_3d(dst, (cw8 & 1) ? &tmV : &tmK, &full[s], csl * 128, c.kvh, pb * BS);
         } else {
           const int which = cw8 - 2 * TL::kSub;  // 0: K scales, 1: V scales
-          float* dst = scales + (s * 2 + which) * TT + cr * BS;
+          float* dst = scales + (s * 2 + which) * kScaleSlot + cr * BS;
           const float* src = (which ? p.v_scales : p.k_scales) + (static_cast<int64_t>(pb) * Hkv + c.kvh) * BS;
           bulk_load(dst, src, BS * 4, &full[s]);
         }
@@ -1281,16 +1310,16 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
             *reinterpret_cast<uint32_t*>(kt + swz8<TT>(tl, lane * 4)) = ck;
             *reinterpret_cast<uint32_t*>(kt + TL::kTileBytes + swz8<TT>(tl, lane * 4)) = cv;
             if (lane == 0) {
-              scales[s * 2 * TT + tl] = sk;
-              scales[(s * 2 + 1) * TT + tl] = sv;
+              scales[s * 2 * kScaleSlot + tl] = sk;
+              scales[(s * 2 + 1) * kScaleSlot + tl] = sv;
             }
             fence_proxy_async_smem();  // the stage and its scales are written by the async proxy again later
             __syncwarp();
           }
         }
         if constexpr (F8)
-          consume_tile_f8<D, TT, NG>(st, kt, kt + TL::kTileBytes, scales + s * 2 * TT, scales + (s * 2 + 1) * TT,
-                                     c.blk * TT, L, sl2, lane);
+          consume_tile_f8<D, TT, NG>(st, kt, kt + TL::kTileBytes, scales + s * 2 * kScaleSlot,
+                                     scales + (s * 2 + 1) * kScaleSlot, c.blk * TT, L, sl2, lane);
         else
           consume_tile<T, D, TT, NG, BS>(st, kt, kt + TL::kTileBytes, c.blk * TT, L, sl2, lane);
         __syncwarp();
@@ -1941,7 +1970,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Kinds of tensor map: 16-bit cache slabs and fp8 (E4M3) cache slabs.
-enum MapKind { kMap16 = 0, kMapFp8 = 1, kMap16Blocks = 2 };
+enum MapKind { kMap16 = 0, kMapFp8 = 1, kMap16Blocks = 2, kMapScales = 3 };
 
 struct MapKey {
   const void* ptr;
@@ -1975,7 +2004,17 @@ bool get_tensor_map(const void* cache, int64_t rows, int hkv, int d, int bs, CUt
   if (!fn) return false;
   CUtensorMap m;
   CUresult r;
-  if (kind == kMap16Blocks) {
+  if (kind == kMapScales) {
+    // fp8 scales [NB, Hkv, BS] floats as `rows` rows of bs: a box of one row
+    // (the tile gathers four rows per copy)
+    cuuint32_t estr[2] = {1, 1};
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(bs), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(bs) * 4};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(bs), 1};
+    r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(cache), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else if (kind == kMap16Blocks) {
     cuuint32_t estr[4] = {1, 1, 1, 1};
     cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(d / 64),
                           static_cast<cuuint64_t>(hkv)};
@@ -2032,7 +2071,8 @@ struct Stages8 {
 };
 
 template <typename T, int D, int BS, int NG, bool F8 = false>
-cudaError_t launch_sk(DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, int max_ctas, cudaStream_t st) {
+cudaError_t launch_sk(DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, int max_ctas, cudaStream_t st,
+                      const CUtensorMap* mks = nullptr, const CUtensorMap* mvs = nullptr) {
   constexpr int kWant = sk_want_tokens(D, NG, F8);
   constexpr int kTileTokens = BS >= kWant ? BS : kWant;  // matches SkCfg::kTileTokens
   constexpr int NST =
@@ -2072,7 +2112,8 @@ cudaError_t launch_sk(DecodeParams& p, const CUtensorMap& mk, const CUtensorMap&
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p, mk, mv);
+  // the scale maps are read only by fp8 tiles that gather their scales
+  return cudaLaunchKernelEx(&cfg, kern, p, mk, mv, mks ? *mks : mk, mvs ? *mvs : mv);
 }
 
 template <typename T, int D, int BS, int NG>
@@ -2348,10 +2389,10 @@ template <typename T>
 cudaError_t launch_fp8_decode(DecodeParams& p, const Plan& pl, const CUtensorMap* maps, cudaStream_t st) {
   const bool ng1 = p.group <= 8;
   if (p.block_size == 16)
-    return ng1 ? launch_sk<T, 128, 16, 1, true>(p, maps[0], maps[1], pl.num_ctas, st)
-               : launch_sk<T, 128, 16, 2, true>(p, maps[0], maps[1], pl.num_ctas, st);
-  return ng1 ? launch_sk<T, 128, 32, 1, true>(p, maps[0], maps[1], pl.num_ctas, st)
-             : launch_sk<T, 128, 32, 2, true>(p, maps[0], maps[1], pl.num_ctas, st);
+    return ng1 ? launch_sk<T, 128, 16, 1, true>(p, maps[0], maps[1], pl.num_ctas, st, &maps[2], &maps[3])
+               : launch_sk<T, 128, 16, 2, true>(p, maps[0], maps[1], pl.num_ctas, st, &maps[2], &maps[3]);
+  return ng1 ? launch_sk<T, 128, 32, 1, true>(p, maps[0], maps[1], pl.num_ctas, st, &maps[2], &maps[3])
+             : launch_sk<T, 128, 32, 2, true>(p, maps[0], maps[1], pl.num_ctas, st, &maps[2], &maps[3]);
 }
 }  // namespace
 
@@ -2434,8 +2475,11 @@ int decode_fp8_impl(void* out, const void* q, const void* k_cache, const void* v
     }
   }
   const int64_t slots = num_blocks * block_size;
-  CUtensorMap maps[2];
-  if (!get_tensor_map(k_cache, slots, num_kv_heads, head_dim, block_size, &maps[0], kMapFp8) ||
+  CUtensorMap maps[4];
+  const int64_t scale_rows = num_blocks * num_kv_heads;
+  if (!get_tensor_map(k_scales, scale_rows, 1, 1, block_size, &maps[2], kMapScales) ||
+      !get_tensor_map(v_scales, scale_rows, 1, 1, block_size, &maps[3], kMapScales) ||
+      !get_tensor_map(k_cache, slots, num_kv_heads, head_dim, block_size, &maps[0], kMapFp8) ||
       !get_tensor_map(v_cache, slots, num_kv_heads, head_dim, block_size, &maps[1], kMapFp8))
     return cuda_status(cudaErrorInvalidValue, "cuTensorMapEncodeTiled failed");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
