@@ -647,6 +647,11 @@ __device__ __forceinline__ void consume_tile_f8(WarpState<D, NG>& st, uint8_t* k
 
 constexpr int kConsumers = 4;
 constexpr int kTcThreads = 32 * (kConsumers + 1);
+// Stream-K kernel: the producer warp, the consumer warps, and a writer warp
+// that does the fused step's cache write while the others stream tiles (the
+// writes belong to no tile of the launch, so their order does not matter)
+constexpr int kSkWriterWarp = kConsumers + 1;
+constexpr int kSkThreads = 32 * (kConsumers + 2);
 
 template <int D, int NG>
 struct MergeArea {
@@ -694,6 +699,13 @@ __device__ __forceinline__ void warp_merge(const float* Os, const float* Ms, con
 // and its own piece from the warp-merge buffer.  Every CTA first rebuilds
 // the per-sequence prefixes of tile counts and costs in shared memory from
 // seq_lens.
+//
+// Warps: a producer (TMA), four consumers (tile j goes to consumer j % 4),
+// and a writer that does a fused step's cache write while the others stream
+// tiles.  At the end of a unit's segment each consumer stores its softmax
+// state into one of two merge buffers and counts itself in; the last of the
+// four merges the segment (output or partial) while the others go on with
+// their next tiles, then frees the buffer for the segment two later.
 // =========================================================================
 
 // Fused step, cache write ("MiniPaged-Qwen" §12): warp gw of nw copies the
@@ -835,7 +847,7 @@ struct SkCfg {
   static constexpr int kScales = F8 ? NST * 2 * kScaleSlot * 4 : 0;
   static constexpr int kMerge = 2 * MergeArea<D, NG>::kBytes;  // double-buffered per segment
   static constexpr int kPartRows = kMaxSkCtas + 8;  // row index per part of a combined unit
-  static constexpr int kFixed = 1024 + kStages + kScales + kMerge + 2 * NST * 8 + 16 + kPartRows * 4;
+  static constexpr int kFixed = 1024 + kStages + kScales + kMerge + 2 * NST * 8 + 16 + 32 + kPartRows * 4;
   static int smem_bytes(int B) { return kFixed + (2 * (B + 1) * 4 + 15) / 16 * 16; }
 };
 
@@ -846,7 +858,7 @@ __device__ __forceinline__ int sk_cta_of(int64_t t, int64_t W, int P) {
 
 
 template <typename T, int D, int BS, int NG, int NST, bool F8 = false>
-__global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)  // two CTAs per SM where shared memory allows
+__global__ void __launch_bounds__(kSkThreads, D <= 128 ? 2 : 1)  // two CTAs per SM where shared memory allows
 decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmKS,
                  const __grid_constant__ CUtensorMap tmVS) {
@@ -874,7 +886,9 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages + C::kScales + C::kMerge);
   uint64_t* empty = full + NST;
   uint64_t* pre_bar = empty + NST;                       // owner: later pieces copied in
-  int* part_row = reinterpret_cast<int*>(pre_bar + 2);  // [kPartRows]
+  uint64_t* seg_free = pre_bar + 2;                      // [2] merge buffer read by its merge
+  int* seg_cnt = reinterpret_cast<int*>(seg_free + 2);   // [2] warps that stored into the buffer
+  int* part_row = seg_cnt + 4;                           // [kPartRows]
   int* CB = part_row + C::kPartRows;  // CB[b] = sum_{b' < b} ceil(L_b' / TT) (tiles)
 
   const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
@@ -883,7 +897,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
 
   // ---- prefixes of block counts and costs over the batch (block-wide scans) ----
   {
-    const int per = (B + kTcThreads - 1) / kTcThreads;
+    const int per = (B + kSkThreads - 1) / kSkThreads;
     const int beg = min(B, tid * per), end = min(B, beg + per);
     int local = 0, local_c = 0;
     for (int i = beg; i < end; ++i) {
@@ -902,7 +916,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
         incl_c += yc;
       }
     }
-    __shared__ int warp_tot[kConsumers + 1], warp_tot_c[kConsumers + 1];
+    __shared__ int warp_tot[kConsumers + 2], warp_tot_c[kConsumers + 2];
     if (lane == 31) {
       warp_tot[warp] = incl;
       warp_tot_c[warp] = incl_c;
@@ -928,6 +942,9 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
         mbar_init(&empty[s], 1);
       }
       mbar_init(pre_bar, 1);
+      mbar_init(&seg_free[0], 1);
+      mbar_init(&seg_free[1], 1);
+      seg_cnt[0] = seg_cnt[1] = 0;
       fence_mbar_init();
     }
     __syncthreads();
@@ -936,7 +953,7 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   for (int bz = blockIdx.x; bz < B; bz += gridDim.x)
     if (CB[bz + 1] == CB[bz]) {
       T* o = static_cast<T*>(p.out) + static_cast<int64_t>(bz) * p.num_heads * D;
-      for (int i = tid; i < p.num_heads * D; i += kTcThreads) o[i] = DType<T>::from_float(0.f);
+      for (int i = tid; i < p.num_heads * D; i += kSkThreads) o[i] = DType<T>::from_float(0.f);
     }
 
   // CTA ranges are drawn in cost space, where unit (b, kvh) occupies
@@ -961,14 +978,16 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   };
   const int64_t t0 = tiles_before(static_cast<int64_t>(pid) * Wc / P);
   const int64_t t1 = tiles_before(static_cast<int64_t>(pid + 1) * Wc / P);
-  if (t0 >= t1) {
-    if (p.new_k != nullptr && warp != 0) {
-      const int64_t gw = static_cast<int64_t>(pid) * kConsumers + warp - 1, nw = static_cast<int64_t>(P) * kConsumers;
-      if constexpr (F8) scatter_new_rows_f8<T>(p, gw, nw, lane);
-      else scatter_new_rows<T>(p, gw, nw, lane);
+  // Fused step: the writer warps of all CTAs copy the step's new rows into
+  // the caches, CTA p's warp rows p, p + P, ... (a CTA with no tiles as well)
+  if (warp == kSkWriterWarp) {
+    if (p.new_k != nullptr) {
+      if constexpr (F8) scatter_new_rows_f8<T>(p, pid, P, lane);
+      else scatter_new_rows<T>(p, pid, P, lane);
     }
     return;
   }
+  if (t0 >= t1) return;
   const int n = static_cast<int>(t1 - t0);
 
   // Tile cursor shared by producer and consumers: advances (blk, kvh, b).
@@ -1219,16 +1238,10 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   if constexpr (F8) load_q_frags_f8<T, D, NG>(st.qf, q_of(c), G, lane);
   else load_q<T, D, NG>(st, q_of(c), G, lane);
   prefetch_next(c, unit_start);
-  // Fused step: the consumer warps write the step's new rows into the
-  // caches while the first tiles are in flight.  No tile of this launch
-  // uses what they write: position L - 1 of a decode sequence (the only
-  // written slot attention reads) is taken from the new row itself below.
+  // Fused step: no tile of this launch uses what the writer warps write:
+  // position L - 1 of a decode sequence (the only written slot attention
+  // reads) is taken from the new row itself below.
   const bool fused = p.new_k != nullptr;
-  if (fused) {
-    const int64_t gw = static_cast<int64_t>(pid) * kConsumers + cw, nw = static_cast<int64_t>(P) * kConsumers;
-    if constexpr (F8) scatter_new_rows_f8<T>(p, gw, nw, lane);
-    else scatter_new_rows<T>(p, gw, nw, lane);
-  }
   // row of the step's new K/V holding sequence b's position L - 1 (-1: none)
   auto new_row_of = [&](int b) -> int {
     if (!fused) return -1;
@@ -1331,62 +1344,79 @@ decode_sk_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       const int64_t unit_end = unit_start + c.nb;
       const bool whole = unit_start >= t0 && unit_end <= t1;
       const int slot = unit_start < t0 ? 0 : 1;
-      // Two merge buffers alternate between segments: the one barrier below
-      // also guarantees that every thread has finished reading the buffer
-      // of the segment before, which the next segment will overwrite.
-      float* Os = merge_base + (seg & 1) * kMergeFloats;
+      // the owner's own piece stays in the merge buffer for its combine
+      const bool keep = kPrefetchParts && j == n - 1 && !whole && slot == 1;
+      // Two merge buffers alternate between segments.  Each warp stores its
+      // state and counts itself in; the last of the four merges the segment
+      // while the others go on to their next tiles, then frees the buffer,
+      // which the segment two later waits for before storing into it.
+      const int mb = seg & 1;
+      float* Os = merge_base + mb * kMergeFloats;
       float* Ms = Os + kConsumers * merge_row<D>() * GP;
       float* Ls = Ms + kConsumers * GP;
+      if (seg >= 2) {
+        int w = 1;
+        if (lane == 0) w = mbar_wait_for(&seg_free[mb], ((seg >> 1) - 1) & 1, p.wait_limit_ns);
+        if (!__shfl_sync(0xffffffffu, w, 0)) ok = 0;
+      }
       ++seg;
       if constexpr (F8) store_state_f8(st, Os, Ms, Ls, cw, lane);
       else store_state(st, Os, Ms, Ls, cw, lane);
-      named_barrier_sync(1, kConsumers * 32);
-      // the owner's own piece stays in the merge buffer for its combine
-      const bool keep = kPrefetchParts && j == n - 1 && !whole && slot == 1;
-      // each thread merges four adjacent outputs of one head (float4 reads)
-      constexpr int kD4 = D / 4, DP = merge_row<D>();
-      for (int v = keep ? G * kD4 : ctid; v < G * kD4; v += kConsumers * 32) {
-        const int g = v / kD4, d = (v - g * kD4) * 4;
-        float mx = -INFINITY;
-#pragma unroll
-        for (int w2 = 0; w2 < kConsumers; ++w2) mx = fmaxf(mx, Ms[w2 * GP + g]);
-        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-        float den = 0.f;
-        if (mx != -INFINITY) {
-#pragma unroll
-          for (int w2 = 0; w2 < kConsumers; ++w2) {
-            const float mw = Ms[w2 * GP + g];
-            if (mw == -INFINITY) continue;
-            const float sc = fast_exp2(mw - mx);
-            const float4 o4 = *reinterpret_cast<const float4*>(Os + (w2 * GP + g) * DP + d);
-            num.x += sc * o4.x;
-            num.y += sc * o4.y;
-            num.z += sc * o4.z;
-            num.w += sc * o4.w;
-            den += sc * Ls[w2 * GP + g];
-          }
-        }
-        if (whole) {
-          const float inv = den > 0.f ? 1.f / den : 0.f;
-          T* o = static_cast<T*>(p.out) + (static_cast<int64_t>(c.b) * p.num_heads + c.kvh * G + g) * D + d;
-          o[0] = DType<T>::from_float(num.x * inv);
-          o[1] = DType<T>::from_float(num.y * inv);
-          o[2] = DType<T>::from_float(num.z * inv);
-          o[3] = DType<T>::from_float(num.w * inv);
-        } else {
-          const int64_t r = (static_cast<int64_t>(pid) * 2 + slot) * G + g;
-          *reinterpret_cast<float4*>(p.ws_o + r * D + d) = num;
-          if (d == 0) {
-            p.ws_ml[r * 2 + 0] = mx;
-            p.ws_ml[r * 2 + 1] = den;
-          }
-        }
+      __syncwarp();
+      int arrived = 0;
+      if (lane == 0) {
+        __threadfence_block();  // this warp's state before its count
+        arrived = atomicAdd(&seg_cnt[mb], 1);
+        if (arrived == kConsumers - 1) seg_cnt[mb] = 0;
+        __threadfence_block();  // the other warps' states after their counts
       }
-      if (!whole && slot == 0) {
-        // publish the partial of a unit that started in an earlier CTA: all
-        // consumer threads' stores precede the release of the flag
-        named_barrier_sync(1, kConsumers * 32);
-        if (ctid == 0) st_release_gpu(p.ws_flags + pid, p.epoch);
+      arrived = __shfl_sync(0xffffffffu, arrived, 0);
+      if (arrived == kConsumers - 1 && !keep) {
+        __syncwarp();  // lane 0's acquire, before every lane's reads
+        // each lane merges four adjacent outputs of one head at a time (float4 reads)
+        constexpr int kD4 = D / 4, DP = merge_row<D>();
+        for (int v = lane; v < G * kD4; v += 32) {
+          const int g = v / kD4, d = (v - g * kD4) * 4;
+          float mx = -INFINITY;
+#pragma unroll
+          for (int w2 = 0; w2 < kConsumers; ++w2) mx = fmaxf(mx, Ms[w2 * GP + g]);
+          float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+          float den = 0.f;
+          if (mx != -INFINITY) {
+#pragma unroll
+            for (int w2 = 0; w2 < kConsumers; ++w2) {
+              const float mw = Ms[w2 * GP + g];
+              if (mw == -INFINITY) continue;
+              const float sc = fast_exp2(mw - mx);
+              const float4 o4 = *reinterpret_cast<const float4*>(Os + (w2 * GP + g) * DP + d);
+              num.x += sc * o4.x;
+              num.y += sc * o4.y;
+              num.z += sc * o4.z;
+              num.w += sc * o4.w;
+              den += sc * Ls[w2 * GP + g];
+            }
+          }
+          if (whole) {
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            T* o = static_cast<T*>(p.out) + (static_cast<int64_t>(c.b) * p.num_heads + c.kvh * G + g) * D + d;
+            o[0] = DType<T>::from_float(num.x * inv);
+            o[1] = DType<T>::from_float(num.y * inv);
+            o[2] = DType<T>::from_float(num.z * inv);
+            o[3] = DType<T>::from_float(num.w * inv);
+          } else {
+            const int64_t r = (static_cast<int64_t>(pid) * 2 + slot) * G + g;
+            *reinterpret_cast<float4*>(p.ws_o + r * D + d) = num;
+            if (d == 0) {
+              p.ws_ml[r * 2 + 0] = mx;
+              p.ws_ml[r * 2 + 1] = den;
+            }
+          }
+        }
+        __syncwarp();
+        // publish the partial of a unit that started in an earlier CTA: the
+        // warp's stores precede the release of the flag
+        if (!whole && slot == 0 && lane == 0) st_release_gpu(p.ws_flags + pid, p.epoch);
+        if (lane == 0) mbar_arrive(&seg_free[mb]);
       }
       if (j + 1 < n) {
         advance(c);
@@ -2089,7 +2119,7 @@ cudaError_t launch_sk(DecodeParams& p, const CUtensorMap& mk, const CUtensorMap&
   if (dev < 0 || dev >= 64) dev = 0;
   if (occ_cache[dev][0] != smem) {
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kTcThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kSkThreads, smem);
     if (e != cudaSuccess) return e;
     occ_cache[dev][0] = smem;
     occ_cache[dev][1] = std::max(1, std::min(occ, kMaxSkCtasPerSm));
@@ -2104,7 +2134,7 @@ cudaError_t launch_sk(DecodeParams& p, const CUtensorMap& mk, const CUtensorMap&
   // resident at once, which the owners' waits on later CTAs rely on.
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(ctas));
-  cfg.blockDim = dim3(kTcThreads);
+  cfg.blockDim = dim3(kSkThreads);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -2456,12 +2486,13 @@ int decode_fp8_impl(void* out, const void* q, const void* k_cache, const void* v
   if (step != nullptr && step->num_tokens > 0) {
     const uintptr_t row_align = reinterpret_cast<uintptr_t>(step->k) | reinterpret_cast<uintptr_t>(step->v) |
                                 static_cast<uintptr_t>(step->k_stride * 2) | static_cast<uintptr_t>(step->v_stride * 2);
-    // One launch when the rows are 8-byte aligned and few: the consumer
-    // warps quantise the rows before their first tile, so a step with many
-    // rows (a prefill chunk: more than two per consumer warp of the grid)
-    // runs the write as its own launch, on SMs the attention does not hold up.
-    const int64_t consumer_warps = static_cast<int64_t>(sm_count()) * 2 * kConsumers;  // two CTAs per SM
-    const bool few_rows = step->num_tokens <= 2 * consumer_warps;
+    // One launch when the rows are 8-byte aligned and few: the writer warps
+    // (one per CTA) quantise the rows while the consumers stream tiles.  A
+    // step with many rows (a prefill chunk: more than 8 per writer warp)
+    // runs the write as its own launch, as one writer warp per CTA would
+    // outlast the attention (mixed batch: 183 us fused against 128 us).
+    const int64_t writer_warps = static_cast<int64_t>(sm_count()) * 2;  // two CTAs per SM
+    const bool few_rows = step->num_tokens <= 8 * writer_warps;
     if (row_align % 8 == 0 && few_rows) {  // one launch: the kernel also quantises and writes the new rows
       p.new_k = step->k;
       p.new_v = step->v;
