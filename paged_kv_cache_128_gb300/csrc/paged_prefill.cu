@@ -403,7 +403,36 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const int nkeys = min(ctx + tok0 + rows_here, L);
   const int ntiles = (nkeys + kTcKeys - 1) / kTcKeys;
 
-  if (threadIdx.x == 0) {
+  const int32_t* table = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
+  const int bs = p.block_size;
+  // K (V) of tile j into stage j % KST (j % VST) once S (P V) of the tile
+  // that stage held before is done (TMA thread only).
+  auto load = [&](int j, bool is_v) -> bool {
+    const int nst = is_v ? VST : KST, st = j % nst;
+    uint64_t* full = (is_v ? bar_vfull : bar_kfull) + st;
+    if (j >= nst && !mbar_wait_bounded((is_v ? bar_vempty : bar_kempty) + st, ((j / nst) - 1) & 1)) return false;
+    const int k0 = j * kTcKeys, k1 = min(k0 + kTcKeys, nkeys);
+    const int blk0 = k0 / bs, blk1 = (k1 + bs - 1) / bs;
+    mbar_arrive_expect_tx(full, static_cast<uint32_t>((blk1 - blk0) * bs * D * 2));
+    uint8_t* dst = sm + (is_v ? Lay::kOffV : Lay::kOffK) + st * Lay::kTile;
+    const CUtensorMap* map = is_v ? &tmV : &tmK;
+    for (int bi = blk0; bi < blk1; ++bi) {
+      int pb = __ldg(table + bi);
+      if (pb < 0 || pb >= p.num_blocks) {
+        record_error(KV_ERR_DEVICE_BOUNDS);
+        pb = 0;
+      }
+      const int r = (bi - blk0) * bs;
+      for (int s = 0; s < kSlabs; ++s) tma_load_3d(dst + s * Lay::kSlab + r * 128, map, full, s * 64, kvh, pb * bs);
+    }
+    return true;
+  };
+  // The TMA thread sets up the barriers and issues Q and the first K tile
+  // before the CTA-wide barrier, so those loads overlap the tensor-memory
+  // allocation and the barrier itself.
+  const bool tma_thread = warp == kTcTmaWarp && lane == 0;
+  bool load_ok = true;
+  if (tma_thread) {
     mbar_init(bar_q, 1);
     for (int s = 0; s < KST; ++s) {
       mbar_init(bar_kfull + s, 1);
@@ -417,6 +446,13 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     mbar_init(bar_p, kTcSoftWarps * 32);
     mbar_init(bar_pv, 1);
     fence_mbar_init();
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+    mbar_arrive_expect_tx(bar_q, kSlabs * kTcRows * 128);
+    for (int s = 0; s < kSlabs; ++s)
+      tma_load_3d(sm + Lay::kOffQ + s * Lay::kSlab, &tmQ, bar_q, s * 64, h0, qs + tok0);
+    load_ok = load(0, false);
   }
   if (warp == kTcMmaWarp) tc::alloc(tmem_slot, kTcCols);
   tc::fence_before();
@@ -426,39 +462,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
   if (warp == kTcTmaWarp) {
     if (lane == 0) {
-      // ---- TMA producer
-      prefetch_tensormap(&tmQ);
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
-      mbar_arrive_expect_tx(bar_q, kSlabs * kTcRows * 128);
-      for (int s = 0; s < kSlabs; ++s)
-        tma_load_3d(sm + Lay::kOffQ + s * Lay::kSlab, &tmQ, bar_q, s * 64, h0, qs + tok0);
-      const int32_t* table = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
-      const int bs = p.block_size;
-      // K (V) of tile j into stage j % KST (j % VST) once S (P V) of the tile
-      // that stage held before is done.  K runs one tile ahead of V.
-      auto load = [&](int j, bool is_v) -> bool {
-        const int nst = is_v ? VST : KST, st = j % nst;
-        uint64_t* full = (is_v ? bar_vfull : bar_kfull) + st;
-        if (j >= nst && !mbar_wait_bounded((is_v ? bar_vempty : bar_kempty) + st, ((j / nst) - 1) & 1))
-          return false;
-        const int k0 = j * kTcKeys, k1 = min(k0 + kTcKeys, nkeys);
-        const int blk0 = k0 / bs, blk1 = (k1 + bs - 1) / bs;
-        mbar_arrive_expect_tx(full, static_cast<uint32_t>((blk1 - blk0) * bs * D * 2));
-        uint8_t* dst = sm + (is_v ? Lay::kOffV : Lay::kOffK) + st * Lay::kTile;
-        const CUtensorMap* map = is_v ? &tmV : &tmK;
-        for (int bi = blk0; bi < blk1; ++bi) {
-          int pb = __ldg(table + bi);
-          if (pb < 0 || pb >= p.num_blocks) {
-            record_error(KV_ERR_DEVICE_BOUNDS);
-            pb = 0;
-          }
-          const int r = (bi - blk0) * bs;
-          for (int s = 0; s < kSlabs; ++s) tma_load_3d(dst + s * Lay::kSlab + r * 128, map, full, s * 64, kvh, pb * bs);
-        }
-        return true;
-      };
-      bool ok = load(0, false);
+      // ---- TMA producer (Q and the first K tile are already issued)
+      bool ok = load_ok;
       for (int j = 0; j < ntiles && ok; ++j) {
         ok = load(j, true);
         if (ok && j + 1 < ntiles) ok = load(j + 1, false);
