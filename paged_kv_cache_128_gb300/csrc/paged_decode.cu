@@ -1845,10 +1845,13 @@ struct Plan {
 constexpr int kMaxSkCtasPerSm = 4;
 
 // Tiles' worth of time one unit boundary costs a stream-K CTA (cross-warp
-// merge, output or partial write): about 48 KB of streaming, at most 4
-// tiles, measured on GB300 (charges of 0-6 tiles swept on the 32-token
-// tiles of head_dim 64 and 128; 3-4 within 1 % of the best everywhere).
-int seg_cost_tiles(int stage_bytes) { return std::max(1, std::min(4, 49152 / stage_bytes)); }
+// merge, output or partial write), at most 4 tiles, measured on GB300:
+// about 32 KB of streaming for 16-bit tiles (2 tiles at head_dim 128, 4 at
+// head_dim 64) and 48 KB for fp8 tiles, whose consumers take longer per
+// tile (charges of 0-6 tiles swept).
+int seg_cost_tiles(int stage_bytes, bool fp8) {
+  return std::max(1, std::min(4, (fp8 ? 49152 : 32768) / stage_bytes));
+}
 
 // Tag of one stream-K call: a per-process random base plus a call counter,
 // so a ready flag left by any other call (or uninitialised workspace) does
@@ -2127,7 +2130,7 @@ cudaError_t launch_sk(DecodeParams& p, const CUtensorMap& mk, const CUtensorMap&
   const int ctas = std::min({max_ctas, sm_count() * occ_cache[dev][1], kMaxSkCtas});
   p.num_ctas = ctas;
   p.epoch = next_epoch();
-  p.seg_cost = seg_cost_tiles(C::TL::kStageBytes);
+  p.seg_cost = seg_cost_tiles(C::TL::kStageBytes, F8);
   p.wait_limit_ns = static_cast<uint64_t>(sk_controls().wait_limit_ns.load());
   p.test_skip_tile = static_cast<int32_t>(sk_controls().skip_tile.load());
   // Cooperative: the driver refuses the launch unless all CTAs can be
