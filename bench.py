@@ -77,6 +77,10 @@ def parse_args():
                     help="time a multi-layer decode step instead: the workload's decode batch over this many "
                          "layers' caches under one block table, through the native runner (metadata once per step, "
                          "one fused launch per layer); decode-only workloads")
+    ap.add_argument("--cache-write", action="store_true",
+                    help="time the cache write alone instead (paged_reshape_and_cache, or the quantised "
+                         "paged_reshape_and_cache_fp8 with --kv-cache fp8) on the workload's first step: its new "
+                         "K/V rows scattered to their slots, L2 flushed before each call")
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="only set the workload up and run this many attention calls (L2 flushed before each); "
                          "the small case used under ncu")
@@ -94,11 +98,36 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text):
+    """C++/CUDA source without comments and blank lines: a comment edit
+    leaves the compiled kernel, and so this hash, unchanged."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # string or character literal, escapes skipped
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_source_hash():
+    """Hash of the decode kernels' source (comments and blank lines left out)."""
     h = hashlib.sha256()
     for rel in ("paged_kv_cache_128_gb300/csrc/paged_decode.cu", "paged_kv_cache_128_gb300/csrc/common.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -375,6 +404,8 @@ def target_rooflines(args, dev, l2, peak, peak_kind):
         if name == args.workload:
             continue
         wl = make_workload(name)
+        if args.kv_cache == "fp8" and wl.head_dim != 128:
+            continue  # fp8 caches are built for head_dim 128 only
         eng = PagedDecodeEngine(wl, dev, max_steps=2, fill_sentinel=False, kv_cache=args.kv_cache)
         vals = make_values(wl, device="cuda")
         eng.setup(vals)
@@ -689,6 +720,81 @@ def run_profile_calls(args):
         sys.exit(1)
 
 
+# ----------------------------------------------------------- cache write
+
+def run_cache_write(args):
+    """The standalone cache write of the workload's first step (the call the
+    two-call step and the history set-up make), L2 flushed before each call,
+    CUDA events on the launching stream around the launch only (queued
+    behind a GPU-side delay).  Algorithmic bytes: each valid new row read
+    once and written once (fp8: its codes and per-head scales), plus the
+    slot of every row.  With --profile-calls only that many calls run (the
+    small fixed launch sequence for ncu)."""
+    import torch
+
+    import paged_kv_cache_128_gb300 as pk
+    from paged_kv_cache_128_gb300.engine import PagedDecodeEngine
+    from paged_kv_cache_128_gb300.inputs import make_values, make_workload
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, peak_kind = measured_peak()
+    wl = make_workload(args.workload)
+    eng = PagedDecodeEngine(wl, dev, max_steps=2, fill_sentinel=False, kv_cache=args.kv_cache)
+    vals = make_values(wl, device="cuda")
+    eng.setup(vals)
+    eng.step(vals.q, vals.k_step, vals.v_step)  # the step's slot mapping now sits on the device
+    torch.cuda.synchronize()
+    nbytes = eng.algorithmic_bytes(eng._views(eng.d_meta.cpu())[2].numpy())["cache_write"]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush_read = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    if args.profile_calls:
+        for _ in range(args.profile_calls):
+            flush.zero_()
+            eng.write_step_kv(vals.k_step, vals.v_step)
+        torch.cuda.synchronize()
+        status = pk.device_error()
+        print(json.dumps({"workload": wl.name, "cache_write_calls": args.profile_calls, "kv_cache": args.kv_cache,
+                          "bytes_per_call": nbytes, "device_error": status}))
+        if status:
+            sys.exit(1)
+        return
+    for _ in range(max(args.warmup, 3)):
+        eng.write_step_kv(vals.k_step, vals.v_step)
+    torch.cuda.synchronize()
+    calls = max(min(args.steps, 200), 30)
+    clocks = ClockSampler(0)
+    clocks.start()
+    ms = []
+    for _ in range(calls):
+        flush.zero_()
+        flush_read.sum()
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(200000)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        eng.write_step_kv(vals.k_step, vals.v_step)
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    clk = clocks.stop()
+    status = pk.device_error()
+    call_s = statistics.fmean(ms[2:]) / 1e3
+    gbs = nbytes / call_s / 1e9
+    kernel = "cache_write_fp8_kernel" if args.kv_cache == "fp8" else "reshape_and_cache_kernel"
+    print(json.dumps({"metric": "standalone cache write HBM GB/s", "value": gbs, "unit": "GB/s",
+                      "higher_is_better": True, "mean_call_us": call_s * 1e6, "calls": calls,
+                      "bytes_per_call": nbytes, "rows": int(eng.n_prefill + wl.num_seqs),
+                      "roofline": {"bound": "hbm", "kernel": kernel, "achieved": gbs, "peak": peak,
+                                   "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)", "unit": "GB/s",
+                                   "frac": gbs / peak},
+                      "config": {"workload": wl.name, "kv_cache": args.kv_cache, "l2": "flushed before each call"},
+                      "clocks": clk, "device_error": status}))
+    if status:
+        sys.exit(1)
+
+
 # ------------------------------------------------------ chunked prefill
 
 def prefill_setup(ctx, dev, seed=5):
@@ -967,6 +1073,9 @@ def main():
         return
     if args.prefill:
         run_prefill(args)
+        return
+    if args.cache_write:
+        run_cache_write(args)
         return
     if args.profile_calls:
         run_profile_calls(args)

@@ -289,7 +289,9 @@ int paged_reshape_and_cache_layers(const void* k, const void* v, void* k_cache, 
  * value divided by the scale in float32 with one correct rounding, then
  * rounded to E4M3, nearest-even, saturating at +-448.  Its dequantised value
  * is code * scale.  The write replaces paged_reshape_and_cache (same slot
- * rules: -1 skipped, out-of-pool slots skipped and recorded); k, v are
+ * rules: -1 skipped, out-of-pool slots skipped and recorded; a padded
+ * token's input row, which must exist like every row t < num_tokens, may be
+ * read); k, v are
  * fp16 or bf16 (dtype), head_dim 64, 128 or 256, token strides even, k/v
  * 4-byte aligned, caches 8-byte aligned.  Bit-exact against the
  * definition above. */

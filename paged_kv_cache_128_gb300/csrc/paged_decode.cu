@@ -6,29 +6,31 @@
 //   out[b, qh] = sum_{j < L_b} softmax_j(scale * q[b, qh] . K_j) V_j,
 //   kvh = qh / (Hq / Hkv),  K_j = k_cache[table[b][j / bs]][j % bs][kvh].
 //
-// Work decomposition: one CTA per (split, kv head, sequence).  A CTA owns a
-// contiguous range of `blocks_per_split` logical blocks of one sequence and
-// serves all G = Hq / Hkv query heads of its kv head, so each K/V byte is
-// read from HBM once.  When a sequence spans more than one split, each CTA
-// writes an unnormalised partial (acc, m, l) to the workspace and a small
-// merge kernel combines them by log-sum-exp (flash-decoding style split-K).
-//
-// Two kernels share that decomposition:
-//  * decode_tc_kernel (fp16/bf16, head_dim 64/128/256, block_size 16/32,
-//    G <= 16): warp-specialised.  One producer warp walks the block table
-//    (entries fetched 32 at a time and shuffled) and issues TMA tensor loads
-//    of each physical block's [bs, D] K and V slices for this kv head into
-//    a ring of shared-memory stages (128-byte swizzle, mbarrier complete_tx).
-//    Four consumer warps take stages round robin.  Each computes
-//    S^T = K Q^T (tokens in M, query heads in N, m16n8k16 mma.sync with fp32
-//    accumulation), an fp32 online softmax in the exp2 domain, turns P^T
-//    into the B operand with movmatrix, and accumulates O^T += V^T P^T with
-//    V^T fragments from ldmatrix.trans.  The warps' states are merged in
-//    shared memory at the end.
-//  * decode_simt_kernel (any dtype, head_dim a multiple of 4 up to 256, any
-//    block size and group): one warp per block, lane-parallel dot products
-//    reduced with shuffles, the same online softmax.  Used for fp32 and for
-//    shapes the tensor-core kernel does not cover.
+// Kernels (the host plan picks one per call):
+//  * decode_sk_kernel, the default for fp16/bf16 caches at head_dim
+//    64/128/256 and fp8 (E4M3) caches at head_dim 128, block_size 16/32,
+//    G = Hq / Hkv <= 16: stream-K
+//    over the ordered tiles (sequence, kv head, 32 or 64 tokens) in one
+//    cooperative wave of persistent CTAs, each CTA a TMA producer warp, four
+//    mma.sync consumer warps and a writer warp; units cut by range
+//    boundaries are combined by their owner CTA (see "Stream-K tensor-core
+//    kernel" below).  It also runs the fused decode step: its writer warps
+//    scatter the step's new K/V rows into the caches.
+//  * decode_split_kernel, the same shapes where the stream-K shared memory
+//    does not fit or a split size is forced: one CTA per (split, kv head,
+//    sequence) over blocks_per_split blocks, serving all G query heads of
+//    its kv head so each K/V byte is read once.  Its producer warp walks the
+//    block table (entries fetched 32 at a time and shuffled) and issues TMA
+//    loads of each block's K and V slices into a ring of shared-memory
+//    stages; four consumer warps compute S^T = K Q^T (tokens in M, query
+//    heads in N, m16n8k16 mma.sync, fp32 accumulation), an fp32 online
+//    softmax in the exp2 domain, and O^T += V^T P^T (P^T turned into the B
+//    operand with movmatrix, V^T from ldmatrix.trans).
+//  * decode_simt_kernel, any dtype, head_dim a multiple of 4 up to 256, any
+//    block size and group: one warp per block, lane-parallel dot products
+//    reduced with shuffles, the same online softmax.
+// Split partials (acc, m, l) of the split and SIMT kernels are combined by
+// lse_merge_kernel (log-sum-exp, flash-decoding style split-K).
 //
 // Tail handling: only ceil(L / bs) table entries are read.  Positions >= L
 // in the last block are excluded by selection (score = -inf), and their V

@@ -280,7 +280,10 @@ extern "C" int paged_copy_blocks_fp8(void* k_cache, void* v_cache, float* k_scal
 // The values are divided by it in float32 (correctly rounded) and rounded to
 // E4M3, nearest-even, saturating at 448.  One warp per token; a lane owns E
 // consecutive values of a row (E = head_dim / 32) and the amax is a warp
-// max-reduction.
+// max-reduction.  A warp loads K and V of kFp8Heads heads before it
+// quantises any of them, and the first heads' loads go out before the
+// token's slot has arrived (a padded token's row is read and dropped), so
+// the memory round trips overlap instead of following one another.
 
 namespace pagedkv {
 namespace {
@@ -291,49 +294,86 @@ __device__ __forceinline__ uint16_t e4m3x2_from(float lo, float hi) {
   return r;
 }
 
+// A read-only 4-byte global load that stays where it is written: volatile,
+// so it is neither dropped nor moved past the slot check into the branch
+// that uses it.
+__device__ __forceinline__ uint32_t load_early(const uint32_t* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
+constexpr int kFp8Heads = 4;
+
 template <typename T, int E>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 cache_write_fp8_kernel(const T* __restrict__ k, const T* __restrict__ v, uint8_t* __restrict__ k_codes,
                        uint8_t* __restrict__ v_codes, float* __restrict__ k_scales, float* __restrict__ v_scales,
                        const int32_t* __restrict__ slot_mapping, int64_t num_tokens, int num_kv_heads,
                        int block_size, int64_t k_stride, int64_t v_stride, int64_t num_slots) {
-  constexpr int D = 32 * E;
+  constexpr int D = 32 * E, W = E / 2;  // W: 32-bit words holding a lane's E values
   const int lane = threadIdx.x & 31;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5); t < num_tokens;
        t += static_cast<int64_t>(gridDim.x) * kWarpsPerCta) {
     const int32_t slot = __ldg(slot_mapping + t);
-    if (slot == -1) continue;
+    // 4-byte aligned: k and v are, token strides are even, lane * E * 2 is a multiple of 4
+    const uint32_t* krow = reinterpret_cast<const uint32_t*>(k + t * k_stride + lane * E);
+    const uint32_t* vrow = reinterpret_cast<const uint32_t*>(v + t * v_stride + lane * E);
+    uint32_t raw[kFp8Heads][2][W];
+    auto load = [&](int h0) {
+#pragma unroll
+      for (int g = 0; g < kFp8Heads; ++g)
+        if (h0 + g < num_kv_heads)
+#pragma unroll
+          for (int w = 0; w < W; ++w) {
+            raw[g][0][w] = load_early(krow + (h0 + g) * (D / 2) + w);
+            raw[g][1][w] = load_early(vrow + (h0 + g) * (D / 2) + w);
+          }
+    };
+    load(0);
+    if (slot == -1) continue;  // padded token: nothing written
     if (slot < 0 || slot >= num_slots) {
       if (lane == 0) record_error(KV_ERR_DEVICE_BOUNDS);
       continue;
     }
     const int64_t blk = slot / block_size, off = slot % block_size;
-    for (int h = 0; h < num_kv_heads; ++h) {
+    for (int h0 = 0; h0 < num_kv_heads; h0 += kFp8Heads) {
+      if (h0 > 0) load(h0);
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const T* src = (which ? v + t * v_stride : k + t * k_stride) + h * D + lane * E;
-        float x[E];
+      for (int g = 0; g < kFp8Heads; ++g) {
+        const int h = h0 + g;
+        if (h >= num_kv_heads) break;
 #pragma unroll
-        for (int e = 0; e < E; ++e) x[e] = DType<T>::to_float(src[e]);
-        float amax = 0.f;
+        for (int which = 0; which < 2; ++which) {
+          float x[E];
 #pragma unroll
-        for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
+          for (int w = 0; w < W; ++w) {  // the lower-addressed value sits in the low half of the word
+            T pair[2];
+            memcpy(pair, &raw[g][which][w], sizeof(pair));
+            x[2 * w] = DType<T>::to_float(pair[0]);
+            x[2 * w + 1] = DType<T>::to_float(pair[1]);
+          }
+          float amax = 0.f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
-        uint16_t packed[E / 2];
+          for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
-        for (int e = 0; e < E; e += 2) packed[e / 2] = e4m3x2_from(__fdiv_rn(x[e], scale), __fdiv_rn(x[e + 1], scale));
-        uint8_t* dst = (which ? v_codes : k_codes) + (static_cast<int64_t>(slot) * num_kv_heads + h) * D + lane * E;
-        if constexpr (E == 2) {
-          *reinterpret_cast<uint16_t*>(dst) = packed[0];
-        } else if constexpr (E == 4) {
-          *reinterpret_cast<uint32_t*>(dst) = packed[0] | (static_cast<uint32_t>(packed[1]) << 16);
-        } else {
-          *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0] | (static_cast<uint32_t>(packed[1]) << 16),
-                                                      packed[2] | (static_cast<uint32_t>(packed[3]) << 16));
+          for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+          uint16_t packed[E / 2];
+#pragma unroll
+          for (int e = 0; e < E; e += 2)
+            packed[e / 2] = e4m3x2_from(__fdiv_rn(x[e], scale), __fdiv_rn(x[e + 1], scale));
+          uint8_t* dst = (which ? v_codes : k_codes) + (static_cast<int64_t>(slot) * num_kv_heads + h) * D + lane * E;
+          if constexpr (E == 2) {
+            *reinterpret_cast<uint16_t*>(dst) = packed[0];
+          } else if constexpr (E == 4) {
+            *reinterpret_cast<uint32_t*>(dst) = packed[0] | (static_cast<uint32_t>(packed[1]) << 16);
+          } else {
+            *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0] | (static_cast<uint32_t>(packed[1]) << 16),
+                                                        packed[2] | (static_cast<uint32_t>(packed[3]) << 16));
+          }
+          if (lane == 0) (which ? v_scales : k_scales)[(blk * num_kv_heads + h) * block_size + off] = scale;
         }
-        if (lane == 0) (which ? v_scales : k_scales)[(blk * num_kv_heads + h) * block_size + off] = scale;
       }
     }
   }

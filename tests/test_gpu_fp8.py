@@ -39,12 +39,15 @@ def _f32(t):
     return t.detach().cpu().float().numpy()
 
 
+# kv heads: fewer than, a multiple of, and not a multiple of the heads the
+# kernel loads ahead together; a token stride wider than the row
+@pytest.mark.parametrize("hkv,pad", [(2, 0), (5, 6), (8, 0)])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("d", [64, 128, 256])
-def test_fp8_cache_write_bit_exact(dtype, d):
-    rng = np.random.default_rng(d)
-    g = torch.Generator().manual_seed(d)
-    nb, bs, hkv, n = 24, 16, 2, 70
+def test_fp8_cache_write_bit_exact(dtype, d, hkv, pad):
+    rng = np.random.default_rng(d + hkv)
+    g = torch.Generator().manual_seed(d + hkv)
+    nb, bs, n = 24, 16, 70
     dt = TORCH[dtype]
     mag = torch.exp(torch.randn(n, hkv, 1, generator=g) * 2)        # row magnitudes over ~e^+-6
     k = (torch.randn(n, hkv, d, generator=g) * mag).to(dt)
@@ -55,7 +58,13 @@ def test_fp8_cache_write_bit_exact(dtype, d):
     dev = torch.device("cuda")
     kc, vc, ks, vs = _empty_fp8(nb, bs, hkv, d, dev)
     pk.device_error()
-    pk.reshape_and_cache_fp8(k.to(dev), v.to(dev), kc, vc, ks, vs, torch.from_numpy(slots).to(dev))
+    def on_device(x):  # rows pad elements apart beyond the dense [Hkv, D] row
+        wide = torch.zeros(n, hkv * d + pad, dtype=dt, device=dev)
+        wide[:, :hkv * d] = x.reshape(n, -1).to(dev)
+        return wide[:, :hkv * d].view(n, hkv, d) if pad == 0 else wide.as_strided((n, hkv, d), (hkv * d + pad, d, 1))
+    kd, vd = on_device(k), on_device(v)
+    assert kd.stride(0) == hkv * d + pad
+    pk.reshape_and_cache_fp8(kd, vd, kc, vc, ks, vs, torch.from_numpy(slots).to(dev))
     assert pk.device_error() == 0
     # oracle: quantise every row, scatter by slot
     kc_o = np.full((nb, bs, hkv, d), CODE_SENTINEL, np.uint8)

@@ -29,6 +29,8 @@ def _case(dtype, n, nb, bs, hkv, d, n_pad, seed):
     ("f16", 300, 64, 16, 2, 64, 15, 0),
     ("bf16", 513, 128, 16, 4, 128, 26, 0),
     ("bf16", 700, 64, 32, 8, 128, 35, 0),
+    ("f16", 90, 32, 16, 8, 256, 9, 0),      # 4 KB rows: two rounds of a lane's vectors
+    ("f32", 45, 16, 16, 4, 160, 4, 0),      # 2560-byte rows: a partial second round
     ("f16", 50, 16, 8, 3, 12, 3, 0),        # 72-byte rows: 8-byte vectors
     ("bf16", 40, 16, 8, 1, 6, 2, 0),        # 12-byte rows: 4-byte vectors
     ("bf16", 33, 16, 4, 1, 3, 1, 0),        # 6-byte rows: 2-byte elements
