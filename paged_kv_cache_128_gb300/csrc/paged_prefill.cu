@@ -9,9 +9,12 @@
 // through the table, GQA head mapping kvh = qh / (Hq / Hkv)).  A chunk of
 // one token is decode.
 //
-// Kernel shape (flash-attention style, tensor cores through mma.sync):
-// one CTA per (64-token query tile, query head, sequence), four warps of 16
-// query rows.  Key tiles of 32 tokens are gathered through the block table
+// Two kernels.  prefill_tc_kernel (tcgen05 MMAs into tensor memory, K/V
+// tiles by TMA through the table) serves block sizes that divide 128 and
+// are multiples of 16; it is described at its definition below.
+// prefill_kernel serves the other block sizes, flash-attention style with
+// mma.sync: one CTA per (64-token query tile, query head, sequence), four
+// warps of 16 query rows.  Key tiles of 32 tokens are gathered through the block table
 // with 16-byte cp.async into a double-buffered, 128-byte-swizzled shared
 // tile while the previous tile is consumed.  Per tile a warp computes
 // S = Q K^T (Q as the A operand from registers, K^T fragments by
