@@ -225,6 +225,14 @@ typedef struct {
 
 int kvbm_stats(kvbm_t h, kvbm_stats_t* out);
 
+/* *out = the number of ranges of consecutive released ids the manager
+ * remembers, so that a second release of an id answers KV_ERR_DOUBLE_FREE
+ * (LLM-algo ch.22 Step 4 raises on a second release) until the id is
+ * prefilled again.  Released ids are kept as merged ranges, so the memory
+ * this takes follows the gaps between released ids, not their number: ids
+ * released in order (a serving loop numbering its requests) stay one range. */
+int kvbm_released_ranges(kvbm_t h, int64_t* out);
+
 /* LLM-algo ch.22 allocation_report for one sequence: allocated tokens,
  * unused tail tokens, utilisation = logical / allocated. */
 int kvbm_allocation_report(kvbm_t h, int64_t seq_id, int64_t* logical_tokens,

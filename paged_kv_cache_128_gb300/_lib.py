@@ -71,6 +71,7 @@ SIGNATURES = {
     "kvbm_export_update": (c_int, [c_void_p, P64, c_int64, c_int64, P32, P64, P32]),
     "kvbm_check_invariants": (c_int, [c_void_p]),
     "kvbm_stats": (c_int, [c_void_p, POINTER(kvbm_stats_t)]),
+    "kvbm_released_ranges": (c_int, [c_void_p, POINTER(c_int64)]),
     "kvbm_allocation_report": (c_int, [c_void_p, c_int64, P64, P64, P64, POINTER(c_double)]),
     "kvbm_owner_table": (c_int, [c_void_p, P64, c_int64]),
     "kv_cache_ledger": (c_int, [c_int64, c_int64, c_int64, c_int64, c_int64, c_int64, P64, P64, P64]),

@@ -209,6 +209,13 @@ class KVBlockManager:
         check(self._lib.kvbm_stats(self._h, ctypes.byref(s)), "kvbm_stats")
         return {name: getattr(s, name) for name, _ in kvbm_stats_t._fields_}
 
+    def released_ranges(self) -> int:
+        """Ranges of consecutive released ids the manager remembers (for
+        KV_ERR_DOUBLE_FREE on a second release)."""
+        n = ctypes.c_int64()
+        check(self._lib.kvbm_released_ranges(self._h, ctypes.byref(n)), "kvbm_released_ranges")
+        return n.value
+
     def allocation_report(self, seq_id: int) -> Dict[str, float]:
         lt, at, ut = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
         u = ctypes.c_double()

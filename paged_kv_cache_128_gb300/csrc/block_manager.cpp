@@ -27,6 +27,8 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <iterator>
+#include <map>
 #include <new>
 #include <unordered_map>
 #include <unordered_set>
@@ -108,6 +110,55 @@ class IdSet {
   uint32_t cur_ = 0;
 };
 
+// Released sequence ids, remembered so that a second release answers
+// KV_ERR_DOUBLE_FREE, kept as disjoint inclusive ranges [first, last].  A
+// serving loop that numbers its requests in order releases runs of
+// consecutive ids, which merge into a few ranges: memory follows the gaps
+// between released ids, not their count.  Ids are >= 0.
+class IdRanges {
+ public:
+  size_t count(int64_t id) const {
+    auto it = r_.upper_bound(id);  // first range starting after id
+    if (it == r_.begin()) return 0;
+    --it;
+    return id <= it->second ? 1 : 0;
+  }
+  void insert(int64_t id) {
+    if (count(id)) return;
+    int64_t last = id;
+    if (id < INT64_MAX) {  // absorb a range starting right after id
+      auto nx = r_.find(id + 1);
+      if (nx != r_.end()) {
+        last = nx->second;
+        r_.erase(nx);
+      }
+    }
+    auto it = r_.lower_bound(id);
+    if (it != r_.begin()) {  // extend a range ending right before id
+      auto pv = std::prev(it);
+      if (pv->second == id - 1) {
+        pv->second = last;
+        return;
+      }
+    }
+    r_.emplace(id, last);
+  }
+  void erase(int64_t id) {
+    auto it = r_.upper_bound(id);
+    if (it == r_.begin()) return;
+    --it;
+    if (id > it->second) return;
+    const int64_t first = it->first, last = it->second;
+    r_.erase(it);
+    if (first < id) r_.emplace(first, id - 1);
+    if (id < last) r_.emplace(id + 1, last);
+  }
+  size_t ranges() const { return r_.size(); }
+
+ private:
+  std::map<int64_t, int64_t> r_;  // first -> last
+};
+
 }  // namespace
 
 struct kvbm_s {
@@ -116,7 +167,7 @@ struct kvbm_s {
   FreeList free_list;
   std::vector<int32_t> ref_count;  // table entries referring to each block; 0 = free
   std::unordered_map<int64_t, Sequence> seqs;
-  std::unordered_set<int64_t> released;
+  IdRanges released;
   std::vector<int32_t> copy_src, copy_dst;  // copy-on-write copies not yet taken
   IdSet step_ids;                      // kvbm_prepare_step's duplicate checks
   std::vector<const Sequence*> export_rows;  // kvbm_export_update's rows, validated before any write
@@ -626,6 +677,12 @@ int kvbm_stats(kvbm_t h, kvbm_stats_t* out) {
   }
   st.unused_tail_tokens = st.allocated_tokens - st.logical_tokens;
   *out = st;
+  return KV_OK;
+}
+
+int kvbm_released_ranges(kvbm_t h, int64_t* out) {
+  if (!h || !out) return KV_ERR_INVALID_ARG;
+  *out = static_cast<int64_t>(h->released.ranges());
   return KV_OK;
 }
 

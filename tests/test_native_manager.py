@@ -121,6 +121,51 @@ def test_double_free_and_reuse_codes():
     assert sorted(nat.block_table(5).tolist()) == [0, 1, 2]
 
 
+@pytest.mark.parametrize("seed", range(4))
+def test_release_and_reprefill_codes_match_oracle(seed):
+    """Ids from a small universe are prefilled, released, released again
+    and prefilled again in random order, so the released-id ranges merge
+    and split often; every result and error code must equal the oracle's
+    (which remembers released ids in a plain set)."""
+    rng = random.Random(700 + seed)
+    nat, ora = KVBlockManager(256, 1), OracleManager(256, 1)
+    for _ in range(1500):
+        sid = rng.randrange(40)
+        if rng.random() < 0.5:
+            _both(lambda: nat.allocate_for_prefill(sid, 1), lambda: ora.allocate_for_prefill(sid, 1))
+        else:
+            _both(lambda: nat.free_sequence(sid), lambda: ora.free_sequence(sid))
+        _same_state(nat, ora)
+
+
+def test_released_ids_are_kept_as_ranges():
+    nat = KVBlockManager(512, 1)
+    for sid in range(300):
+        nat.allocate_for_prefill(sid, 1)
+    for sid in range(300):                    # released in order: one range
+        nat.free_sequence(sid)
+    assert nat.released_ranges() == 1
+    for sid in (0, 150, 299):
+        with pytest.raises(KVError) as e:
+            nat.free_sequence(sid)
+        assert e.value.code == "DOUBLE_FREE"
+    with pytest.raises(KVError) as e:
+        nat.free_sequence(300)
+    assert e.value.code == "UNKNOWN_SEQ"
+    nat.allocate_for_prefill(150, 1)          # prefilled again: the range splits
+    assert nat.released_ranges() == 2
+    nat.free_sequence(150)
+    assert nat.released_ranges() == 1
+    for sid in range(400, 500, 2):            # every other id: one range each
+        nat.allocate_for_prefill(sid, 1)
+        nat.free_sequence(sid)
+    assert nat.released_ranges() == 51
+    for sid in range(401, 500, 2):            # the gaps filled: merged into one
+        nat.allocate_for_prefill(sid, 1)
+        nat.free_sequence(sid)
+    assert nat.released_ranges() == 2
+
+
 def test_pages_examples_on_native():
     g = G_CH22["prefill_decode"]
     m = KVBlockManager(g["num_blocks"], g["block_size"])
