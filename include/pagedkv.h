@@ -82,6 +82,9 @@ typedef struct kvbm_s* kvbm_t;
  * *out receives the handle; release it with kvbm_destroy. */
 int kvbm_create(int64_t num_blocks, int32_t block_size, const int32_t* initial_free_order,
                 kvbm_t* out);
+/* Release the handle and everything it holds (h may be NULL).  No passage:
+ * the pages' managers are Python objects their runtime frees; a C ABI needs
+ * an explicit release. */
 int kvbm_destroy(kvbm_t h);
 
 /* *ok = 1 iff ceil(num_tokens / block_size) blocks are free (num_tokens >= 1). */
@@ -173,6 +176,9 @@ int kvbm_prepare_step(kvbm_t h, const int64_t* free_ids, int64_t n_free, const i
  * never seen. */
 int kvbm_free_sequence(kvbm_t h, int64_t seq_id);
 
+/* *out = the number of free blocks: get_num_free_blocks, one of the three
+ * actions of the minimal block manager ("从零实现一个 mini vLLM: Block
+ * Manager", section "Block Manager 要维护哪些东西"). */
 int kvbm_num_free_blocks(kvbm_t h, int64_t* out);
 
 /* Copy the free list, front first, into out[cap]; *n_out = its length.
@@ -432,7 +438,12 @@ int paged_decode_plan(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
                       size_t* workspace_bytes_out);
 
 /* Bytes of device workspace paged_decode_attention needs for these sizes
- * (0 when no split is needed); same arguments as paged_decode_plan. */
+ * (0 when no split is needed); same arguments as paged_decode_plan.  The
+ * workspace holds the partial results (acc, m, l) of the library's work
+ * partition (split-K, or stream-K ranges that cut a sequence) and its ready
+ * flags.  No passage: the pages' decode attention ("MiniPaged-Qwen" §13)
+ * reads each sequence whole; the partition is this library's way of
+ * keeping every SM busy when the batch alone would not. */
 int paged_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
                                 int32_t head_dim, int32_t block_size, int64_t max_seq_len,
                                 int32_t blocks_per_split, int dtype, size_t* bytes_out);
