@@ -56,7 +56,8 @@ typedef enum {
                                to that sequence's newest slot (inconsistent step metadata) */
 } kv_status_t;
 
-/* Static, NUL-terminated text for a status code (never NULL). */
+/* Static, NUL-terminated text for a status code (never NULL).  No passage:
+ * the pages raise Python exceptions with messages; this is their C form. */
 const char* kv_status_string(int status);
 
 typedef enum { KV_DTYPE_F32 = 0, KV_DTYPE_F16 = 1, KV_DTYPE_BF16 = 2 } kv_dtype_t;
@@ -79,7 +80,9 @@ typedef struct kvbm_s* kvbm_t;
  * initial_free_order: NULL for 0..num_blocks-1, else a host array of
  * num_blocks int32 that must be a permutation of the pool (else
  * KV_ERR_INVALID_ARG).  num_blocks * block_size must fit in int32.
- * *out receives the handle; release it with kvbm_destroy. */
+ * *out receives the handle; release it with kvbm_destroy.  The pool of
+ * MiniPaged-Qwen §8 (KVBlockManager(num_blocks, block_size)) and LLM-algo
+ * ch.22 Step 4 (KVCacheManager: every block free at the start). */
 int kvbm_create(int64_t num_blocks, int32_t block_size, const int32_t* initial_free_order,
                 kvbm_t* out);
 /* Release the handle and everything it holds (h may be NULL).  No passage:
@@ -87,7 +90,8 @@ int kvbm_create(int64_t num_blocks, int32_t block_size, const int32_t* initial_f
  * an explicit release. */
 int kvbm_destroy(kvbm_t h);
 
-/* *ok = 1 iff ceil(num_tokens / block_size) blocks are free (num_tokens >= 1). */
+/* *ok = 1 iff ceil(num_tokens / block_size) blocks are free (num_tokens >= 1):
+ * can_allocate of "从零实现一个 mini vLLM: Block Manager" (prefill admission). */
 int kvbm_can_allocate(kvbm_t h, int64_t num_tokens, int* ok);
 
 /* Prefill: allocate ceil(num_tokens / block_size) blocks at once for a new
@@ -103,7 +107,9 @@ int kvbm_allocate_for_prefill(kvbm_t h, int64_t seq_id, int64_t num_tokens, int3
 int kvbm_append_slot_for_decode(kvbm_t h, int64_t seq_id, int32_t* slot_out);
 
 /* num_tokens consecutive appends to a live sequence (chunked prefill), all
- * or nothing on OOM.  slots_out (nullable) receives num_tokens slots. */
+ * or nothing on OOM.  slots_out (nullable) receives num_tokens slots.  The
+ * chunk of a chunked prefill in "从零实现一个 mini vLLM: Block Manager" takes
+ * its slots this way: MiniPaged-Qwen §9's append, num_tokens times. */
 int kvbm_append_slots(kvbm_t h, int64_t seq_id, int64_t num_tokens, int32_t* slots_out);
 
 /* Prefix sharing ("paged-attention-impl-detail", section Copy-on-Write共享:
@@ -134,18 +140,21 @@ int kvbm_fork(kvbm_t h, int64_t parent_id, int64_t child_id, int64_t prefix_len)
 int kvbm_take_copies(kvbm_t h, int32_t* src, int32_t* dst, int64_t cap, int64_t* n_out);
 
 /* *out = the number of table entries (over all live sequences) that refer
- * to block (0 = free). */
+ * to block (0 = free): the per-block reference count of
+ * "paged-attention-impl-detail", section Copy-on-Write共享. */
 int kvbm_block_refcount(kvbm_t h, int32_t block, int32_t* out);
 
 /* *ok = 1 iff one decode append to each listed sequence fits in the free
  * blocks (counts sequences whose next write opens a new block or copies a
- * shared one). */
+ * shared one): can_append_slots of "从零实现一个 mini vLLM: Block
+ * Manager" (decode admission). */
 int kvbm_can_append_slots(kvbm_t h, const int64_t* seq_ids, int64_t n, int* ok);
 
 /* One decode step for n distinct live sequences: append one slot to each
  * (slots_out[n], nullable), then export their tables and lengths as
  * kvbm_export does (block_tables / seq_lens nullable).  All or nothing on
- * OOM.  A repeated id is KV_ERR_INVALID_ARG. */
+ * OOM (LLM-algo ch.22 Step 4, decode rollback).  A repeated id is
+ * KV_ERR_INVALID_ARG.  MiniPaged-Qwen §9 (append) then §16.2 (export). */
 int kvbm_decode_step(kvbm_t h, const int64_t* seq_ids, int64_t n, int64_t max_blocks,
                      int32_t* slots_out, int32_t* block_tables, int32_t* seq_lens);
 
@@ -182,12 +191,17 @@ int kvbm_free_sequence(kvbm_t h, int64_t seq_id);
 int kvbm_num_free_blocks(kvbm_t h, int64_t* out);
 
 /* Copy the free list, front first, into out[cap]; *n_out = its length.
- * KV_ERR_INVALID_ARG if cap is too small. */
+ * KV_ERR_INVALID_ARG if cap is too small.  The free_blocks list of
+ * MiniPaged-Qwen §8 and LLM-algo ch.22 Step 4, for inspection and tests. */
 int kvbm_get_free_list(kvbm_t h, int32_t* out, int64_t cap, int64_t* n_out);
 
+/* *out = seq_id's length (MiniPaged-Qwen §8 SequenceState.length).
+ * KV_ERR_UNKNOWN_SEQ if it is not live. */
 int kvbm_seq_len(kvbm_t h, int64_t seq_id, int64_t* out);
 
-/* Copy seq_id's block table into out[cap]; *n_out = its length. */
+/* Copy seq_id's block table into out[cap]; *n_out = its length
+ * (MiniPaged-Qwen §8 SequenceState.block_table).  KV_ERR_UNKNOWN_SEQ if it
+ * is not live, KV_ERR_INVALID_ARG if cap is too small. */
 int kvbm_get_block_table(kvbm_t h, int64_t seq_id, int32_t* out, int64_t cap, int64_t* n_out);
 
 /* Metadata export (MiniPaged-Qwen §16.2 get_block_table_tensor /
@@ -197,8 +211,8 @@ int kvbm_get_block_table(kvbm_t h, int64_t seq_id, int32_t* out, int64_t cap, in
 int kvbm_export(kvbm_t h, const int64_t* seq_ids, int64_t n, int64_t max_blocks,
                 int32_t* block_tables, int32_t* seq_lens);
 
-/* kvbm_export's block tables written as an update of a buffer that already
- * holds an earlier export: for row i, prev_ids[i] and prev_nblocks[i] say
+/* kvbm_export's block tables (MiniPaged-Qwen §16.2) written as an update of
+ * a buffer that already holds an earlier export: for row i, prev_ids[i] and prev_nblocks[i] say
  * which sequence the row held and how many of its entries were blocks (the
  * rest -1), as this call left them (initialise prev_ids to -1 for a buffer
  * never exported into).  A row that held the same sequence gets its block
@@ -229,6 +243,9 @@ typedef struct {
   int64_t unused_tail_tokens; /* allocated - logical (MiniPaged-Qwen §6.2) */
 } kvbm_stats_t;
 
+/* Pool and usage counts: free blocks, live sequences, logical and allocated
+ * tokens and the unused block tails between them (MiniPaged-Qwen §6.2;
+ * LLM-algo ch.22 Step 4's allocation report, summed over sequences). */
 int kvbm_stats(kvbm_t h, kvbm_stats_t* out);
 
 /* *out = the number of ranges of consecutive released ids the manager
@@ -316,7 +333,8 @@ int paged_reshape_and_cache_fp8(const void* k, const void* v, void* k_cache, voi
                                 int64_t v_token_stride, int dtype, void* stream);
 
 /* paged_decode_attention over fp8 caches and their scales: K_j, V_j are the
- * dequantised rows.  q and out are fp16 or bf16 (dtype); head_dim 128,
+ * dequantised rows (the fp8 KV cache of "paged-attention-impl-detail",
+ * 实践建议 4, read by MiniPaged-Qwen §13's decode attention).  q and out are fp16 or bf16 (dtype); head_dim 128,
  * block_size 16 or 32, at most 16 query heads per kv head and 4096
  * sequences (else KV_ERR_INVALID_ARG).  The stream-K tensor-core kernel:
  * TMA brings the E4M3 rows and the scales, E4M3 pairs convert exactly to
@@ -333,7 +351,8 @@ int paged_decode_attention_fp8(void* out, const void* q, const void* k_cache, co
                                int64_t max_seq_len, float scale, int dtype, void* workspace,
                                size_t workspace_bytes, void* stream);
 
-/* paged_decode_step for fp8 caches: the step's quantised cache write
+/* paged_decode_step for fp8 caches ("paged-attention-impl-detail", 实践建议
+ * 4; MiniPaged-Qwen §12-§13): the step's quantised cache write
  * (exactly as paged_reshape_and_cache_fp8) and decode attention over the
  * fp8 caches (exactly as paged_decode_attention_fp8) in one call, under the
  * requirement and with the checks of paged_decode_step (new_token_row,
@@ -430,7 +449,9 @@ int paged_copy_blocks_fp8(void* k_cache, void* v_cache, float* k_scales, float* 
  * block) tiles, and combining cut sequences inside the same launch); the
  * blocks per split and number of splits S (split kernels); the workspace
  * bytes.  Kernel 2 launches one kernel; kernels 0 and 1 add a log-sum-exp
- * merge kernel when S > 1.
+ * merge kernel when S > 1.  No passage: the pages' decode attention
+ * (MiniPaged-Qwen §13) reads each sequence whole; the partition is this
+ * library's, and the merge restates §17.3's online softmax across pieces.
  * max_seq_len is an upper bound of the seq_lens the call will see. */
 int paged_decode_plan(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                       int32_t block_size, int64_t max_seq_len, int32_t blocks_per_split, int dtype,
@@ -549,17 +570,19 @@ int paged_decode_attention_static_scratch(void* out, const void* q, const void* 
                                           void* stream);
 
 /* Size in bytes of the fixed scratch array behind
- * paged_decode_attention_static_scratch. */
+ * paged_decode_attention_static_scratch (no passage; see that entry). */
 size_t paged_decode_static_scratch_bytes(void);
 
 /* Read (and, if reset != 0, clear) the device error word of the current
  * device: *status_out = KV_OK or the first KV_ERR_DEVICE_* code recorded by
- * a kernel since the last reset.  Synchronises the current device. */
+ * a kernel since the last reset.  Synchronises the current device.  The
+ * device side of LLM-algo ch.22's rule that invalid input raises an error
+ * rather than passing silently: kernels record, they do not trap. */
 int kv_device_error(int reset, int* status_out);
 
 /* Text of the last CUDA error an entry point of this library met on the
  * calling thread (the cause of its most recent KV_ERR_CUDA); static storage,
- * never NULL. */
+ * never NULL.  No passage (diagnostics of the C ABI). */
 const char* kv_last_cuda_error(void);
 
 /* ------------------------------------------------ native step runner */
@@ -617,9 +640,16 @@ typedef struct {
   float* v_scales;             /*   layers back to back */
 } kvstep_config_t;
 
+/* Create a runner over manager mgr (not owned; it must outlive the runner)
+ * with the sizes, caches and workspace of cfg (caller-owned device memory).
+ * The runner owns its page-locked and device metadata buffers, side
+ * streams and events.  KV_ERR_INVALID_ARG for inconsistent sizes or a
+ * missing cache; KV_ERR_CUDA if an allocation fails.  The ModelRunner of
+ * "从零实现一个 mini vLLM: Block Manager" (above). */
 int kvstep_create(kvbm_t mgr, const kvstep_config_t* cfg, kvstep_t* out);
 
-/* Wait for the runner's outstanding work, then release it. */
+/* Wait for the runner's outstanding work, then release it (no passage: C
+ * ABI lifetime). */
 int kvstep_destroy(kvstep_t h);
 
 /* One step.  q [num_seqs, num_heads, head_dim], k and v dense
@@ -656,11 +686,15 @@ int kvstep_run(kvstep_t h, const void* q, const void* k, const void* v, void* ou
  * slot out of range. */
 int kvstep_stage_buffer(kvstep_t h, int32_t slot, void** q, void** k, void** v, int32_t* slot_out);
 
-/* Make `stream` wait for every copy and kernel the runner has issued. */
+/* Make `stream` wait for every copy and kernel the runner has issued (an
+ * event wait; nothing blocks the host).  No passage: stream ordering of
+ * the step runner above. */
 int kvstep_join(kvstep_t h, void* stream);
 
 /* Host copies of the last step's metadata (valid until the next
- * kvstep_run): slot mapping, block tables, seq_lens and the decode rows. */
+ * kvstep_run): slot mapping, block tables, seq_lens and the decode rows,
+ * the ModelRunner's inputs of "从零实现一个 mini vLLM: Block Manager"; for
+ * inspection and tests.  Any output may be NULL. */
 int kvstep_last_buffers(kvstep_t h, const int32_t** slot_mapping, const int32_t** block_tables,
                         const int32_t** seq_lens, const int32_t** new_token_row);
 
@@ -678,7 +712,7 @@ int kvstep_last_buffers(kvstep_t h, const int32_t** slot_mapping, const int32_t*
 enum { KV_DEBUG_WAIT_LIMIT_NS = 1, KV_DEBUG_SKIP_TILE = 2 };
 int kv_debug_set(int key, int64_t value);
 
-/* Library version string (static). */
+/* Library version string (static; no passage). */
 const char* kv_version(void);
 
 #ifdef __cplusplus
